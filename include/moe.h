@@ -1,0 +1,222 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) DSV3-style MXFP8 MoE layer.
+ *
+ * The layer is the one the Mixture-of-Kittens write-ups describe: a
+ * DeepSeek-V3-style MoE layer trained in MXFP8 (Cursor blog summary, "method
+ * points"), whose forward pass dispatches tokens to experts, runs the expert
+ * FFNs and combines the results, and whose backward pass runs reverse-combine
+ * and reverse-dispatch on the forward schedule (same section, bullet on
+ * communication direction). On one GPU, dispatch is a schedule-driven gather
+ * into fixed-capacity ring token buffers and combine a fixed-order weighted
+ * sum (techlab report, section on ring buffers; mlqm commentary, section
+ * "signalling cut to 18 us").
+ *
+ * Conventions for every entry point
+ *   - Pointers named in the signature are DEVICE pointers unless stated.
+ *     bf16 tensors are row-major, dense (row pitch = row length).
+ *   - The caller allocates and frees every buffer, including the workspace
+ *     (moe_workspace_size) and the quantised-weight blob (moe_weights_size).
+ *     The library never allocates device memory and never synchronises the
+ *     stream, except moe_status, which reads one device word.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and runs asynchronously.
+ *   - Return value: MOE_OK, or an MOE_ERR_* code for argument, architecture
+ *     or launch errors, in which case nothing further was enqueued.
+ *     Device-side failures (a bounded wait that ran out, a bounds check)
+ *     are recorded in a status word in the workspace; read it with
+ *     moe_status after synchronising.
+ *   - Results are bitwise deterministic: no floating-point atomics, every
+ *     reduction has a fixed order.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+typedef void* moe_stream_t; /* cudaStream_t */
+
+enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,     /* bad shape, null pointer, misaligned pointer */
+  MOE_ERR_UNSUPPORTED_ARCH = 2,/* current device is not compute capability 10.3 */
+  MOE_ERR_CUDA = 3,            /* a CUDA runtime / driver call failed */
+  MOE_ERR_WORKSPACE = 4,       /* workspace or weight blob too small */
+  MOE_ERR_TIMEOUT = 5,         /* (device status) a bounded wait gave up */
+  MOE_ERR_BOUNDS = 6           /* (device status) an index check failed */
+};
+
+/* Layer shape.
+ *   T tokens, d hidden size, E routed experts, k experts per token,
+ *   n_groups / topk_groups: DSV3 group-limited routing (1/1 = plain top-k),
+ *   I expert SwiGLU inner size, n_shared shared experts (0 or 1),
+ *   capacity: ring capacity per routed expert (rows); 0 = default
+ *   ceil128(2*T*k/E). Constraints: d, I, capacity multiples of 128;
+ *   E a multiple of n_groups with at least 2 experts per group when
+ *   n_groups > 1; 1 <= k <= 8 and k <= E; E <= 512. */
+typedef struct moe_config {
+  int T, d, E, k, n_groups, topk_groups, I, n_shared;
+  int capacity;
+  int flags; /* reserved, must be 0 */
+} moe_config_t;
+
+/* Bytes of workspace the layer needs for this shape (schedule, saved
+ * activations for backward, ring buffers, staging). */
+MOE_API int moe_workspace_size(const moe_config_t* cfg, size_t* bytes);
+
+/* Bytes of the quantised-weight blob written by moe_quantize_weights. */
+MOE_API int moe_weights_size(const moe_config_t* cfg, size_t* bytes);
+
+/* MXFP8 quantisation (write-ups: the layer runs "in MXFP8", Cursor blog
+ * summary "method points"; read as OCP MX v1.0: E4M3 elements, one E8M0
+ * scale per 32 elements, scale byte floor(log2 amax) - 8 + 127, elements
+ * rounded to nearest-even and saturated to +-448).
+ *   src: bf16 [rows][K] row-major.
+ *   axis = 1: blocks of 32 along K. codes [rows][K], scales [rows][K/32].
+ *             K must be a multiple of 32.
+ *   axis = 0: blocks of 32 consecutive rows of one column (token axis).
+ *             codes [K][rows_pad], scales [K][rows_pad/32] (transposed),
+ *             rows_pad = ceil32(rows), zero-padded. K must be a multiple of 32.
+ * Scales are written in this canonical row-major layout. */
+MOE_API int moe_quantize_mxfp8(const void* src_bf16, int rows, int K, int axis, void* codes, void* scales,
+                       moe_stream_t stream);
+
+/* Quantise the expert weights (bf16 masters) into the blob in the four MX
+ * orientations the forward and backward GEMMs read.
+ *   w_gu [E][2I][d]  rows 0..I-1 gate, I..2I-1 up;   w_d [E][d][I];
+ *   ws_gu [n_shared][2I][d], ws_d [n_shared][d][I] (may be NULL if n_shared = 0).
+ *   wq: blob of moe_weights_size bytes. Layout is private to the library
+ *   (see moe_wq_view). Run once per optimiser step; not part of a layer step. */
+MOE_API int moe_quantize_weights(const moe_config_t* cfg, const void* w_gu, const void* w_d, const void* ws_gu,
+                         const void* ws_d, void* wq, moe_stream_t stream);
+
+/* Router (write-ups: DSV3-style router, Cursor blog summary "method points").
+ *   x [T][d] bf16, w_router [E][d] bf16, bias [E] fp32.
+ *   logits = x w_router^T (fp32), s = sigmoid(logits) in a specified fp32
+ *   arithmetic, v = s + bias; keep the topk_groups groups with the largest
+ *   sum of their two best v; pick the k best v of kept experts (ties to the
+ *   lower index), slots ordered by descending v; gates w = s / sum(s).
+ *   Outputs topk_idx [T][k] int32 and topk_w [T][k] fp32. Saves logits and
+ *   selected scores in ws for backward. */
+MOE_API int moe_route(const moe_config_t* cfg, const void* x, const void* w_router, const float* bias, int32_t* topk_idx,
+              float* topk_w, void* ws, moe_stream_t stream);
+
+/* Device-side schedule (write-ups: scheduling runs entirely on the device,
+ * under 3 % of MoE time, reused by backward without re-sorting; Cursor blog
+ * summary "method points").
+ *   topk_idx [T][k] int32. Builds in ws: per-expert counts, exclusive
+ *   offsets, stable ranks in (t, j) order, positions offsets[e] + rank,
+ *   the inverse permutation, 128-row padded segments and per-lap tile
+ *   lists of the ring buffers. No host synchronisation. */
+MOE_API int moe_schedule(const moe_config_t* cfg, const int32_t* topk_idx, void* ws, moe_stream_t stream);
+
+/* Forward pass on the schedule in ws (write-ups: dispatch -> expert FFN ->
+ * combine, Cursor blog summary "method points"; ring token buffers reused
+ * lap by lap without dropping tokens, techlab report).
+ *   x [T][d] bf16, wq from moe_quantize_weights, topk_w [T][k] fp32 (from
+ *   moe_route). y [T][d] bf16 = sum_j w[t,j] expert_{idx[t,j]}(x_t) +
+ *   shared(x_t), each expert a SwiGLU FFN on MXFP8 operands. Saves what
+ *   backward needs in ws. */
+MOE_API int moe_forward(const moe_config_t* cfg, const void* x, const void* wq, const float* topk_w, void* y, void* ws,
+                moe_stream_t stream);
+
+/* Backward pass (write-ups: reverse-combine and reverse-dispatch on the
+ * reused schedule, Cursor blog summary "method points").
+ *   x, w_router, topk_idx, topk_w: the forward inputs / router outputs.
+ *   dy [T][d] bf16. Outputs (bf16): dx [T][d], dw_router [E][d],
+ *   dw_gu [E][2I][d], dw_d [E][d][I], dws_gu [n_shared][2I][d],
+ *   dws_d [n_shared][d][I]. The router bias receives no gradient. */
+MOE_API int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, const int32_t* topk_idx,
+                 const float* topk_w, const void* dy, const void* wq, void* dx, void* dw_router, void* dw_gu,
+                 void* dw_d, void* dws_gu, void* dws_d, void* ws, moe_stream_t stream);
+
+/* Device status word of the workspace: MOE_OK or the first device-side
+ * error (code, site). Synchronous: copies 8 bytes to the host on `stream`
+ * and waits for it. Clears the word when `clear` is non-zero. */
+MOE_API int moe_status(const moe_config_t* cfg, void* ws, int* code, int* site, int clear, moe_stream_t stream);
+
+/* Named views into the workspace (for inspection and tests). */
+enum {
+  MOE_WS_STATUS = 0,   /* int32[4] */
+  MOE_WS_META,         /* int32[16]: [0] laps used, [1] padded rows used */
+  MOE_WS_COUNTS,       /* int32[E+S]   per-expert assignment counts (shared last) */
+  MOE_WS_OFFSETS,      /* int32[E+S+1] exclusive prefix sum of counts */
+  MOE_WS_POFF,         /* int32[E+S+1] prefix sum of ceil128(counts) */
+  MOE_WS_RANK,         /* int32[T*(k+S)] rank of assignment a within its expert */
+  MOE_WS_POS,          /* int32[T*(k+S)] offsets[e] + rank */
+  MOE_WS_INV,          /* int32[T*(k+S)] inverse of POS */
+  MOE_WS_ROWSRC,       /* int32[Rmax]   padded row -> assignment (-1 = padding) */
+  MOE_WS_LAPTILES,     /* int32[Lb][E+S+1] per-lap tile prefix sums */
+  MOE_WS_HIST,         /* int32[units][E+S] schedule histogram */
+  MOE_WS_BASE,         /* int32[units][E+S] schedule scan */
+  MOE_WS_LOGITS,       /* fp32[T][E] */
+  MOE_WS_SSEL,         /* fp32[T][k] selected sigmoid scores */
+  MOE_WS_XQ,           /* u8[Tpad][d]       MX(x) along d */
+  MOE_WS_XQ_SF,        /* tiled scales of XQ */
+  MOE_WS_RING_X,       /* u8[E][C][d]       ring token buffer (dispatch) */
+  MOE_WS_RING_X_SF,
+  MOE_WS_GU,           /* bf16[Rmax][2I]    saved g|u */
+  MOE_WS_HQ,           /* u8[Rmax][I]       MX(h) along I */
+  MOE_WS_HQ_SF,
+  MOE_WS_HTOK,         /* u8[I][Rmax]       MX(h) along tokens */
+  MOE_WS_HTOK_SF,
+  MOE_WS_O,            /* bf16[T*(k+S)][d]  expert outputs per assignment */
+  MOE_WS_DW,           /* fp32[T][k]        gate gradients */
+  MOE_WS_DL,           /* fp32[T][k]        router logit gradients */
+  MOE_WS_RING_DO,      /* u8[E][C][d]       ring buffer of MX(w dy) (reverse-combine) */
+  MOE_WS_RING_DO_SF,
+  MOE_WS_DOS,          /* u8[Tpad][d]       MX(dy) along d (shared expert) */
+  MOE_WS_DOS_SF,
+  MOE_WS_DOTOK,        /* u8[d][Rmax]       MX(w dy) along tokens */
+  MOE_WS_DOTOK_SF,
+  MOE_WS_DGU,          /* u8[Rmax][2I]      MX(dGU) along 2I */
+  MOE_WS_DGU_SF,
+  MOE_WS_DGUTOK,       /* u8[2I][Rmax]      MX(dGU) along tokens */
+  MOE_WS_DGUTOK_SF,
+  MOE_WS_XTOK,         /* u8[d][Rmax]       MX(x) along tokens */
+  MOE_WS_XTOK_SF,
+  MOE_WS_DXE,          /* bf16[T*(k+S)][d]  expert input gradients per assignment */
+  MOE_WS_DWR_PART,     /* fp32[Rmax/32][d]  router weight-gradient partial sums */
+  MOE_WS_COUNT
+};
+MOE_API int moe_ws_view(const moe_config_t* cfg, void* ws, int which, void** ptr, size_t* bytes);
+
+/* Named views into the quantised-weight blob. Expert e's rows start at
+ * e * rows_per_expert; shared experts follow the E routed ones.
+ *   W1F: [E+S][2I][d] along d, rows interleaved in 128-row blocks
+ *        (gate 128b..128b+127, then up 128b..128b+127);
+ *   W2F: [E+S][d][I] along I;  W2B: [E+S][I][d] along d (W_d^T);
+ *   W1B: [E+S][d][2I] along 2I (W_gu^T). Scales in the tiled layout. */
+enum {
+  MOE_WQ_W1F = 0, MOE_WQ_W1F_SF, MOE_WQ_W2F, MOE_WQ_W2F_SF,
+  MOE_WQ_W2B, MOE_WQ_W2B_SF, MOE_WQ_W1B, MOE_WQ_W1B_SF, MOE_WQ_COUNT
+};
+MOE_API int moe_wq_view(const moe_config_t* cfg, void* wq, int which, void** ptr, size_t* bytes);
+
+/* Plain MXFP8 GEMM on the tensor cores (the expert GEMMs' core, exposed for
+ * testing): c[M][N] (fp32) = dequant(a)[M][K] . dequant(b)[N][K]^T.
+ *   a, b: E4M3 codes, K-major. a_sf, b_sf: scales in the tiled layout
+ *   (moe_scales_to_tiled). M, N, K multiples of 128. */
+MOE_API int moe_gemm_mxfp8(int M, int N, int K, const void* a, const void* a_sf, const void* b, const void* b_sf, float* c,
+                   moe_stream_t stream);
+
+/* Re-lay canonical scales [rows][K/32] into the tiled layout the tensor
+ * cores read: 512-byte atoms of 128 rows x 4 blocks, atom (r/128, kb/4) at
+ * ((r/128)*(K/128) + kb/4)*512, byte (r%32)*16 + (r/32%4)*4 + kb%4.
+ * rows, K multiples of 128. */
+MOE_API int moe_scales_to_tiled(const void* canon, int rows, int K, void* tiled, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

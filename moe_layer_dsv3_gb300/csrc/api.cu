@@ -1,0 +1,467 @@
+// C ABI: argument checks, workspace layout, and the launch sequence of the
+// forward and backward passes. Every step runs in this library's kernels.
+#include <cstring>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+struct Builder {
+  size_t cur = 0;
+  void add(size_t* off, size_t* bytes, int which, size_t n) {
+    off[which] = cur;
+    bytes[which] = n;
+    cur += (n + kAlign - 1) / kAlign * kAlign;
+  }
+};
+
+bool arch_ok() {
+  static int ok = -1;
+  if (ok < 0) {
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      ok = 0;
+    } else {
+      ok = (major == 10 && minor == 3) ? 1 : 0;
+    }
+  }
+  return ok == 1;
+}
+
+inline cudaStream_t S(moe_stream_t s) { return static_cast<cudaStream_t>(s); }
+
+int launch_status() { return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+}  // namespace
+
+int validate(const moe_config_t* c) {
+  if (c == nullptr) return MOE_ERR_INVALID_ARG;
+  if (c->T < 0 || c->d <= 0 || c->E <= 0 || c->k <= 0 || c->I <= 0) return MOE_ERR_INVALID_ARG;
+  if (c->d % 128 || c->I % 128) return MOE_ERR_INVALID_ARG;
+  if (c->E > 512 || c->k > 8 || c->k > c->E) return MOE_ERR_INVALID_ARG;
+  if (c->n_shared < 0 || c->n_shared > 1) return MOE_ERR_INVALID_ARG;
+  if (c->n_groups <= 0 || c->topk_groups <= 0 || c->topk_groups > c->n_groups || c->n_groups > 32)
+    return MOE_ERR_INVALID_ARG;
+  if (c->E % c->n_groups) return MOE_ERR_INVALID_ARG;
+  if (c->n_groups > 1 && (c->E / c->n_groups < 2 || c->k > c->topk_groups * (c->E / c->n_groups)))
+    return MOE_ERR_INVALID_ARG;
+  if (c->capacity < 0 || c->capacity % 128) return MOE_ERR_INVALID_ARG;
+  if (c->flags != 0) return MOE_ERR_INVALID_ARG;
+  const int64_t Ap = static_cast<int64_t>(c->T) * (c->k + c->n_shared);
+  if (Ap + 128LL * (c->E + c->n_shared) >= (1LL << 31)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+Dims make_dims(const moe_config_t* c) {
+  Dims m{};
+  m.T = c->T;
+  m.d = c->d;
+  m.E = c->E;
+  m.k = c->k;
+  m.G = c->n_groups;
+  m.gtop = c->topk_groups;
+  m.I = c->I;
+  m.S = c->n_shared;
+  const int64_t avg2 = c->E > 0 ? ceil_div(2LL * c->T * c->k, c->E) : 0;
+  m.C = c->capacity > 0 ? c->capacity : static_cast<int>(round_up(avg2 > 128 ? avg2 : 128, 128));
+  m.Ep = m.E + m.S;
+  m.kp = m.k + m.S;
+  m.A = static_cast<int64_t>(m.T) * m.k;
+  m.Ap = static_cast<int64_t>(m.T) * m.kp;
+  m.Tpad = round_up(m.T, 128);
+  m.Rmax = round_up(m.Ap, 128) + 128LL * m.Ep;
+  m.Lb = m.T > 0 ? static_cast<int>(ceil_div(m.T, m.C)) : 0;
+  m.units = static_cast<int>(ceil_div(m.Ap, kSchedUnit));
+  return m;
+}
+
+Layout make_layout(const moe_config_t* c) {
+  Layout L{};
+  L.m = make_dims(c);
+  const Dims& m = L.m;
+  Builder b;
+  const size_t T = m.T, d = m.d, E = m.E, k = m.k, I = m.I, Ep = m.Ep;
+  const size_t Ap = m.Ap, R = m.Rmax, Tp = m.Tpad, C = m.C;
+  b.add(L.off, L.bytes, MOE_WS_STATUS, 16);
+  b.add(L.off, L.bytes, MOE_WS_META, 64);
+  b.add(L.off, L.bytes, MOE_WS_COUNTS, 4 * Ep);
+  b.add(L.off, L.bytes, MOE_WS_OFFSETS, 4 * (Ep + 1));
+  b.add(L.off, L.bytes, MOE_WS_POFF, 4 * (Ep + 1));
+  b.add(L.off, L.bytes, MOE_WS_RANK, 4 * Ap);
+  b.add(L.off, L.bytes, MOE_WS_POS, 4 * Ap);
+  b.add(L.off, L.bytes, MOE_WS_INV, 4 * Ap);
+  b.add(L.off, L.bytes, MOE_WS_ROWSRC, 4 * R);
+  b.add(L.off, L.bytes, MOE_WS_LAPTILES, 4 * static_cast<size_t>(m.Lb > 0 ? m.Lb : 1) * (Ep + 1));
+  b.add(L.off, L.bytes, MOE_WS_HIST, 4 * static_cast<size_t>(m.units) * Ep);
+  b.add(L.off, L.bytes, MOE_WS_BASE, 4 * static_cast<size_t>(m.units) * Ep);
+  b.add(L.off, L.bytes, MOE_WS_LOGITS, 4 * T * E);
+  b.add(L.off, L.bytes, MOE_WS_SSEL, 4 * T * k);
+  b.add(L.off, L.bytes, MOE_WS_XQ, Tp * d);
+  b.add(L.off, L.bytes, MOE_WS_XQ_SF, Tp * d / 32);
+  b.add(L.off, L.bytes, MOE_WS_RING_X, E * C * d);
+  b.add(L.off, L.bytes, MOE_WS_RING_X_SF, E * C * d / 32);
+  b.add(L.off, L.bytes, MOE_WS_GU, 2 * R * 2 * I);
+  b.add(L.off, L.bytes, MOE_WS_HQ, R * I);
+  b.add(L.off, L.bytes, MOE_WS_HQ_SF, R * I / 32);
+  b.add(L.off, L.bytes, MOE_WS_HTOK, I * R);
+  b.add(L.off, L.bytes, MOE_WS_HTOK_SF, I * R / 32);
+  b.add(L.off, L.bytes, MOE_WS_O, 2 * Ap * d);
+  b.add(L.off, L.bytes, MOE_WS_DW, 4 * T * k);
+  b.add(L.off, L.bytes, MOE_WS_DL, 4 * T * k);
+  b.add(L.off, L.bytes, MOE_WS_RING_DO, E * C * d);
+  b.add(L.off, L.bytes, MOE_WS_RING_DO_SF, E * C * d / 32);
+  b.add(L.off, L.bytes, MOE_WS_DOS, Tp * d);
+  b.add(L.off, L.bytes, MOE_WS_DOS_SF, Tp * d / 32);
+  b.add(L.off, L.bytes, MOE_WS_DOTOK, d * R);
+  b.add(L.off, L.bytes, MOE_WS_DOTOK_SF, d * R / 32);
+  b.add(L.off, L.bytes, MOE_WS_DGU, R * 2 * I);
+  b.add(L.off, L.bytes, MOE_WS_DGU_SF, R * 2 * I / 32);
+  b.add(L.off, L.bytes, MOE_WS_DGUTOK, 2 * I * R);
+  b.add(L.off, L.bytes, MOE_WS_DGUTOK_SF, 2 * I * R / 32);
+  b.add(L.off, L.bytes, MOE_WS_XTOK, d * R);
+  b.add(L.off, L.bytes, MOE_WS_XTOK_SF, d * R / 32);
+  b.add(L.off, L.bytes, MOE_WS_DXE, 2 * Ap * d);
+  b.add(L.off, L.bytes, MOE_WS_DWR_PART, 4 * (R / 32) * d);
+  L.total = b.cur;
+  return L;
+}
+
+WLayout make_wlayout(const moe_config_t* c) {
+  WLayout W{};
+  const Dims m = make_dims(c);
+  Builder b;
+  const size_t Ep = m.Ep, d = m.d, I = m.I;
+  b.add(W.off, W.bytes, MOE_WQ_W1F, Ep * 2 * I * d);
+  b.add(W.off, W.bytes, MOE_WQ_W1F_SF, Ep * 2 * I * d / 32);
+  b.add(W.off, W.bytes, MOE_WQ_W2F, Ep * d * I);
+  b.add(W.off, W.bytes, MOE_WQ_W2F_SF, Ep * d * I / 32);
+  b.add(W.off, W.bytes, MOE_WQ_W2B, Ep * I * d);
+  b.add(W.off, W.bytes, MOE_WQ_W2B_SF, Ep * I * d / 32);
+  b.add(W.off, W.bytes, MOE_WQ_W1B, Ep * d * 2 * I);
+  b.add(W.off, W.bytes, MOE_WQ_W1B_SF, Ep * d * 2 * I / 32);
+  W.total = b.cur;
+  return W;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_workspace_size(const moe_config_t* cfg, size_t* bytes) {
+  if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+  if (int r = validate(cfg)) return r;
+  *bytes = make_layout(cfg).total;
+  return MOE_OK;
+}
+
+int moe_weights_size(const moe_config_t* cfg, size_t* bytes) {
+  if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+  if (int r = validate(cfg)) return r;
+  *bytes = make_wlayout(cfg).total;
+  return MOE_OK;
+}
+
+int moe_ws_view(const moe_config_t* cfg, void* ws, int which, void** ptr, size_t* bytes) {
+  if (int r = validate(cfg)) return r;
+  if (which < 0 || which >= MOE_WS_COUNT || ptr == nullptr) return MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(cfg);
+  *ptr = static_cast<char*>(ws) + L.off[which];
+  if (bytes) *bytes = L.bytes[which];
+  return MOE_OK;
+}
+
+int moe_wq_view(const moe_config_t* cfg, void* wq, int which, void** ptr, size_t* bytes) {
+  if (int r = validate(cfg)) return r;
+  if (which < 0 || which >= MOE_WQ_COUNT || ptr == nullptr) return MOE_ERR_INVALID_ARG;
+  const WLayout W = make_wlayout(cfg);
+  *ptr = static_cast<char*>(wq) + W.off[which];
+  if (bytes) *bytes = W.bytes[which];
+  return MOE_OK;
+}
+
+int moe_quantize_mxfp8(const void* src, int rows, int K, int axis, void* codes, void* scales, moe_stream_t stream) {
+  if (src == nullptr || codes == nullptr || scales == nullptr || rows < 0 || K <= 0 || K % 32)
+    return MOE_ERR_INVALID_ARG;
+  if (axis != 0 && axis != 1) return MOE_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(src) % 16 || reinterpret_cast<uintptr_t>(codes) % 16) return MOE_ERR_INVALID_ARG;
+  if (!arch_ok()) return MOE_ERR_UNSUPPORTED_ARCH;
+  if (rows == 0) return MOE_OK;
+  if (axis == 1) {
+    launch_quant_rows(src, rows, K, K, static_cast<uint8_t*>(codes), static_cast<uint8_t*>(scales), false, 0, S(stream));
+  } else {
+    launch_quant_cols(src, rows, K, K, round_up(rows, 32), static_cast<uint8_t*>(codes), static_cast<uint8_t*>(scales),
+                      false, 1, S(stream));
+  }
+  return launch_status();
+}
+
+int moe_quantize_weights(const moe_config_t* cfg, const void* w_gu, const void* w_d, const void* ws_gu,
+                         const void* ws_d, void* wq, moe_stream_t stream) {
+  if (int r = validate(cfg)) return r;
+  if (w_gu == nullptr || w_d == nullptr || wq == nullptr) return MOE_ERR_INVALID_ARG;
+  if (cfg->n_shared > 0 && (ws_gu == nullptr || ws_d == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (!arch_ok()) return MOE_ERR_UNSUPPORTED_ARCH;
+  const Dims m = make_dims(cfg);
+  const WLayout W = make_wlayout(cfg);
+  cudaStream_t s = S(stream);
+  const int64_t d = m.d, I = m.I, E = m.E;
+  uint8_t* w1f = wq_ptr<uint8_t>(W, wq, MOE_WQ_W1F);
+  uint8_t* w1f_sf = wq_ptr<uint8_t>(W, wq, MOE_WQ_W1F_SF);
+  uint8_t* w2f = wq_ptr<uint8_t>(W, wq, MOE_WQ_W2F);
+  uint8_t* w2f_sf = wq_ptr<uint8_t>(W, wq, MOE_WQ_W2F_SF);
+  uint8_t* w2b = wq_ptr<uint8_t>(W, wq, MOE_WQ_W2B);
+  uint8_t* w2b_sf = wq_ptr<uint8_t>(W, wq, MOE_WQ_W2B_SF);
+  uint8_t* w1b = wq_ptr<uint8_t>(W, wq, MOE_WQ_W1B);
+  uint8_t* w1b_sf = wq_ptr<uint8_t>(W, wq, MOE_WQ_W1B_SF);
+  for (int part = 0; part < 2; ++part) {
+    const void* gu = part == 0 ? w_gu : ws_gu;
+    const void* dd = part == 0 ? w_d : ws_d;
+    const int64_t n = part == 0 ? E : m.S;
+    const int64_t e0 = part == 0 ? 0 : E;
+    if (n == 0) continue;
+    // GEMM1 forward operand: [2I][d] along d, gate/up rows interleaved by 128.
+    launch_quant_rows(gu, n * 2 * I, static_cast<int>(d), d, w1f + e0 * 2 * I * d, w1f_sf + e0 * 2 * I * d / 32, true,
+                      static_cast<int>(I), s);
+    // GEMM2 forward operand: [d][I] along I.
+    launch_quant_rows(dd, n * d, static_cast<int>(I), I, w2f + e0 * d * I, w2f_sf + e0 * d * I / 32, true, 0, s);
+    // GEMM2 dgrad operand: W_d^T = [I][d] along d.
+    launch_quant_cols(dd, d, static_cast<int>(I), I, d, w2b + e0 * I * d, w2b_sf + e0 * I * d / 32, true,
+                      static_cast<int>(n), s);
+    // GEMM1 dgrad operand: W_gu^T = [d][2I] along 2I.
+    launch_quant_cols(gu, 2 * I, static_cast<int>(d), d, 2 * I, w1b + e0 * d * 2 * I, w1b_sf + e0 * d * 2 * I / 32,
+                      true, static_cast<int>(n), s);
+  }
+  return launch_status();
+}
+
+int moe_route(const moe_config_t* cfg, const void* x, const void* w_router, const float* bias, int32_t* topk_idx,
+              float* topk_w, void* ws, moe_stream_t stream) {
+  if (int r = validate(cfg)) return r;
+  if (!x || !w_router || !bias || !topk_idx || !topk_w || !ws) return MOE_ERR_INVALID_ARG;
+  if (!arch_ok()) return MOE_ERR_UNSUPPORTED_ARCH;
+  const Layout L = make_layout(cfg);
+  const Dims& m = L.m;
+  if (m.T == 0) return MOE_OK;
+  float* logits = ws_ptr<float>(L, ws, MOE_WS_LOGITS);
+  launch_router_logits(m, x, w_router, logits, S(stream));
+  launch_router_topk(m, logits, bias, topk_idx, topk_w, ws_ptr<float>(L, ws, MOE_WS_SSEL), S(stream));
+  return launch_status();
+}
+
+int moe_schedule(const moe_config_t* cfg, const int32_t* topk_idx, void* ws, moe_stream_t stream) {
+  if (int r = validate(cfg)) return r;
+  if (!topk_idx || !ws) return MOE_ERR_INVALID_ARG;
+  if (!arch_ok()) return MOE_ERR_UNSUPPORTED_ARCH;
+  const Layout L = make_layout(cfg);
+  launch_schedule(L.m, topk_idx, L, ws, S(stream));
+  return launch_status();
+}
+
+int moe_forward(const moe_config_t* cfg, const void* x, const void* wq, const float* topk_w, void* y, void* ws,
+                moe_stream_t stream) {
+  if (int r = validate(cfg)) return r;
+  if (!x || !wq || !topk_w || !y || !ws) return MOE_ERR_INVALID_ARG;
+  if (!arch_ok()) return MOE_ERR_UNSUPPORTED_ARCH;
+  const Layout L = make_layout(cfg);
+  const WLayout W = make_wlayout(cfg);
+  const Dims& m = L.m;
+  if (m.T == 0) return MOE_OK;
+  cudaStream_t s = S(stream);
+  void* wqm = const_cast<void*>(wq);
+  uint8_t* xq = ws_ptr<uint8_t>(L, ws, MOE_WS_XQ);
+  uint8_t* xq_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_XQ_SF);
+  if (m.Tpad > m.T) {
+    cudaMemsetAsync(xq + m.T * m.d, 0, (m.Tpad - m.T) * m.d, s);
+    cudaMemsetAsync(xq_sf + (m.T / 128) * 128 * (m.d / 32), 0, (m.Tpad - m.T / 128 * 128) * (m.d / 32), s);
+  }
+  launch_quant_rows(x, m.T, m.d, m.d, xq, xq_sf, true, 0, s);
+  int* counts = ws_ptr<int>(L, ws, MOE_WS_COUNTS);
+  int* poff = ws_ptr<int>(L, ws, MOE_WS_POFF);
+  int* lap_tiles = ws_ptr<int>(L, ws, MOE_WS_LAPTILES);
+  int* row_src = ws_ptr<int>(L, ws, MOE_WS_ROWSRC);
+  int* status = ws_ptr<int>(L, ws, MOE_WS_STATUS);
+
+  GemmOperands op1{};
+  op1.a = ws_ptr<uint8_t>(L, ws, MOE_WS_RING_X);
+  op1.a_rows = static_cast<int64_t>(m.E) * m.C;
+  op1.a_cols = m.d;
+  op1.a_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_RING_X_SF);
+  op1.a2 = xq;
+  op1.a2_rows = m.Tpad;
+  op1.a2_sf = xq_sf;
+  op1.b = wq_ptr<uint8_t>(W, wqm, MOE_WQ_W1F);
+  op1.b_rows = static_cast<int64_t>(m.Ep) * 2 * m.I;
+  op1.b_cols = m.d;
+  op1.b_sf = wq_ptr<uint8_t>(W, wqm, MOE_WQ_W1F_SF);
+  GemmEpilogue ep1{};
+  ep1.gu = ws_ptr<void>(L, ws, MOE_WS_GU);
+  ep1.q_rows = ws_ptr<uint8_t>(L, ws, MOE_WS_HQ);
+  ep1.q_rows_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_HQ_SF);
+  ep1.q_rows_ktiles = m.I / 128;
+  ep1.q_tok = ws_ptr<uint8_t>(L, ws, MOE_WS_HTOK);
+  ep1.q_tok_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_HTOK_SF);
+  ep1.q_tok_pitch = m.Rmax;
+  for (int lap = 0; lap < m.Lb; ++lap) {
+    launch_permute_lap(m, lap, L, ws, s);
+    if (int r = gemm_dispatch(kSwigluFwd, m, lap, 2 * m.I, m.d, 0, op1, ep1, counts, poff, lap_tiles, row_src, status, s))
+      return r;
+  }
+  GemmOperands op2{};
+  op2.a = ws_ptr<uint8_t>(L, ws, MOE_WS_HQ);
+  op2.a_rows = m.Rmax;
+  op2.a_cols = m.I;
+  op2.a_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_HQ_SF);
+  op2.b = wq_ptr<uint8_t>(W, wqm, MOE_WQ_W2F);
+  op2.b_rows = static_cast<int64_t>(m.Ep) * m.d;
+  op2.b_cols = m.I;
+  op2.b_sf = wq_ptr<uint8_t>(W, wqm, MOE_WQ_W2F_SF);
+  GemmEpilogue ep2{};
+  ep2.out = ws_ptr<void>(L, ws, MOE_WS_O);
+  ep2.ldo = m.d;
+  if (int r = gemm_dispatch(kPush, m, 0, m.d, m.I, 0, op2, ep2, counts, poff, lap_tiles, row_src, status, s)) return r;
+  launch_combine(m, topk_w, L, ws, y, s);
+  return launch_status();
+}
+
+int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, const int32_t* topk_idx,
+                 const float* topk_w, const void* dy, const void* wq, void* dx, void* dw_router, void* dw_gu,
+                 void* dw_d, void* dws_gu, void* dws_d, void* ws, moe_stream_t stream) {
+  if (int r = validate(cfg)) return r;
+  if (!x || !w_router || !topk_idx || !topk_w || !dy || !wq || !dx || !dw_router || !dw_gu || !dw_d || !ws)
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->n_shared > 0 && (!dws_gu || !dws_d)) return MOE_ERR_INVALID_ARG;
+  if (!arch_ok()) return MOE_ERR_UNSUPPORTED_ARCH;
+  const Layout L = make_layout(cfg);
+  const WLayout W = make_wlayout(cfg);
+  const Dims& m = L.m;
+  cudaStream_t s = S(stream);
+  void* wqm = const_cast<void*>(wq);
+  int* counts = ws_ptr<int>(L, ws, MOE_WS_COUNTS);
+  int* poff = ws_ptr<int>(L, ws, MOE_WS_POFF);
+  int* lap_tiles = ws_ptr<int>(L, ws, MOE_WS_LAPTILES);
+  int* row_src = ws_ptr<int>(L, ws, MOE_WS_ROWSRC);
+  int* status = ws_ptr<int>(L, ws, MOE_WS_STATUS);
+  if (m.T == 0) {
+    // No tokens: every gradient is zero.
+    cudaMemsetAsync(dw_router, 0, static_cast<size_t>(m.E) * m.d * 2, s);
+    cudaMemsetAsync(dw_gu, 0, static_cast<size_t>(m.E) * 2 * m.I * m.d * 2, s);
+    cudaMemsetAsync(dw_d, 0, static_cast<size_t>(m.E) * m.d * m.I * 2, s);
+    if (m.S) {
+      cudaMemsetAsync(dws_gu, 0, static_cast<size_t>(m.S) * 2 * m.I * m.d * 2, s);
+      cudaMemsetAsync(dws_d, 0, static_cast<size_t>(m.S) * m.d * m.I * 2, s);
+    }
+    return launch_status();
+  }
+  // Reverse-combine: gate gradients, router logit gradients.
+  launch_rev_combine_dw(m, dy, topk_w, L, ws, s);
+  // Shared-expert dgrad input MX(dy) along d (token order; rows past T zero).
+  uint8_t* dos = ws_ptr<uint8_t>(L, ws, MOE_WS_DOS);
+  uint8_t* dos_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_DOS_SF);
+  if (m.S) {
+    if (m.Tpad > m.T) {
+      cudaMemsetAsync(dos + m.T * m.d, 0, (m.Tpad - m.T) * m.d, s);
+      cudaMemsetAsync(dos_sf + (m.T / 128) * 128 * (m.d / 32), 0, (m.Tpad - m.T / 128 * 128) * (m.d / 32), s);
+    }
+    launch_quant_rows(dy, m.T, m.d, m.d, dos, dos_sf, true, 0, s);
+  }
+  // Token-axis operands of the weight gradients (and router dW partial sums).
+  launch_tok_gather(m, x, false, topk_w, true, L, ws, ws_ptr<uint8_t>(L, ws, MOE_WS_XTOK),
+                    ws_ptr<uint8_t>(L, ws, MOE_WS_XTOK_SF), s);
+  launch_tok_gather(m, dy, true, topk_w, false, L, ws, ws_ptr<uint8_t>(L, ws, MOE_WS_DOTOK),
+                    ws_ptr<uint8_t>(L, ws, MOE_WS_DOTOK_SF), s);
+  // dgrad of GEMM2 + SwiGLU backward, lap by lap through the dO ring.
+  GemmOperands opb2{};
+  opb2.a = ws_ptr<uint8_t>(L, ws, MOE_WS_RING_DO);
+  opb2.a_rows = static_cast<int64_t>(m.E) * m.C;
+  opb2.a_cols = m.d;
+  opb2.a_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_RING_DO_SF);
+  opb2.a2 = dos;
+  opb2.a2_rows = m.Tpad;
+  opb2.a2_sf = dos_sf;
+  opb2.b = wq_ptr<uint8_t>(W, wqm, MOE_WQ_W2B);
+  opb2.b_rows = static_cast<int64_t>(m.Ep) * m.I;
+  opb2.b_cols = m.d;
+  opb2.b_sf = wq_ptr<uint8_t>(W, wqm, MOE_WQ_W2B_SF);
+  GemmEpilogue epb2{};
+  epb2.gu = ws_ptr<void>(L, ws, MOE_WS_GU);
+  epb2.q_rows = ws_ptr<uint8_t>(L, ws, MOE_WS_DGU);
+  epb2.q_rows_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_DGU_SF);
+  epb2.q_rows_ktiles = 2 * m.I / 128;
+  epb2.q_tok = ws_ptr<uint8_t>(L, ws, MOE_WS_DGUTOK);
+  epb2.q_tok_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_DGUTOK_SF);
+  epb2.q_tok_pitch = m.Rmax;
+  for (int lap = 0; lap < m.Lb; ++lap) {
+    launch_rev_combine_lap(m, lap, dy, topk_w, L, ws, s);
+    if (int r = gemm_dispatch(kSwigluBwd, m, lap, m.I, m.d, 0, opb2, epb2, counts, poff, lap_tiles, row_src, status, s))
+      return r;
+  }
+  // dgrad of GEMM1: DX rows pushed to their assignment.
+  GemmOperands opb4{};
+  opb4.a = ws_ptr<uint8_t>(L, ws, MOE_WS_DGU);
+  opb4.a_rows = m.Rmax;
+  opb4.a_cols = 2 * m.I;
+  opb4.a_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_DGU_SF);
+  opb4.b = wq_ptr<uint8_t>(W, wqm, MOE_WQ_W1B);
+  opb4.b_rows = static_cast<int64_t>(m.Ep) * m.d;
+  opb4.b_cols = 2 * m.I;
+  opb4.b_sf = wq_ptr<uint8_t>(W, wqm, MOE_WQ_W1B_SF);
+  GemmEpilogue epb4{};
+  epb4.out = ws_ptr<void>(L, ws, MOE_WS_DXE);
+  epb4.ldo = m.d;
+  if (int r = gemm_dispatch(kPush, m, 0, m.d, 2 * m.I, 0, opb4, epb4, counts, poff, lap_tiles, row_src, status, s))
+    return r;
+  // Weight gradients: K = the expert's ranks (token axis), all laps at once.
+  GemmOperands opw{};
+  opw.a = ws_ptr<uint8_t>(L, ws, MOE_WS_DOTOK);
+  opw.a_rows = m.d;
+  opw.a_cols = static_cast<int>(m.Rmax);
+  opw.a_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_DOTOK_SF);
+  opw.b = ws_ptr<uint8_t>(L, ws, MOE_WS_HTOK);
+  opw.b_rows = m.I;
+  opw.b_cols = static_cast<int>(m.Rmax);
+  opw.b_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_HTOK_SF);
+  GemmEpilogue epw{};
+  epw.out = dw_d;
+  epw.out2 = dws_d;
+  epw.ldo = m.I;
+  if (int r = gemm_dispatch(kWgrad, m, 0, m.I, 0, m.d, opw, epw, counts, poff, lap_tiles, row_src, status, s)) return r;
+  opw.a = ws_ptr<uint8_t>(L, ws, MOE_WS_DGUTOK);
+  opw.a_rows = 2 * m.I;
+  opw.a_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_DGUTOK_SF);
+  opw.b = ws_ptr<uint8_t>(L, ws, MOE_WS_XTOK);
+  opw.b_rows = m.d;
+  opw.b_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_XTOK_SF);
+  epw.out = dw_gu;
+  epw.out2 = dws_gu;
+  epw.ldo = m.d;
+  if (int r = gemm_dispatch(kWgrad, m, 0, m.d, 0, 2 * m.I, opw, epw, counts, poff, lap_tiles, row_src, status, s))
+    return r;
+  // Reverse-dispatch (+ router input gradient) and the router weight gradient.
+  launch_reverse_dispatch(m, topk_idx, w_router, L, ws, dx, s);
+  launch_router_dwr(m, L, ws, dw_router, s);
+  return launch_status();
+}
+
+int moe_status(const moe_config_t* cfg, void* ws, int* code, int* site, int clear, moe_stream_t stream) {
+  if (int r = validate(cfg)) return r;
+  if (!ws || !code || !site) return MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(cfg);
+  int h[2] = {0, 0};
+  int* st = ws_ptr<int>(L, ws, MOE_WS_STATUS);
+  if (cudaMemcpyAsync(h, st, sizeof(h), cudaMemcpyDeviceToHost, S(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(S(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  *code = h[0];
+  *site = h[1];
+  if (clear && cudaMemsetAsync(st, 0, 16, S(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+}  // extern "C"

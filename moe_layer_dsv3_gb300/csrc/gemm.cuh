@@ -1,0 +1,455 @@
+// Persistent, warp-specialised grouped GEMM on the 5th-generation tensor cores.
+//
+//   D[128 x BN] (TMEM, fp32) = sum_k A[128 x k] . B[BN x k]^T
+//
+// A and B are K-major tiles staged by TMA (128-byte swizzle, 128 bytes of K
+// per stage: 128 E4M3 values or 64 bf16 values). For MXFP8 the E8M0 scales
+// of each stage arrive by bulk copy in the tiled atom layout and are moved
+// into TMEM with tcgen05.cp; tcgen05.mma.kind::mxf8f6f4.block_scale applies
+// them per 32-element block. The bf16 path (router logits) uses
+// tcgen05.mma.kind::f16.
+//
+// Roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer and TMEM
+// owner, warps 2-5 = epilogue (each reads the TMEM lane quarter warp%4).
+// Work list: "tiles" of 128 rows x BN columns, decoded from the device-side
+// schedule, so the host never learns per-expert counts.
+#pragma once
+#include <cuda_bf16.h>
+
+#include "moe_internal.h"
+#include "mx.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+
+constexpr int kRouterMode = 5;   // bf16 x bf16 router logits
+
+struct GemmParams {
+  int N;                 // B rows per expert (output columns per expert)
+  int K;                 // reduction length (elements) for fixed-K modes
+  int a_ktiles, b_ktiles;// 128-wide K tiles per row of the stored A / B operand (scale atoms)
+  const uint8_t* a_sf; const uint8_t* a2_sf; const uint8_t* b_sf;
+  const int* counts; const int* poff; const int* lap_tiles; const int* row_src;
+  int E, Ep, C, lap, T, k;
+  int M;                 // plain / router / wgrad output rows per expert
+  int static_tiles;      // tile count when it does not depend on the schedule
+  void* out; void* out2; int ldo;
+  uint8_t* q_rows; uint8_t* q_rows_sf; int q_rows_ktiles;
+  uint8_t* q_tok; uint8_t* q_tok_sf; int64_t q_tok_pitch;
+  __nv_bfloat16* gu; int I;
+  int* status;
+};
+
+template <int BN, int MODE>
+struct GemmCfg {
+  static constexpr bool kBf16 = MODE == kRouterMode;
+  static constexpr int kStages = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);
+  static constexpr int kABytes = 128 * 128;
+  static constexpr int kBBytes = BN * 128;
+  static constexpr int kSfaBytes = kBf16 ? 0 : 512;
+  static constexpr int kSfbBytes = kBf16 ? 0 : (BN / 128) * 512;
+  static constexpr int kTx = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+  static constexpr int kStageBytes = ((kTx + 1023) / 1024) * 1024;
+  static constexpr int kSfCols = kBf16 ? 0 : 4 + (BN / 128) * 4;   // TMEM columns of scales per stage
+  static constexpr int kSfCol0 = 256;
+  static constexpr int kKElems = kBf16 ? 64 : 128;                  // K elements per stage
+  static constexpr int kBarBytes = 256;
+  static constexpr int kScratchBytes = 4 * 32 * 33 * 4;
+  static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes + kScratchBytes;
+  static_assert(kSmem <= 232448, "shared memory budget");
+  static_assert(kSfCol0 + kStages * kSfCols <= 512, "TMEM budget");
+  static_assert(BN <= 256, "accumulator budget");
+};
+
+struct TileInfo {
+  int e;
+  int64_t a_row;     // A row of the tile's first row
+  int64_t b_row;     // B row of the tile's first column
+  int k0;            // first K stage
+  int nk;            // number of K stages
+  int64_t prow0;     // padded rank row of the tile's first row (grouped-M modes)
+  int valid;         // rows of the tile that hold real assignments
+  int n0;            // first output column
+  int m0;            // first output row (wgrad / plain / router)
+  bool use_a2;
+};
+
+// Largest e in [0, n) with v[e] <= x < v[e+1] (v nondecreasing, v[0] <= x < v[n]).
+__device__ __forceinline__ int seg_search(const int* v, int n, int64_t x) {
+  int lo = 0, hi = n;   // invariant v[lo] <= x < v[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (v[mid] <= x) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+template <int BN, int MODE>
+__device__ __forceinline__ int gemm_num_tiles(const GemmParams& p) {
+  if constexpr (MODE == kSwigluFwd || MODE == kSwigluBwd) {
+    return p.lap_tiles[p.lap * (p.Ep + 1) + p.Ep] * (p.N / BN);
+  } else if constexpr (MODE == kPush) {
+    return (p.poff[p.Ep] / 128) * (p.N / BN);
+  } else {
+    return p.static_tiles;
+  }
+}
+
+template <int BN, int MODE>
+__device__ __forceinline__ bool gemm_decode(const GemmParams& p, int tile, TileInfo& t) {
+  using Cf = GemmCfg<BN, MODE>;
+  if constexpr (MODE == kSwigluFwd || MODE == kSwigluBwd) {
+    const int nt = p.N / BN;
+    const int g = tile / nt, n = tile - (tile / nt) * nt;
+    const int* lt = p.lap_tiles + p.lap * (p.Ep + 1);
+    const int e = seg_search(lt, p.Ep, g);
+    const int mt = g - lt[e];
+    const bool shared = e >= p.E;
+    const int64_t rank0 = shared ? static_cast<int64_t>(mt) * 128 : static_cast<int64_t>(p.lap) * p.C + mt * 128;
+    const int cnt = p.counts[e];
+    t.e = e;
+    t.use_a2 = shared;
+    t.a_row = shared ? static_cast<int64_t>(mt) * 128 : static_cast<int64_t>(e) * p.C + mt * 128;
+    t.b_row = static_cast<int64_t>(e) * p.N + static_cast<int64_t>(n) * BN;
+    t.k0 = 0;
+    t.nk = p.K / Cf::kKElems;
+    t.prow0 = p.poff[e] + rank0;
+    const int64_t v = cnt - rank0;
+    t.valid = v < 0 ? 0 : (v > 128 ? 128 : static_cast<int>(v));
+    t.n0 = n * BN;
+    t.m0 = 0;
+    return t.prow0 + 128 <= p.poff[e + 1] && t.valid > 0;
+  } else if constexpr (MODE == kPush) {
+    const int nt = p.N / BN;
+    const int g = tile / nt, n = tile - (tile / nt) * nt;
+    const int64_t prow0 = static_cast<int64_t>(g) * 128;
+    const int e = seg_search(p.poff, p.Ep, prow0);
+    t.e = e;
+    t.use_a2 = false;
+    t.a_row = prow0;
+    t.b_row = static_cast<int64_t>(e) * p.N + static_cast<int64_t>(n) * BN;
+    t.k0 = 0;
+    t.nk = p.K / Cf::kKElems;
+    t.prow0 = prow0;
+    const int64_t v = p.counts[e] - (prow0 - p.poff[e]);
+    t.valid = v < 0 ? 0 : (v > 128 ? 128 : static_cast<int>(v));
+    t.n0 = n * BN;
+    t.m0 = 0;
+    return true;
+  } else if constexpr (MODE == kWgrad) {
+    const int nt = p.N / BN, mt = p.M / 128;
+    const int per = nt * mt;
+    const int e = tile / per;
+    const int rem = tile - e * per;
+    const int mi = rem / nt, n = rem - (rem / nt) * nt;
+    t.e = e;
+    t.use_a2 = false;
+    t.a_row = static_cast<int64_t>(mi) * 128;
+    t.b_row = static_cast<int64_t>(n) * BN;
+    t.k0 = p.poff[e] / 128;
+    t.nk = (p.poff[e + 1] - p.poff[e]) / 128;
+    t.prow0 = 0;
+    t.valid = 128;
+    t.n0 = n * BN;
+    t.m0 = mi * 128;
+    return true;
+  } else {   // plain, router
+    const int nt = (p.N + BN - 1) / BN;
+    const int mi = tile / nt, n = tile - (tile / nt) * nt;
+    t.e = 0;
+    t.use_a2 = false;
+    t.a_row = static_cast<int64_t>(mi) * 128;
+    t.b_row = static_cast<int64_t>(n) * BN;
+    t.k0 = 0;
+    t.nk = p.K / Cf::kKElems;
+    t.prow0 = 0;
+    t.valid = 128;
+    t.n0 = n * BN;
+    t.m0 = mi * 128;
+    return true;
+  }
+}
+
+// Row-wise MX of 32 values: codes to dst (16-byte aligned), scale byte to sf.
+__device__ __forceinline__ void emit_rowq(const float* v, uint8_t* dst, uint8_t* sf_byte) {
+  const int b = mx_scale_byte(amax32(v));
+  uint32_t w[8];
+  mx_pack32(v, mx_inv_scale(b), w);
+  store32(dst, w);
+  *sf_byte = static_cast<uint8_t>(b);
+}
+
+// Token-axis MX of a warp's 32x32 block (lane = row): transposes through
+// shared memory so that lane j owns column j, then writes 32 codes of that
+// column (32 consecutive ranks) and its scale.
+__device__ __forceinline__ void emit_tokq(const float* v, float* scr, int lane, uint8_t* q_tok, uint8_t* q_tok_sf,
+                                          int64_t pitch, int64_t col0, int64_t prow_base) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) scr[lane * 33 + j] = v[j];
+  __syncwarp();
+  float c[32];
+#pragma unroll
+  for (int r = 0; r < 32; ++r) c[r] = scr[r * 33 + lane];
+  __syncwarp();
+  const int b = mx_scale_byte(amax32(c));
+  uint32_t w[8];
+  mx_pack32(c, mx_inv_scale(b), w);
+  const int64_t col = col0 + lane;
+  store32(q_tok + col * pitch + prow_base, w);
+  q_tok_sf[sf_off(col, prow_base >> 5, pitch >> 7)] = static_cast<uint8_t>(b);
+}
+
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v) {
+  uint4* p = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    p[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                      pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+}
+
+__device__ __forceinline__ void load_bf16x32_g(const __nv_bfloat16* src, float* v) { load_bf16x32(src, v); }
+
+template <int BN, int MODE>
+__device__ __forceinline__ void gemm_epilogue_tile(const GemmParams& p, const TileInfo& t, uint32_t tacc, int q,
+                                                   int lane, float* scr) {
+  const int row = q * 32 + lane;
+  const bool have_acc = t.nk > 0;
+  const bool valid = row < t.valid;
+  if constexpr (MODE == kSwigluFwd) {
+    const int64_t prow = t.prow0 + row;
+    const int I = p.I;
+    const int i_base = t.n0 / 2;                     // interleaved: BN/2 gate + BN/2 up columns
+#pragma unroll 1
+    for (int c = 0; c < BN / 64; ++c) {
+      float g[32], u[32], h[32];
+      tmem_ld32(tacc + c * 32, g);
+      tmem_ld32(tacc + BN / 2 + c * 32, u);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (!valid) { g[j] = 0.0f; u[j] = 0.0f; }
+        h[j] = g[j] / (1.0f + __expf(-g[j])) * u[j];
+      }
+      const int64_t icol = i_base + c * 32;
+      store_bf16x32(p.gu + prow * (2 * I) + icol, g);
+      store_bf16x32(p.gu + prow * (2 * I) + I + icol, u);
+      emit_rowq(h, p.q_rows + prow * I + icol, p.q_rows_sf + sf_off(prow, icol >> 5, p.q_rows_ktiles));
+      emit_tokq(h, scr, lane, p.q_tok, p.q_tok_sf, p.q_tok_pitch, icol, t.prow0 + q * 32);
+    }
+  } else if constexpr (MODE == kSwigluBwd) {
+    const int64_t prow = t.prow0 + row;
+    const int I = p.I;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      float dh[32], g[32], u[32], dg[32], du[32];
+      tmem_ld32(tacc + c * 32, dh);
+      const int64_t icol = t.n0 + c * 32;
+      if (valid) {
+        load_bf16x32_g(p.gu + prow * (2 * I) + icol, g);
+        load_bf16x32_g(p.gu + prow * (2 * I) + I + icol, u);
+      }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (valid) {
+          const float sg = 1.0f / (1.0f + __expf(-g[j]));
+          dg[j] = dh[j] * u[j] * sg * (1.0f + g[j] * (1.0f - sg));
+          du[j] = dh[j] * (g[j] * sg);
+        } else {
+          dg[j] = 0.0f;
+          du[j] = 0.0f;
+        }
+      }
+      const int ktl = p.q_rows_ktiles;
+      emit_rowq(dg, p.q_rows + prow * (2 * I) + icol, p.q_rows_sf + sf_off(prow, icol >> 5, ktl));
+      emit_rowq(du, p.q_rows + prow * (2 * I) + I + icol, p.q_rows_sf + sf_off(prow, (I + icol) >> 5, ktl));
+      emit_tokq(dg, scr, lane, p.q_tok, p.q_tok_sf, p.q_tok_pitch, icol, t.prow0 + q * 32);
+      emit_tokq(du, scr, lane, p.q_tok, p.q_tok_sf, p.q_tok_pitch, I + icol, t.prow0 + q * 32);
+    }
+  } else if constexpr (MODE == kPush) {
+    const int64_t prow = t.prow0 + row;
+    const int a = valid ? p.row_src[prow] : -1;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      float v[32];
+      tmem_ld32(tacc + c * 32, v);
+      if (a >= 0) store_bf16x32(out + static_cast<int64_t>(a) * p.ldo + t.n0 + c * 32, v);
+    }
+  } else if constexpr (MODE == kWgrad) {
+    __nv_bfloat16* out = t.e < p.E ? static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(t.e) * p.M * p.ldo
+                                   : static_cast<__nv_bfloat16*>(p.out2) +
+                                         static_cast<int64_t>(t.e - p.E) * p.M * p.ldo;
+    const int64_t orow = t.m0 + row;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      float v[32];
+      if (have_acc) {
+        tmem_ld32(tacc + c * 32, v);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+      }
+      store_bf16x32(out + orow * p.ldo + t.n0 + c * 32, v);
+    }
+  } else {   // plain (fp32 out, M x N) and router logits (fp32 [M][N] for columns < N)
+    float* out = static_cast<float*>(p.out);
+    const int64_t orow = t.m0 + row;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      float v[32];
+      tmem_ld32(tacc + c * 32, v);
+      if (orow < p.M) {
+        const int col0 = t.n0 + c * 32;
+        if (col0 + 32 <= p.N && (p.ldo % 4) == 0) {
+          float4* dst = reinterpret_cast<float4*>(out + orow * p.ldo + col0);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        } else {
+          for (int j = 0; j < 32; ++j)
+            if (col0 + j < p.N) out[orow * p.ldo + col0 + j] = v[j];
+        }
+      }
+    }
+  }
+}
+
+template <int BN, int MODE>
+__global__ void __launch_bounds__(192, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_a2,
+                const __grid_constant__ CUtensorMap tma_b, const __grid_constant__ GemmParams p) {
+  using Cf = GemmCfg<BN, MODE>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cf::kStages * Cf::kStageBytes);
+  uint64_t* empty = full + Cf::kStages;
+  uint64_t* accf = empty + Cf::kStages;
+  uint64_t* acce = accf + 1;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(acce + 1);
+  float* scratch = reinterpret_cast<float*>(smem + Cf::kStages * Cf::kStageBytes + Cf::kBarBytes);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Cf::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accf, 1);
+    mbar_init(acce, 128);
+    fence_barrier_init();
+    fence_proxy_async();
+    tma_prefetch(&tma_a);
+    tma_prefetch(&tma_b);
+    if (MODE == kSwigluFwd || MODE == kSwigluBwd) tma_prefetch(&tma_a2);
+  }
+  if (warp == 1) {
+    tmem_alloc(tslot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  const int n_tiles = gemm_num_tiles<BN, MODE>(p);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+        TileInfo t;
+        if (!gemm_decode<BN, MODE>(p, tile, t)) continue;
+        for (int ks = 0; ks < t.nk; ++ks) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, p.status, 10)) { ok = false; break; }
+          uint8_t* sa = smem + stage * Cf::kStageBytes;
+          uint8_t* sb = sa + Cf::kABytes;
+          mbar_arrive_expect_tx(&full[stage], Cf::kTx);
+          const int kt = t.k0 + ks;
+          const int kx = kt * Cf::kKElems;
+          tma_load_2d(sa, t.use_a2 ? &tma_a2 : &tma_a, kx, static_cast<int>(t.a_row), &full[stage]);
+          tma_load_2d(sb, &tma_b, kx, static_cast<int>(t.b_row), &full[stage]);
+          if constexpr (!Cf::kBf16) {
+            uint8_t* ssfa = sb + Cf::kBBytes;
+            const uint8_t* asf = (t.use_a2 ? p.a2_sf : p.a_sf) + ((t.a_row >> 7) * p.a_ktiles + kt) * 512;
+            bulk_load(ssfa, asf, 512, &full[stage]);
+#pragma unroll
+            for (int j = 0; j < BN / 128; ++j)
+              bulk_load(ssfa + 512 + 512 * j, p.b_sf + (((t.b_row >> 7) + j) * p.b_ktiles + kt) * 512, 512,
+                        &full[stage]);
+          }
+          ++issued;
+          if (++stage == Cf::kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // Let every copy this CTA started land before its shared memory is released.
+      const int tail = issued < Cf::kStages ? issued : Cf::kStages;
+      for (int i = 0; i < tail; ++i) {
+        if (--stage < 0) { stage = Cf::kStages - 1; phase ^= 1u; }
+        mbar_wait(&full[stage], phase, p.status, 11);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      constexpr uint32_t idesc0 = Cf::kBf16 ? idesc_bf16(128, BN) : idesc_mxf8(128, BN);
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+        TileInfo t;
+        if (!gemm_decode<BN, MODE>(p, tile, t)) continue;
+        if (!mbar_wait(acce, acc_phase ^ 1u, p.status, 20)) break;
+        tc_fence_after();
+        for (int ks = 0; ks < t.nk; ++ks) {
+          if (!mbar_wait(&full[stage], phase, p.status, 21)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * Cf::kStageBytes);
+          const uint32_t sb = sa + Cf::kABytes;
+          if constexpr (Cf::kBf16) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma_bf16(tmem, desc_kmajor_sw128(sa + kk * 32), desc_kmajor_sw128(sb + kk * 32), idesc0,
+                          (ks | kk) != 0);
+          } else {
+            const uint32_t sfa_t = tmem + Cf::kSfCol0 + stage * Cf::kSfCols;
+            const uint32_t sfb_t = sfa_t + 4;
+            const uint32_t ssf = sb + Cf::kBBytes;
+            tc_cp_sf(sfa_t, desc_sf_chunk(ssf));
+#pragma unroll
+            for (int j = 0; j < BN / 128; ++j) tc_cp_sf(sfb_t + 4 * j, desc_sf_chunk(ssf + 512 + 512 * j));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma_mxf8(tmem, desc_kmajor_sw128(sa + kk * 32), desc_kmajor_sw128(sb + kk * 32),
+                          idesc_mxf8_sf(idesc0, kk, kk), sfa_t, sfb_t, (ks | kk) != 0);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == Cf::kStages) { stage = 0; phase ^= 1u; }
+        }
+        tc_commit(accf);
+        acc_phase ^= 1u;
+      }
+    }
+  } else {
+    const int q = warp & 3;
+    float* scr = scratch + (warp - 2) * 32 * 33;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+      TileInfo t;
+      if (!gemm_decode<BN, MODE>(p, tile, t)) continue;
+      if (!mbar_wait(accf, acc_phase, p.status, 30)) break;
+      tc_fence_after();
+      gemm_epilogue_tile<BN, MODE>(p, t, tmem + (static_cast<uint32_t>(q * 32) << 16), q, lane, scr);
+      tc_fence_before();
+      mbar_arrive(acce);
+      acc_phase ^= 1u;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace moe

@@ -1,0 +1,174 @@
+// Host side of the tcgen05 grouped GEMM: tensor maps, grid sizing, dispatch.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "gemm.cuh"
+
+namespace moe {
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// 2-D K-major operand [rows][cols] (elements of `esize` bytes), box 128 bytes x box_rows.
+bool make_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows, bool bf16) {
+  const int esize = bf16 ? 2 : 1;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * esize)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                              const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int BN, int MODE>
+int run(const CUtensorMap& ta, const CUtensorMap& ta2, const CUtensorMap& tb, const GemmParams& p, int grid,
+        cudaStream_t s) {
+  using Cf = GemmCfg<BN, MODE>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(gemm_kernel<BN, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmem);
+  });
+  if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
+  if (grid <= 0) return MOE_OK;
+  gemm_kernel<BN, MODE><<<grid, 192, Cf::kSmem, s>>>(ta, ta2, tb, p);
+  return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  }
+  return n;
+}
+
+// Dispatch one grouped GEMM. Returns an MOE_* code.
+int gemm_dispatch(int mode, const Dims& m, int lap, int N, int K, int M, const GemmOperands& op,
+                  const GemmEpilogue& ep, const int* counts, const int* poff, const int* lap_tiles,
+                  const int* row_src, int* status, cudaStream_t s) {
+  if (!get_encode()) return MOE_ERR_CUDA;
+  const bool bf16 = mode == kRouterMode;
+  int BN;
+  if (mode == kSwigluFwd) BN = 256;
+  else if (mode == kRouterMode) BN = N <= 32 ? 32 : (N % 256 == 0 ? 256 : 128);
+  else BN = (N % 256 == 0) ? 256 : 128;
+  if (!bf16 && N % BN) return MOE_ERR_INVALID_ARG;
+
+  CUtensorMap ta, ta2, tb;
+  if (!make_tmap(&ta, op.a, op.a_rows, op.a_cols, 128, bf16)) return MOE_ERR_CUDA;
+  if (op.a2 != nullptr) {
+    if (!make_tmap(&ta2, op.a2, op.a2_rows, op.a_cols, 128, bf16)) return MOE_ERR_CUDA;
+  } else {
+    ta2 = ta;
+  }
+  if (!make_tmap(&tb, op.b, op.b_rows, op.b_cols, BN, bf16)) return MOE_ERR_CUDA;
+
+  GemmParams p{};
+  p.N = N;
+  p.K = K;
+  p.a_ktiles = op.a_cols / 128;
+  p.b_ktiles = op.b_cols / 128;
+  p.a_sf = op.a_sf;
+  p.a2_sf = op.a2_sf;
+  p.b_sf = op.b_sf;
+  p.counts = counts;
+  p.poff = poff;
+  p.lap_tiles = lap_tiles;
+  p.row_src = row_src;
+  p.E = m.E;
+  p.Ep = m.Ep;
+  p.C = m.C;
+  p.lap = lap;
+  p.T = m.T;
+  p.k = m.k;
+  p.M = M;
+  p.out = ep.out;
+  p.out2 = ep.out2;
+  p.ldo = ep.ldo;
+  p.q_rows = ep.q_rows;
+  p.q_rows_sf = ep.q_rows_sf;
+  p.q_rows_ktiles = ep.q_rows_ktiles;
+  p.q_tok = ep.q_tok;
+  p.q_tok_sf = ep.q_tok_sf;
+  p.q_tok_pitch = ep.q_tok_pitch;
+  p.gu = static_cast<__nv_bfloat16*>(ep.gu);
+  p.I = m.I;
+  p.status = status;
+
+  const int nt = (N + BN - 1) / BN;
+  int64_t upper;
+  if (mode == kSwigluFwd || mode == kSwigluBwd) {
+    upper = (static_cast<int64_t>(m.E) * (m.C / 128) + (lap == 0 ? m.S * (m.Tpad / 128) : 0)) * nt;
+  } else if (mode == kPush) {
+    upper = (m.Rmax / 128) * nt;
+  } else if (mode == kWgrad) {
+    upper = static_cast<int64_t>(m.Ep) * (M / 128) * nt;
+    p.static_tiles = static_cast<int>(upper);
+  } else {
+    upper = ceil_div(M, 128) * nt;
+    p.static_tiles = static_cast<int>(upper);
+  }
+  const int grid = static_cast<int>(upper < num_sms() ? upper : num_sms());
+
+  switch (mode) {
+    case kSwigluFwd: return run<256, kSwigluFwd>(ta, ta2, tb, p, grid, s);
+    case kSwigluBwd:
+      return BN == 256 ? run<256, kSwigluBwd>(ta, ta2, tb, p, grid, s) : run<128, kSwigluBwd>(ta, ta2, tb, p, grid, s);
+    case kPush:
+      return BN == 256 ? run<256, kPush>(ta, ta2, tb, p, grid, s) : run<128, kPush>(ta, ta2, tb, p, grid, s);
+    case kWgrad:
+      return BN == 256 ? run<256, kWgrad>(ta, ta2, tb, p, grid, s) : run<128, kWgrad>(ta, ta2, tb, p, grid, s);
+    case kPlain:
+      return BN == 256 ? run<256, kPlain>(ta, ta2, tb, p, grid, s) : run<128, kPlain>(ta, ta2, tb, p, grid, s);
+    case kRouterMode:
+      if (BN == 32) return run<32, kRouterMode>(ta, ta2, tb, p, grid, s);
+      return BN == 256 ? run<256, kRouterMode>(ta, ta2, tb, p, grid, s) : run<128, kRouterMode>(ta, ta2, tb, p, grid, s);
+    default: return MOE_ERR_INVALID_ARG;
+  }
+}
+
+}  // namespace moe
+
+extern "C" int moe_gemm_mxfp8(int M, int N, int K, const void* a, const void* a_sf, const void* b, const void* b_sf,
+                              float* c, moe_stream_t stream) {
+  if (M <= 0 || N <= 0 || K <= 0 || M % 128 || N % 128 || K % 128 || !a || !a_sf || !b || !b_sf || !c)
+    return MOE_ERR_INVALID_ARG;
+  moe::Dims m{};
+  moe::GemmOperands op{};
+  op.a = static_cast<const uint8_t*>(a);
+  op.a_rows = M;
+  op.a_cols = K;
+  op.a_sf = static_cast<const uint8_t*>(a_sf);
+  op.b = static_cast<const uint8_t*>(b);
+  op.b_rows = N;
+  op.b_cols = K;
+  op.b_sf = static_cast<const uint8_t*>(b_sf);
+  moe::GemmEpilogue ep{};
+  ep.out = c;
+  ep.ldo = N;
+  return moe::gemm_dispatch(moe::kPlain, m, 0, N, K, M, op, ep, nullptr, nullptr, nullptr, nullptr, nullptr,
+                            static_cast<cudaStream_t>(stream));
+}

@@ -1,0 +1,324 @@
+// Data movement on the schedule: dispatch into the ring (permute), combine,
+// reverse-combine and reverse-dispatch, and the router's backward reductions.
+//
+// Write-ups: dispatch pulls tokens into fixed-capacity ring token buffers
+// whose regions are reused once a batch is computed (techlab report, section
+// on the ring buffer); combine pushes expert results back to their token;
+// backward reverse-combine pulls and reverse-dispatch pushes on the same
+// schedule (Cursor blog summary, "method points"). On one GPU the pull is a
+// gather through the schedule and the push a fixed-order per-token sum.
+#include "moe_internal.h"
+#include "mx.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+__device__ __forceinline__ int token_of(int a, int T, int k) {
+  const int A = T * k;
+  return a < A ? a / k : (a - A) % T;
+}
+
+__device__ __forceinline__ int seg_search_dev(const int* v, int n, int64_t x) {
+  int lo = 0, hi = n;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (v[mid] <= x) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// Locate routed tile g of lap L. Returns false when g is past the lap's routed tiles.
+struct LapTile { int e; int slot0; int rows; int64_t rank0; };
+__device__ __forceinline__ bool lap_tile(const int* lap_tiles, const int* counts, int E, int Ep, int C, int L, int g,
+                                         LapTile& lt) {
+  const int* v = lap_tiles + static_cast<int64_t>(L) * (Ep + 1);
+  if (g >= v[E]) return false;
+  const int e = seg_search_dev(v, E, g);
+  const int mt = g - v[e];
+  int len = counts[e] - L * C;
+  len = len > C ? C : len;
+  lt.e = e;
+  lt.slot0 = mt * 128;
+  lt.rows = min(128, len - mt * 128);
+  lt.rank0 = static_cast<int64_t>(L) * C + mt * 128;
+  return lt.rows > 0;
+}
+
+// ring[e*C + slot] <- x_q[t] for the rows of lap L (codes and scales), zeros past the segment.
+__global__ void permute_lap_kernel(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xq_sf,
+                                   const int* __restrict__ lap_tiles, const int* __restrict__ counts,
+                                   const int* __restrict__ poff, const int* __restrict__ row_src, int T, int k, int d,
+                                   int E, int Ep, int C, int L, uint8_t* __restrict__ ring,
+                                   uint8_t* __restrict__ ring_sf) {
+  LapTile lt;
+  if (!lap_tile(lap_tiles, counts, E, Ep, C, L, blockIdx.x, lt)) return;
+  __shared__ int s_tok[128];
+  if (threadIdx.x < 128) {
+    const int i = threadIdx.x;
+    s_tok[i] = i < lt.rows ? token_of(row_src[poff[lt.e] + lt.rank0 + i], T, k) : -1;
+  }
+  __syncthreads();
+  const int64_t row0 = static_cast<int64_t>(lt.e) * C + lt.slot0;
+  const int chunks = d / 16;
+  for (int i = threadIdx.x; i < 128 * chunks; i += blockDim.x) {
+    const int r = i / chunks, c = i - r * chunks;
+    const int t = s_tok[r];
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (t >= 0) v = reinterpret_cast<const uint4*>(xq + static_cast<int64_t>(t) * d)[c];
+    reinterpret_cast<uint4*>(ring + (row0 + r) * d)[c] = v;
+  }
+  const int ktiles = d / 128;
+  for (int i = threadIdx.x; i < 128 * ktiles; i += blockDim.x) {
+    const int r = i / ktiles, kt = i - r * ktiles;
+    const int t = s_tok[r];
+    uint32_t v = 0;
+    if (t >= 0) v = *reinterpret_cast<const uint32_t*>(xq_sf + sf_off(t, kt * 4, ktiles));
+    *reinterpret_cast<uint32_t*>(ring_sf + sf_off(row0 + r, kt * 4, ktiles)) = v;
+  }
+}
+
+// ring_dO[e*C + slot] <- MX(fp32(w_a * dy[t])) along d for the rows of lap L.
+__global__ void rev_combine_lap_kernel(const __nv_bfloat16* __restrict__ dy, const float* __restrict__ topk_w,
+                                       const int* __restrict__ lap_tiles, const int* __restrict__ counts,
+                                       const int* __restrict__ poff, const int* __restrict__ row_src, int T, int k,
+                                       int d, int E, int Ep, int C, int L, uint8_t* __restrict__ ring,
+                                       uint8_t* __restrict__ ring_sf) {
+  LapTile lt;
+  if (!lap_tile(lap_tiles, counts, E, Ep, C, L, blockIdx.x, lt)) return;
+  __shared__ int s_tok[128];
+  __shared__ float s_w[128];
+  if (threadIdx.x < 128) {
+    const int i = threadIdx.x;
+    int t = -1;
+    float w = 0.0f;
+    if (i < lt.rows) {
+      const int a = row_src[poff[lt.e] + lt.rank0 + i];
+      t = token_of(a, T, k);
+      w = topk_w[a];
+    }
+    s_tok[i] = t;
+    s_w[i] = w;
+  }
+  __syncthreads();
+  const int64_t row0 = static_cast<int64_t>(lt.e) * C + lt.slot0;
+  const int nb = d / 32, ktiles = d / 128;
+  for (int i = threadIdx.x; i < 128 * nb; i += blockDim.x) {
+    const int r = i / nb, kb = i - r * nb;
+    const int t = s_tok[r];
+    float v[32];
+    if (t >= 0) {
+      load_bf16x32(dy + static_cast<int64_t>(t) * d + kb * 32, v);
+      const float w = s_w[r];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(w, v[j]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+    }
+    const int b = mx_scale_byte(amax32(v));
+    uint32_t wq[8];
+    mx_pack32(v, mx_inv_scale(b), wq);
+    store32(ring + (row0 + r) * d + kb * 32, wq);
+    ring_sf[sf_off(row0 + r, kb, ktiles)] = static_cast<uint8_t>(b);
+  }
+}
+
+// y[t] = bf16(sum_{j<k} w[t,j] O[t,j] + sum_s O_shared[s][t]), fp32 in slot order.
+__global__ void combine_kernel(const __nv_bfloat16* __restrict__ O, const float* __restrict__ topk_w, int T, int k,
+                               int S, int d, __nv_bfloat16* __restrict__ y) {
+  const int chunks = d / 8;
+  const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (gid >= static_cast<int64_t>(T) * chunks) return;
+  const int t = static_cast<int>(gid / chunks), c = static_cast<int>(gid - static_cast<int64_t>(t) * chunks);
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int j = 0; j < k; ++j) {
+    const int64_t a = static_cast<int64_t>(t) * k + j;
+    const float w = topk_w[a];
+    const uint4 u = reinterpret_cast<const uint4*>(O + a * d)[c];
+    const uint32_t q[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc[2 * i] = fmaf(w, __uint_as_float(q[i] << 16), acc[2 * i]);
+      acc[2 * i + 1] = fmaf(w, __uint_as_float(q[i] & 0xFFFF0000u), acc[2 * i + 1]);
+    }
+  }
+  for (int s = 0; s < S; ++s) {
+    const int64_t a = static_cast<int64_t>(T) * k + static_cast<int64_t>(s) * T + t;
+    const uint4 u = reinterpret_cast<const uint4*>(O + a * d)[c];
+    const uint32_t q[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc[2 * i] += __uint_as_float(q[i] << 16);
+      acc[2 * i + 1] += __uint_as_float(q[i] & 0xFFFF0000u);
+    }
+  }
+  reinterpret_cast<uint4*>(y + static_cast<int64_t>(t) * d)[c] =
+      make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                 pack_bf16x2(acc[6], acc[7]));
+}
+
+// One warp per token: dw[t,j] = <dy[t], O[t,j]> (fixed lane-strided order and
+// a fixed butterfly), then the router logit gradient
+//   Z = sum_j s_j, c = sum_j dw_j w_j, dl_j = (dw_j - c) / Z * s_j (1 - s_j).
+__global__ void rev_combine_dw_kernel(const __nv_bfloat16* __restrict__ dy, const __nv_bfloat16* __restrict__ O,
+                                      const float* __restrict__ topk_w, const float* __restrict__ s_sel, int T, int k,
+                                      int d, float* __restrict__ dw, float* __restrict__ dl) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + warp;
+  if (t >= T) return;
+  const int chunks = d / 8;
+  float dws[8];
+  for (int j = 0; j < k; ++j) {
+    const int64_t a = static_cast<int64_t>(t) * k + j;
+    float acc = 0.0f;
+    for (int c = lane; c < chunks; c += 32) {
+      const uint4 u = reinterpret_cast<const uint4*>(dy + static_cast<int64_t>(t) * d)[c];
+      const uint4 o = reinterpret_cast<const uint4*>(O + a * d)[c];
+      const uint32_t qu[4] = {u.x, u.y, u.z, u.w};
+      const uint32_t qo[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc = fmaf(__uint_as_float(qu[i] << 16), __uint_as_float(qo[i] << 16), acc);
+        acc = fmaf(__uint_as_float(qu[i] & 0xFFFF0000u), __uint_as_float(qo[i] & 0xFFFF0000u), acc);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    dws[j & 7] = acc;
+  }
+  if (lane == 0) {
+    const int64_t base = static_cast<int64_t>(t) * k;
+    float Z = s_sel[base];
+    for (int j = 1; j < k; ++j) Z = __fadd_rn(Z, s_sel[base + j]);
+    float c = 0.0f;
+    for (int j = 0; j < k; ++j) c = fmaf(dws[j], topk_w[base + j], c);
+    for (int j = 0; j < k; ++j) {
+      const float s = s_sel[base + j];
+      dw[base + j] = dws[j];
+      dl[base + j] = (dws[j] - c) / Z * (s * (1.0f - s));
+    }
+  }
+}
+
+// dx[t] = bf16(sum_{j<k} DX[t,j] + sum_s DX_shared[s][t] + sum_j dl[t,j] Wr[idx[t,j]]), fixed order.
+__global__ void reverse_dispatch_kernel(const __nv_bfloat16* __restrict__ DX, const float* __restrict__ dl,
+                                        const int32_t* __restrict__ idx, const __nv_bfloat16* __restrict__ wr, int T,
+                                        int k, int S, int d, __nv_bfloat16* __restrict__ dx) {
+  const int chunks = d / 8;
+  const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (gid >= static_cast<int64_t>(T) * chunks) return;
+  const int t = static_cast<int>(gid / chunks), c = static_cast<int>(gid - static_cast<int64_t>(t) * chunks);
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  auto add_row = [&](const __nv_bfloat16* row, float scale, bool scaled) {
+    const uint4 u = reinterpret_cast<const uint4*>(row)[c];
+    const uint32_t q[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float lo = __uint_as_float(q[i] << 16), hi = __uint_as_float(q[i] & 0xFFFF0000u);
+      if (scaled) {
+        acc[2 * i] = fmaf(scale, lo, acc[2 * i]);
+        acc[2 * i + 1] = fmaf(scale, hi, acc[2 * i + 1]);
+      } else {
+        acc[2 * i] += lo;
+        acc[2 * i + 1] += hi;
+      }
+    }
+  };
+  for (int j = 0; j < k; ++j) add_row(DX + (static_cast<int64_t>(t) * k + j) * d, 1.0f, false);
+  for (int s = 0; s < S; ++s) add_row(DX + (static_cast<int64_t>(T) * k + static_cast<int64_t>(s) * T + t) * d, 1.0f, false);
+  for (int j = 0; j < k; ++j) {
+    const int64_t a = static_cast<int64_t>(t) * k + j;
+    add_row(wr + static_cast<int64_t>(idx[a]) * d, dl[a], true);
+  }
+  reinterpret_cast<uint4*>(dx + static_cast<int64_t>(t) * d)[c] =
+      make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                 pack_bf16x2(acc[6], acc[7]));
+}
+
+// dWr[e][c] = bf16(sum over the 32-row blocks of expert e of part[b][c]).
+// 8 groups of 32 threads each sum a contiguous run of blocks; the 8 group
+// sums are then added in group order (a fixed order).
+__global__ void router_dwr_kernel(const float* __restrict__ part, const int* __restrict__ poff, int d,
+                                  __nv_bfloat16* __restrict__ dwr) {
+  __shared__ float4 red[8][32];
+  const int e = blockIdx.y;
+  const int grp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = (blockIdx.x * 32 + lane) * 4;
+  const int b0 = poff[e] / 32, b1 = poff[e + 1] / 32;
+  const int nb = b1 - b0;
+  const int per = (nb + 7) / 8;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (c < d) {
+    for (int b = b0 + grp * per; b < b0 + (grp + 1) * per && b < b1; ++b) {
+      const float4 v = *reinterpret_cast<const float4*>(part + static_cast<int64_t>(b) * d + c);
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+  }
+  red[grp][lane] = acc;
+  __syncthreads();
+  if (grp == 0 && c < d) {
+    float4 s = red[0][lane];
+    for (int g = 1; g < 8; ++g) {
+      const float4 v = red[g][lane];
+      s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+    }
+    uint2 o = make_uint2(pack_bf16x2(s.x, s.y), pack_bf16x2(s.z, s.w));
+    *reinterpret_cast<uint2*>(dwr + static_cast<int64_t>(e) * d + c) = o;
+  }
+}
+
+}  // namespace
+
+void launch_permute_lap(const Dims& m, int lap, const Layout& L, void* ws, cudaStream_t s) {
+  const int blocks = m.E * (m.C / 128);
+  if (blocks == 0) return;
+  permute_lap_kernel<<<blocks, 256, 0, s>>>(
+      ws_ptr<uint8_t>(L, ws, MOE_WS_XQ), ws_ptr<uint8_t>(L, ws, MOE_WS_XQ_SF), ws_ptr<int>(L, ws, MOE_WS_LAPTILES),
+      ws_ptr<int>(L, ws, MOE_WS_COUNTS), ws_ptr<int>(L, ws, MOE_WS_POFF), ws_ptr<int>(L, ws, MOE_WS_ROWSRC), m.T, m.k,
+      m.d, m.E, m.Ep, m.C, lap, ws_ptr<uint8_t>(L, ws, MOE_WS_RING_X), ws_ptr<uint8_t>(L, ws, MOE_WS_RING_X_SF));
+}
+
+void launch_rev_combine_lap(const Dims& m, int lap, const void* dy, const float* topk_w, const Layout& L, void* ws,
+                            cudaStream_t s) {
+  const int blocks = m.E * (m.C / 128);
+  if (blocks == 0) return;
+  rev_combine_lap_kernel<<<blocks, 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(dy), topk_w, ws_ptr<int>(L, ws, MOE_WS_LAPTILES),
+      ws_ptr<int>(L, ws, MOE_WS_COUNTS), ws_ptr<int>(L, ws, MOE_WS_POFF), ws_ptr<int>(L, ws, MOE_WS_ROWSRC), m.T, m.k,
+      m.d, m.E, m.Ep, m.C, lap, ws_ptr<uint8_t>(L, ws, MOE_WS_RING_DO), ws_ptr<uint8_t>(L, ws, MOE_WS_RING_DO_SF));
+}
+
+void launch_combine(const Dims& m, const float* topk_w, const Layout& L, void* ws, void* y, cudaStream_t s) {
+  const int64_t n = static_cast<int64_t>(m.T) * (m.d / 8);
+  if (n == 0) return;
+  combine_kernel<<<static_cast<unsigned>(ceil_div(n, 256)), 256, 0, s>>>(
+      ws_ptr<__nv_bfloat16>(L, ws, MOE_WS_O), topk_w, m.T, m.k, m.S, m.d, static_cast<__nv_bfloat16*>(y));
+}
+
+void launch_rev_combine_dw(const Dims& m, const void* dy, const float* topk_w, const Layout& L, void* ws,
+                           cudaStream_t s) {
+  if (m.T == 0) return;
+  rev_combine_dw_kernel<<<static_cast<unsigned>(ceil_div(m.T, 8)), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(dy), ws_ptr<__nv_bfloat16>(L, ws, MOE_WS_O), topk_w,
+      ws_ptr<float>(L, ws, MOE_WS_SSEL), m.T, m.k, m.d, ws_ptr<float>(L, ws, MOE_WS_DW),
+      ws_ptr<float>(L, ws, MOE_WS_DL));
+}
+
+void launch_reverse_dispatch(const Dims& m, const int32_t* idx, const void* w_router, const Layout& L, void* ws,
+                             void* dx, cudaStream_t s) {
+  const int64_t n = static_cast<int64_t>(m.T) * (m.d / 8);
+  if (n == 0) return;
+  reverse_dispatch_kernel<<<static_cast<unsigned>(ceil_div(n, 256)), 256, 0, s>>>(
+      ws_ptr<__nv_bfloat16>(L, ws, MOE_WS_DXE), ws_ptr<float>(L, ws, MOE_WS_DL), idx,
+      static_cast<const __nv_bfloat16*>(w_router), m.T, m.k, m.S, m.d, static_cast<__nv_bfloat16*>(dx));
+}
+
+void launch_router_dwr(const Dims& m, const Layout& L, void* ws, void* dw_router, cudaStream_t s) {
+  dim3 grid(static_cast<unsigned>(ceil_div(m.d, 128)), static_cast<unsigned>(m.E));
+  router_dwr_kernel<<<grid, 256, 0, s>>>(ws_ptr<float>(L, ws, MOE_WS_DWR_PART), ws_ptr<int>(L, ws, MOE_WS_POFF), m.d,
+                                         static_cast<__nv_bfloat16*>(dw_router));
+}
+
+}  // namespace moe

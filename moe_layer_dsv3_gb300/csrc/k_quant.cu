@@ -1,0 +1,164 @@
+// MX quantisers: along rows (K axis), along columns (token axis, transposed),
+// token-axis gathers through the schedule, and scale re-tiling.
+#include "moe_internal.h"
+#include "mx.cuh"
+
+namespace moe {
+
+// Row of the interleaved GEMM1 weight layout for source row r of w_gu:
+// blocks of 128 gate rows followed by the matching 128 up rows.
+__device__ __forceinline__ int64_t gu_interleave_row(int64_t r, int I) {
+  const int64_t e = r / (2 * I);
+  const int64_t i = r % (2 * I);
+  const int64_t up = i >= I ? 1 : 0;
+  const int64_t ii = i - up * I;
+  return e * 2 * I + (ii >> 7) * 256 + up * 128 + (ii & 127);
+}
+
+// One thread per 32-element block along K.
+__global__ void quant_rows_kernel(const __nv_bfloat16* __restrict__ src, int64_t rows, int K, int64_t ld,
+                                  uint8_t* __restrict__ codes, uint8_t* __restrict__ sf, int tiled,
+                                  int interleave_I) {
+  const int64_t nb = K / 32;
+  const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (gid >= rows * nb) return;
+  const int64_t r = gid / nb;
+  const int64_t kb = gid - r * nb;
+  float v[32];
+  load_bf16x32(src + r * ld + kb * 32, v);
+  const int b = mx_scale_byte(amax32(v));
+  uint32_t w[8];
+  mx_pack32(v, mx_inv_scale(b), w);
+  const int64_t orow = interleave_I > 0 ? gu_interleave_row(r, interleave_I) : r;
+  store32(codes + orow * K + kb * 32, w);
+  sf[tiled ? sf_off(orow, kb, K / 128) : orow * nb + kb] = static_cast<uint8_t>(b);
+}
+
+// Token-axis MX of src[rows][K]: block = 32 consecutive rows of one column.
+// codes[K][rows_pad], scales per (column, row block). CTA: 32 rows x 256 cols.
+__global__ void quant_cols_kernel(const __nv_bfloat16* __restrict__ src, int64_t rows, int K, int64_t ld,
+                                  int64_t rows_pad, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+                                  int tiled) {
+  // blockIdx.z selects one matrix of a batch of equally shaped ones.
+  src += static_cast<int64_t>(blockIdx.z) * rows * ld;
+  codes += static_cast<int64_t>(blockIdx.z) * K * rows_pad;
+  sf += static_cast<int64_t>(blockIdx.z) * K * (rows_pad / 32);
+  const int c = blockIdx.x * 256 + threadIdx.x;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 32;
+  if (c >= K) return;
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int64_t r = r0 + i;
+    v[i] = r < rows ? __bfloat162float(src[r * ld + c]) : 0.0f;
+  }
+  const int b = mx_scale_byte(amax32(v));
+  uint32_t w[8];
+  mx_pack32(v, mx_inv_scale(b), w);
+  store32(codes + static_cast<int64_t>(c) * rows_pad + r0, w);
+  const int64_t kb = r0 / 32;
+  sf[tiled ? sf_off(c, kb, rows_pad / 128) : static_cast<int64_t>(c) * (rows_pad / 32) + kb] = static_cast<uint8_t>(b);
+}
+
+// Token of assignment a (routed a < T*k: a / k; shared: (a - T*k) % T).
+__device__ __forceinline__ int token_of(int a, int T, int k) {
+  const int A = T * k;
+  return a < A ? a / k : (a - A) % T;
+}
+
+// Token-axis MX of gathered rows: padded row pr holds assignment a = row_src[pr]
+// (or padding). value = src[t_a][c], times the gate w_a when scale_by_gate
+// (shared-expert assignments have gate 1). Optionally also accumulates the
+// router weight-gradient partial sums part[pr/32][c] = sum_r dl_a x[t_a][c]
+// over the routed rows of the 32-row block, in rank order.
+__global__ void tok_gather_kernel(const __nv_bfloat16* __restrict__ src, const int* __restrict__ row_src,
+                                  const int* __restrict__ poff_end, int T, int k, int d, int64_t Rmax,
+                                  const float* __restrict__ topk_w, int scale_by_gate,
+                                  const float* __restrict__ dl, float* __restrict__ part,
+                                  uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
+  const int c = blockIdx.x * 256 + threadIdx.x;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 32;
+  if (r0 >= *poff_end) return;
+  __shared__ int s_a[32];
+  __shared__ float s_w[32];
+  __shared__ float s_dl[32];
+  if (threadIdx.x < 32) {
+    const int a = row_src[r0 + threadIdx.x];
+    s_a[threadIdx.x] = a;
+    float w = 1.0f, g = 0.0f;
+    if (a >= 0 && a < T * k) {
+      if (scale_by_gate) w = topk_w[a];
+      if (dl != nullptr) g = dl[a];
+    }
+    s_w[threadIdx.x] = w;
+    s_dl[threadIdx.x] = g;
+  }
+  __syncthreads();
+  if (c >= d) return;
+  float v[32];
+  float acc = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int a = s_a[i];
+    float x = 0.0f;
+    if (a >= 0) {
+      x = __bfloat162float(src[static_cast<int64_t>(token_of(a, T, k)) * d + c]);
+      acc = fmaf(s_dl[i], x, acc);
+      x = scale_by_gate ? s_w[i] * x : x;
+    }
+    v[i] = x;
+  }
+  const int b = mx_scale_byte(amax32(v));
+  uint32_t w[8];
+  mx_pack32(v, mx_inv_scale(b), w);
+  store32(codes + static_cast<int64_t>(c) * Rmax + r0, w);
+  sf[sf_off(c, r0 / 32, Rmax / 128)] = static_cast<uint8_t>(b);
+  if (part != nullptr) part[(r0 / 32) * d + c] = acc;
+}
+
+__global__ void scales_to_tiled_kernel(const uint8_t* __restrict__ canon, int64_t rows, int nb, uint8_t* tiled) {
+  const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (gid >= rows * nb) return;
+  const int64_t r = gid / nb, kb = gid - (gid / nb) * nb;
+  tiled[sf_off(r, kb, nb / 4)] = canon[gid];
+}
+
+void launch_quant_rows(const void* src, int64_t rows, int K, int64_t ld, uint8_t* codes, uint8_t* sf, bool tiled,
+                       int interleave_I, cudaStream_t s) {
+  const int64_t n = rows * (K / 32);
+  if (n == 0) return;
+  const int threads = 256;
+  quant_rows_kernel<<<static_cast<unsigned>(ceil_div(n, threads)), threads, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(src), rows, K, ld, codes, sf, tiled ? 1 : 0, interleave_I);
+}
+
+void launch_quant_cols(const void* src, int64_t rows, int K, int64_t ld, int64_t rows_pad, uint8_t* codes,
+                       uint8_t* sf, bool tiled, int batch, cudaStream_t s) {
+  if (rows_pad == 0 || K == 0 || batch == 0) return;
+  dim3 grid(static_cast<unsigned>(ceil_div(K, 256)), static_cast<unsigned>(rows_pad / 32), static_cast<unsigned>(batch));
+  quant_cols_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(src), rows, K, ld, rows_pad, codes, sf,
+                                         tiled ? 1 : 0);
+}
+
+void launch_tok_gather(const Dims& m, const void* src_rows, bool scale_by_gate, const float* topk_w,
+                       bool router_partials, const Layout& L, void* ws, uint8_t* codes, uint8_t* sf,
+                       cudaStream_t s) {
+  dim3 grid(static_cast<unsigned>(ceil_div(m.d, 256)), static_cast<unsigned>(m.Rmax / 32));
+  const int* poff = ws_ptr<int>(L, ws, MOE_WS_POFF);
+  tok_gather_kernel<<<grid, 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(src_rows), ws_ptr<int>(L, ws, MOE_WS_ROWSRC), poff + m.Ep, m.T, m.k, m.d,
+      m.Rmax, topk_w, scale_by_gate ? 1 : 0, router_partials ? ws_ptr<float>(L, ws, MOE_WS_DL) : nullptr,
+      router_partials ? ws_ptr<float>(L, ws, MOE_WS_DWR_PART) : nullptr, codes, sf);
+}
+
+}  // namespace moe
+
+extern "C" int moe_scales_to_tiled(const void* canon, int rows, int K, void* tiled, moe_stream_t stream) {
+  if (canon == nullptr || tiled == nullptr || rows <= 0 || K <= 0 || rows % 128 || K % 128) return MOE_ERR_INVALID_ARG;
+  const int nb = K / 32;
+  const int64_t n = static_cast<int64_t>(rows) * nb;
+  moe::scales_to_tiled_kernel<<<static_cast<unsigned>(moe::ceil_div(n, 256)), 256, 0,
+                                static_cast<cudaStream_t>(stream)>>>(static_cast<const uint8_t*>(canon), rows, nb,
+                                                                      static_cast<uint8_t*>(tiled));
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

@@ -1,0 +1,160 @@
+// Router: logits on the tensor cores, then sigmoid + bias + group-limited
+// top-k + gate normalisation as warp-shuffle reductions (one warp per token).
+//
+// Reading of "DSV3-style router" (Cursor blog summary, "method points"):
+// s = sigmoid(logit) in the specified fp32 arithmetic below, v = s + bias,
+// group score = sum of the two largest v of the group, keep the topk_groups
+// best groups (ties to the lower group), take the k best v among kept
+// experts (ties to the lower expert), slots in descending-v order, gates
+// w = s / sum(s) summed in slot order.
+#include "moe_internal.h"
+#include "gemm.cuh"
+
+namespace moe {
+
+// sigma(l) = 1 / (1 + E(-clamp(l, -80, 80))), E by Cody-Waite reduction
+// (W. J. Cody and W. Waite, 1980) and a degree-7 Taylor polynomial, every
+// operation an IEEE binary32 round-to-nearest op without contraction.
+__device__ __forceinline__ float sigmoid_spec(float l) {
+  constexpr double kLn2 = 0.6931471805599453094;
+  constexpr float kLog2e = static_cast<float>(1.0 / kLn2);
+  constexpr float kC1 = 355.0f / 512.0f;                               // ln2 to 9 significant bits
+  constexpr float kC2 = static_cast<float>(kLn2 - 355.0 / 512.0);      // remainder
+  constexpr float c0 = 1.0f, c1 = 1.0f, c2 = 0.5f;
+  constexpr float c3 = static_cast<float>(1.0 / 6.0), c4 = static_cast<float>(1.0 / 24.0);
+  constexpr float c5 = static_cast<float>(1.0 / 120.0), c6 = static_cast<float>(1.0 / 720.0);
+  constexpr float c7 = static_cast<float>(1.0 / 5040.0);
+  const float lc = fminf(fmaxf(l, -80.0f), 80.0f);
+  const float z = -lc;
+  const float n = rintf(__fmul_rn(z, kLog2e));
+  const float r = __fsub_rn(__fsub_rn(z, __fmul_rn(n, kC1)), __fmul_rn(n, kC2));
+  float p = c7;
+  p = __fadd_rn(__fmul_rn(p, r), c6);
+  p = __fadd_rn(__fmul_rn(p, r), c5);
+  p = __fadd_rn(__fmul_rn(p, r), c4);
+  p = __fadd_rn(__fmul_rn(p, r), c3);
+  p = __fadd_rn(__fmul_rn(p, r), c2);
+  p = __fadd_rn(__fmul_rn(p, r), c1);
+  p = __fadd_rn(__fmul_rn(p, r), c0);
+  const float two_n = __int_as_float((static_cast<int>(n) + 127) << 23);
+  const float e = __fmul_rn(p, two_n);
+  return __fdiv_rn(1.0f, __fadd_rn(1.0f, e));
+}
+
+// (v1, e1) ranks above (v2, e2): larger value, ties to the lower index.
+__device__ __forceinline__ bool better(float v1, int e1, float v2, int e2) {
+  return v1 > v2 || (v1 == v2 && e1 < e2);
+}
+
+__device__ __forceinline__ void warp_best(float& v, int& e) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    const int oe = __shfl_xor_sync(0xffffffffu, e, o);
+    if (better(ov, oe, v, e)) { v = ov; e = oe; }
+  }
+}
+
+constexpr int kMaxPerLane = 16;   // E <= 512
+
+// One warp per token. Lane l owns experts e = l + 32 i.
+__global__ void router_topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E,
+                                   int k, int G, int gtop, int32_t* __restrict__ idx_out,
+                                   float* __restrict__ w_out, float* __restrict__ s_out) {
+  extern __shared__ float sv_all[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + warp;
+  float* sv = sv_all + warp * E;
+  if (t >= T) return;
+  float s[kMaxPerLane], v[kMaxPerLane];
+  const int per_lane = (E + 31) / 32;
+#pragma unroll
+  for (int i = 0; i < kMaxPerLane; ++i) {
+    const int e = lane + 32 * i;
+    if (i < per_lane && e < E) {
+      s[i] = sigmoid_spec(logits[static_cast<int64_t>(t) * E + e]);
+      v[i] = __fadd_rn(s[i], bias[e]);
+      sv[e] = v[i];
+    } else {
+      s[i] = 0.0f;
+      v[i] = -INFINITY;
+    }
+  }
+  __syncwarp();
+  uint32_t kept = 0xffffffffu;
+  if (G > 1) {
+    const int per = E / G;
+    float gs = -INFINITY;
+    if (lane < G) {
+      float m1 = -INFINITY, m2 = -INFINITY;
+      for (int e = lane * per; e < (lane + 1) * per; ++e) {
+        const float x = sv[e];
+        if (x > m1) { m2 = m1; m1 = x; } else if (x > m2) { m2 = x; }
+      }
+      gs = __fadd_rn(m1, m2);
+    }
+    kept = 0;
+    for (int r = 0; r < gtop; ++r) {
+      float bv = (lane < G && !((kept >> lane) & 1u)) ? gs : -INFINITY;
+      int be = lane < G && !((kept >> lane) & 1u) ? lane : 0x7fffffff;
+      warp_best(bv, be);
+      kept |= 1u << be;
+    }
+  }
+  const int per = G > 1 ? E / G : E;
+  uint32_t taken = 0;
+  int sel_e[8];
+  float sel_s[8];
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i) {
+      const int e = lane + 32 * i;
+      if (i < per_lane && e < E && !((taken >> i) & 1u) && ((kept >> (e / per)) & 1u)) {
+        if (better(v[i], e, bv, be)) { bv = v[i]; be = e; }
+      }
+    }
+    warp_best(bv, be);
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    float sw = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i)
+      if (i == (be >> 5)) sw = s[i];
+    sel_s[j] = __shfl_sync(0xffffffffu, sw, be & 31);
+    sel_e[j] = be;
+  }
+  if (lane == 0) {
+    float tot = sel_s[0];
+    for (int j = 1; j < k; ++j) tot = __fadd_rn(tot, sel_s[j]);
+    for (int j = 0; j < k; ++j) {
+      idx_out[static_cast<int64_t>(t) * k + j] = sel_e[j];
+      w_out[static_cast<int64_t>(t) * k + j] = __fdiv_rn(sel_s[j], tot);
+      s_out[static_cast<int64_t>(t) * k + j] = sel_s[j];
+    }
+  }
+}
+
+void launch_router_logits(const Dims& m, const void* x, const void* w_router, float* logits, cudaStream_t s) {
+  GemmOperands op{};
+  op.a = static_cast<const uint8_t*>(x);
+  op.a_rows = m.T;
+  op.a_cols = m.d;
+  op.b = static_cast<const uint8_t*>(w_router);
+  op.b_rows = m.E;
+  op.b_cols = m.d;
+  GemmEpilogue ep{};
+  ep.out = logits;
+  ep.ldo = m.E;
+  gemm_dispatch(kRouterMode, m, 0, m.E, m.d, m.T, op, ep, nullptr, nullptr, nullptr, nullptr, nullptr, s);
+}
+
+void launch_router_topk(const Dims& m, const float* logits, const float* bias, int32_t* idx, float* w, float* s_sel,
+                        cudaStream_t s) {
+  if (m.T == 0) return;
+  const int warps = 4;
+  router_topk_kernel<<<static_cast<unsigned>(ceil_div(m.T, warps)), warps * 32, warps * m.E * sizeof(float), s>>>(
+      logits, bias, m.T, m.E, m.k, m.G, m.gtop, idx, w, s_sel);
+}
+
+}  // namespace moe

@@ -1,0 +1,192 @@
+// Device-side schedule (write-ups: the schedule is built on the device, costs
+// under 3 % of the MoE runtime and is reused by backward without re-sorting;
+// Cursor blog summary, "method points").
+//
+// Assignments are taken in (t, j) order over k routed slots plus the shared
+// experts' slots (slot k + s always picks shared expert E + s). Three passes:
+//   1. per-unit histograms (unit = 256 consecutive assignments, one warp);
+//   2. per-expert exclusive scan over units, then a single-block pass for
+//      offsets, 128-row padded offsets and the per-lap tile lists;
+//   3. stable ranks: each warp walks its unit in order, 32 assignments at a
+//      time, ranking equal experts with __match_any_sync.
+// Only integer arithmetic; the result does not depend on scheduling order.
+#include "moe_internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kWarps = 8;
+
+__device__ __forceinline__ int expert_of(const int32_t* idx, int64_t ap, int k, int kp, int E) {
+  const int64_t t = ap / kp;
+  const int j = static_cast<int>(ap - t * kp);
+  return j < k ? idx[t * k + j] : E + (j - k);
+}
+
+// Canonical assignment id: routed a = t*k + j, shared a = T*k + s*T + t.
+__device__ __forceinline__ int canon_of(int64_t ap, int T, int k, int kp) {
+  const int64_t t = ap / kp;
+  const int j = static_cast<int>(ap - t * kp);
+  return static_cast<int>(j < k ? t * k + j : static_cast<int64_t>(T) * k + static_cast<int64_t>(j - k) * T + t);
+}
+
+__global__ void sched_hist_kernel(const int32_t* __restrict__ idx, int k, int kp, int E, int Ep, int64_t Ap,
+                                  int units, int* __restrict__ hist, int* status) {
+  extern __shared__ int sh[];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int u = blockIdx.x * kWarps + w;
+  int* h = sh + w * Ep;
+  for (int e = lane; e < Ep; e += 32) h[e] = 0;
+  __syncwarp();
+  if (u < units) {
+    for (int i = lane; i < kSchedUnit; i += 32) {
+      const int64_t ap = static_cast<int64_t>(u) * kSchedUnit + i;
+      if (ap < Ap) {
+        const int e = expert_of(idx, ap, k, kp, E);
+        if (e >= 0 && e < Ep) atomicAdd(&h[e], 1);
+        else report_error(status, kErrBounds, 100);
+      }
+    }
+  }
+  __syncwarp();
+  if (u < units)
+    for (int e = lane; e < Ep; e += 32) hist[static_cast<int64_t>(u) * Ep + e] = h[e];
+}
+
+// One block per expert: exclusive scan of hist[.][e] over units.
+__global__ void sched_scan_kernel(const int* __restrict__ hist, int Ep, int units, int* __restrict__ base,
+                                  int* __restrict__ counts) {
+  __shared__ int sums[256];
+  const int e = blockIdx.x;
+  const int per = (units + 255) / 256;
+  const int u0 = threadIdx.x * per;
+  int s = 0;
+  for (int u = u0; u < u0 + per && u < units; ++u) s += hist[static_cast<int64_t>(u) * Ep + e];
+  sums[threadIdx.x] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int i = 0; i < 256; ++i) {
+      const int v = sums[i];
+      sums[i] = run;
+      run += v;
+    }
+    counts[e] = run;
+  }
+  __syncthreads();
+  int run = sums[threadIdx.x];
+  for (int u = u0; u < u0 + per && u < units; ++u) {
+    const int64_t o = static_cast<int64_t>(u) * Ep + e;
+    const int v = hist[o];
+    base[o] = run;
+    run += v;
+  }
+}
+
+// Offsets, padded offsets, laps and per-lap tile prefix sums.
+// lap_tiles[L][e] = sum_{e' < e} ceil(len(e', L) / 128), where a routed
+// expert's lap L holds ranks [L*C, min(n, (L+1)*C)) and a shared expert is
+// processed whole in lap 0 (it is read in token order, not from the ring).
+__global__ void sched_offsets_kernel(const int* __restrict__ counts, int E, int Ep, int C, int Lb,
+                                     int* __restrict__ offsets, int* __restrict__ poff, int* __restrict__ lap_tiles,
+                                     int* __restrict__ meta) {
+  if (threadIdx.x == 0) {
+    int o = 0, po = 0, laps = 0;
+    for (int e = 0; e < Ep; ++e) {
+      offsets[e] = o;
+      poff[e] = po;
+      const int n = counts[e];
+      o += n;
+      po += (n + 127) / 128 * 128;
+      if (e < E) laps = max(laps, (n + C - 1) / C);
+    }
+    offsets[Ep] = o;
+    poff[Ep] = po;
+    meta[0] = laps;
+    meta[1] = po;
+  }
+  for (int L = threadIdx.x; L < Lb; L += blockDim.x) {
+    int run = 0;
+    int* lt = lap_tiles + static_cast<int64_t>(L) * (Ep + 1);
+    for (int e = 0; e < Ep; ++e) {
+      lt[e] = run;
+      const int n = counts[e];
+      int len;
+      if (e < E) {
+        len = n - L * C;
+        len = len < 0 ? 0 : (len > C ? C : len);
+      } else {
+        len = L == 0 ? n : 0;
+      }
+      run += (len + 127) / 128;
+    }
+    lt[Ep] = run;
+  }
+}
+
+__global__ void sched_rank_kernel(const int32_t* __restrict__ idx, int T, int k, int kp, int E, int Ep, int64_t Ap,
+                                  int units, const int* __restrict__ base, const int* __restrict__ offsets,
+                                  const int* __restrict__ poff, int* __restrict__ rank, int* __restrict__ pos,
+                                  int* __restrict__ inv, int* __restrict__ row_src) {
+  extern __shared__ int sh[];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int u = blockIdx.x * kWarps + w;
+  if (u >= units) return;
+  int* run = sh + w * Ep;
+  for (int e = lane; e < Ep; e += 32) run[e] = base[static_cast<int64_t>(u) * Ep + e];
+  __syncwarp();
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int b = 0; b < kSchedUnit / 32; ++b) {
+    const int64_t ap = static_cast<int64_t>(u) * kSchedUnit + b * 32 + lane;
+    const bool valid = ap < Ap;
+    int e = valid ? expert_of(idx, ap, k, kp, E) : -1 - lane;
+    if (valid && (e < 0 || e >= Ep)) e = -1000 - lane;   // already reported by the histogram pass
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const bool ok = valid && e >= 0;
+    int r = 0;
+    if (ok) r = run[e] + __popc(peers & lt_mask);
+    __syncwarp();
+    if (ok && (31 - __clz(peers)) == lane) run[e] += __popc(peers);
+    __syncwarp();
+    if (ok) {
+      const int a = canon_of(ap, T, k, kp);
+      rank[a] = r;
+      const int p = offsets[e] + r;
+      pos[a] = p;
+      inv[p] = a;
+      row_src[static_cast<int64_t>(poff[e]) + r] = a;
+    }
+  }
+}
+
+}  // namespace
+
+void launch_schedule(const Dims& m, const int32_t* idx, const Layout& L, void* ws, cudaStream_t s) {
+  int* hist = ws_ptr<int>(L, ws, MOE_WS_HIST);
+  int* base = ws_ptr<int>(L, ws, MOE_WS_BASE);
+  int* counts = ws_ptr<int>(L, ws, MOE_WS_COUNTS);
+  int* offsets = ws_ptr<int>(L, ws, MOE_WS_OFFSETS);
+  int* poff = ws_ptr<int>(L, ws, MOE_WS_POFF);
+  int* lap_tiles = ws_ptr<int>(L, ws, MOE_WS_LAPTILES);
+  int* meta = ws_ptr<int>(L, ws, MOE_WS_META);
+  int* status = ws_ptr<int>(L, ws, MOE_WS_STATUS);
+  const unsigned blocks = static_cast<unsigned>(ceil_div(m.units, kWarps));
+  const size_t shm = static_cast<size_t>(kWarps) * m.Ep * sizeof(int);
+  cudaMemsetAsync(ws_ptr<int>(L, ws, MOE_WS_ROWSRC), 0xFF, L.bytes[MOE_WS_ROWSRC], s);
+  if (m.units > 0) {
+    sched_hist_kernel<<<blocks, kWarps * 32, shm, s>>>(idx, m.k, m.kp, m.E, m.Ep, m.Ap, m.units, hist, status);
+    sched_scan_kernel<<<m.Ep, 256, 0, s>>>(hist, m.Ep, m.units, base, counts);
+  } else {
+    cudaMemsetAsync(counts, 0, sizeof(int) * m.Ep, s);
+  }
+  sched_offsets_kernel<<<1, 256, 0, s>>>(counts, m.E, m.Ep, m.C, m.Lb, offsets, poff, lap_tiles, meta);
+  if (m.units > 0)
+    sched_rank_kernel<<<blocks, kWarps * 32, shm, s>>>(idx, m.T, m.k, m.kp, m.E, m.Ep, m.Ap, m.units, base, offsets,
+                                                       poff, ws_ptr<int>(L, ws, MOE_WS_RANK),
+                                                       ws_ptr<int>(L, ws, MOE_WS_POS), ws_ptr<int>(L, ws, MOE_WS_INV),
+                                                       ws_ptr<int>(L, ws, MOE_WS_ROWSRC));
+}
+
+}  // namespace moe

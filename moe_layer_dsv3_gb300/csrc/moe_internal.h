@@ -1,0 +1,127 @@
+// Internal host-side declarations: workspace layout and kernel launchers.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kTileM = 128;     // rows per GEMM tile / scale atom
+constexpr int kTileK = 128;     // fp8 elements per K stage (one 128-byte swizzle row)
+constexpr int kSchedUnit = 256; // assignments per schedule unit (one warp)
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+// Byte offset of scale byte (row r, 32-block kb) in the MMA-ready tiled scale
+// layout of a [R][K] MX operand: 512-byte atoms of 128 rows x 4 blocks,
+// atoms ordered (row tile, k tile), inside an atom (r%32)*16 + (r/32%4)*4 + kb%4.
+__host__ __device__ inline int64_t sf_tiled_offset(int64_t r, int64_t kb, int64_t k_tiles) {
+  return ((r >> 7) * k_tiles + (kb >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (kb & 3);
+}
+
+struct Dims {
+  int T, d, E, k, G, gtop, I, S, C;
+  int Ep;          // routed + shared experts
+  int kp;          // routed + shared slots per token
+  int64_t A;       // routed assignments T*k
+  int64_t Ap;      // all assignments T*(k+S)
+  int64_t Tpad;    // ceil128(T)
+  int64_t Rmax;    // padded-row capacity of rank-ordered buffers
+  int Lb;          // upper bound on ring laps: ceil(T / C)
+  int units;       // schedule units
+};
+
+struct Layout {
+  Dims m;
+  size_t off[MOE_WS_COUNT];
+  size_t bytes[MOE_WS_COUNT];
+  size_t total;
+};
+
+struct WLayout {
+  size_t off[MOE_WQ_COUNT];
+  size_t bytes[MOE_WQ_COUNT];
+  size_t total;
+};
+
+int validate(const moe_config_t* cfg);
+Dims make_dims(const moe_config_t* cfg);
+Layout make_layout(const moe_config_t* cfg);
+WLayout make_wlayout(const moe_config_t* cfg);
+
+template <typename T>
+inline T* ws_ptr(const Layout& L, void* ws, int which) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + L.off[which]);
+}
+template <typename T>
+inline T* wq_ptr(const WLayout& L, void* wq, int which) {
+  return reinterpret_cast<T*>(static_cast<char*>(wq) + L.off[which]);
+}
+
+int num_sms();
+
+// ---------------------------------------------------------------- quantisers
+// Row-wise MX quantisation of bf16 src[rows][K] (row pitch ld elements).
+// Output row r goes to row out_row(r) = (interleave ? gate/up interleave : r).
+// Scales canonical [rows][K/32] (sf_k_tiles == 0) or tiled with K/128 k-tiles.
+void launch_quant_rows(const void* src, int64_t rows, int K, int64_t ld, uint8_t* codes, uint8_t* sf, bool tiled,
+                       int interleave_I, cudaStream_t s);
+// Column-wise (token-axis) MX quantisation: src[rows][K] bf16 -> codes[K][rows_pad], blocks of 32 rows.
+// `batch` equally shaped matrices laid out back to back (grid z).
+void launch_quant_cols(const void* src, int64_t rows, int K, int64_t ld, int64_t rows_pad, uint8_t* codes,
+                       uint8_t* sf, bool tiled, int batch, cudaStream_t s);
+
+// ---------------------------------------------------------------- router
+void launch_router_logits(const Dims& m, const void* x, const void* w_router, float* logits, cudaStream_t s);
+void launch_router_topk(const Dims& m, const float* logits, const float* bias, int32_t* idx, float* w,
+                        float* s_sel, cudaStream_t s);
+
+// ---------------------------------------------------------------- schedule
+void launch_schedule(const Dims& m, const int32_t* idx, const Layout& L, void* ws, cudaStream_t s);
+
+// ---------------------------------------------------------------- data movement
+void launch_permute_lap(const Dims& m, int lap, const Layout& L, void* ws, cudaStream_t s);
+void launch_combine(const Dims& m, const float* topk_w, const Layout& L, void* ws, void* y, cudaStream_t s);
+void launch_rev_combine_dw(const Dims& m, const void* dy, const float* topk_w, const Layout& L, void* ws,
+                           cudaStream_t s);
+void launch_rev_combine_lap(const Dims& m, int lap, const void* dy, const float* topk_w, const Layout& L,
+                            void* ws, cudaStream_t s);
+void launch_tok_gather(const Dims& m, const void* src_rows, bool scale_by_gate, const float* topk_w,
+                       bool router_partials, const Layout& L, void* ws, uint8_t* codes, uint8_t* sf,
+                       cudaStream_t s);
+void launch_reverse_dispatch(const Dims& m, const int32_t* idx, const void* w_router, const Layout& L, void* ws,
+                             void* dx, cudaStream_t s);
+void launch_router_dwr(const Dims& m, const Layout& L, void* ws, void* dw_router, cudaStream_t s);
+
+// ---------------------------------------------------------------- GEMM
+enum GemmMode : int {
+  kSwigluFwd = 0,   // lap tiles, A = ring / x_q, epilogue SwiGLU + MX(h) two ways + saved g,u
+  kPush = 1,        // padded tiles, epilogue bf16 rows pushed to their assignment
+  kSwigluBwd = 2,   // lap tiles, A = ring dO / dO_s, epilogue SwiGLU backward + MX(dGU) two ways
+  kWgrad = 3,       // per-expert K ranges, epilogue bf16 weight gradient
+  kPlain = 4,       // single dense problem, fp32 output (unit test entry)
+};
+
+struct GemmOperands {
+  const uint8_t* a;  int64_t a_rows; int a_cols; const uint8_t* a_sf;
+  const uint8_t* a2; int64_t a2_rows; const uint8_t* a2_sf;   // identity-ordered A for shared experts
+  const uint8_t* b;  int64_t b_rows; int b_cols; const uint8_t* b_sf;
+};
+
+struct GemmEpilogue {
+  void* out;            // bf16 rows (push / wgrad) or fp32 (plain)
+  void* out2;           // second output (shared-expert wgrad)
+  uint8_t* q_rows; uint8_t* q_rows_sf; int q_rows_ktiles;     // MX along the N axis
+  uint8_t* q_tok;  uint8_t* q_tok_sf;  int64_t q_tok_pitch;   // MX along tokens (transposed)
+  void* gu;             // saved bf16 g|u rows
+  int ldo;              // output row pitch (elements)
+};
+
+int gemm_dispatch(int mode, const Dims& m, int lap, int N, int K, int M, const GemmOperands& op,
+                  const GemmEpilogue& ep, const int* counts, const int* poff, const int* lap_tiles,
+                  const int* row_src, int* status, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,81 @@
+// MXFP8 device helpers: E8M0 block scale and E4M3 element conversion.
+//
+// Reading of "MXFP8" (Cursor blog summary, "method points"): OCP MX v1.0,
+// E4M3 elements, one E8M0 scale per 32 elements, scale byte
+// floor(log2(amax)) - 8 + 127 clamped to [0, 254] (0 for an all-zero block),
+// elements converted by round-to-nearest-even with saturation to +-448.
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+namespace moe {
+
+// Scale byte of a block from its absolute maximum. floor(log2(amax)) is the
+// unbiased exponent field of the fp32 value; subnormal amax clamps to 0.
+__device__ __forceinline__ int mx_scale_byte(float amax) {
+  const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu) - 127;
+  int b = e - 8 + 127;
+  b = b < 0 ? 0 : (b > 254 ? 254 : b);
+  return amax > 0.0f ? b : 0;
+}
+
+// 2^(127 - b) for b in [0, 253] (b <= 246 for any finite fp32 amax).
+__device__ __forceinline__ float mx_inv_scale(int b) { return __uint_as_float(static_cast<uint32_t>(254 - b) << 23); }
+
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
+}
+
+// Quantise 32 values with a common inverse scale into 8 packed words.
+__device__ __forceinline__ void mx_pack32(const float* v, float inv, uint32_t* w) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t a = e4m3x2(v[4 * i] * inv, v[4 * i + 1] * inv);
+    const uint32_t b = e4m3x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv);
+    w[i] = a | (b << 16);
+  }
+}
+
+__device__ __forceinline__ float amax32(const float* v) {
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(v[i]));
+  return m;
+}
+
+__device__ __forceinline__ void store32(uint8_t* dst, const uint32_t* w) {
+  uint4* p = reinterpret_cast<uint4*>(dst);
+  p[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  p[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* v) {
+  const uint4* p = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 u = p[q];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[8 * q + 2 * i] = __uint_as_float(w[i] << 16);
+      v[8 * q + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&p);
+}
+
+// Tiled scale layout offset (see moe_scales_to_tiled in the public header).
+__device__ __forceinline__ int64_t sf_off(int64_t r, int64_t kb, int64_t k_tiles) {
+  return ((r >> 7) * k_tiles + (kb >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (kb & 3);
+}
+
+}  // namespace moe

@@ -1,0 +1,374 @@
+"""GPU parity of the whole layer (route -> schedule -> forward -> backward)
+against the oracle, element by element, at sizes the oracle finishes in
+seconds that still span several tiles, ring laps and ragged tails.
+
+Bars (spec reading): route indices, counts, ranks, permutation and
+quantised bytes bit-exact; bf16 outputs and gradients within relative
+Frobenius error 1e-3 of the oracle on identical quantised operands
+("stage-wise"), and end to end.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gen
+from oracle import layer as OL
+from oracle import mxfp8
+from oracle import route as OR
+from oracle import schedule as OS
+from tests.helpers import np_f64, np_u8, rel_frob, untile_scales
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-3
+
+
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+
+
+def _shapes():
+    return {
+        "tiny": gen.config("tiny"),
+        "ragged": gen.make_shape("ragged", 300, 256, 16, 4, 4, 2, 256, 1, "custom", 0.02, C=128),
+        "wrap_plain": gen.make_shape("wrap_plain", 515, 384, 8, 3, 1, 1, 384, 1, "zero", 0.02, C=128),
+    }
+
+
+def _inputs(shape, seed=0):
+    inp = gen.make_inputs(shape, seed=seed) if shape.bias != "custom" else None
+    if inp is None:
+        s2 = gen.make_shape(shape.name, shape.T, shape.d, shape.E, shape.k, shape.G, shape.g_top, shape.I, shape.S,
+                            "zero", shape.w_std, C=shape.C)
+        inp = gen.make_inputs(s2, seed=seed)
+        b = np.random.default_rng(seed + 11).normal(0, 0.3, shape.E).astype(np.float32)
+        b[5] = -10.0                       # expert 5 is never picked: empty expert
+        inp["bias"] = torch.from_numpy(b)
+    return inp
+
+
+class Run:
+    """GPU run + oracle on the GPU's logits, with helpers to read buffers."""
+
+    def __init__(self, shape, seed=0):
+        from moe_layer_dsv3_gb300.layer import MoELayer
+        self.shape = shape
+        self.inp = _inputs(shape, seed)
+        dev = {k: v.cuda() for k, v in self.inp.items()}
+        self.dev = dev
+        L = MoELayer.from_shape(shape)
+        self.L = L
+        L.quantize_weights(dev["w_gu"], dev["w_d"], dev["ws_gu"], dev["ws_d"])
+        L.forward(dev["x"], dev["w_router"], dev["bias"])
+        L.backward(dev["dy"])
+        torch.cuda.synchronize()
+        assert L.status() == (0, 0)
+        self.host = {k: (v.to(torch.float64).numpy() if v.dtype == torch.bfloat16 else v.numpy())
+                     for k, v in self.inp.items()}
+        self.logits = L.ws_tensor("LOGITS", torch.float32, (shape.T, shape.E)).cpu().numpy()
+        self.f = OL.layer_forward(self.host, shape, logits=self.logits)
+        self.b = OL.layer_backward(self.f, self.host, shape)
+        m = shape
+        self.Ep = m.E + m.S
+        self.A = m.T * m.k
+        self.Ap = m.T * (m.k + m.S)
+        self.Tpad = -(-m.T // 128) * 128
+        self.Rmax = -(-self.Ap // 128) * 128 + 128 * self.Ep
+
+    def ws(self, name, dtype=torch.uint8, shape=None):
+        return self.L.ws_tensor(name, dtype, shape)
+
+    def u8(self, name, rows, cols):
+        return np_u8(self.ws(name, torch.uint8, (rows, cols)))
+
+    def sf(self, name, rows, K):
+        return untile_scales(np_u8(self.ws(name)), rows, K)
+
+    def poff(self):
+        return self.ws("POFF", torch.int32, (self.Ep + 1,)).cpu().numpy().astype(np.int64)
+
+    def expert_rows(self, e):
+        """(assignments a in rank order, padded rows) of expert e (routed or shared)."""
+        m = self.shape
+        po = self.poff()
+        if e < m.E:
+            a = OS.expert_rows(self.f["sched"], e)
+        else:
+            a = self.A + (e - m.E) * m.T + np.arange(m.T)
+        return a, po[e] + np.arange(len(a))
+
+    def token(self, a):
+        m = self.shape
+        a = np.asarray(a)
+        return np.where(a < self.A, a // m.k, (a - self.A) % m.T)
+
+
+@pytest.fixture(scope="module", params=list(_shapes()))
+def run(request):
+    _need_gpu()
+    return Run(_shapes()[request.param])
+
+
+# ------------------------------------------------------------------ route + schedule
+def test_router_logits(run):
+    ref = OR.router_logits(run.host["x"], run.host["w_router"])
+    assert rel_frob(run.logits, ref) < 1e-5
+
+
+def test_route_bit_exact(run):
+    m = run.shape
+    idx = run.L.topk_idx.cpu().numpy()
+    w = run.L.topk_w.cpu().numpy()
+    assert np.array_equal(idx, run.f["idx"])                 # selection on the GPU's logits
+    assert np.array_equal(w.view(np.uint32), run.f["w"].view(np.uint32))
+    ssel = run.ws("SSEL", torch.float32, (m.T, m.k)).cpu().numpy()
+    assert np.array_equal(ssel.view(np.uint32), run.f["s_sel"].view(np.uint32))
+    # end to end against the oracle's own (correctly rounded) logits: only near-ties may differ
+    idx2, _, _, lg2 = OR.route(run.host["x"], run.host["w_router"], run.host["bias"], m.k, m.G, m.g_top)
+    bad = np.flatnonzero((idx2 != idx).any(axis=1))
+    if len(bad):
+        margin = OR.selection_margin(lg2[bad], run.host["bias"], idx2[bad], m.G, m.g_top)
+        assert np.all(margin < 1e-5), margin
+
+
+def test_schedule_bit_exact(run):
+    m = run.shape
+    sch = run.f["sched"]
+    counts = run.ws("COUNTS", torch.int32, (run.Ep,)).cpu().numpy()
+    assert np.array_equal(counts[:m.E], sch["counts"])
+    assert np.all(counts[m.E:] == m.T)
+    offs = run.ws("OFFSETS", torch.int32, (run.Ep + 1,)).cpu().numpy()
+    assert np.array_equal(offs[:m.E + 1], sch["offsets"])
+    rank = run.ws("RANK", torch.int32, (run.Ap,)).cpu().numpy()
+    pos = run.ws("POS", torch.int32, (run.Ap,)).cpu().numpy()
+    inv = run.ws("INV", torch.int32, (run.Ap,)).cpu().numpy()
+    assert np.array_equal(rank[:run.A], sch["rank"])
+    assert np.array_equal(pos[:run.A], sch["pos"])
+    assert np.array_equal(inv[:run.A], sch["inv"])
+    assert np.array_equal(rank[run.A:], np.tile(np.arange(m.T), m.S))       # shared: rank = token
+    assert sorted(pos.tolist()) == list(range(run.Ap))                      # bijection
+    po = run.poff()
+    rs = run.ws("ROWSRC", torch.int32, (run.Rmax,)).cpu().numpy()
+    for e in range(run.Ep):
+        a, rows = run.expert_rows(e)
+        assert np.array_equal(rs[rows], a)
+        assert np.all(rs[po[e] + len(a):po[e + 1]] == -1)
+    meta = run.ws("META", torch.int32, (16,)).cpu().numpy()
+    assert meta[0] == sch["n_laps"] and meta[1] == po[-1]
+
+
+def test_quantised_activation_bytes(run):
+    m = run.shape
+    xq = run.u8("XQ", run.Tpad, m.d)[:m.T]
+    xsf = run.sf("XQ_SF", run.Tpad, m.d)[:m.T]
+    assert np.array_equal(xq, run.f["xq"].codes)
+    assert np.array_equal(xsf, run.f["xq"].scales)
+
+
+def test_ring_holds_last_laps(run):
+    """Ring of expert e after forward: slots of its final lap, and earlier-lap rows behind them."""
+    m = run.shape
+    ring = run.u8("RING_X", m.E * m.C, m.d).reshape(m.E, m.C, m.d)
+    rsf = run.sf("RING_X_SF", m.E * m.C, m.d).reshape(m.E, m.C, m.d // 32)
+    sch = run.f["sched"]
+    xq = run.f["xq"]
+    wrapped = 0
+    for e in range(m.E):
+        n = sch["counts"][e]
+        if n == 0:
+            continue
+        a = OS.expert_rows(sch, e)
+        last = (n - 1) // m.C
+        lo = last * m.C
+        tok = a[lo:] // m.k
+        assert np.array_equal(ring[e, :n - lo], xq.codes[tok])
+        assert np.array_equal(rsf[e, :n - lo], xq.scales[tok])
+        if last > 0:
+            wrapped += 1
+            prev = a[(last - 1) * m.C:last * m.C] // m.k
+            tail = slice(n - lo, -(-(n - lo) // 128) * 128)
+            # rows of the final lap's last tile past the segment are cleared; later slots keep lap last-1
+            assert not ring[e, tail].any()
+            keep = -(-(n - lo) // 128) * 128
+            assert np.array_equal(ring[e, keep:], xq.codes[prev[keep:]])
+    if m.name != "tiny":
+        assert wrapped > 0, "case should exercise ring wrap-around"
+
+
+# ------------------------------------------------------------------ forward stages
+def _expert_weights(run, e):
+    m = run.shape
+    if e < m.E:
+        return run.f["weights"][e], run.f["experts"][e], run.b["experts"][e]
+    s = e - m.E
+    return run.f["shared_weights"][s], run.f["shared"][s], run.b["shared"][s]
+
+
+def test_gemm1_swiglu_stage(run):
+    m = run.shape
+    gu = np_f64(run.ws("GU", torch.bfloat16, (run.Rmax, 2 * m.I)))
+    hq = run.u8("HQ", run.Rmax, m.I)
+    hsf = run.sf("HQ_SF", run.Rmax, m.I)
+    for e in range(run.Ep):
+        a, rows = run.expert_rows(e)
+        if len(a) == 0:
+            continue
+        W, fe, _ = _expert_weights(run, e)
+        xv = run.f["xq"].val[run.token(a)]
+        r = OL.expert_gemm1(xv, W)
+        assert rel_frob(gu[rows], r["gu_saved"]) < TOL, e
+        h_gpu = mxfp8.dequantize(hq[rows], hsf[rows], 1)
+        # MX(h) on both sides: codes differ only where GEMM rounding moves h across an E4M3 rounding point
+        assert rel_frob(h_gpu, mxfp8.roundtrip(r["h"], 1)) < TOL, e
+        # h_q is exactly MX(h) of some h within GEMM rounding: re-quantising the GPU's values is a fixed point
+        q2, s2 = mxfp8.quantize(h_gpu, 1)
+        assert np.array_equal(q2, hq[rows]) and np.array_equal(s2, hsf[rows])
+
+
+def test_gemm2_stage_and_output(run):
+    m = run.shape
+    hq = run.u8("HQ", run.Rmax, m.I)
+    hsf = run.sf("HQ_SF", run.Rmax, m.I)
+    O = np_f64(run.ws("O", torch.bfloat16, (run.Ap, m.d)))
+    for e in range(run.Ep):
+        a, rows = run.expert_rows(e)
+        if len(a) == 0:
+            continue
+        W, _, _ = _expert_weights(run, e)
+        ref = OL.expert_gemm2(mxfp8.dequantize(hq[rows], hsf[rows], 1), W)
+        assert rel_frob(O[a], ref) < TOL, e
+    # combine on the GPU's expert outputs, and end to end
+    y = np_f64(run.L.y)
+    S = O[run.A:].reshape(m.S, m.T, m.d).sum(axis=0) if m.S else np.zeros((m.T, m.d))
+    yc = OL.combine(run.f["w"], O[:run.A].reshape(m.T, m.k, m.d), S)
+    assert rel_frob(y, yc) < 1e-5
+    assert rel_frob(y, run.f["y"]) < TOL
+
+
+# ------------------------------------------------------------------ backward stages
+def test_reverse_combine(run):
+    m = run.shape
+    O = np_f64(run.ws("O", torch.bfloat16, (run.Ap, m.d)))
+    dy = run.host["dy"]
+    dw = run.ws("DW", torch.float32, (m.T, m.k)).cpu().numpy()
+    ref = np.einsum("tc,tjc->tj", dy, O[:run.A].reshape(m.T, m.k, m.d))
+    assert rel_frob(dw, ref) < 1e-6
+    # dO = fp32(w * dy): token-axis bytes bit-exact
+    dtok = run.u8("DOTOK", m.d, run.Rmax)
+    dtsf = run.sf("DOTOK_SF", m.d, run.Rmax)
+    xtok = run.u8("XTOK", m.d, run.Rmax)
+    xtsf = run.sf("XTOK_SF", m.d, run.Rmax)
+    po = run.poff()
+    for e in range(run.Ep):
+        a, rows = run.expert_rows(e)
+        seg = slice(po[e], po[e + 1])
+        n_pad = po[e + 1] - po[e]
+        if e < m.E:
+            dO = run.b["dO"][a]
+        else:
+            dO = dy
+        q, s = mxfp8.quantize_tokens(dO, n_pad)
+        assert np.array_equal(dtok[:, seg], q) and np.array_equal(dtsf[:, po[e] // 32:po[e + 1] // 32], s), e
+        q, s = mxfp8.quantize_tokens(run.host["x"][run.token(a)], n_pad)
+        assert np.array_equal(xtok[:, seg], q) and np.array_equal(xtsf[:, po[e] // 32:po[e + 1] // 32], s), e
+
+
+def test_dO_ring_holds_last_laps(run):
+    m = run.shape
+    ring = run.u8("RING_DO", m.E * m.C, m.d).reshape(m.E, m.C, m.d)
+    rsf = run.sf("RING_DO_SF", m.E * m.C, m.d).reshape(m.E, m.C, m.d // 32)
+    sch = run.f["sched"]
+    for e in range(m.E):
+        n = sch["counts"][e]
+        if n == 0:
+            continue
+        last = (n - 1) // m.C
+        dq = run.b["experts"][e]["dOq"]
+        assert np.array_equal(ring[e, :n - last * m.C], dq.codes[last * m.C:])
+        assert np.array_equal(rsf[e, :n - last * m.C], dq.scales[last * m.C:])
+
+
+def test_dgrad_down_swiglu_stage(run):
+    m = run.shape
+    gu = np_f64(run.ws("GU", torch.bfloat16, (run.Rmax, 2 * m.I)))
+    dq = run.u8("DGU", run.Rmax, 2 * m.I)
+    dsf = run.sf("DGU_SF", run.Rmax, 2 * m.I)
+    for e in range(run.Ep):
+        a, rows = run.expert_rows(e)
+        if len(a) == 0:
+            continue
+        W, _, be = _expert_weights(run, e)
+        dOv = be["dOq"].val                        # identical bytes on both sides (bit-exact checks above)
+        r = OL.expert_backward(dOv, gu[rows], W)
+        got = mxfp8.dequantize(dq[rows], dsf[rows], 1)
+        assert rel_frob(got, mxfp8.roundtrip(r["dgu"], 1)) < TOL, e
+
+
+def test_dgrad_gate_up_stage(run):
+    m = run.shape
+    dq = run.u8("DGU", run.Rmax, 2 * m.I)
+    dsf = run.sf("DGU_SF", run.Rmax, 2 * m.I)
+    DX = np_f64(run.ws("DXE", torch.bfloat16, (run.Ap, m.d)))
+    for e in range(run.Ep):
+        a, rows = run.expert_rows(e)
+        if len(a) == 0:
+            continue
+        W, _, _ = _expert_weights(run, e)
+        ref = OL.bf16(mxfp8.dequantize(dq[rows], dsf[rows], 1) @ W.gu_bwd.val.T)
+        assert rel_frob(DX[a], ref) < TOL, e
+
+
+def test_wgrad_stage(run):
+    m = run.shape
+    po = run.poff()
+    dtok = mxfp8.dequantize(run.u8("DOTOK", m.d, run.Rmax), run.sf("DOTOK_SF", m.d, run.Rmax), 1)
+    htok = mxfp8.dequantize(run.u8("HTOK", m.I, run.Rmax), run.sf("HTOK_SF", m.I, run.Rmax), 1)
+    gtok = mxfp8.dequantize(run.u8("DGUTOK", 2 * m.I, run.Rmax), run.sf("DGUTOK_SF", 2 * m.I, run.Rmax), 1)
+    xtok = mxfp8.dequantize(run.u8("XTOK", m.d, run.Rmax), run.sf("XTOK_SF", m.d, run.Rmax), 1)
+    for e in range(run.Ep):
+        seg = slice(po[e], po[e + 1])
+        if e < m.E:
+            gd, ggu = np_f64(run.L.dw_d[e]), np_f64(run.L.dw_gu[e])
+        else:
+            gd, ggu = np_f64(run.L.dws_d[e - m.E]), np_f64(run.L.dws_gu[e - m.E])
+        ref_d = OL.bf16(dtok[:, seg] @ htok[:, seg].T)
+        ref_gu = OL.bf16(gtok[:, seg] @ xtok[:, seg].T)
+        if po[e + 1] == po[e]:
+            assert not gd.any() and not ggu.any()
+            continue
+        assert rel_frob(gd, ref_d) < TOL, e
+        assert rel_frob(ggu, ref_gu) < TOL, e
+
+
+def test_backward_end_to_end(run):
+    m = run.shape
+    b = run.b
+    assert rel_frob(np_f64(run.L.dx), b["dx"]) < TOL * 5
+    assert rel_frob(np_f64(run.L.dw_router), b["dw_router"]) < TOL * 5
+    assert rel_frob(np_f64(run.L.dw_d), b["dW_d"]) < TOL * 5
+    assert rel_frob(np_f64(run.L.dw_gu), b["dW_gu"]) < TOL * 5
+    if m.S:
+        assert rel_frob(np_f64(run.L.dws_d[:m.S]), b["dWs_d"]) < TOL * 5
+        assert rel_frob(np_f64(run.L.dws_gu[:m.S]), b["dWs_gu"]) < TOL * 5
+
+
+def test_router_backward_stage(run):
+    """dW_r and the router term of dx from the GPU's own gate gradients."""
+    m = run.shape
+    dw = run.ws("DW", torch.float32, (m.T, m.k)).cpu().numpy()
+    rb = OL.router_backward(dw, run.f["w"], run.f["s_sel"], run.f["idx"], run.host["x"], run.host["w_router"], m.E)
+    dl = run.ws("DL", torch.float32, (m.T, m.k)).cpu().numpy()
+    assert rel_frob(dl, rb["dl"]) < 1e-5
+    assert rel_frob(np_f64(run.L.dw_router), OL.bf16(rb["dw_router"])) < TOL
+
+
+def test_deterministic_rerun(run):
+    L, dev = run.L, run.dev
+    outs1 = [t.clone() for t in (L.y, L.dx, L.dw_router, L.dw_gu, L.dw_d, L.dws_gu, L.dws_d, L.topk_w)]
+    L.forward(dev["x"], dev["w_router"], dev["bias"])
+    L.backward(dev["dy"])
+    torch.cuda.synchronize()
+    outs2 = (L.y, L.dx, L.dw_router, L.dw_gu, L.dw_d, L.dws_gu, L.dws_d, L.topk_w)
+    for a, b in zip(outs1, outs2):
+        assert torch.equal(a.view(torch.uint8) if a.dtype != torch.float32 else a.view(torch.int32),
+                           b.view(torch.uint8) if b.dtype != torch.float32 else b.view(torch.int32))
