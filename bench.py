@@ -1,0 +1,473 @@
+#!/usr/bin/env python
+"""Benchmark of the MXFP8 DSV3-style MoE layer, forward + backward, on GB300.
+
+One step = route -> schedule -> forward -> backward of one synthetic batch
+(every row of the hot path). Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload dsv3_zipf|dsv3_fwd|small|tiny|e384] [--T tokens]
+
+N > 1 runs under torch.distributed.run, one rank per GPU, each rank an
+independent replica of the layer on its own batch ("replicas only": the
+layer has no exchange step on one GPU, so no collective is on the data path;
+scaling is weak). `--impl reference` times the CPU oracle on a bounded
+sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import gen  # noqa: E402
+
+METRIC = "MoE-layer tokens/s fwd+bwd MXFP8 (1xGB300)"
+
+
+# ---------------------------------------------------------------- helpers
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16": d["bf16_tflops"], "bf16_sus": d["bf16_tflops_sustained"],
+                "src": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sus": 1700.0, "src": "fallback"}
+
+
+def gemm_flops(shape):
+    """Algorithmic FLOPs per step of each grouped GEMM (rows = all expert assignments)."""
+    R = shape.T * (shape.k + shape.S)
+    d, I = shape.d, shape.I
+    return {
+        "gemm1_fwd": 2.0 * R * 2 * I * d,
+        "gemm2_fwd": 2.0 * R * d * I,
+        "gemm_dgrad_down": 2.0 * R * I * d,
+        "gemm_dgrad_gu": 2.0 * R * d * 2 * I,
+        "gemm_wgrad_d": 2.0 * d * I * R,
+        "gemm_wgrad_gu": 2.0 * 2 * I * d * R,
+        "router_gemm": 2.0 * shape.T * shape.E * d,
+    }
+
+
+def hbm_bytes(shape):
+    """Algorithmic bytes per step of the memory-bound kernels (read + write, once)."""
+    T, d, k, S, E = shape.T, shape.d, shape.k, shape.S, shape.E
+    Rr = T * k                    # routed rows (ring traffic)
+    R = T * (k + S)
+    row_q = d + d // 32           # one MX row (codes + scales)
+    return {
+        "permute_lap": 2.0 * Rr * row_q,
+        "combine": T * (k + S) * d * 2.0 + T * k * 4.0 + T * d * 2.0,
+        "rev_combine_dw": T * k * d * 2.0 + T * d * 2.0 + T * k * 12.0,
+        "rev_combine_lap": Rr * d * 2.0 + Rr * row_q,
+        "reverse_dispatch": T * (k + S) * d * 2.0 + T * k * 12.0 + T * d * 2.0,
+        "tok_gather_x": R * d * 2.0 + R * row_q,
+        "tok_gather_dO": R * d * 2.0 + R * row_q,
+        "quant_rows": T * d * 2.0 * (1 + S) + T * row_q * (1 + S),
+    }
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = None
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- CPU oracle sample
+def oracle_sample(shape, host, idx_full=None, n_experts=2, shared_rows=256, seed=0):
+    """Time the CPU oracle on a bounded sample of one layer step and extrapolate.
+
+    Sample: router logits + selection for 1024 tokens, the schedule of all
+    tokens, the full forward+backward of `n_experts` routed experts of
+    near-average load (all their rows) and of the shared expert on
+    `shared_rows` tokens, and combine + router backward for 1024 tokens.
+    Each timed part is scaled by the share of the step it stands for. Weight
+    MX quantisation is done before timing (it is not part of a layer step).
+    Returns (tokens/s, description).
+    """
+    from oracle import layer as OL
+    from oracle import mxfp8
+    from oracle import route as OR
+    from oracle import schedule as OS
+
+    T, d, E, k, I, S = shape.T, shape.d, shape.E, shape.k, shape.I, shape.S
+    x = host["x"]
+    nt = min(1024, T)
+    t0 = time.perf_counter()
+    idx_s, w_s, s_s, lg = OR.route(x[:nt], host["w_router"], host["bias"], k, shape.G, shape.g_top)
+    t_route = (time.perf_counter() - t0) * T / nt
+    if idx_full is None:
+        idx_full, _, _, _ = OR.route(x, host["w_router"], host["bias"], k, shape.G, shape.g_top)
+    t0 = time.perf_counter()
+    sch = OS.schedule(idx_full, E, shape.C)
+    t_sched = time.perf_counter() - t0
+    counts = sch["counts"]
+    order = np.argsort(np.abs(counts - counts.mean()), kind="stable")
+    experts = [int(e) for e in order[:n_experts] if counts[e] > 0]
+    rng = np.random.default_rng(seed)
+    prepared = []
+    for e in experts:
+        wgu = host["w_gu_of"](e)
+        wd = host["w_d_of"](e)
+        prepared.append(("routed", e, OL.ExpertWeights(wgu, wd), OS.expert_rows(sch, e) // k))
+    if S:
+        toks = np.sort(rng.choice(T, min(shared_rows, T), replace=False))
+        prepared.append(("shared", E, OL.ExpertWeights(host["ws_gu_of"](0), host["ws_d_of"](0)), toks))
+    dy = host["dy"]
+    rows_done = 0
+    t0 = time.perf_counter()
+    for kind, e, W, toks in prepared:
+        xq = OL.Q(x[toks], 1, False)
+        r = OL.expert_forward(xq.val, W)
+        dO = dy[toks].astype(np.float32).astype(np.float64)
+        dOq = OL.Q(dO, 1, False)
+        b = OL.expert_backward(dOq.val, r["gu_saved"], W)
+        OL.wgrad(OL.tokq(dO, False), OL.tokq(r["h"], False))
+        OL.wgrad(OL.tokq(b["dgu"], False), OL.tokq(x[toks], False))
+        rows_done += len(toks)
+    t_exp = time.perf_counter() - t0
+    R = T * (k + S)
+    t0 = time.perf_counter()
+    O = np.zeros((nt, k, d))
+    OL.combine(w_s, O, np.zeros((nt, d)))
+    OL.router_backward(np.zeros((nt, k)), w_s, s_s, idx_s, x[:nt], host["w_router"], E)
+    t_comb = (time.perf_counter() - t0) * T / nt
+    total = t_route + t_sched + t_exp * R / max(rows_done, 1) + t_comb
+    desc = ("router on %d tokens, schedule of all %d tokens, fwd+bwd of %d routed experts (%d rows) and the "
+            "shared expert on %d tokens, combine/router-bwd on %d tokens; extrapolated to the %d-row step"
+            % (nt, T, len(experts), rows_done - (len(prepared[-1][3]) if S else 0), len(prepared[-1][3]) if S else 0,
+               nt, R))
+    return T / total, desc
+
+
+def host_inputs_for_oracle(shape, dev_inputs):
+    """Host copies the oracle sample needs; expert weights fetched one expert at a time."""
+    h = {
+        "x": dev_inputs["x"].float().cpu().numpy().astype(np.float64),
+        "dy": dev_inputs["dy"].float().cpu().numpy().astype(np.float64),
+        "w_router": dev_inputs["w_router"].float().cpu().numpy().astype(np.float64),
+        "bias": dev_inputs["bias"].cpu().numpy(),
+    }
+    h["w_gu_of"] = lambda e: dev_inputs["w_gu"][e].float().cpu().numpy().astype(np.float64)
+    h["w_d_of"] = lambda e: dev_inputs["w_d"][e].float().cpu().numpy().astype(np.float64)
+    h["ws_gu_of"] = lambda e: dev_inputs["ws_gu"][e].float().cpu().numpy().astype(np.float64)
+    h["ws_d_of"] = lambda e: dev_inputs["ws_d"][e].float().cpu().numpy().astype(np.float64)
+    return h
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def workload_config(shape, extra=None):
+    c = {"workload": "%s: T=%d d=%d E=%d(+%d shared) top-%d groups %d/%d I=%d ring C=%d bias %s"
+         % (shape.name, shape.T, shape.d, shape.E, shape.S, shape.k, shape.G, shape.g_top, shape.I, shape.C,
+            shape.bias),
+         "T": shape.T, "d": shape.d, "E": shape.E, "n_shared": shape.S, "k": shape.k, "I": shape.I,
+         "ring_capacity": shape.C, "l2": "inputs larger than L2 (x, dy 2*T*d bytes each; weights >10 GB)",
+         "parallelism": "replicas"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    shape = gen.config(args.workload, T=args.T)
+    inp = gen.make_inputs(shape, seed=0, device="cpu", weights=False)
+    host = {
+        "x": inp["x"].double().numpy(), "dy": inp["dy"].double().numpy(),
+        "w_router": inp["w_router"].double().numpy(), "bias": inp["bias"].numpy(),
+    }
+    # Expert weights: same shapes and distribution, drawn per expert from their own seed
+    # (the oracle sample touches only a few experts).
+    def wgen(e, shp, shared=False):
+        g = torch.Generator().manual_seed(1000 + e + (100000 if shared else 0))
+        return (torch.randn(shp, generator=g) * shape.w_std).to(torch.bfloat16).double().numpy()
+    host["w_gu_of"] = lambda e: wgen(e, (2 * shape.I, shape.d))
+    host["w_d_of"] = lambda e: wgen(e + 5000, (shape.d, shape.I))
+    host["ws_gu_of"] = lambda e: wgen(e, (2 * shape.I, shape.d), True)
+    host["ws_d_of"] = lambda e: wgen(e + 5000, (shape.d, shape.I), True)
+    from oracle import route as OR
+    idx_full, _, _, _ = OR.route(host["x"], host["w_router"], host["bias"], shape.k, shape.G, shape.g_top)
+    vals = []
+    desc = ""
+    for i in range(args.warmup + args.steps):
+        v, desc = oracle_sample(shape, host, idx_full=idx_full, n_experts=1, shared_rows=128, seed=i)
+        if i >= args.warmup:
+            vals.append(v)
+    val = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * shape.T / val,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(shape),
+            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores(), "kind": "oracle", "sample": desc},
+            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local_rank):
+    import moe_layer_dsv3_gb300 as M
+    from moe_layer_dsv3_gb300.layer import MoELayer
+
+    torch.cuda.set_device(local_rank)
+    shape = gen.config(args.workload, T=args.T)
+    inp = gen.make_inputs(shape, seed=rank, device="cuda")
+    L = MoELayer.from_shape(shape)
+    L.quantize_weights(inp["w_gu"], inp["w_d"], inp["ws_gu"], inp["ws_d"])
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    x, dy, wr, bias = inp["x"], inp["dy"], inp["w_router"], inp["bias"]
+
+    def step():
+        L.forward(x, wr, bias, sp)
+        L.backward(dy, sp)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    code, site = L.status()
+    if code:
+        raise RuntimeError("device status %d at site %d after warm-up" % (code, site))
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    # ---- timed region: K steps, inputs resident in HBM
+    clocks = ClockSampler(local_rank)
+    M.moe_profile_enable(True)
+    M.moe_profile_read()
+    n0 = M.moe_launch_count()
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    launches = M.moe_launch_count() - n0
+    kern = M.moe_profile_read()
+    M.moe_profile_enable(False)
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    value = shape.T * world / (ms_step / 1000.0)
+
+    # ---- per-stage split (one extra, separately timed step)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    ev[0].record(stream)
+    L.route(x, wr, bias, sp)
+    ev[1].record(stream)
+    L.schedule(sp)
+    ev[2].record(stream)
+    L.forward_experts(x, sp)
+    ev[3].record(stream)
+    L.backward(dy, sp)
+    ev[4].record(stream)
+    torch.cuda.synchronize()
+    stages = {n: ev[i].elapsed_time(ev[i + 1]) for i, n in enumerate(("route", "schedule", "forward", "backward"))}
+
+    # ---- end to end through the C ABI with host buffers (H2D of x, dy; D2H of y, dx)
+    xh = x.cpu().pin_memory()
+    dyh = dy.cpu().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    dxh = torch.empty_like(xh).pin_memory()
+    xd, dyd = torch.empty_like(x), torch.empty_like(dy)
+
+    def e2e_step():
+        xd.copy_(xh, non_blocking=True)
+        dyd.copy_(dyh, non_blocking=True)
+        L.forward(xd, wr, bias, sp)
+        L.backward(dyd, sp)
+        yh.copy_(L.y, non_blocking=True)
+        dxh.copy_(L.dx, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms_e2e], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+    code, site = L.status()
+    if code:
+        raise RuntimeError("device status %d at site %d" % (code, site))
+    if rank != 0:
+        return
+
+    # ---- roofline of the dominant kernel and per-kernel summary
+    pk = peaks()
+    fl = gemm_flops(shape)
+    hb = hbm_bytes(shape)
+    per_kernel = {}
+    for name, (n, tms) in sorted(kern.items(), key=lambda kv: -kv[1][1]):
+        ent = {"launches": n, "ms_per_step": tms / args.steps, "share": tms / ms if ms > 0 else None}
+        if name in fl:
+            ent["tflops"] = fl[name] * args.steps / (tms / 1000.0) / 1e12
+        if name in hb:
+            ent["gbs"] = hb[name] * args.steps / (tms / 1000.0) / 1e9
+        per_kernel[name] = ent
+    dom = max(kern.items(), key=lambda kv: kv[1][1])[0]
+    fp8_peak = 2.0 * pk["bf16_sus"]
+    if dom in fl:
+        achieved = per_kernel[dom]["tflops"]
+        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
+                "frac": achieved / fp8_peak, "traffic": None,
+                "peak_note": "dense MXFP8 = 2 x %s sustained bf16 (%s TFLOP/s), the nominal fp8/bf16 ratio"
+                             % ("measured" if pk["src"] == "measured" else "fallback", pk["bf16_sus"]),
+                "flop_per_step": fl[dom]}
+    else:
+        achieved = per_kernel[dom].get("gbs", 0.0)
+        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"], "traffic": None}
+    traffic_file = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(traffic_file):
+        with open(traffic_file) as f:
+            tr = json.load(f)
+        ent = tr.get(shape.name, {}).get(dom)
+        if ent is not None:
+            roof["traffic"] = ent
+    gemm_names = [n for n in fl if n in kern and n != "router_gemm"]
+    gemm_ms = sum(kern[n][1] for n in gemm_names) / args.steps
+    gemm_tflops = sum(fl[n] for n in gemm_names) / (gemm_ms / 1000.0) / 1e12 if gemm_ms else None
+    perm = per_kernel.get("permute_lap", {}).get("gbs")
+    extra = {
+        "stages_ms": stages,
+        "grouped_gemm_tflops": gemm_tflops,
+        "grouped_gemm_frac_fp8_peak": gemm_tflops / fp8_peak if gemm_tflops else None,
+        "permute_gbs": perm,
+        "permute_frac_hbm": perm / pk["hbm_gbs"] if perm else None,
+        "schedule_share": (stages["schedule"]) / sum(stages.values()),
+        "kernels": per_kernel,
+    }
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        host = host_inputs_for_oracle(shape, inp)
+        idx = L.topk_idx.cpu().numpy()
+        v, desc = oracle_sample(shape, host, idx_full=idx)
+        cpu = {"value": v, "unit": "tokens/s", "cores": cores(), "kind": "oracle", "sample": desc}
+    counts = L.ws_tensor("COUNTS", torch.int32, (shape.E + shape.S,)).cpu().numpy()[:shape.E]
+    extra["routing"] = {"max_count": int(counts.max()), "min_count": int(counts.min()),
+                        "laps": int(L.ws_tensor("META", torch.int32, (16,))[0].item()),
+                        "ring_capacity": shape.C}
+    h2d = 2 * x.numel() * x.element_size()
+    d2h = 2 * x.numel() * x.element_size()
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "mxfp8", "data": "synthetic (seeded, random-init weights)",
+        "config": workload_config(shape),
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": shape.T * world / (ms_e2e / 1000.0), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    line.update(extra)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="dsv3_zipf")
+    ap.add_argument("--T", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -54,10 +54,10 @@ def _ceil(a: int, b: int) -> int:
 
 def make_shape(name: str, T: int, d: int, E: int, k: int, G: int, g_top: int,
                I: int, S: int, bias: str, w_std: float, C: int | None = None) -> LayerShape:
-    # Default capacity: every token may pick an expert at most once, so
-    # n_e <= T; ceil128(T) therefore never wraps.
+    # Default ring capacity per routed expert: twice the mean load, rounded
+    # to the 128-row tile (the layer's own default). Hot experts wrap.
     if C is None:
-        C = max(128, _ceil(T, 128))
+        C = max(128, _ceil(-(-2 * T * k // E), 128))
     return LayerShape(name, T, d, E, k, G, g_top, I, S, C, bias, w_std)
 
 

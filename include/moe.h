@@ -216,6 +216,22 @@ MOE_API int moe_gemm_mxfp8(int M, int N, int K, const void* a, const void* a_sf,
  * rows, K multiples of 128. */
 MOE_API int moe_scales_to_tiled(const void* canon, int rows, int K, void* tiled, moe_stream_t stream);
 
+/* Measurement hooks (process-wide, for benchmarks; not part of the layer).
+ * moe_profile_enable(1): every kernel launch of the library is bracketed by a
+ * pair of CUDA events recorded on its launch stream (events come from a pool
+ * created here; no device memory is allocated). moe_profile_read synchronises
+ * the recorded events and returns, per kernel name, the number of launches
+ * and their total device time in milliseconds, then clears the records.
+ * moe_launch_count: kernels launched by the library since it was loaded. */
+typedef struct moe_kernel_time {
+  char name[32];
+  int launches;
+  double ms;
+} moe_kernel_time_t;
+MOE_API int moe_profile_enable(int enable);
+MOE_API int moe_profile_read(moe_kernel_time_t* out, int max_entries, int* n_entries);
+MOE_API long long moe_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -70,11 +70,18 @@ _SIGS = {
     "moe_wq_view": [_CFG, _P, _I, ctypes.POINTER(_P), _SZ],
     "moe_gemm_mxfp8": [_I, _I, _I, _P, _P, _P, _P, _P, _P],
     "moe_scales_to_tiled": [_P, _I, _I, _P, _P],
+    "moe_profile_enable": [_I],
+    "moe_profile_read": [ctypes.c_void_p, _I, ctypes.POINTER(_I)],
+    "moe_launch_count": [],
 }
 for _name, _args in _SIGS.items():
     _fn = getattr(_lib, _name)
     _fn.argtypes = _args
-    _fn.restype = ctypes.c_int
+    _fn.restype = ctypes.c_longlong if _name == "moe_launch_count" else ctypes.c_int
+
+
+class MoeKernelTime(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_int), ("ms", ctypes.c_double)]
 
 
 def exported_symbols():
@@ -161,3 +168,19 @@ def moe_gemm_mxfp8(M, N, K, a, a_sf, b, b_sf, c, stream=0):
 
 def moe_scales_to_tiled(canon, rows, K, tiled, stream=0):
     _check("moe_scales_to_tiled", _lib.moe_scales_to_tiled(_p(canon), rows, K, _p(tiled), _p(stream)))
+
+
+def moe_profile_enable(enable=True):
+    _check("moe_profile_enable", _lib.moe_profile_enable(1 if enable else 0))
+
+
+def moe_profile_read(max_entries=64):
+    """{kernel name: (launches, total ms)} of the launches recorded since the last read."""
+    buf = (MoeKernelTime * max_entries)()
+    n = ctypes.c_int()
+    _check("moe_profile_read", _lib.moe_profile_read(ctypes.cast(buf, ctypes.c_void_p), max_entries, ctypes.byref(n)))
+    return {buf[i].name.decode(): (buf[i].launches, buf[i].ms) for i in range(min(n.value, max_entries))}
+
+
+def moe_launch_count():
+    return int(_lib.moe_launch_count())

@@ -311,7 +311,7 @@ int moe_forward(const moe_config_t* cfg, const void* x, const void* wq, const fl
   ep1.q_tok_pitch = m.Rmax;
   for (int lap = 0; lap < m.Lb; ++lap) {
     launch_permute_lap(m, lap, L, ws, s);
-    if (int r = gemm_dispatch(kSwigluFwd, m, lap, 2 * m.I, m.d, 0, op1, ep1, counts, poff, lap_tiles, row_src, status, s))
+    if (int r = gemm_dispatch("gemm1_fwd", kSwigluFwd, m, lap, 2 * m.I, m.d, 0, op1, ep1, counts, poff, lap_tiles, row_src, status, s))
       return r;
   }
   GemmOperands op2{};
@@ -326,7 +326,7 @@ int moe_forward(const moe_config_t* cfg, const void* x, const void* wq, const fl
   GemmEpilogue ep2{};
   ep2.out = ws_ptr<void>(L, ws, MOE_WS_O);
   ep2.ldo = m.d;
-  if (int r = gemm_dispatch(kPush, m, 0, m.d, m.I, 0, op2, ep2, counts, poff, lap_tiles, row_src, status, s)) return r;
+  if (int r = gemm_dispatch("gemm2_fwd", kPush, m, 0, m.d, m.I, 0, op2, ep2, counts, poff, lap_tiles, row_src, status, s)) return r;
   launch_combine(m, topk_w, L, ws, y, s);
   return launch_status();
 }
@@ -400,7 +400,7 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
   epb2.q_tok_pitch = m.Rmax;
   for (int lap = 0; lap < m.Lb; ++lap) {
     launch_rev_combine_lap(m, lap, dy, topk_w, L, ws, s);
-    if (int r = gemm_dispatch(kSwigluBwd, m, lap, m.I, m.d, 0, opb2, epb2, counts, poff, lap_tiles, row_src, status, s))
+    if (int r = gemm_dispatch("gemm_dgrad_down", kSwigluBwd, m, lap, m.I, m.d, 0, opb2, epb2, counts, poff, lap_tiles, row_src, status, s))
       return r;
   }
   // dgrad of GEMM1: DX rows pushed to their assignment.
@@ -416,7 +416,7 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
   GemmEpilogue epb4{};
   epb4.out = ws_ptr<void>(L, ws, MOE_WS_DXE);
   epb4.ldo = m.d;
-  if (int r = gemm_dispatch(kPush, m, 0, m.d, 2 * m.I, 0, opb4, epb4, counts, poff, lap_tiles, row_src, status, s))
+  if (int r = gemm_dispatch("gemm_dgrad_gu", kPush, m, 0, m.d, 2 * m.I, 0, opb4, epb4, counts, poff, lap_tiles, row_src, status, s))
     return r;
   // Weight gradients: K = the expert's ranks (token axis), all laps at once.
   GemmOperands opw{};
@@ -432,7 +432,7 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
   epw.out = dw_d;
   epw.out2 = dws_d;
   epw.ldo = m.I;
-  if (int r = gemm_dispatch(kWgrad, m, 0, m.I, 0, m.d, opw, epw, counts, poff, lap_tiles, row_src, status, s)) return r;
+  if (int r = gemm_dispatch("gemm_wgrad_d", kWgrad, m, 0, m.I, 0, m.d, opw, epw, counts, poff, lap_tiles, row_src, status, s)) return r;
   opw.a = ws_ptr<uint8_t>(L, ws, MOE_WS_DGUTOK);
   opw.a_rows = 2 * m.I;
   opw.a_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_DGUTOK_SF);
@@ -442,7 +442,7 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
   epw.out = dw_gu;
   epw.out2 = dws_gu;
   epw.ldo = m.d;
-  if (int r = gemm_dispatch(kWgrad, m, 0, m.d, 0, 2 * m.I, opw, epw, counts, poff, lap_tiles, row_src, status, s))
+  if (int r = gemm_dispatch("gemm_wgrad_gu", kWgrad, m, 0, m.d, 0, 2 * m.I, opw, epw, counts, poff, lap_tiles, row_src, status, s))
     return r;
   // Reverse-dispatch (+ router input gradient) and the router weight gradient.
   launch_reverse_dispatch(m, topk_idx, w_router, L, ws, dx, s);

@@ -4,6 +4,7 @@
 #include <mutex>
 
 #include "gemm.cuh"
+#include "prof.h"
 
 namespace moe {
 
@@ -39,8 +40,8 @@ bool make_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int
 }
 
 template <int BN, int MODE>
-int run(const CUtensorMap& ta, const CUtensorMap& ta2, const CUtensorMap& tb, const GemmParams& p, int grid,
-        cudaStream_t s) {
+int run(const char* name, const CUtensorMap& ta, const CUtensorMap& ta2, const CUtensorMap& tb, const GemmParams& p,
+        int grid, cudaStream_t s) {
   using Cf = GemmCfg<BN, MODE>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
@@ -49,6 +50,7 @@ int run(const CUtensorMap& ta, const CUtensorMap& ta2, const CUtensorMap& tb, co
   });
   if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
   if (grid <= 0) return MOE_OK;
+  Prof prof(name, s);
   gemm_kernel<BN, MODE><<<grid, 192, Cf::kSmem, s>>>(ta, ta2, tb, p);
   return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -66,7 +68,7 @@ int num_sms() {
 }
 
 // Dispatch one grouped GEMM. Returns an MOE_* code.
-int gemm_dispatch(int mode, const Dims& m, int lap, int N, int K, int M, const GemmOperands& op,
+int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int K, int M, const GemmOperands& op,
                   const GemmEpilogue& ep, const int* counts, const int* poff, const int* lap_tiles,
                   const int* row_src, int* status, cudaStream_t s) {
   if (!get_encode()) return MOE_ERR_CUDA;
@@ -134,18 +136,18 @@ int gemm_dispatch(int mode, const Dims& m, int lap, int N, int K, int M, const G
   const int grid = static_cast<int>(upper < num_sms() ? upper : num_sms());
 
   switch (mode) {
-    case kSwigluFwd: return run<256, kSwigluFwd>(ta, ta2, tb, p, grid, s);
+    case kSwigluFwd: return run<256, kSwigluFwd>(name, ta, ta2, tb, p, grid, s);
     case kSwigluBwd:
-      return BN == 256 ? run<256, kSwigluBwd>(ta, ta2, tb, p, grid, s) : run<128, kSwigluBwd>(ta, ta2, tb, p, grid, s);
+      return BN == 256 ? run<256, kSwigluBwd>(name, ta, ta2, tb, p, grid, s) : run<128, kSwigluBwd>(name, ta, ta2, tb, p, grid, s);
     case kPush:
-      return BN == 256 ? run<256, kPush>(ta, ta2, tb, p, grid, s) : run<128, kPush>(ta, ta2, tb, p, grid, s);
+      return BN == 256 ? run<256, kPush>(name, ta, ta2, tb, p, grid, s) : run<128, kPush>(name, ta, ta2, tb, p, grid, s);
     case kWgrad:
-      return BN == 256 ? run<256, kWgrad>(ta, ta2, tb, p, grid, s) : run<128, kWgrad>(ta, ta2, tb, p, grid, s);
+      return BN == 256 ? run<256, kWgrad>(name, ta, ta2, tb, p, grid, s) : run<128, kWgrad>(name, ta, ta2, tb, p, grid, s);
     case kPlain:
-      return BN == 256 ? run<256, kPlain>(ta, ta2, tb, p, grid, s) : run<128, kPlain>(ta, ta2, tb, p, grid, s);
+      return BN == 256 ? run<256, kPlain>(name, ta, ta2, tb, p, grid, s) : run<128, kPlain>(name, ta, ta2, tb, p, grid, s);
     case kRouterMode:
-      if (BN == 32) return run<32, kRouterMode>(ta, ta2, tb, p, grid, s);
-      return BN == 256 ? run<256, kRouterMode>(ta, ta2, tb, p, grid, s) : run<128, kRouterMode>(ta, ta2, tb, p, grid, s);
+      if (BN == 32) return run<32, kRouterMode>(name, ta, ta2, tb, p, grid, s);
+      return BN == 256 ? run<256, kRouterMode>(name, ta, ta2, tb, p, grid, s) : run<128, kRouterMode>(name, ta, ta2, tb, p, grid, s);
     default: return MOE_ERR_INVALID_ARG;
   }
 }
@@ -169,6 +171,6 @@ extern "C" int moe_gemm_mxfp8(int M, int N, int K, const void* a, const void* a_
   moe::GemmEpilogue ep{};
   ep.out = c;
   ep.ldo = N;
-  return moe::gemm_dispatch(moe::kPlain, m, 0, N, K, M, op, ep, nullptr, nullptr, nullptr, nullptr, nullptr,
+  return moe::gemm_dispatch("gemm_plain", moe::kPlain, m, 0, N, K, M, op, ep, nullptr, nullptr, nullptr, nullptr, nullptr,
                             static_cast<cudaStream_t>(stream));
 }

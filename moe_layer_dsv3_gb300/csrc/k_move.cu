@@ -10,6 +10,7 @@
 #include "moe_internal.h"
 #include "mx.cuh"
 #include "ptx.cuh"
+#include "prof.h"
 
 namespace moe {
 
@@ -274,6 +275,7 @@ __global__ void router_dwr_kernel(const float* __restrict__ part, const int* __r
 void launch_permute_lap(const Dims& m, int lap, const Layout& L, void* ws, cudaStream_t s) {
   const int blocks = m.E * (m.C / 128);
   if (blocks == 0) return;
+  Prof prof("permute_lap", s);
   permute_lap_kernel<<<blocks, 256, 0, s>>>(
       ws_ptr<uint8_t>(L, ws, MOE_WS_XQ), ws_ptr<uint8_t>(L, ws, MOE_WS_XQ_SF), ws_ptr<int>(L, ws, MOE_WS_LAPTILES),
       ws_ptr<int>(L, ws, MOE_WS_COUNTS), ws_ptr<int>(L, ws, MOE_WS_POFF), ws_ptr<int>(L, ws, MOE_WS_ROWSRC), m.T, m.k,
@@ -284,6 +286,7 @@ void launch_rev_combine_lap(const Dims& m, int lap, const void* dy, const float*
                             cudaStream_t s) {
   const int blocks = m.E * (m.C / 128);
   if (blocks == 0) return;
+  Prof prof("rev_combine_lap", s);
   rev_combine_lap_kernel<<<blocks, 256, 0, s>>>(
       static_cast<const __nv_bfloat16*>(dy), topk_w, ws_ptr<int>(L, ws, MOE_WS_LAPTILES),
       ws_ptr<int>(L, ws, MOE_WS_COUNTS), ws_ptr<int>(L, ws, MOE_WS_POFF), ws_ptr<int>(L, ws, MOE_WS_ROWSRC), m.T, m.k,
@@ -293,6 +296,7 @@ void launch_rev_combine_lap(const Dims& m, int lap, const void* dy, const float*
 void launch_combine(const Dims& m, const float* topk_w, const Layout& L, void* ws, void* y, cudaStream_t s) {
   const int64_t n = static_cast<int64_t>(m.T) * (m.d / 8);
   if (n == 0) return;
+  Prof prof("combine", s);
   combine_kernel<<<static_cast<unsigned>(ceil_div(n, 256)), 256, 0, s>>>(
       ws_ptr<__nv_bfloat16>(L, ws, MOE_WS_O), topk_w, m.T, m.k, m.S, m.d, static_cast<__nv_bfloat16*>(y));
 }
@@ -300,6 +304,7 @@ void launch_combine(const Dims& m, const float* topk_w, const Layout& L, void* w
 void launch_rev_combine_dw(const Dims& m, const void* dy, const float* topk_w, const Layout& L, void* ws,
                            cudaStream_t s) {
   if (m.T == 0) return;
+  Prof prof("rev_combine_dw", s);
   rev_combine_dw_kernel<<<static_cast<unsigned>(ceil_div(m.T, 8)), 256, 0, s>>>(
       static_cast<const __nv_bfloat16*>(dy), ws_ptr<__nv_bfloat16>(L, ws, MOE_WS_O), topk_w,
       ws_ptr<float>(L, ws, MOE_WS_SSEL), m.T, m.k, m.d, ws_ptr<float>(L, ws, MOE_WS_DW),
@@ -310,6 +315,7 @@ void launch_reverse_dispatch(const Dims& m, const int32_t* idx, const void* w_ro
                              void* dx, cudaStream_t s) {
   const int64_t n = static_cast<int64_t>(m.T) * (m.d / 8);
   if (n == 0) return;
+  Prof prof("reverse_dispatch", s);
   reverse_dispatch_kernel<<<static_cast<unsigned>(ceil_div(n, 256)), 256, 0, s>>>(
       ws_ptr<__nv_bfloat16>(L, ws, MOE_WS_DXE), ws_ptr<float>(L, ws, MOE_WS_DL), idx,
       static_cast<const __nv_bfloat16*>(w_router), m.T, m.k, m.S, m.d, static_cast<__nv_bfloat16*>(dx));
@@ -317,6 +323,7 @@ void launch_reverse_dispatch(const Dims& m, const int32_t* idx, const void* w_ro
 
 void launch_router_dwr(const Dims& m, const Layout& L, void* ws, void* dw_router, cudaStream_t s) {
   dim3 grid(static_cast<unsigned>(ceil_div(m.d, 128)), static_cast<unsigned>(m.E));
+  Prof prof("router_dwr", s);
   router_dwr_kernel<<<grid, 256, 0, s>>>(ws_ptr<float>(L, ws, MOE_WS_DWR_PART), ws_ptr<int>(L, ws, MOE_WS_POFF), m.d,
                                          static_cast<__nv_bfloat16*>(dw_router));
 }

@@ -2,6 +2,7 @@
 // token-axis gathers through the schedule, and scale re-tiling.
 #include "moe_internal.h"
 #include "mx.cuh"
+#include "prof.h"
 
 namespace moe {
 
@@ -128,6 +129,7 @@ void launch_quant_rows(const void* src, int64_t rows, int K, int64_t ld, uint8_t
   const int64_t n = rows * (K / 32);
   if (n == 0) return;
   const int threads = 256;
+  Prof prof("quant_rows", s);
   quant_rows_kernel<<<static_cast<unsigned>(ceil_div(n, threads)), threads, 0, s>>>(
       static_cast<const __nv_bfloat16*>(src), rows, K, ld, codes, sf, tiled ? 1 : 0, interleave_I);
 }
@@ -136,6 +138,7 @@ void launch_quant_cols(const void* src, int64_t rows, int K, int64_t ld, int64_t
                        uint8_t* sf, bool tiled, int batch, cudaStream_t s) {
   if (rows_pad == 0 || K == 0 || batch == 0) return;
   dim3 grid(static_cast<unsigned>(ceil_div(K, 256)), static_cast<unsigned>(rows_pad / 32), static_cast<unsigned>(batch));
+  Prof prof("quant_cols", s);
   quant_cols_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(src), rows, K, ld, rows_pad, codes, sf,
                                          tiled ? 1 : 0);
 }
@@ -145,6 +148,7 @@ void launch_tok_gather(const Dims& m, const void* src_rows, bool scale_by_gate, 
                        cudaStream_t s) {
   dim3 grid(static_cast<unsigned>(ceil_div(m.d, 256)), static_cast<unsigned>(m.Rmax / 32));
   const int* poff = ws_ptr<int>(L, ws, MOE_WS_POFF);
+  Prof prof(scale_by_gate ? "tok_gather_dO" : "tok_gather_x", s);
   tok_gather_kernel<<<grid, 256, 0, s>>>(
       static_cast<const __nv_bfloat16*>(src_rows), ws_ptr<int>(L, ws, MOE_WS_ROWSRC), poff + m.Ep, m.T, m.k, m.d,
       m.Rmax, topk_w, scale_by_gate ? 1 : 0, router_partials ? ws_ptr<float>(L, ws, MOE_WS_DL) : nullptr,
@@ -157,6 +161,7 @@ extern "C" int moe_scales_to_tiled(const void* canon, int rows, int K, void* til
   if (canon == nullptr || tiled == nullptr || rows <= 0 || K <= 0 || rows % 128 || K % 128) return MOE_ERR_INVALID_ARG;
   const int nb = K / 32;
   const int64_t n = static_cast<int64_t>(rows) * nb;
+  moe::Prof prof("scales_to_tiled", static_cast<cudaStream_t>(stream));
   moe::scales_to_tiled_kernel<<<static_cast<unsigned>(moe::ceil_div(n, 256)), 256, 0,
                                 static_cast<cudaStream_t>(stream)>>>(static_cast<const uint8_t*>(canon), rows, nb,
                                                                       static_cast<uint8_t*>(tiled));

@@ -9,6 +9,7 @@
 // w = s / sum(s) summed in slot order.
 #include "moe_internal.h"
 #include "gemm.cuh"
+#include "prof.h"
 
 namespace moe {
 
@@ -146,13 +147,14 @@ void launch_router_logits(const Dims& m, const void* x, const void* w_router, fl
   GemmEpilogue ep{};
   ep.out = logits;
   ep.ldo = m.E;
-  gemm_dispatch(kRouterMode, m, 0, m.E, m.d, m.T, op, ep, nullptr, nullptr, nullptr, nullptr, nullptr, s);
+  gemm_dispatch("router_gemm", kRouterMode, m, 0, m.E, m.d, m.T, op, ep, nullptr, nullptr, nullptr, nullptr, nullptr, s);
 }
 
 void launch_router_topk(const Dims& m, const float* logits, const float* bias, int32_t* idx, float* w, float* s_sel,
                         cudaStream_t s) {
   if (m.T == 0) return;
   const int warps = 4;
+  Prof prof("router_topk", s);
   router_topk_kernel<<<static_cast<unsigned>(ceil_div(m.T, warps)), warps * 32, warps * m.E * sizeof(float), s>>>(
       logits, bias, m.T, m.E, m.k, m.G, m.gtop, idx, w, s_sel);
 }

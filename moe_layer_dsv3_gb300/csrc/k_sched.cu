@@ -12,6 +12,7 @@
 // Only integer arithmetic; the result does not depend on scheduling order.
 #include "moe_internal.h"
 #include "ptx.cuh"
+#include "prof.h"
 
 namespace moe {
 
@@ -176,17 +177,22 @@ void launch_schedule(const Dims& m, const int32_t* idx, const Layout& L, void* w
   const size_t shm = static_cast<size_t>(kWarps) * m.Ep * sizeof(int);
   cudaMemsetAsync(ws_ptr<int>(L, ws, MOE_WS_ROWSRC), 0xFF, L.bytes[MOE_WS_ROWSRC], s);
   if (m.units > 0) {
-    sched_hist_kernel<<<blocks, kWarps * 32, shm, s>>>(idx, m.k, m.kp, m.E, m.Ep, m.Ap, m.units, hist, status);
-    sched_scan_kernel<<<m.Ep, 256, 0, s>>>(hist, m.Ep, m.units, base, counts);
+    { Prof prof("sched_hist", s);
+    sched_hist_kernel<<<blocks, kWarps * 32, shm, s>>>(idx, m.k, m.kp, m.E, m.Ep, m.Ap, m.units, hist, status); }
+    { Prof prof("sched_scan", s);
+    sched_scan_kernel<<<m.Ep, 256, 0, s>>>(hist, m.Ep, m.units, base, counts); }
   } else {
     cudaMemsetAsync(counts, 0, sizeof(int) * m.Ep, s);
   }
-  sched_offsets_kernel<<<1, 256, 0, s>>>(counts, m.E, m.Ep, m.C, m.Lb, offsets, poff, lap_tiles, meta);
-  if (m.units > 0)
+  { Prof prof("sched_offsets", s);
+  sched_offsets_kernel<<<1, 256, 0, s>>>(counts, m.E, m.Ep, m.C, m.Lb, offsets, poff, lap_tiles, meta); }
+  if (m.units > 0) {
+    Prof prof("sched_rank", s);
     sched_rank_kernel<<<blocks, kWarps * 32, shm, s>>>(idx, m.T, m.k, m.kp, m.E, m.Ep, m.Ap, m.units, base, offsets,
                                                        poff, ws_ptr<int>(L, ws, MOE_WS_RANK),
                                                        ws_ptr<int>(L, ws, MOE_WS_POS), ws_ptr<int>(L, ws, MOE_WS_INV),
                                                        ws_ptr<int>(L, ws, MOE_WS_ROWSRC));
+  }
 }
 
 }  // namespace moe

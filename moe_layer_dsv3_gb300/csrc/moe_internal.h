@@ -120,7 +120,7 @@ struct GemmEpilogue {
   int ldo;              // output row pitch (elements)
 };
 
-int gemm_dispatch(int mode, const Dims& m, int lap, int N, int K, int M, const GemmOperands& op,
+int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int K, int M, const GemmOperands& op,
                   const GemmEpilogue& ep, const int* counts, const int* poff, const int* lap_tiles,
                   const int* row_src, int* status, cudaStream_t s);
 

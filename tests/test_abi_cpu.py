@@ -10,7 +10,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 def _declared():
     src = open(os.path.join(ROOT, "include", "moe.h")).read()
-    return sorted(set(re.findall(r"MOE_API\s+int\s+(moe_\w+)\s*\(", src)))
+    return sorted(set(re.findall(r"MOE_API\s+[a-z ]+?\s(moe_\w+)\s*\(", src)))
 
 
 def _lib():

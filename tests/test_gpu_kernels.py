@@ -24,7 +24,7 @@ def _edge_matrix(rows, K, seed):
     v[0, :32] = 0.0                                   # all-zero block
     v[1, :32] = 2.0 ** -130                           # subnormal-range block (bf16 keeps it)
     v[2, :32] = np.linspace(-448, 448, 32)            # exact E4M3 range
-    v[3, 32:64] = 2.0 ** np.arange(-15, 17)           # powers of two over 32 binades
+    v[3, :32] = 2.0 ** np.arange(-15, 17)             # powers of two over 32 binades
     v[4, :] = -0.0
     t = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16)
     return t, t.to(torch.float64).numpy()

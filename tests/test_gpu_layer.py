@@ -241,7 +241,7 @@ def test_gemm2_stage_and_output(run):
     y = np_f64(run.L.y)
     S = O[run.A:].reshape(m.S, m.T, m.d).sum(axis=0) if m.S else np.zeros((m.T, m.d))
     yc = OL.combine(run.f["w"], O[:run.A].reshape(m.T, m.k, m.d), S)
-    assert rel_frob(y, yc) < 1e-5
+    assert rel_frob(y, yc) < 1e-4       # fp32 vs fp64 sums: rare 1-ulp bf16 rounding flips
     assert rel_frob(y, run.f["y"]) < TOL
 
 
