@@ -53,7 +53,8 @@ enum {
   MOE_ERR_CUDA = 3,            /* a CUDA runtime / driver call failed */
   MOE_ERR_WORKSPACE = 4,       /* workspace or weight blob too small */
   MOE_ERR_TIMEOUT = 5,         /* (device status) a bounded wait gave up */
-  MOE_ERR_BOUNDS = 6           /* (device status) an index check failed */
+  MOE_ERR_BOUNDS = 6,          /* (device status) an index check failed */
+  MOE_ERR_SCRATCH = 7          /* moe_route_noalloc: T * E exceeds its fixed scratch */
 };
 
 /* Layer shape.
@@ -110,6 +111,27 @@ MOE_API int moe_quantize_weights(const moe_config_t* cfg, const void* w_gu, cons
  *   selected scores in ws for backward. */
 MOE_API int moe_route(const moe_config_t* cfg, const void* x, const void* w_router, const float* bias, int32_t* topk_idx,
               float* topk_w, void* ws, moe_stream_t stream);
+
+/* moe_route without a workspace, for callers that cannot allocate device
+ * memory: code that runs while another allocator (for example a framework's
+ * caching allocator) has reserved all of the GPU's memory, or code on a path
+ * where cudaMalloc's implicit device-wide synchronisation is not allowed.
+ * The write-ups have no counterpart to this entry point.
+ *   Same arguments and outputs (topk_idx, topk_w) as moe_route, minus ws;
+ *   the selected scores are not saved, so backward still needs moe_route.
+ *   The fp32 logits live in a fixed 16 MiB array of device memory inside
+ *   the library (held by every GPU that loads it, until the process exits):
+ *   T * E must be at most 4,194,304 (T = 16384 at E = 256), otherwise the
+ *   call returns MOE_ERR_SCRATCH and enqueues nothing.
+ *   It calls no cudaMalloc, cudaFree or other allocating routine. Its first
+ *   call on a device looks up the array's device address (once per device,
+ *   with that device current); make that first call before any stream
+ *   capture. Every call shares the one array and overwrites the logits it
+ *   reads, so nothing needs clearing between calls; calls that overlap on
+ *   the GPU (different streams, or different host threads, on one device)
+ *   race on it and must be ordered by the caller. */
+MOE_API int moe_route_noalloc(const moe_config_t* cfg, const void* x, const void* w_router, const float* bias,
+                              int32_t* topk_idx, float* topk_w, moe_stream_t stream);
 
 /* Device-side schedule (write-ups: scheduling runs entirely on the device,
  * under 3 % of MoE time, reused by backward without re-sorting; Cursor blog

@@ -30,6 +30,7 @@ MOE_ERR_CUDA = 3
 MOE_ERR_WORKSPACE = 4
 MOE_ERR_TIMEOUT = 5
 MOE_ERR_BOUNDS = 6
+MOE_ERR_SCRATCH = 7
 
 WS_NAMES = ["STATUS", "META", "COUNTS", "OFFSETS", "POFF", "RANK", "POS", "INV", "ROWSRC", "LAPTILES", "HIST",
             "BASE", "LOGITS", "SSEL", "XQ", "XQ_SF", "RING_X", "RING_X_SF", "GU", "HQ", "HQ_SF", "HTOK", "HTOK_SF",
@@ -62,6 +63,7 @@ _SIGS = {
     "moe_quantize_mxfp8": [_P, _I, _I, _I, _P, _P, _P],
     "moe_quantize_weights": [_CFG, _P, _P, _P, _P, _P, _P],
     "moe_route": [_CFG, _P, _P, _P, _P, _P, _P, _P],
+    "moe_route_noalloc": [_CFG, _P, _P, _P, _P, _P, _P],
     "moe_schedule": [_CFG, _P, _P, _P],
     "moe_forward": [_CFG, _P, _P, _P, _P, _P, _P],
     "moe_backward": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
@@ -125,6 +127,12 @@ def moe_quantize_weights(cfg, w_gu, w_d, ws_gu, ws_d, wq, stream=0):
 def moe_route(cfg, x, w_router, bias, topk_idx, topk_w, ws, stream=0):
     _check("moe_route", _lib.moe_route(ctypes.byref(cfg), _p(x), _p(w_router), _p(bias), _p(topk_idx), _p(topk_w),
                                        _p(ws), _p(stream)))
+
+
+def moe_route_noalloc(cfg, x, w_router, bias, topk_idx, topk_w, stream=0):
+    """moe_route with its logits in the library's fixed device scratch (no workspace, no allocation)."""
+    _check("moe_route_noalloc", _lib.moe_route_noalloc(ctypes.byref(cfg), _p(x), _p(w_router), _p(bias),
+                                                       _p(topk_idx), _p(topk_w), _p(stream)))
 
 
 def moe_schedule(cfg, topk_idx, ws, stream=0):

@@ -19,6 +19,8 @@ struct Builder {
   }
 };
 
+}  // namespace
+
 bool arch_ok() {
   static int ok = -1;
   if (ok < 0) {
@@ -33,6 +35,8 @@ bool arch_ok() {
   }
   return ok == 1;
 }
+
+namespace {
 
 inline cudaStream_t S(moe_stream_t s) { return static_cast<cudaStream_t>(s); }
 

@@ -7,6 +7,8 @@
 // best groups (ties to the lower group), take the k best v among kept
 // experts (ties to the lower expert), slots in descending-v order, gates
 // w = s / sum(s) summed in slot order.
+#include <mutex>
+
 #include "moe_internal.h"
 #include "gemm.cuh"
 #include "prof.h"
@@ -131,7 +133,7 @@ __global__ void router_topk_kernel(const float* __restrict__ logits, const float
     for (int j = 0; j < k; ++j) {
       idx_out[static_cast<int64_t>(t) * k + j] = sel_e[j];
       w_out[static_cast<int64_t>(t) * k + j] = __fdiv_rn(sel_s[j], tot);
-      s_out[static_cast<int64_t>(t) * k + j] = sel_s[j];
+      if (s_out != nullptr) s_out[static_cast<int64_t>(t) * k + j] = sel_s[j];
     }
   }
 }
@@ -159,4 +161,49 @@ void launch_router_topk(const Dims& m, const float* logits, const float* bias, i
       logits, bias, m.T, m.E, m.k, m.G, m.gtop, idx, w, s_sel);
 }
 
+// ---------------------------------------------------------------- router without allocation
+// Scratch of moe_route_noalloc: the fp32 logits of one call, in a fixed
+// file-scope device array (every GPU that loads the library holds it until
+// the process exits). Host code must not pass the array's name to a kernel:
+// on the host it is only a stand-in symbol, so its device address is looked
+// up once per device with cudaGetSymbolAddress.
+constexpr int64_t kRouteScratchFloats = int64_t(1) << 22;   // 16 MiB: T * E <= 4,194,304
+static __device__ __align__(256) float g_route_scratch[kRouteScratchFloats];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+float* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of the scratch on the current device (set up on first use).
+int route_scratch(float** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
+    g_scratch_addr[dev] = static_cast<float*>(p);
+  }
+  *out = g_scratch_addr[dev];
+  return MOE_OK;
+}
+}  // namespace
+
 }  // namespace moe
+
+extern "C" int moe_route_noalloc(const moe_config_t* cfg, const void* x, const void* w_router, const float* bias,
+                                 int32_t* topk_idx, float* topk_w, moe_stream_t stream) {
+  if (int r = moe::validate(cfg)) return r;
+  if (!x || !w_router || !bias || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(cfg->T) * cfg->E > moe::kRouteScratchFloats) return MOE_ERR_SCRATCH;
+  if (!moe::arch_ok()) return MOE_ERR_UNSUPPORTED_ARCH;
+  if (cfg->T == 0) return MOE_OK;
+  float* logits = nullptr;
+  if (int r = moe::route_scratch(&logits)) return r;
+  const moe::Dims m = moe::make_dims(cfg);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  moe::launch_router_logits(m, x, w_router, logits, s);
+  moe::launch_router_topk(m, logits, bias, topk_idx, topk_w, nullptr, s);
+  return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

@@ -62,6 +62,8 @@ inline T* wq_ptr(const WLayout& L, void* wq, int which) {
 }
 
 int num_sms();
+// Current device is compute capability 10.3 (GB300).
+bool arch_ok();
 
 // ---------------------------------------------------------------- quantisers
 // Row-wise MX quantisation of bf16 src[rows][K] (row pitch ld elements).
