@@ -404,7 +404,7 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
   epb2.q_tok_pitch = m.Rmax;
   for (int lap = 0; lap < m.Lb; ++lap) {
     launch_rev_combine_lap(m, lap, dy, topk_w, L, ws, s);
-    if (int r = gemm_dispatch("gemm_dgrad_down", kSwigluBwd, m, lap, m.I, m.d, 0, opb2, epb2, counts, poff, lap_tiles, row_src, status, s))
+    if (int r = gemm_dispatch("gemm_dgrad_down", kSwigluBwd, m, lap, m.I, m.d, 0, opb2, epb2, counts, poff, lap_tiles, row_src, status, s, 128))
       return r;
   }
   // dgrad of GEMM1: DX rows pushed to their assignment.
@@ -436,7 +436,7 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
   epw.out = dw_d;
   epw.out2 = dws_d;
   epw.ldo = m.I;
-  if (int r = gemm_dispatch("gemm_wgrad_d", kWgrad, m, 0, m.I, 0, m.d, opw, epw, counts, poff, lap_tiles, row_src, status, s)) return r;
+  if (int r = gemm_dispatch("gemm_wgrad_d", kWgrad, m, 0, m.I, 0, m.d, opw, epw, counts, poff, lap_tiles, row_src, status, s, 128)) return r;
   opw.a = ws_ptr<uint8_t>(L, ws, MOE_WS_DGUTOK);
   opw.a_rows = 2 * m.I;
   opw.a_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_DGUTOK_SF);
@@ -446,7 +446,7 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
   epw.out = dw_gu;
   epw.out2 = dws_gu;
   epw.ldo = m.d;
-  if (int r = gemm_dispatch("gemm_wgrad_gu", kWgrad, m, 0, m.d, 0, 2 * m.I, opw, epw, counts, poff, lap_tiles, row_src, status, s))
+  if (int r = gemm_dispatch("gemm_wgrad_gu", kWgrad, m, 0, m.d, 0, 2 * m.I, opw, epw, counts, poff, lap_tiles, row_src, status, s, 128))
     return r;
   // Reverse-dispatch (+ router input gradient) and the router weight gradient.
   launch_reverse_dispatch(m, topk_idx, w_router, L, ws, dx, s);

@@ -52,6 +52,9 @@ struct GemmCfg {
   static constexpr int kStageBytes = ((kTx + 1023) / 1024) * 1024;
   static constexpr int kSfCols = kBf16 ? 0 : 4 + (BN / 128) * 4;   // TMEM columns of scales per stage
   static constexpr int kSfCol0 = 256;
+  // Accumulator buffers in TMEM: two when they fit below the scale columns, so
+  // the epilogue of one tile overlaps the mainloop of the next.
+  static constexpr int kNumAcc = (2 * BN <= kSfCol0) ? 2 : 1;
   static constexpr int kKElems = kBf16 ? 64 : 128;                  // K elements per stage
   static constexpr int kBarBytes = 256;
   static constexpr int kScratchBytes = 4 * 32 * 33 * 4;
@@ -322,8 +325,8 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cf::kStages * Cf::kStageBytes);
   uint64_t* empty = full + Cf::kStages;
   uint64_t* accf = empty + Cf::kStages;
-  uint64_t* acce = accf + 1;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(acce + 1);
+  uint64_t* acce = accf + Cf::kNumAcc;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(acce + Cf::kNumAcc);
   float* scratch = reinterpret_cast<float*>(smem + Cf::kStages * Cf::kStageBytes + Cf::kBarBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -333,8 +336,10 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(accf, 1);
-    mbar_init(acce, 128);
+    for (int a = 0; a < Cf::kNumAcc; ++a) {
+      mbar_init(&accf[a], 1);
+      mbar_init(&acce[a], 128);
+    }
     fence_barrier_init();
     fence_proxy_async();
     tma_prefetch(&tma_a);
@@ -391,15 +396,16 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      int stage = 0;
+      int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       constexpr uint32_t idesc0 = Cf::kBf16 ? idesc_bf16(128, BN) : idesc_mxf8(128, BN);
       for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
         TileInfo t;
         if (!gemm_decode<BN, MODE>(p, tile, t)) continue;
-        if (!mbar_wait(acce, acc_phase ^ 1u, p.status, 20)) break;
+        if (!mbar_wait(&acce[acc], acc_phase ^ 1u, p.status, 20)) break;
         tc_fence_after();
+        const uint32_t dacc = tmem + static_cast<uint32_t>(acc * BN);
         for (int ks = 0; ks < t.nk; ++ks) {
           if (!mbar_wait(&full[stage], phase, p.status, 21)) { ok = false; break; }
           tc_fence_after();
@@ -408,7 +414,7 @@ __global__ void __launch_bounds__(192, 1)
           if constexpr (Cf::kBf16) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              tc_mma_bf16(tmem, desc_kmajor_sw128(sa + kk * 32), desc_kmajor_sw128(sb + kk * 32), idesc0,
+              tc_mma_bf16(dacc, desc_kmajor_sw128(sa + kk * 32), desc_kmajor_sw128(sb + kk * 32), idesc0,
                           (ks | kk) != 0);
           } else {
             const uint32_t sfa_t = tmem + Cf::kSfCol0 + stage * Cf::kSfCols;
@@ -419,29 +425,31 @@ __global__ void __launch_bounds__(192, 1)
             for (int j = 0; j < BN / 128; ++j) tc_cp_sf(sfb_t + 4 * j, desc_sf_chunk(ssf + 512 + 512 * j));
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              tc_mma_mxf8(tmem, desc_kmajor_sw128(sa + kk * 32), desc_kmajor_sw128(sb + kk * 32),
+              tc_mma_mxf8(dacc, desc_kmajor_sw128(sa + kk * 32), desc_kmajor_sw128(sb + kk * 32),
                           idesc_mxf8_sf(idesc0, kk, kk), sfa_t, sfb_t, (ks | kk) != 0);
           }
           tc_commit(&empty[stage]);
           if (++stage == Cf::kStages) { stage = 0; phase ^= 1u; }
         }
-        tc_commit(accf);
-        acc_phase ^= 1u;
+        tc_commit(&accf[acc]);
+        if (++acc == Cf::kNumAcc) { acc = 0; acc_phase ^= 1u; }
       }
     }
   } else {
     const int q = warp & 3;
     float* scr = scratch + (warp - 2) * 32 * 33;
     uint32_t acc_phase = 0;
+    int acc = 0;
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
       TileInfo t;
       if (!gemm_decode<BN, MODE>(p, tile, t)) continue;
-      if (!mbar_wait(accf, acc_phase, p.status, 30)) break;
+      if (!mbar_wait(&accf[acc], acc_phase, p.status, 30)) break;
       tc_fence_after();
-      gemm_epilogue_tile<BN, MODE>(p, t, tmem + (static_cast<uint32_t>(q * 32) << 16), q, lane, scr);
+      gemm_epilogue_tile<BN, MODE>(p, t, tmem + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(q * 32) << 16),
+                                   q, lane, scr);
       tc_fence_before();
-      mbar_arrive(acce);
-      acc_phase ^= 1u;
+      mbar_arrive(&acce[acc]);
+      if (++acc == Cf::kNumAcc) { acc = 0; acc_phase ^= 1u; }
     }
   }
   tc_fence_before();

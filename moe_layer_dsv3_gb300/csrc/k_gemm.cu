@@ -70,12 +70,13 @@ int num_sms() {
 // Dispatch one grouped GEMM. Returns an MOE_* code.
 int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int K, int M, const GemmOperands& op,
                   const GemmEpilogue& ep, const int* counts, const int* poff, const int* lap_tiles,
-                  const int* row_src, int* status, cudaStream_t s) {
+                  const int* row_src, int* status, cudaStream_t s, int bn_hint) {
   if (!get_encode()) return MOE_ERR_CUDA;
   const bool bf16 = mode == kRouterMode;
   int BN;
   if (mode == kSwigluFwd) BN = 256;
   else if (mode == kRouterMode) BN = N <= 32 ? 32 : (N % 256 == 0 ? 256 : 128);
+  else if ((bn_hint == 128 || bn_hint == 256) && N % bn_hint == 0) BN = bn_hint;
   else BN = (N % 256 == 0) ? 256 : 128;
   if (!bf16 && N % BN) return MOE_ERR_INVALID_ARG;
 

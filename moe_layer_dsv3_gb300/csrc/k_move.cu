@@ -47,82 +47,80 @@ __device__ __forceinline__ bool lap_tile(const int* lap_tiles, const int* counts
   return lt.rows > 0;
 }
 
-// ring[e*C + slot] <- x_q[t] for the rows of lap L (codes and scales), zeros past the segment.
-__global__ void permute_lap_kernel(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xq_sf,
-                                   const int* __restrict__ lap_tiles, const int* __restrict__ counts,
-                                   const int* __restrict__ poff, const int* __restrict__ row_src, int T, int k, int d,
-                                   int E, int Ep, int C, int L, uint8_t* __restrict__ ring,
-                                   uint8_t* __restrict__ ring_sf) {
+// The rows of lap L are the 128-row tiles of its tile list; each tile is
+// covered by 16 groups of 8 rows and each row by one warp, so that even a
+// lap with a few hot experts spreads over the whole GPU. Grid-stride loop
+// over row groups. Rows past an expert's segment are written as zeros.
+constexpr int kRowsPerGroup = 8;
+
+__device__ __forceinline__ bool lap_row(const int* lap_tiles, const int* counts, const int* poff,
+                                        const int* row_src, int T, int k, int E, int Ep, int C, int L, int gid,
+                                        int warp, int64_t& ring_row, int& tok, int& a_out) {
   LapTile lt;
-  if (!lap_tile(lap_tiles, counts, E, Ep, C, L, blockIdx.x, lt)) return;
-  __shared__ int s_tok[128];
-  if (threadIdx.x < 128) {
-    const int i = threadIdx.x;
-    s_tok[i] = i < lt.rows ? token_of(row_src[poff[lt.e] + lt.rank0 + i], T, k) : -1;
+  if (!lap_tile(lap_tiles, counts, E, Ep, C, L, gid >> 4, lt)) return false;
+  const int r = (gid & 15) * kRowsPerGroup + warp;
+  ring_row = static_cast<int64_t>(lt.e) * C + lt.slot0 + r;
+  tok = -1;
+  a_out = -1;
+  if (r < lt.rows) {
+    a_out = row_src[poff[lt.e] + lt.rank0 + r];
+    tok = token_of(a_out, T, k);
   }
-  __syncthreads();
-  const int64_t row0 = static_cast<int64_t>(lt.e) * C + lt.slot0;
-  const int chunks = d / 16;
-  for (int i = threadIdx.x; i < 128 * chunks; i += blockDim.x) {
-    const int r = i / chunks, c = i - r * chunks;
-    const int t = s_tok[r];
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (t >= 0) v = reinterpret_cast<const uint4*>(xq + static_cast<int64_t>(t) * d)[c];
-    reinterpret_cast<uint4*>(ring + (row0 + r) * d)[c] = v;
-  }
-  const int ktiles = d / 128;
-  for (int i = threadIdx.x; i < 128 * ktiles; i += blockDim.x) {
-    const int r = i / ktiles, kt = i - r * ktiles;
-    const int t = s_tok[r];
-    uint32_t v = 0;
-    if (t >= 0) v = *reinterpret_cast<const uint32_t*>(xq_sf + sf_off(t, kt * 4, ktiles));
-    *reinterpret_cast<uint32_t*>(ring_sf + sf_off(row0 + r, kt * 4, ktiles)) = v;
+  return true;
+}
+
+// ring[e*C + slot] <- x_q[t] (codes and scales) for the rows of lap L.
+__global__ void __launch_bounds__(256) permute_lap_kernel(
+    const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xq_sf, const int* __restrict__ lap_tiles,
+    const int* __restrict__ counts, const int* __restrict__ poff, const int* __restrict__ row_src, int T, int k,
+    int d, int E, int Ep, int C, int L, uint8_t* __restrict__ ring, uint8_t* __restrict__ ring_sf) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_groups = lap_tiles[static_cast<int64_t>(L) * (Ep + 1) + E] * 16;
+  const int chunks = d / 16, ktiles = d / 128;
+  for (int gid = blockIdx.x; gid < n_groups; gid += gridDim.x) {
+    int64_t row;
+    int t, a;
+    if (!lap_row(lap_tiles, counts, poff, row_src, T, k, E, Ep, C, L, gid, warp, row, t, a)) continue;
+    const uint4* src = reinterpret_cast<const uint4*>(xq + static_cast<int64_t>(t < 0 ? 0 : t) * d);
+    uint4* dst = reinterpret_cast<uint4*>(ring + row * d);
+#pragma unroll 4
+    for (int c = lane; c < chunks; c += 32) dst[c] = t >= 0 ? src[c] : make_uint4(0, 0, 0, 0);
+    for (int kt = lane; kt < ktiles; kt += 32) {
+      const uint32_t v = t >= 0 ? *reinterpret_cast<const uint32_t*>(xq_sf + sf_off(t, kt * 4, ktiles)) : 0u;
+      *reinterpret_cast<uint32_t*>(ring_sf + sf_off(row, kt * 4, ktiles)) = v;
+    }
   }
 }
 
 // ring_dO[e*C + slot] <- MX(fp32(w_a * dy[t])) along d for the rows of lap L.
-__global__ void rev_combine_lap_kernel(const __nv_bfloat16* __restrict__ dy, const float* __restrict__ topk_w,
-                                       const int* __restrict__ lap_tiles, const int* __restrict__ counts,
-                                       const int* __restrict__ poff, const int* __restrict__ row_src, int T, int k,
-                                       int d, int E, int Ep, int C, int L, uint8_t* __restrict__ ring,
-                                       uint8_t* __restrict__ ring_sf) {
-  LapTile lt;
-  if (!lap_tile(lap_tiles, counts, E, Ep, C, L, blockIdx.x, lt)) return;
-  __shared__ int s_tok[128];
-  __shared__ float s_w[128];
-  if (threadIdx.x < 128) {
-    const int i = threadIdx.x;
-    int t = -1;
-    float w = 0.0f;
-    if (i < lt.rows) {
-      const int a = row_src[poff[lt.e] + lt.rank0 + i];
-      t = token_of(a, T, k);
-      w = topk_w[a];
-    }
-    s_tok[i] = t;
-    s_w[i] = w;
-  }
-  __syncthreads();
-  const int64_t row0 = static_cast<int64_t>(lt.e) * C + lt.slot0;
+__global__ void __launch_bounds__(256) rev_combine_lap_kernel(
+    const __nv_bfloat16* __restrict__ dy, const float* __restrict__ topk_w, const int* __restrict__ lap_tiles,
+    const int* __restrict__ counts, const int* __restrict__ poff, const int* __restrict__ row_src, int T, int k,
+    int d, int E, int Ep, int C, int L, uint8_t* __restrict__ ring, uint8_t* __restrict__ ring_sf) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_groups = lap_tiles[static_cast<int64_t>(L) * (Ep + 1) + E] * 16;
   const int nb = d / 32, ktiles = d / 128;
-  for (int i = threadIdx.x; i < 128 * nb; i += blockDim.x) {
-    const int r = i / nb, kb = i - r * nb;
-    const int t = s_tok[r];
-    float v[32];
-    if (t >= 0) {
-      load_bf16x32(dy + static_cast<int64_t>(t) * d + kb * 32, v);
-      const float w = s_w[r];
+  for (int gid = blockIdx.x; gid < n_groups; gid += gridDim.x) {
+    int64_t row;
+    int t, a;
+    if (!lap_row(lap_tiles, counts, poff, row_src, T, k, E, Ep, C, L, gid, warp, row, t, a)) continue;
+    const float w = t >= 0 ? topk_w[a] : 0.0f;
+    for (int kb = lane; kb < nb; kb += 32) {
+      float v[32];
+      if (t >= 0) {
+        load_bf16x32(dy + static_cast<int64_t>(t) * d + kb * 32, v);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(w, v[j]);
-    } else {
+        for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(w, v[j]);
+      } else {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+        for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+      }
+      const int b = mx_scale_byte(amax32(v));
+      uint32_t wq[8];
+      mx_pack32(v, mx_inv_scale(b), wq);
+      store32(ring + row * d + kb * 32, wq);
+      ring_sf[sf_off(row, kb, ktiles)] = static_cast<uint8_t>(b);
     }
-    const int b = mx_scale_byte(amax32(v));
-    uint32_t wq[8];
-    mx_pack32(v, mx_inv_scale(b), wq);
-    store32(ring + (row0 + r) * d + kb * 32, wq);
-    ring_sf[sf_off(row0 + r, kb, ktiles)] = static_cast<uint8_t>(b);
   }
 }
 
@@ -272,8 +270,15 @@ __global__ void router_dwr_kernel(const float* __restrict__ part, const int* __r
 
 }  // namespace
 
+// Blocks of the lap kernels: enough row groups to cover a full lap, capped at 16 per SM.
+static int lap_blocks(const Dims& m) {
+  const int64_t groups = static_cast<int64_t>(m.E) * (m.C / 128) * 16;
+  const int64_t cap = static_cast<int64_t>(num_sms()) * 16;
+  return static_cast<int>(groups < cap ? groups : cap);
+}
+
 void launch_permute_lap(const Dims& m, int lap, const Layout& L, void* ws, cudaStream_t s) {
-  const int blocks = m.E * (m.C / 128);
+  const int blocks = lap_blocks(m);
   if (blocks == 0) return;
   Prof prof("permute_lap", s);
   permute_lap_kernel<<<blocks, 256, 0, s>>>(
@@ -284,7 +289,7 @@ void launch_permute_lap(const Dims& m, int lap, const Layout& L, void* ws, cudaS
 
 void launch_rev_combine_lap(const Dims& m, int lap, const void* dy, const float* topk_w, const Layout& L, void* ws,
                             cudaStream_t s) {
-  const int blocks = m.E * (m.C / 128);
+  const int blocks = lap_blocks(m);
   if (blocks == 0) return;
   Prof prof("rev_combine_lap", s);
   rev_combine_lap_kernel<<<blocks, 256, 0, s>>>(

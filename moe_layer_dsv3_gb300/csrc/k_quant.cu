@@ -72,49 +72,79 @@ __device__ __forceinline__ int token_of(int a, int T, int k) {
 // (shared-expert assignments have gate 1). Optionally also accumulates the
 // router weight-gradient partial sums part[pr/32][c] = sum_r dl_a x[t_a][c]
 // over the routed rows of the 32-row block, in rank order.
-__global__ void tok_gather_kernel(const __nv_bfloat16* __restrict__ src, const int* __restrict__ row_src,
-                                  const int* __restrict__ poff_end, int T, int k, int d, int64_t Rmax,
-                                  const float* __restrict__ topk_w, int scale_by_gate,
-                                  const float* __restrict__ dl, float* __restrict__ part,
-                                  uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
-  const int c = blockIdx.x * 256 + threadIdx.x;
+// CTA: 32 rows x 1024 columns; each thread loads 8 bytes (4 columns) of each
+// of the 32 rows, then owns those 4 columns.
+constexpr int kTokCols = 4;
+constexpr int kTokThreads = 256;
+
+__device__ __forceinline__ float bf16_lane(const uint2& u, int j) {
+  const uint32_t w = j < 2 ? u.x : u.y;
+  return (j & 1) ? __uint_as_float(w & 0xFFFF0000u) : __uint_as_float(w << 16);
+}
+
+__global__ void __launch_bounds__(kTokThreads) tok_gather_kernel(
+    const __nv_bfloat16* __restrict__ src, const int* __restrict__ row_src, const int* __restrict__ poff_end, int T,
+    int k, int d, int64_t Rmax, const float* __restrict__ topk_w, int scale_by_gate, const float* __restrict__ dl,
+    float* __restrict__ part, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
   const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 32;
   if (r0 >= *poff_end) return;
-  __shared__ int s_a[32];
+  __shared__ int s_tok[32];
   __shared__ float s_w[32];
   __shared__ float s_dl[32];
   if (threadIdx.x < 32) {
     const int a = row_src[r0 + threadIdx.x];
-    s_a[threadIdx.x] = a;
     float w = 1.0f, g = 0.0f;
     if (a >= 0 && a < T * k) {
       if (scale_by_gate) w = topk_w[a];
       if (dl != nullptr) g = dl[a];
     }
+    s_tok[threadIdx.x] = a >= 0 ? token_of(a, T, k) : -1;
     s_w[threadIdx.x] = w;
     s_dl[threadIdx.x] = g;
   }
   __syncthreads();
-  if (c >= d) return;
-  float v[32];
-  float acc = 0.0f;
+  const int c0 = (blockIdx.x * kTokThreads + threadIdx.x) * kTokCols;
+  if (c0 >= d) return;
+  uint2 raw[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
-    const int a = s_a[i];
-    float x = 0.0f;
-    if (a >= 0) {
-      x = __bfloat162float(src[static_cast<int64_t>(token_of(a, T, k)) * d + c]);
-      acc = fmaf(s_dl[i], x, acc);
-      x = scale_by_gate ? s_w[i] * x : x;
-    }
-    v[i] = x;
+    const int t = s_tok[i];
+    raw[i] = t >= 0 ? *reinterpret_cast<const uint2*>(src + static_cast<int64_t>(t) * d + c0) : make_uint2(0, 0);
   }
-  const int b = mx_scale_byte(amax32(v));
-  uint32_t w[8];
-  mx_pack32(v, mx_inv_scale(b), w);
-  store32(codes + static_cast<int64_t>(c) * Rmax + r0, w);
-  sf[sf_off(c, r0 / 32, Rmax / 128)] = static_cast<uint8_t>(b);
-  if (part != nullptr) part[(r0 / 32) * d + c] = acc;
+  float amax[kTokCols], acc[kTokCols];
+#pragma unroll
+  for (int j = 0; j < kTokCols; ++j) { amax[j] = 0.0f; acc[j] = 0.0f; }
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+#pragma unroll
+    for (int j = 0; j < kTokCols; ++j) {
+      float x = bf16_lane(raw[i], j);
+      acc[j] = fmaf(s_dl[i], x, acc[j]);
+      if (scale_by_gate) x = s_w[i] * x;
+      amax[j] = fmaxf(amax[j], fabsf(x));
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kTokCols; ++j) {
+    const int b = mx_scale_byte(amax[j]);
+    const float inv = mx_inv_scale(b);
+    uint32_t w[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      float v4[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        float x = bf16_lane(raw[4 * q + u], j);
+        if (scale_by_gate) x = s_w[4 * q + u] * x;
+        v4[u] = x * inv;
+      }
+      w[q] = e4m3x2(v4[0], v4[1]) | (e4m3x2(v4[2], v4[3]) << 16);
+    }
+    store32(codes + static_cast<int64_t>(c0 + j) * Rmax + r0, w);
+    sf[sf_off(c0 + j, r0 / 32, Rmax / 128)] = static_cast<uint8_t>(b);
+  }
+  if (part != nullptr)
+    *reinterpret_cast<float4*>(part + (r0 / 32) * d + c0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
 }
 
 __global__ void scales_to_tiled_kernel(const uint8_t* __restrict__ canon, int64_t rows, int nb, uint8_t* tiled) {
@@ -146,10 +176,10 @@ void launch_quant_cols(const void* src, int64_t rows, int K, int64_t ld, int64_t
 void launch_tok_gather(const Dims& m, const void* src_rows, bool scale_by_gate, const float* topk_w,
                        bool router_partials, const Layout& L, void* ws, uint8_t* codes, uint8_t* sf,
                        cudaStream_t s) {
-  dim3 grid(static_cast<unsigned>(ceil_div(m.d, 256)), static_cast<unsigned>(m.Rmax / 32));
+  dim3 grid(static_cast<unsigned>(ceil_div(m.d, kTokThreads * kTokCols)), static_cast<unsigned>(m.Rmax / 32));
   const int* poff = ws_ptr<int>(L, ws, MOE_WS_POFF);
   Prof prof(scale_by_gate ? "tok_gather_dO" : "tok_gather_x", s);
-  tok_gather_kernel<<<grid, 256, 0, s>>>(
+  tok_gather_kernel<<<grid, kTokThreads, 0, s>>>(
       static_cast<const __nv_bfloat16*>(src_rows), ws_ptr<int>(L, ws, MOE_WS_ROWSRC), poff + m.Ep, m.T, m.k, m.d,
       m.Rmax, topk_w, scale_by_gate ? 1 : 0, router_partials ? ws_ptr<float>(L, ws, MOE_WS_DL) : nullptr,
       router_partials ? ws_ptr<float>(L, ws, MOE_WS_DWR_PART) : nullptr, codes, sf);
