@@ -378,7 +378,11 @@ def run_ours(args, rank, world, local_rank):
         if name in hb:
             ent["gbs"] = hb[name] * args.steps / (tms / 1000.0) / 1e9
         per_kernel[name] = ent
-    dom = max(kern.items(), key=lambda kv: kv[1][1])[0]
+    # Ring-lap kernels run on two streams and overlap one another, so their
+    # event times are not additive; the dominant kernel is taken among the
+    # kernels that run alone on the launch stream.
+    lap_kernels = {"gemm1_fwd", "gemm_dgrad_down", "permute_lap", "rev_combine_lap"}
+    dom = max(((n, v) for n, v in kern.items() if n not in lap_kernels), key=lambda kv: kv[1][1])[0]
     fp8_peak = 2.0 * pk["bf16_sus"]
     if dom in fl:
         achieved = per_kernel[dom]["tflops"]
@@ -409,6 +413,7 @@ def run_ours(args, rank, world, local_rank):
         "permute_gbs": perm,
         "permute_frac_hbm": perm / pk["hbm_gbs"] if perm else None,
         "schedule_share": (stages["schedule"]) / sum(stages.values()),
+        "lap_kernels_overlap": sorted(lap_kernels),
         "kernels": per_kernel,
     }
     cpu = None

@@ -185,7 +185,7 @@ enum {
   MOE_WS_SSEL,         /* fp32[T][k] selected sigmoid scores */
   MOE_WS_XQ,           /* u8[Tpad][d]       MX(x) along d */
   MOE_WS_XQ_SF,        /* tiled scales of XQ */
-  MOE_WS_RING_X,       /* u8[E][C][d]       ring token buffer (dispatch) */
+  MOE_WS_RING_X,       /* u8[2][E][C][d]    two ring token buffers (dispatch); lap L uses buffer L % 2 */
   MOE_WS_RING_X_SF,
   MOE_WS_GU,           /* bf16[Rmax][2I]    saved g|u */
   MOE_WS_HQ,           /* u8[Rmax][I]       MX(h) along I */
@@ -195,7 +195,7 @@ enum {
   MOE_WS_O,            /* bf16[T*(k+S)][d]  expert outputs per assignment */
   MOE_WS_DW,           /* fp32[T][k]        gate gradients */
   MOE_WS_DL,           /* fp32[T][k]        router logit gradients */
-  MOE_WS_RING_DO,      /* u8[E][C][d]       ring buffer of MX(w dy) (reverse-combine) */
+  MOE_WS_RING_DO,      /* u8[2][E][C][d]    two ring buffers of MX(w dy) (reverse-combine), as RING_X */
   MOE_WS_RING_DO_SF,
   MOE_WS_DOS,          /* u8[Tpad][d]       MX(dy) along d (shared expert) */
   MOE_WS_DOS_SF,

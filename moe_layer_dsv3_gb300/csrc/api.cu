@@ -1,6 +1,7 @@
 // C ABI: argument checks, workspace layout, and the launch sequence of the
 // forward and backward passes. Every step runs in this library's kernels.
 #include <cstring>
+#include <mutex>
 
 #include "moe_internal.h"
 
@@ -39,6 +40,32 @@ bool arch_ok() {
 namespace {
 
 inline cudaStream_t S(moe_stream_t s) { return static_cast<cudaStream_t>(s); }
+
+// Consecutive ring laps alternate between the caller's stream and one
+// auxiliary stream per device (and between the two ring buffers), so a lap's
+// dispatch and GEMM overlap the previous lap's GEMM. The fork and join are
+// event record / wait pairs on the caller's stream.
+struct LapStreams {
+  std::mutex mu;
+  cudaStream_t aux = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+constexpr int kMaxDev = 64;
+LapStreams g_lap[kMaxDev];
+
+LapStreams* lap_streams() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
+  LapStreams& l = g_lap[dev];
+  std::lock_guard<std::mutex> lk(l.mu);
+  if (l.aux == nullptr) {
+    if (cudaStreamCreateWithFlags(&l.aux, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&l.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&l.join, cudaEventDisableTiming) != cudaSuccess)
+      return nullptr;
+  }
+  return &l;
+}
 
 int launch_status() { return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
@@ -108,8 +135,8 @@ Layout make_layout(const moe_config_t* c) {
   b.add(L.off, L.bytes, MOE_WS_SSEL, 4 * T * k);
   b.add(L.off, L.bytes, MOE_WS_XQ, Tp * d);
   b.add(L.off, L.bytes, MOE_WS_XQ_SF, Tp * d / 32);
-  b.add(L.off, L.bytes, MOE_WS_RING_X, E * C * d);
-  b.add(L.off, L.bytes, MOE_WS_RING_X_SF, E * C * d / 32);
+  b.add(L.off, L.bytes, MOE_WS_RING_X, kRingBufs * E * C * d);
+  b.add(L.off, L.bytes, MOE_WS_RING_X_SF, kRingBufs * E * C * d / 32);
   b.add(L.off, L.bytes, MOE_WS_GU, 2 * R * 2 * I);
   b.add(L.off, L.bytes, MOE_WS_HQ, R * I);
   b.add(L.off, L.bytes, MOE_WS_HQ_SF, R * I / 32);
@@ -118,8 +145,8 @@ Layout make_layout(const moe_config_t* c) {
   b.add(L.off, L.bytes, MOE_WS_O, 2 * Ap * d);
   b.add(L.off, L.bytes, MOE_WS_DW, 4 * T * k);
   b.add(L.off, L.bytes, MOE_WS_DL, 4 * T * k);
-  b.add(L.off, L.bytes, MOE_WS_RING_DO, E * C * d);
-  b.add(L.off, L.bytes, MOE_WS_RING_DO_SF, E * C * d / 32);
+  b.add(L.off, L.bytes, MOE_WS_RING_DO, kRingBufs * E * C * d);
+  b.add(L.off, L.bytes, MOE_WS_RING_DO_SF, kRingBufs * E * C * d / 32);
   b.add(L.off, L.bytes, MOE_WS_DOS, Tp * d);
   b.add(L.off, L.bytes, MOE_WS_DOS_SF, Tp * d / 32);
   b.add(L.off, L.bytes, MOE_WS_DOTOK, d * R);
@@ -313,10 +340,27 @@ int moe_forward(const moe_config_t* cfg, const void* x, const void* wq, const fl
   ep1.q_tok = ws_ptr<uint8_t>(L, ws, MOE_WS_HTOK);
   ep1.q_tok_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_HTOK_SF);
   ep1.q_tok_pitch = m.Rmax;
-  for (int lap = 0; lap < m.Lb; ++lap) {
-    launch_permute_lap(m, lap, L, ws, s);
-    if (int r = gemm_dispatch("gemm1_fwd", kSwigluFwd, m, lap, 2 * m.I, m.d, 0, op1, ep1, counts, poff, lap_tiles, row_src, status, s))
-      return r;
+  {
+    LapStreams* ls = lap_streams();
+    if (ls == nullptr) return MOE_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(ls->mu);
+    cudaEventRecord(ls->fork, s);
+    cudaStreamWaitEvent(ls->aux, ls->fork, 0);
+    const uint8_t* ring = op1.a;
+    const uint8_t* ring_sf = op1.a_sf;
+    const size_t rb = static_cast<size_t>(m.E) * m.C * m.d;
+    int rc = MOE_OK;
+    for (int lap = 0; lap < m.Lb && rc == MOE_OK; ++lap) {
+      cudaStream_t cs = (lap & 1) ? ls->aux : s;
+      op1.a = ring + (lap & 1) * rb;
+      op1.a_sf = ring_sf + (lap & 1) * rb / 32;
+      launch_permute_lap(m, lap, L, ws, cs);
+      rc = gemm_dispatch("gemm1_fwd", kSwigluFwd, m, lap, 2 * m.I, m.d, 0, op1, ep1, counts, poff, lap_tiles, row_src,
+                         status, cs);
+    }
+    cudaEventRecord(ls->join, ls->aux);
+    cudaStreamWaitEvent(s, ls->join, 0);
+    if (rc) return rc;
   }
   GemmOperands op2{};
   op2.a = ws_ptr<uint8_t>(L, ws, MOE_WS_HQ);
@@ -402,10 +446,27 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
   epb2.q_tok = ws_ptr<uint8_t>(L, ws, MOE_WS_DGUTOK);
   epb2.q_tok_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_DGUTOK_SF);
   epb2.q_tok_pitch = m.Rmax;
-  for (int lap = 0; lap < m.Lb; ++lap) {
-    launch_rev_combine_lap(m, lap, dy, topk_w, L, ws, s);
-    if (int r = gemm_dispatch("gemm_dgrad_down", kSwigluBwd, m, lap, m.I, m.d, 0, opb2, epb2, counts, poff, lap_tiles, row_src, status, s, 128))
-      return r;
+  {
+    LapStreams* ls = lap_streams();
+    if (ls == nullptr) return MOE_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(ls->mu);
+    cudaEventRecord(ls->fork, s);
+    cudaStreamWaitEvent(ls->aux, ls->fork, 0);
+    const uint8_t* ring = opb2.a;
+    const uint8_t* ring_sf = opb2.a_sf;
+    const size_t rb = static_cast<size_t>(m.E) * m.C * m.d;
+    int rc = MOE_OK;
+    for (int lap = 0; lap < m.Lb && rc == MOE_OK; ++lap) {
+      cudaStream_t cs = (lap & 1) ? ls->aux : s;
+      opb2.a = ring + (lap & 1) * rb;
+      opb2.a_sf = ring_sf + (lap & 1) * rb / 32;
+      launch_rev_combine_lap(m, lap, dy, topk_w, L, ws, cs);
+      rc = gemm_dispatch("gemm_dgrad_down", kSwigluBwd, m, lap, m.I, m.d, 0, opb2, epb2, counts, poff, lap_tiles,
+                         row_src, status, cs, 128);
+    }
+    cudaEventRecord(ls->join, ls->aux);
+    cudaStreamWaitEvent(s, ls->join, 0);
+    if (rc) return rc;
   }
   // dgrad of GEMM1: DX rows pushed to their assignment.
   GemmOperands opb4{};
@@ -436,7 +497,7 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
   epw.out = dw_d;
   epw.out2 = dws_d;
   epw.ldo = m.I;
-  if (int r = gemm_dispatch("gemm_wgrad_d", kWgrad, m, 0, m.I, 0, m.d, opw, epw, counts, poff, lap_tiles, row_src, status, s, 128)) return r;
+  if (int r = gemm_dispatch("gemm_wgrad_d", kWgrad, m, 0, m.I, 0, m.d, opw, epw, counts, poff, lap_tiles, row_src, status, s, 256)) return r;
   opw.a = ws_ptr<uint8_t>(L, ws, MOE_WS_DGUTOK);
   opw.a_rows = 2 * m.I;
   opw.a_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_DGUTOK_SF);
@@ -446,7 +507,7 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
   epw.out = dw_gu;
   epw.out2 = dws_gu;
   epw.ldo = m.d;
-  if (int r = gemm_dispatch("gemm_wgrad_gu", kWgrad, m, 0, m.d, 0, 2 * m.I, opw, epw, counts, poff, lap_tiles, row_src, status, s, 128))
+  if (int r = gemm_dispatch("gemm_wgrad_gu", kWgrad, m, 0, m.d, 0, 2 * m.I, opw, epw, counts, poff, lap_tiles, row_src, status, s, 256))
     return r;
   // Reverse-dispatch (+ router input gradient) and the router weight gradient.
   launch_reverse_dispatch(m, topk_idx, w_router, L, ws, dx, s);

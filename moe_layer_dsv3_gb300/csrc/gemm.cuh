@@ -43,7 +43,11 @@ struct GemmParams {
 template <int BN, int MODE>
 struct GemmCfg {
   static constexpr bool kBf16 = MODE == kRouterMode;
-  static constexpr int kStages = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);
+  // Weight gradients stage their bf16 output tile in shared memory and write
+  // it with TMA stores, so the tile's DRAM write overlaps the next mainloop.
+  static constexpr bool kTmaOut = MODE == kWgrad;
+  static constexpr int kStages = kTmaOut ? 3 : (BN >= 256 ? 4 : (BN >= 128 ? 6 : 8));
+  static constexpr int kOutBytes = kTmaOut ? 128 * BN * 2 : 0;
   static constexpr int kABytes = 128 * 128;
   static constexpr int kBBytes = BN * 128;
   static constexpr int kSfaBytes = kBf16 ? 0 : 512;
@@ -57,8 +61,8 @@ struct GemmCfg {
   static constexpr int kNumAcc = (2 * BN <= kSfCol0) ? 2 : 1;
   static constexpr int kKElems = kBf16 ? 64 : 128;                  // K elements per stage
   static constexpr int kBarBytes = 256;
-  static constexpr int kScratchBytes = 4 * 32 * 33 * 4;
-  static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes + kScratchBytes;
+  static constexpr int kScratchBytes = (MODE == kSwigluFwd || MODE == kSwigluBwd) ? 4 * 32 * 33 * 4 : 0;
+  static constexpr int kSmem = 1024 + kStages * kStageBytes + kOutBytes + kBarBytes + kScratchBytes;
   static_assert(kSmem <= 232448, "shared memory budget");
   static_assert(kSfCol0 + kStages * kSfCols <= 512, "TMEM budget");
   static_assert(BN <= 256, "accumulator budget");
@@ -214,7 +218,8 @@ __device__ __forceinline__ void load_bf16x32_g(const __nv_bfloat16* src, float* 
 
 template <int BN, int MODE>
 __device__ __forceinline__ void gemm_epilogue_tile(const GemmParams& p, const TileInfo& t, uint32_t tacc, int q,
-                                                   int lane, float* scr) {
+                                                   int lane, float* scr, uint8_t* out_smem, const CUtensorMap* tma_o,
+                                                   const CUtensorMap* tma_o2) {
   const int row = q * 32 + lane;
   const bool have_acc = t.nk > 0;
   const bool valid = row < t.valid;
@@ -278,10 +283,11 @@ __device__ __forceinline__ void gemm_epilogue_tile(const GemmParams& p, const Ti
       if (a >= 0) store_bf16x32(out + static_cast<int64_t>(a) * p.ldo + t.n0 + c * 32, v);
     }
   } else if constexpr (MODE == kWgrad) {
-    __nv_bfloat16* out = t.e < p.E ? static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(t.e) * p.M * p.ldo
-                                   : static_cast<__nv_bfloat16*>(p.out2) +
-                                         static_cast<int64_t>(t.e - p.E) * p.M * p.ldo;
-    const int64_t orow = t.m0 + row;
+    // bf16 tile -> shared staging (boxes of 128 rows x 64 columns, 128-byte
+    // swizzle) -> TMA store to dW[e][m0.., n0..]. One thread issues the stores.
+    const bool leader = (q == 2 && lane == 0);
+    if (leader) bulk_wait_read_all();          // the previous tile's stores have read the staging
+    named_barrier(1, 128);
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
       float v[32];
@@ -291,7 +297,24 @@ __device__ __forceinline__ void gemm_epilogue_tile(const GemmParams& p, const Ti
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = 0.0f;
       }
-      store_bf16x32(out + orow * p.ldo + t.n0 + c * 32, v);
+      uint8_t* box = out_smem + (c >> 1) * (128 * 128) + row * 128;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int j = (c & 1) * 4 + q4;
+        const float* w = v + 8 * q4;
+        *reinterpret_cast<uint4*>(box + ((j ^ (row & 7)) << 4)) =
+            make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]), pack_bf16x2(w[4], w[5]),
+                       pack_bf16x2(w[6], w[7]));
+      }
+    }
+    fence_proxy_async();
+    named_barrier(1, 128);
+    if (leader) {
+      const bool routed = t.e < p.E;
+      const int y = (routed ? t.e : t.e - p.E) * p.M + t.m0;
+#pragma unroll
+      for (int b = 0; b < BN / 64; ++b) tma_store_2d(routed ? tma_o : tma_o2, t.n0 + 64 * b, y, out_smem + b * 128 * 128);
+      bulk_commit();
     }
   } else {   // plain (fp32 out, M x N) and router logits (fp32 [M][N] for columns < N)
     float* out = static_cast<float*>(p.out);
@@ -318,16 +341,18 @@ __device__ __forceinline__ void gemm_epilogue_tile(const GemmParams& p, const Ti
 template <int BN, int MODE>
 __global__ void __launch_bounds__(192, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_a2,
-                const __grid_constant__ CUtensorMap tma_b, const __grid_constant__ GemmParams p) {
+                const __grid_constant__ CUtensorMap tma_b, const __grid_constant__ CUtensorMap tma_o,
+                const __grid_constant__ CUtensorMap tma_o2, const __grid_constant__ GemmParams p) {
   using Cf = GemmCfg<BN, MODE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cf::kStages * Cf::kStageBytes);
+  uint8_t* out_smem = smem + Cf::kStages * Cf::kStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(out_smem + Cf::kOutBytes);
   uint64_t* empty = full + Cf::kStages;
   uint64_t* accf = empty + Cf::kStages;
   uint64_t* acce = accf + Cf::kNumAcc;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(acce + Cf::kNumAcc);
-  float* scratch = reinterpret_cast<float*>(smem + Cf::kStages * Cf::kStageBytes + Cf::kBarBytes);
+  float* scratch = reinterpret_cast<float*>(out_smem + Cf::kOutBytes + Cf::kBarBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
@@ -345,6 +370,10 @@ __global__ void __launch_bounds__(192, 1)
     tma_prefetch(&tma_a);
     tma_prefetch(&tma_b);
     if (MODE == kSwigluFwd || MODE == kSwigluBwd) tma_prefetch(&tma_a2);
+    if (Cf::kTmaOut) {
+      tma_prefetch(&tma_o);
+      tma_prefetch(&tma_o2);
+    }
   }
   if (warp == 1) {
     tmem_alloc(tslot, 512);
@@ -446,11 +475,12 @@ __global__ void __launch_bounds__(192, 1)
       if (!mbar_wait(&accf[acc], acc_phase, p.status, 30)) break;
       tc_fence_after();
       gemm_epilogue_tile<BN, MODE>(p, t, tmem + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(q * 32) << 16),
-                                   q, lane, scr);
+                                   q, lane, scr, out_smem, &tma_o, &tma_o2);
       tc_fence_before();
       mbar_arrive(&acce[acc]);
       if (++acc == Cf::kNumAcc) { acc = 0; acc_phase ^= 1u; }
     }
+    if (Cf::kTmaOut && q == 2 && lane == 0) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();

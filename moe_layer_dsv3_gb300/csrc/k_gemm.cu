@@ -39,9 +39,20 @@ bool make_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int
   return r == CUDA_SUCCESS;
 }
 
+// 2-D bf16 output [rows][cols] written by TMA stores, box 64 columns x 128 rows, 128-byte swizzle.
+bool make_tmap_out(CUtensorMap* m, void* base, int64_t rows, int64_t cols) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int BN, int MODE>
-int run(const char* name, const CUtensorMap& ta, const CUtensorMap& ta2, const CUtensorMap& tb, const GemmParams& p,
-        int grid, cudaStream_t s) {
+int run(const char* name, const CUtensorMap& ta, const CUtensorMap& ta2, const CUtensorMap& tb, const CUtensorMap& to,
+        const CUtensorMap& to2, const GemmParams& p, int grid, cudaStream_t s) {
   using Cf = GemmCfg<BN, MODE>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
@@ -51,7 +62,7 @@ int run(const char* name, const CUtensorMap& ta, const CUtensorMap& ta2, const C
   if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
   if (grid <= 0) return MOE_OK;
   Prof prof(name, s);
-  gemm_kernel<BN, MODE><<<grid, 192, Cf::kSmem, s>>>(ta, ta2, tb, p);
+  gemm_kernel<BN, MODE><<<grid, 192, Cf::kSmem, s>>>(ta, ta2, tb, to, to2, p);
   return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -88,6 +99,15 @@ int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int
     ta2 = ta;
   }
   if (!make_tmap(&tb, op.b, op.b_rows, op.b_cols, BN, bf16)) return MOE_ERR_CUDA;
+  CUtensorMap to = tb, to2 = tb;
+  if (mode == kWgrad) {
+    if (!make_tmap_out(&to, ep.out, static_cast<int64_t>(m.E) * M, N)) return MOE_ERR_CUDA;
+    if (m.S > 0 && ep.out2 != nullptr) {
+      if (!make_tmap_out(&to2, ep.out2, static_cast<int64_t>(m.S) * M, N)) return MOE_ERR_CUDA;
+    } else {
+      to2 = to;
+    }
+  }
 
   GemmParams p{};
   p.N = N;
@@ -137,18 +157,18 @@ int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int
   const int grid = static_cast<int>(upper < num_sms() ? upper : num_sms());
 
   switch (mode) {
-    case kSwigluFwd: return run<256, kSwigluFwd>(name, ta, ta2, tb, p, grid, s);
+    case kSwigluFwd: return run<256, kSwigluFwd>(name, ta, ta2, tb, to, to2, p, grid, s);
     case kSwigluBwd:
-      return BN == 256 ? run<256, kSwigluBwd>(name, ta, ta2, tb, p, grid, s) : run<128, kSwigluBwd>(name, ta, ta2, tb, p, grid, s);
+      return BN == 256 ? run<256, kSwigluBwd>(name, ta, ta2, tb, to, to2, p, grid, s) : run<128, kSwigluBwd>(name, ta, ta2, tb, to, to2, p, grid, s);
     case kPush:
-      return BN == 256 ? run<256, kPush>(name, ta, ta2, tb, p, grid, s) : run<128, kPush>(name, ta, ta2, tb, p, grid, s);
+      return BN == 256 ? run<256, kPush>(name, ta, ta2, tb, to, to2, p, grid, s) : run<128, kPush>(name, ta, ta2, tb, to, to2, p, grid, s);
     case kWgrad:
-      return BN == 256 ? run<256, kWgrad>(name, ta, ta2, tb, p, grid, s) : run<128, kWgrad>(name, ta, ta2, tb, p, grid, s);
+      return BN == 256 ? run<256, kWgrad>(name, ta, ta2, tb, to, to2, p, grid, s) : run<128, kWgrad>(name, ta, ta2, tb, to, to2, p, grid, s);
     case kPlain:
-      return BN == 256 ? run<256, kPlain>(name, ta, ta2, tb, p, grid, s) : run<128, kPlain>(name, ta, ta2, tb, p, grid, s);
+      return BN == 256 ? run<256, kPlain>(name, ta, ta2, tb, to, to2, p, grid, s) : run<128, kPlain>(name, ta, ta2, tb, to, to2, p, grid, s);
     case kRouterMode:
-      if (BN == 32) return run<32, kRouterMode>(name, ta, ta2, tb, p, grid, s);
-      return BN == 256 ? run<256, kRouterMode>(name, ta, ta2, tb, p, grid, s) : run<128, kRouterMode>(name, ta, ta2, tb, p, grid, s);
+      if (BN == 32) return run<32, kRouterMode>(name, ta, ta2, tb, to, to2, p, grid, s);
+      return BN == 256 ? run<256, kRouterMode>(name, ta, ta2, tb, to, to2, p, grid, s) : run<128, kRouterMode>(name, ta, ta2, tb, to, to2, p, grid, s);
     default: return MOE_ERR_INVALID_ARG;
   }
 }

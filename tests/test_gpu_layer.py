@@ -165,11 +165,20 @@ def test_quantised_activation_bytes(run):
     assert np.array_equal(xsf, run.f["xq"].scales)
 
 
-def test_ring_holds_last_laps(run):
-    """Ring of expert e after forward: slots of its final lap, and earlier-lap rows behind them."""
+def _rings(run, name):
+    """The two ring buffers [2][E][C][d] (codes) and their scales [2][E][C][d/32]."""
     m = run.shape
-    ring = run.u8("RING_X", m.E * m.C, m.d).reshape(m.E, m.C, m.d)
-    rsf = run.sf("RING_X_SF", m.E * m.C, m.d).reshape(m.E, m.C, m.d // 32)
+    rows = 2 * m.E * m.C
+    codes = run.u8(name, rows, m.d).reshape(2, m.E, m.C, m.d)
+    sf = run.sf(name + "_SF", rows, m.d).reshape(2, m.E, m.C, m.d // 32)
+    return codes, sf
+
+
+def test_ring_holds_last_laps(run):
+    """Lap L of an expert goes to ring buffer L % 2: after forward, buffer (last % 2) holds the
+    expert's final lap (zeros past it up to the tile end) and the other buffer its previous lap."""
+    m = run.shape
+    ring, rsf = _rings(run, "RING_X")
     sch = run.f["sched"]
     xq = run.f["xq"]
     wrapped = 0
@@ -180,17 +189,17 @@ def test_ring_holds_last_laps(run):
         a = OS.expert_rows(sch, e)
         last = (n - 1) // m.C
         lo = last * m.C
+        b = last % 2
         tok = a[lo:] // m.k
-        assert np.array_equal(ring[e, :n - lo], xq.codes[tok])
-        assert np.array_equal(rsf[e, :n - lo], xq.scales[tok])
+        assert np.array_equal(ring[b, e, :n - lo], xq.codes[tok])
+        assert np.array_equal(rsf[b, e, :n - lo], xq.scales[tok])
+        tail = slice(n - lo, -(-(n - lo) // 128) * 128)
+        assert not ring[b, e, tail].any() and not rsf[b, e, tail].any()
         if last > 0:
             wrapped += 1
             prev = a[(last - 1) * m.C:last * m.C] // m.k
-            tail = slice(n - lo, -(-(n - lo) // 128) * 128)
-            # rows of the final lap's last tile past the segment are cleared; later slots keep lap last-1
-            assert not ring[e, tail].any()
-            keep = -(-(n - lo) // 128) * 128
-            assert np.array_equal(ring[e, keep:], xq.codes[prev[keep:]])
+            assert np.array_equal(ring[1 - b, e], xq.codes[prev])
+            assert np.array_equal(rsf[1 - b, e], xq.scales[prev])
     if m.name != "tiny":
         assert wrapped > 0, "case should exercise ring wrap-around"
 
@@ -275,17 +284,19 @@ def test_reverse_combine(run):
 
 def test_dO_ring_holds_last_laps(run):
     m = run.shape
-    ring = run.u8("RING_DO", m.E * m.C, m.d).reshape(m.E, m.C, m.d)
-    rsf = run.sf("RING_DO_SF", m.E * m.C, m.d).reshape(m.E, m.C, m.d // 32)
+    ring, rsf = _rings(run, "RING_DO")
     sch = run.f["sched"]
     for e in range(m.E):
         n = sch["counts"][e]
         if n == 0:
             continue
         last = (n - 1) // m.C
+        b = last % 2
         dq = run.b["experts"][e]["dOq"]
-        assert np.array_equal(ring[e, :n - last * m.C], dq.codes[last * m.C:])
-        assert np.array_equal(rsf[e, :n - last * m.C], dq.scales[last * m.C:])
+        assert np.array_equal(ring[b, e, :n - last * m.C], dq.codes[last * m.C:])
+        assert np.array_equal(rsf[b, e, :n - last * m.C], dq.scales[last * m.C:])
+        if last > 0:
+            assert np.array_equal(ring[1 - b, e], dq.codes[(last - 1) * m.C:last * m.C])
 
 
 def test_dgrad_down_swiglu_stage(run):
