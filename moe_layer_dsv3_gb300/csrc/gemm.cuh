@@ -216,10 +216,31 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v
 
 __device__ __forceinline__ void load_bf16x32_g(const __nv_bfloat16* src, float* v) { load_bf16x32(src, v); }
 
+// Read this thread's whole accumulator row (BN fp32 columns) into packed bf16
+// pairs, then hand the TMEM buffer back to the MMA warp at once, so the next
+// tile's MMAs start while the row is still being written out.
+template <int BN>
+__device__ __forceinline__ void drain_acc_bf16(uint32_t tacc, bool have_acc, uint32_t* packed, uint64_t* acce) {
+#pragma unroll
+  for (int c = 0; c < BN / 32; ++c) {
+    float v[32];
+    if (have_acc) {
+      tmem_ld32(tacc + c * 32, v);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) packed[c * 16 + j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+  }
+  tc_fence_before();
+  mbar_arrive(acce);
+}
+
 template <int BN, int MODE>
 __device__ __forceinline__ void gemm_epilogue_tile(const GemmParams& p, const TileInfo& t, uint32_t tacc, int q,
                                                    int lane, float* scr, uint8_t* out_smem, const CUtensorMap* tma_o,
-                                                   const CUtensorMap* tma_o2) {
+                                                   const CUtensorMap* tma_o2, uint64_t* acce) {
   const int row = q * 32 + lane;
   const bool have_acc = t.nk > 0;
   const bool valid = row < t.valid;
@@ -275,37 +296,27 @@ __device__ __forceinline__ void gemm_epilogue_tile(const GemmParams& p, const Ti
   } else if constexpr (MODE == kPush) {
     const int64_t prow = t.prow0 + row;
     const int a = valid ? p.row_src[prow] : -1;
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
-#pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-      float v[32];
-      tmem_ld32(tacc + c * 32, v);
-      if (a >= 0) store_bf16x32(out + static_cast<int64_t>(a) * p.ldo + t.n0 + c * 32, v);
+    uint32_t packed[BN / 2];
+    drain_acc_bf16<BN>(tacc, true, packed, acce);
+    if (a >= 0) {
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(a) * p.ldo + t.n0);
+#pragma unroll
+      for (int i = 0; i < BN / 8; ++i)
+        dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
     }
   } else if constexpr (MODE == kWgrad) {
     // bf16 tile -> shared staging (boxes of 128 rows x 64 columns, 128-byte
     // swizzle) -> TMA store to dW[e][m0.., n0..]. One thread issues the stores.
     const bool leader = (q == 2 && lane == 0);
+    uint32_t packed[BN / 2];
+    drain_acc_bf16<BN>(tacc, have_acc, packed, acce);
     if (leader) bulk_wait_read_all();          // the previous tile's stores have read the staging
     named_barrier(1, 128);
-#pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-      float v[32];
-      if (have_acc) {
-        tmem_ld32(tacc + c * 32, v);
-      } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = 0.0f;
-      }
-      uint8_t* box = out_smem + (c >> 1) * (128 * 128) + row * 128;
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int j = (c & 1) * 4 + q4;
-        const float* w = v + 8 * q4;
-        *reinterpret_cast<uint4*>(box + ((j ^ (row & 7)) << 4)) =
-            make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]), pack_bf16x2(w[4], w[5]),
-                       pack_bf16x2(w[6], w[7]));
-      }
+    for (int i = 0; i < BN / 8; ++i) {         // 16-byte chunk i of the row: box i / 8, chunk i % 8
+      uint8_t* box = out_smem + (i >> 3) * (128 * 128) + row * 128;
+      *reinterpret_cast<uint4*>(box + (((i & 7) ^ (row & 7)) << 4)) =
+          make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
     }
     fence_proxy_async();
     named_barrier(1, 128);
@@ -475,9 +486,11 @@ __global__ void __launch_bounds__(192, 1)
       if (!mbar_wait(&accf[acc], acc_phase, p.status, 30)) break;
       tc_fence_after();
       gemm_epilogue_tile<BN, MODE>(p, t, tmem + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(q * 32) << 16),
-                                   q, lane, scr, out_smem, &tma_o, &tma_o2);
-      tc_fence_before();
-      mbar_arrive(&acce[acc]);
+                                   q, lane, scr, out_smem, &tma_o, &tma_o2, &acce[acc]);
+      if constexpr (MODE != kPush && MODE != kWgrad) {   // those release TMEM inside the epilogue
+        tc_fence_before();
+        mbar_arrive(&acce[acc]);
+      }
       if (++acc == Cf::kNumAcc) { acc = 0; acc_phase ^= 1u; }
     }
     if (Cf::kTmaOut && q == 2 && lane == 0) bulk_wait_all();

@@ -85,7 +85,7 @@ int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int
   if (!get_encode()) return MOE_ERR_CUDA;
   const bool bf16 = mode == kRouterMode;
   int BN;
-  if (mode == kSwigluFwd) BN = 256;
+  if (mode == kSwigluFwd) BN = kGemm1BN;
   else if (mode == kRouterMode) BN = N <= 32 ? 32 : (N % 256 == 0 ? 256 : 128);
   else if ((bn_hint == 128 || bn_hint == 256) && N % bn_hint == 0) BN = bn_hint;
   else BN = (N % 256 == 0) ? 256 : 128;
@@ -157,7 +157,9 @@ int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int
   const int grid = static_cast<int>(upper < num_sms() ? upper : num_sms());
 
   switch (mode) {
-    case kSwigluFwd: return run<256, kSwigluFwd>(name, ta, ta2, tb, to, to2, p, grid, s);
+    case kSwigluFwd:
+      if (BN == 128) return run<128, kSwigluFwd>(name, ta, ta2, tb, to, to2, p, grid, s);
+      return run<256, kSwigluFwd>(name, ta, ta2, tb, to, to2, p, grid, s);
     case kSwigluBwd:
       return BN == 256 ? run<256, kSwigluBwd>(name, ta, ta2, tb, to, to2, p, grid, s) : run<128, kSwigluBwd>(name, ta, ta2, tb, to, to2, p, grid, s);
     case kPush:

@@ -7,13 +7,13 @@
 namespace moe {
 
 // Row of the interleaved GEMM1 weight layout for source row r of w_gu:
-// blocks of 128 gate rows followed by the matching 128 up rows.
+// blocks of kGuBlock gate rows followed by the matching kGuBlock up rows.
 __device__ __forceinline__ int64_t gu_interleave_row(int64_t r, int I) {
   const int64_t e = r / (2 * I);
   const int64_t i = r % (2 * I);
   const int64_t up = i >= I ? 1 : 0;
   const int64_t ii = i - up * I;
-  return e * 2 * I + (ii >> 7) * 256 + up * 128 + (ii & 127);
+  return e * 2 * I + (ii / kGuBlock) * (2 * kGuBlock) + up * kGuBlock + (ii % kGuBlock);
 }
 
 // One thread per 32-element block along K.
@@ -82,7 +82,7 @@ __device__ __forceinline__ float bf16_lane(const uint2& u, int j) {
   return (j & 1) ? __uint_as_float(w & 0xFFFF0000u) : __uint_as_float(w << 16);
 }
 
-__global__ void __launch_bounds__(kTokThreads) tok_gather_kernel(
+__global__ void __launch_bounds__(kTokThreads, 2) tok_gather_kernel(
     const __nv_bfloat16* __restrict__ src, const int* __restrict__ row_src, const int* __restrict__ poff_end, int T,
     int k, int d, int64_t Rmax, const float* __restrict__ topk_w, int scale_by_gate, const float* __restrict__ dl,
     float* __restrict__ part, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {

@@ -12,6 +12,11 @@ constexpr int kTileM = 128;     // rows per GEMM tile / scale atom
 constexpr int kTileK = 128;     // fp8 elements per K stage (one 128-byte swizzle row)
 constexpr int kSchedUnit = 256; // assignments per schedule unit (one warp)
 constexpr int kRingBufs = 2;    // ring token buffers, used by alternate laps
+// Tile width of the GEMM1 (gate|up) kernel. Its weight rows are interleaved
+// in blocks of kGemm1BN / 2 gate rows followed by the matching up rows, so a
+// tile holds matching g and u columns.
+constexpr int kGemm1BN = 256;
+constexpr int kGuBlock = kGemm1BN / 2;
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
