@@ -14,6 +14,7 @@ points"), made concrete:
   dsv3_fwd    T=4096   d=7168  E=256 (+1) k=8 G=8/4 I=2048 bias N(0,0.1)
   dsv3_zipf   T=16384  d=7168  E=256 (+1) k=8 G=8/4 I=2048 bias Zipf(1.1), C=640
   e384        T in {512..65536} d=7168 E=384 (+1) k=8 G=1/1 I=2048 bias 0
+  dsv3_e64    T=4096   d=7168  E=64 (+1)  k=8 G=8/4 I=2048 bias N(0,0.1)  (profiling case)
 
 Value recipe: x ~ N(0,1), dy ~ N(0,1) (seed+1), router W ~ N(0,0.02),
 expert and shared-expert W ~ N(0, w_std); all drawn in fp32 by torch's
@@ -74,6 +75,10 @@ def config(name: str, T: int | None = None) -> LayerShape:
         # capacity 1.25 * T * k / E, rounded to the 128-row tile
         cap = _ceil(int(round(1.25 * t * 8 / 256)), 128)
         return make_shape("dsv3_zipf", t, 7168, 256, 8, 8, 4, 2048, 1, "zipf1.1", 0.006, C=cap)
+    if name == "dsv3_e64":
+        # DSV3 expert shape with a quarter of the experts and tokens: the same mean
+        # rows per expert (512) in a few GB, for detailed kernel profiles.
+        return make_shape("dsv3_e64", T or 4096, 7168, 64, 8, 8, 4, 2048, 1, "normal0.1", 0.006)
     if name == "e384":
         return make_shape("e384", T or 4096, 7168, 384, 8, 1, 1, 2048, 1, "zero", 0.006)
     raise KeyError(name)

@@ -237,10 +237,50 @@ __device__ __forceinline__ void drain_acc_bf16(uint32_t tacc, bool have_acc, uin
   mbar_arrive(acce);
 }
 
+// SwiGLU backward reads the saved bf16 g,u of its rows. The epilogue warps
+// issue those loads before waiting for the accumulator, so their latency
+// hides behind the tile's mainloop.
+template <int BN, int MODE>
+struct GuPrefetch {
+  static constexpr int kN = MODE == kSwigluBwd ? (BN / 32) * 8 : 1;
+  uint4 v[kN];
+};
+
+template <int BN, int MODE>
+__device__ __forceinline__ void prefetch_gu(const GemmParams& p, const TileInfo& t, int row, GuPrefetch<BN, MODE>& g) {
+  if constexpr (MODE == kSwigluBwd) {
+    const bool valid = row < t.valid;
+    const int64_t prow = t.prow0 + row;
+#pragma unroll
+    for (int c = 0; c < BN / 32; ++c) {
+      const uint4* pg = reinterpret_cast<const uint4*>(p.gu + prow * (2 * p.I) + t.n0 + c * 32);
+      const uint4* pu = reinterpret_cast<const uint4*>(p.gu + prow * (2 * p.I) + p.I + t.n0 + c * 32);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        g.v[c * 8 + i] = valid ? pg[i] : make_uint4(0, 0, 0, 0);
+        g.v[c * 8 + 4 + i] = valid ? pu[i] : make_uint4(0, 0, 0, 0);
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void unpack_bf16x32(const uint4* q, float* v) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t w[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[8 * k + 2 * i] = __uint_as_float(w[i] << 16);
+      v[8 * k + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+}
+
 template <int BN, int MODE>
 __device__ __forceinline__ void gemm_epilogue_tile(const GemmParams& p, const TileInfo& t, uint32_t tacc, int q,
                                                    int lane, float* scr, uint8_t* out_smem, const CUtensorMap* tma_o,
-                                                   const CUtensorMap* tma_o2, uint64_t* acce) {
+                                                   const CUtensorMap* tma_o2, uint64_t* acce,
+                                                   const GuPrefetch<BN, MODE>& gp) {
   const int row = q * 32 + lane;
   const bool have_acc = t.nk > 0;
   const bool valid = row < t.valid;
@@ -267,15 +307,13 @@ __device__ __forceinline__ void gemm_epilogue_tile(const GemmParams& p, const Ti
   } else if constexpr (MODE == kSwigluBwd) {
     const int64_t prow = t.prow0 + row;
     const int I = p.I;
-#pragma unroll 1
+#pragma unroll
     for (int c = 0; c < BN / 32; ++c) {
       float dh[32], g[32], u[32], dg[32], du[32];
       tmem_ld32(tacc + c * 32, dh);
       const int64_t icol = t.n0 + c * 32;
-      if (valid) {
-        load_bf16x32_g(p.gu + prow * (2 * I) + icol, g);
-        load_bf16x32_g(p.gu + prow * (2 * I) + I + icol, u);
-      }
+      unpack_bf16x32(&gp.v[c * 8], g);
+      unpack_bf16x32(&gp.v[c * 8 + 4], u);
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         if (valid) {
@@ -483,10 +521,12 @@ __global__ void __launch_bounds__(192, 1)
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
       TileInfo t;
       if (!gemm_decode<BN, MODE>(p, tile, t)) continue;
+      GuPrefetch<BN, MODE> gp;
+      prefetch_gu<BN, MODE>(p, t, q * 32 + lane, gp);
       if (!mbar_wait(&accf[acc], acc_phase, p.status, 30)) break;
       tc_fence_after();
       gemm_epilogue_tile<BN, MODE>(p, t, tmem + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(q * 32) << 16),
-                                   q, lane, scr, out_smem, &tma_o, &tma_o2, &acce[acc]);
+                                   q, lane, scr, out_smem, &tma_o, &tma_o2, &acce[acc], gp);
       if constexpr (MODE != kPush && MODE != kWgrad) {   // those release TMEM inside the epilogue
         tc_fence_before();
         mbar_arrive(&acce[acc]);
