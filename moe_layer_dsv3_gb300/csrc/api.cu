@@ -41,14 +41,16 @@ namespace {
 
 inline cudaStream_t S(moe_stream_t s) { return static_cast<cudaStream_t>(s); }
 
-// Consecutive ring laps alternate between the caller's stream and one
-// auxiliary stream per device (and between the two ring buffers), so a lap's
-// dispatch and GEMM overlap the previous lap's GEMM. The fork and join are
-// event record / wait pairs on the caller's stream.
+// Ring lap L runs on lap stream L % kRingBufs (stream 0 is the caller's, the
+// others are auxiliary streams of this device) and uses ring buffer
+// L % kRingBufs, so up to kRingBufs laps are in flight: a lap waits only for
+// the lap that used its ring buffer before. Fork and join are event record /
+// wait pairs on the caller's stream.
 struct LapStreams {
   std::mutex mu;
-  cudaStream_t aux = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
+  cudaStream_t aux[kRingBufs - 1] = {};
+  cudaEvent_t fork = nullptr;
+  cudaEvent_t join[kRingBufs - 1] = {};
 };
 constexpr int kMaxDev = 64;
 LapStreams g_lap[kMaxDev];
@@ -58,11 +60,12 @@ LapStreams* lap_streams() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
   LapStreams& l = g_lap[dev];
   std::lock_guard<std::mutex> lk(l.mu);
-  if (l.aux == nullptr) {
-    if (cudaStreamCreateWithFlags(&l.aux, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaEventCreateWithFlags(&l.fork, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&l.join, cudaEventDisableTiming) != cudaSuccess)
-      return nullptr;
+  if (l.fork == nullptr) {
+    for (int i = 0; i < kRingBufs - 1; ++i)
+      if (cudaStreamCreateWithFlags(&l.aux[i], cudaStreamNonBlocking) != cudaSuccess ||
+          cudaEventCreateWithFlags(&l.join[i], cudaEventDisableTiming) != cudaSuccess)
+        return nullptr;
+    if (cudaEventCreateWithFlags(&l.fork, cudaEventDisableTiming) != cudaSuccess) return nullptr;
   }
   return &l;
 }
@@ -345,21 +348,24 @@ int moe_forward(const moe_config_t* cfg, const void* x, const void* wq, const fl
     if (ls == nullptr) return MOE_ERR_CUDA;
     std::lock_guard<std::mutex> lk(ls->mu);
     cudaEventRecord(ls->fork, s);
-    cudaStreamWaitEvent(ls->aux, ls->fork, 0);
+    for (int i = 0; i < kRingBufs - 1; ++i) cudaStreamWaitEvent(ls->aux[i], ls->fork, 0);
     const uint8_t* ring = op1.a;
     const uint8_t* ring_sf = op1.a_sf;
     const size_t rb = static_cast<size_t>(m.E) * m.C * m.d;
     int rc = MOE_OK;
     for (int lap = 0; lap < m.Lb && rc == MOE_OK; ++lap) {
-      cudaStream_t cs = (lap & 1) ? ls->aux : s;
-      op1.a = ring + (lap & 1) * rb;
-      op1.a_sf = ring_sf + (lap & 1) * rb / 32;
+      const int rbuf = lap % kRingBufs;
+      cudaStream_t cs = rbuf ? ls->aux[rbuf - 1] : s;
+      op1.a = ring + rbuf * rb;
+      op1.a_sf = ring_sf + rbuf * rb / 32;
       launch_permute_lap(m, lap, L, ws, cs);
       rc = gemm_dispatch("gemm1_fwd", kSwigluFwd, m, lap, 2 * m.I, m.d, 0, op1, ep1, counts, poff, lap_tiles, row_src,
                          status, cs);
     }
-    cudaEventRecord(ls->join, ls->aux);
-    cudaStreamWaitEvent(s, ls->join, 0);
+    for (int i = 0; i < kRingBufs - 1; ++i) {
+      cudaEventRecord(ls->join[i], ls->aux[i]);
+      cudaStreamWaitEvent(s, ls->join[i], 0);
+    }
     if (rc) return rc;
   }
   GemmOperands op2{};
@@ -451,21 +457,24 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
     if (ls == nullptr) return MOE_ERR_CUDA;
     std::lock_guard<std::mutex> lk(ls->mu);
     cudaEventRecord(ls->fork, s);
-    cudaStreamWaitEvent(ls->aux, ls->fork, 0);
+    for (int i = 0; i < kRingBufs - 1; ++i) cudaStreamWaitEvent(ls->aux[i], ls->fork, 0);
     const uint8_t* ring = opb2.a;
     const uint8_t* ring_sf = opb2.a_sf;
     const size_t rb = static_cast<size_t>(m.E) * m.C * m.d;
     int rc = MOE_OK;
     for (int lap = 0; lap < m.Lb && rc == MOE_OK; ++lap) {
-      cudaStream_t cs = (lap & 1) ? ls->aux : s;
-      opb2.a = ring + (lap & 1) * rb;
-      opb2.a_sf = ring_sf + (lap & 1) * rb / 32;
+      const int rbuf = lap % kRingBufs;
+      cudaStream_t cs = rbuf ? ls->aux[rbuf - 1] : s;
+      opb2.a = ring + rbuf * rb;
+      opb2.a_sf = ring_sf + rbuf * rb / 32;
       launch_rev_combine_lap(m, lap, dy, topk_w, L, ws, cs);
       rc = gemm_dispatch("gemm_dgrad_down", kSwigluBwd, m, lap, m.I, m.d, 0, opb2, epb2, counts, poff, lap_tiles,
                          row_src, status, cs, 128);
     }
-    cudaEventRecord(ls->join, ls->aux);
-    cudaStreamWaitEvent(s, ls->join, 0);
+    for (int i = 0; i < kRingBufs - 1; ++i) {
+      cudaEventRecord(ls->join[i], ls->aux[i]);
+      cudaStreamWaitEvent(s, ls->join[i], 0);
+    }
     if (rc) return rc;
   }
   // dgrad of GEMM1: DX rows pushed to their assignment.

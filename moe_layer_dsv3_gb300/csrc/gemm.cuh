@@ -46,7 +46,7 @@ struct GemmCfg {
   // Weight gradients stage their bf16 output tile in shared memory and write
   // it with TMA stores, so the tile's DRAM write overlaps the next mainloop.
   static constexpr bool kTmaOut = MODE == kWgrad;
-  static constexpr int kStages = kTmaOut ? 3 : (BN >= 256 ? 4 : (BN >= 128 ? 6 : 8));
+  static constexpr int kStages = kTmaOut ? (BN >= 256 ? 3 : 5) : (BN >= 256 ? 4 : (BN >= 128 ? 6 : 8));
   static constexpr int kOutBytes = kTmaOut ? 128 * BN * 2 : 0;
   static constexpr int kABytes = 128 * 128;
   static constexpr int kBBytes = BN * 128;
@@ -288,21 +288,30 @@ __device__ __forceinline__ void gemm_epilogue_tile(const GemmParams& p, const Ti
     const int64_t prow = t.prow0 + row;
     const int I = p.I;
     const int i_base = t.n0 / 2;                     // interleaved: BN/2 gate + BN/2 up columns
-#pragma unroll 1
+    // Drain g, u from TMEM (saving them as bf16) and keep h in registers, then
+    // hand the accumulator back before the two MX quantisations of h.
+    float h[BN / 2];
+#pragma unroll
     for (int c = 0; c < BN / 64; ++c) {
-      float g[32], u[32], h[32];
+      float g[32], u[32];
       tmem_ld32(tacc + c * 32, g);
       tmem_ld32(tacc + BN / 2 + c * 32, u);
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         if (!valid) { g[j] = 0.0f; u[j] = 0.0f; }
-        h[j] = g[j] / (1.0f + __expf(-g[j])) * u[j];
+        h[c * 32 + j] = g[j] / (1.0f + __expf(-g[j])) * u[j];
       }
       const int64_t icol = i_base + c * 32;
       store_bf16x32(p.gu + prow * (2 * I) + icol, g);
       store_bf16x32(p.gu + prow * (2 * I) + I + icol, u);
-      emit_rowq(h, p.q_rows + prow * I + icol, p.q_rows_sf + sf_off(prow, icol >> 5, p.q_rows_ktiles));
-      emit_tokq(h, scr, lane, p.q_tok, p.q_tok_sf, p.q_tok_pitch, icol, t.prow0 + q * 32);
+    }
+    tc_fence_before();
+    mbar_arrive(acce);
+#pragma unroll
+    for (int c = 0; c < BN / 64; ++c) {
+      const int64_t icol = i_base + c * 32;
+      emit_rowq(&h[c * 32], p.q_rows + prow * I + icol, p.q_rows_sf + sf_off(prow, icol >> 5, p.q_rows_ktiles));
+      emit_tokq(&h[c * 32], scr, lane, p.q_tok, p.q_tok_sf, p.q_tok_pitch, icol, t.prow0 + q * 32);
     }
   } else if constexpr (MODE == kSwigluBwd) {
     const int64_t prow = t.prow0 + row;
@@ -527,7 +536,7 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
       gemm_epilogue_tile<BN, MODE>(p, t, tmem + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(q * 32) << 16),
                                    q, lane, scr, out_smem, &tma_o, &tma_o2, &acce[acc], gp);
-      if constexpr (MODE != kPush && MODE != kWgrad) {   // those release TMEM inside the epilogue
+      if constexpr (MODE != kPush && MODE != kWgrad && MODE != kSwigluFwd) {   // those release TMEM inside
         tc_fence_before();
         mbar_arrive(&acce[acc]);
       }

@@ -287,8 +287,8 @@ void launch_permute_lap(const Dims& m, int lap, const Layout& L, void* ws, cudaS
   permute_lap_kernel<<<blocks, 256, 0, s>>>(
       ws_ptr<uint8_t>(L, ws, MOE_WS_XQ), ws_ptr<uint8_t>(L, ws, MOE_WS_XQ_SF), ws_ptr<int>(L, ws, MOE_WS_LAPTILES),
       ws_ptr<int>(L, ws, MOE_WS_COUNTS), ws_ptr<int>(L, ws, MOE_WS_POFF), ws_ptr<int>(L, ws, MOE_WS_ROWSRC), m.T, m.k,
-      m.d, m.E, m.Ep, m.C, lap, ws_ptr<uint8_t>(L, ws, MOE_WS_RING_X) + (lap & 1) * ring_bytes(m),
-      ws_ptr<uint8_t>(L, ws, MOE_WS_RING_X_SF) + (lap & 1) * ring_bytes(m) / 32);
+      m.d, m.E, m.Ep, m.C, lap, ws_ptr<uint8_t>(L, ws, MOE_WS_RING_X) + (lap % kRingBufs) * ring_bytes(m),
+      ws_ptr<uint8_t>(L, ws, MOE_WS_RING_X_SF) + (lap % kRingBufs) * ring_bytes(m) / 32);
 }
 
 void launch_rev_combine_lap(const Dims& m, int lap, const void* dy, const float* topk_w, const Layout& L, void* ws,
@@ -299,8 +299,8 @@ void launch_rev_combine_lap(const Dims& m, int lap, const void* dy, const float*
   rev_combine_lap_kernel<<<blocks, 256, 0, s>>>(
       static_cast<const __nv_bfloat16*>(dy), topk_w, ws_ptr<int>(L, ws, MOE_WS_LAPTILES),
       ws_ptr<int>(L, ws, MOE_WS_COUNTS), ws_ptr<int>(L, ws, MOE_WS_POFF), ws_ptr<int>(L, ws, MOE_WS_ROWSRC), m.T, m.k,
-      m.d, m.E, m.Ep, m.C, lap, ws_ptr<uint8_t>(L, ws, MOE_WS_RING_DO) + (lap & 1) * ring_bytes(m),
-      ws_ptr<uint8_t>(L, ws, MOE_WS_RING_DO_SF) + (lap & 1) * ring_bytes(m) / 32);
+      m.d, m.E, m.Ep, m.C, lap, ws_ptr<uint8_t>(L, ws, MOE_WS_RING_DO) + (lap % kRingBufs) * ring_bytes(m),
+      ws_ptr<uint8_t>(L, ws, MOE_WS_RING_DO_SF) + (lap % kRingBufs) * ring_bytes(m) / 32);
 }
 
 void launch_combine(const Dims& m, const float* topk_w, const Layout& L, void* ws, void* y, cudaStream_t s) {

@@ -11,7 +11,7 @@ namespace moe {
 constexpr int kTileM = 128;     // rows per GEMM tile / scale atom
 constexpr int kTileK = 128;     // fp8 elements per K stage (one 128-byte swizzle row)
 constexpr int kSchedUnit = 256; // assignments per schedule unit (one warp)
-constexpr int kRingBufs = 2;    // ring token buffers, used by alternate laps
+constexpr int kRingBufs = 2;    // ring token buffers; lap L uses buffer L % kRingBufs
 // Tile width of the GEMM1 (gate|up) kernel. Its weight rows are interleaved
 // in blocks of kGemm1BN / 2 gate rows followed by the matching up rows, so a
 // tile holds matching g and u columns.

@@ -165,18 +165,22 @@ def test_quantised_activation_bytes(run):
     assert np.array_equal(xsf, run.f["xq"].scales)
 
 
+NBUF = 2     # ring buffers; lap L of an expert uses buffer L % NBUF
+
+
 def _rings(run, name):
-    """The two ring buffers [2][E][C][d] (codes) and their scales [2][E][C][d/32]."""
+    """The ring buffers [NBUF][E][C][d] (codes) and their scales [NBUF][E][C][d/32]."""
     m = run.shape
-    rows = 2 * m.E * m.C
-    codes = run.u8(name, rows, m.d).reshape(2, m.E, m.C, m.d)
-    sf = run.sf(name + "_SF", rows, m.d).reshape(2, m.E, m.C, m.d // 32)
+    rows = NBUF * m.E * m.C
+    codes = run.u8(name, rows, m.d).reshape(NBUF, m.E, m.C, m.d)
+    sf = run.sf(name + "_SF", rows, m.d).reshape(NBUF, m.E, m.C, m.d // 32)
     return codes, sf
 
 
 def test_ring_holds_last_laps(run):
-    """Lap L of an expert goes to ring buffer L % 2: after forward, buffer (last % 2) holds the
-    expert's final lap (zeros past it up to the tile end) and the other buffer its previous lap."""
+    """Lap L of an expert goes to ring buffer L % NBUF: after forward, buffer (last % NBUF) holds
+    the expert's final lap (zeros past it up to the tile end) and buffer ((last-1) % NBUF) its
+    previous lap."""
     m = run.shape
     ring, rsf = _rings(run, "RING_X")
     sch = run.f["sched"]
@@ -189,7 +193,7 @@ def test_ring_holds_last_laps(run):
         a = OS.expert_rows(sch, e)
         last = (n - 1) // m.C
         lo = last * m.C
-        b = last % 2
+        b = last % NBUF
         tok = a[lo:] // m.k
         assert np.array_equal(ring[b, e, :n - lo], xq.codes[tok])
         assert np.array_equal(rsf[b, e, :n - lo], xq.scales[tok])
@@ -198,8 +202,8 @@ def test_ring_holds_last_laps(run):
         if last > 0:
             wrapped += 1
             prev = a[(last - 1) * m.C:last * m.C] // m.k
-            assert np.array_equal(ring[1 - b, e], xq.codes[prev])
-            assert np.array_equal(rsf[1 - b, e], xq.scales[prev])
+            assert np.array_equal(ring[(last - 1) % NBUF, e], xq.codes[prev])
+            assert np.array_equal(rsf[(last - 1) % NBUF, e], xq.scales[prev])
     if m.name != "tiny":
         assert wrapped > 0, "case should exercise ring wrap-around"
 
@@ -291,12 +295,12 @@ def test_dO_ring_holds_last_laps(run):
         if n == 0:
             continue
         last = (n - 1) // m.C
-        b = last % 2
+        b = last % NBUF
         dq = run.b["experts"][e]["dOq"]
         assert np.array_equal(ring[b, e, :n - last * m.C], dq.codes[last * m.C:])
         assert np.array_equal(rsf[b, e, :n - last * m.C], dq.scales[last * m.C:])
         if last > 0:
-            assert np.array_equal(ring[1 - b, e], dq.codes[(last - 1) * m.C:last * m.C])
+            assert np.array_equal(ring[(last - 1) % NBUF, e], dq.codes[(last - 1) * m.C:last * m.C])
 
 
 def test_dgrad_down_swiglu_stage(run):
