@@ -157,14 +157,22 @@ def oracle_sample(shape, host, idx_full=None, n_experts=2, shared_rows=256, seed
     order = np.argsort(np.abs(counts - counts.mean()), kind="stable")
     experts = [int(e) for e in order[:n_experts] if counts[e] > 0]
     rng = np.random.default_rng(seed)
+    wcache = host.setdefault("_weights", {})      # MX weights are prepared once, outside the timing
+
+    def expert_weights(e):
+        if e not in wcache:
+            if e < E:
+                wcache[e] = OL.ExpertWeights(host["w_gu_of"](e), host["w_d_of"](e))
+            else:
+                wcache[e] = OL.ExpertWeights(host["ws_gu_of"](e - E), host["ws_d_of"](e - E))
+        return wcache[e]
+
     prepared = []
     for e in experts:
-        wgu = host["w_gu_of"](e)
-        wd = host["w_d_of"](e)
-        prepared.append(("routed", e, OL.ExpertWeights(wgu, wd), OS.expert_rows(sch, e) // k))
+        prepared.append(("routed", e, expert_weights(e), OS.expert_rows(sch, e) // k))
     if S:
         toks = np.sort(rng.choice(T, min(shared_rows, T), replace=False))
-        prepared.append(("shared", E, OL.ExpertWeights(host["ws_gu_of"](0), host["ws_d_of"](0)), toks))
+        prepared.append(("shared", E, expert_weights(E), toks))
     dy = host["dy"]
     rows_done = 0
     t0 = time.perf_counter()
@@ -423,6 +431,16 @@ def run_ours(args, rank, world, local_rank):
         v, desc = oracle_sample(shape, host, idx_full=idx)
         cpu = {"value": v, "unit": "tokens/s", "cores": cores(), "kind": "oracle", "sample": desc}
     counts = L.ws_tensor("COUNTS", torch.int32, (shape.E + shape.S,)).cpu().numpy()[:shape.E]
+    # Waves of each grouped GEMM: output tiles / SM count (the commentary's rule asks for >= 2).
+    sms = torch.cuda.get_device_properties(local_rank).multi_processor_count
+    all_counts = L.ws_tensor("COUNTS", torch.int32, (shape.E + shape.S,)).cpu().numpy().astype(np.int64)
+    mt = int(((all_counts + 127) // 128).sum())
+    E_all = shape.E + shape.S
+    extra["waves"] = {"sm_count": sms,
+                      "gemm1_fwd": mt * (2 * shape.I // 256) / sms, "gemm2_fwd": mt * (shape.d // 256) / sms,
+                      "gemm_dgrad_down": mt * (shape.I // 128) / sms, "gemm_dgrad_gu": mt * (shape.d // 256) / sms,
+                      "gemm_wgrad_d": E_all * (shape.d // 128) * (shape.I // 256) / sms,
+                      "gemm_wgrad_gu": E_all * (2 * shape.I // 128) * (shape.d // 256) / sms}
     extra["routing"] = {"max_count": int(counts.max()), "min_count": int(counts.min()),
                         "laps": int(L.ws_tensor("META", torch.int32, (16,))[0].item()),
                         "ring_capacity": shape.C}
