@@ -209,6 +209,7 @@ enum {
   MOE_WS_XTOK_SF,
   MOE_WS_DXE,          /* bf16[T*(k+S)][d]  expert input gradients per assignment */
   MOE_WS_DWR_PART,     /* fp32[Rmax/32][d]  router weight-gradient partial sums */
+  MOE_WS_ORDER,        /* int32[E+S]   experts by descending count (ties: lower index first) */
   MOE_WS_COUNT
 };
 MOE_API int moe_ws_view(const moe_config_t* cfg, void* ws, int which, void** ptr, size_t* bytes);

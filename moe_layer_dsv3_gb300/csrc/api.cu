@@ -162,6 +162,7 @@ Layout make_layout(const moe_config_t* c) {
   b.add(L.off, L.bytes, MOE_WS_XTOK_SF, d * R / 32);
   b.add(L.off, L.bytes, MOE_WS_DXE, 2 * Ap * d);
   b.add(L.off, L.bytes, MOE_WS_DWR_PART, 4 * (R / 32) * d);
+  b.add(L.off, L.bytes, MOE_WS_ORDER, 4 * Ep);
   L.total = b.cur;
   return L;
 }
@@ -506,7 +507,7 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
   epw.out = dw_d;
   epw.out2 = dws_d;
   epw.ldo = m.I;
-  if (int r = gemm_dispatch("gemm_wgrad_d", kWgrad, m, 0, m.I, 0, m.d, opw, epw, counts, poff, lap_tiles, row_src, status, s, 256)) return r;
+  if (int r = gemm_dispatch("gemm_wgrad_d", kWgrad, m, 0, m.I, 0, m.d, opw, epw, counts, poff, lap_tiles, row_src, status, s, 256, ws_ptr<int>(L, ws, MOE_WS_ORDER))) return r;
   opw.a = ws_ptr<uint8_t>(L, ws, MOE_WS_DGUTOK);
   opw.a_rows = 2 * m.I;
   opw.a_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_DGUTOK_SF);
@@ -516,7 +517,7 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
   epw.out = dw_gu;
   epw.out2 = dws_gu;
   epw.ldo = m.d;
-  if (int r = gemm_dispatch("gemm_wgrad_gu", kWgrad, m, 0, m.d, 0, 2 * m.I, opw, epw, counts, poff, lap_tiles, row_src, status, s, 256))
+  if (int r = gemm_dispatch("gemm_wgrad_gu", kWgrad, m, 0, m.d, 0, 2 * m.I, opw, epw, counts, poff, lap_tiles, row_src, status, s, 256, ws_ptr<int>(L, ws, MOE_WS_ORDER)))
     return r;
   // Reverse-dispatch (+ router input gradient) and the router weight gradient.
   launch_reverse_dispatch(m, topk_idx, w_router, L, ws, dx, s);

@@ -30,6 +30,7 @@ struct GemmParams {
   int a_ktiles, b_ktiles;// 128-wide K tiles per row of the stored A / B operand (scale atoms)
   const uint8_t* a_sf; const uint8_t* a2_sf; const uint8_t* b_sf;
   const int* counts; const int* poff; const int* lap_tiles; const int* row_src;
+  const int* order;      // experts by descending count (weight-gradient tile order)
   int E, Ep, C, lap, T, k;
   int M;                 // plain / router / wgrad output rows per expert
   int static_tiles;      // tile count when it does not depend on the schedule
@@ -97,6 +98,12 @@ __device__ __forceinline__ int gemm_num_tiles(const GemmParams& p) {
     return p.lap_tiles[p.lap * (p.Ep + 1) + p.Ep] * (p.N / BN);
   } else if constexpr (MODE == kPush) {
     return (p.poff[p.Ep] / 128) * (p.N / BN);
+  } else if constexpr (MODE == kWgrad) {
+    // positions of the two-ended schedule (see gemm_decode): enough rounds for the heavy half
+    const int g = gridDim.x;
+    if (g < 2 || (g & 1)) return p.static_tiles;
+    const int heavy = (p.static_tiles + 1) / 2;
+    return ((heavy + g / 2 - 1) / (g / 2)) * g;
   } else {
     return p.static_tiles;
   }
@@ -144,10 +151,29 @@ __device__ __forceinline__ bool gemm_decode(const GemmParams& p, int tile, TileI
     t.m0 = 0;
     return true;
   } else if constexpr (MODE == kWgrad) {
+    // Two-ended schedule: in each round half of the CTAs take the next tile from
+    // the front of the tile list (experts with the most tokens: long K,
+    // compute-bound) and half from the back (experts with few or no tokens:
+    // bound by writing their gradient tile); a CTA alternates ends from round
+    // to round. Compute and DRAM writes then overlap throughout the launch.
     const int nt = p.N / BN, mt = p.M / 128;
     const int per = nt * mt;
-    const int e = tile / per;
-    const int rem = tile - e * per;
+    const int N = p.static_tiles;
+    int q = tile;
+    const int g = gridDim.x;
+    if (g >= 2 && !(g & 1)) {
+      const int round = tile / g, b = tile - round * g;
+      const int k = round * (g / 2) + (b >> 1);
+      if (((b + round) & 1) == 0) {
+        if (k >= (N + 1) / 2) return false;
+        q = k;
+      } else {
+        if (k >= N / 2) return false;
+        q = N - 1 - k;
+      }
+    }
+    const int e = p.order[q / per];
+    const int rem = q - (q / per) * per;
     const int mi = rem / nt, n = rem - (rem / nt) * nt;
     t.e = e;
     t.use_a2 = false;
@@ -221,17 +247,28 @@ __device__ __forceinline__ void load_bf16x32_g(const __nv_bfloat16* src, float* 
 // tile's MMAs start while the row is still being written out.
 template <int BN>
 __device__ __forceinline__ void drain_acc_bf16(uint32_t tacc, bool have_acc, uint32_t* packed, uint64_t* acce) {
+  if (have_acc) {
+    // two loads in flight per wait
 #pragma unroll
-  for (int c = 0; c < BN / 32; ++c) {
-    float v[32];
-    if (have_acc) {
-      tmem_ld32(tacc + c * 32, v);
-    } else {
+    for (int c = 0; c < BN / 32; c += 2) {
+      uint32_t r0[32], r1[32];
+      tmem_ld32_async(tacc + c * 32, r0);
+      tmem_ld32_async(tacc + (c + 1) * 32, r1);
+      tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+      for (int j = 0; j < 32; ++j) {
+        reg_fence(r0[j]);
+        reg_fence(r1[j]);
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        packed[c * 16 + j] = pack_bf16x2(__uint_as_float(r0[2 * j]), __uint_as_float(r0[2 * j + 1]));
+        packed[(c + 1) * 16 + j] = pack_bf16x2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]));
+      }
     }
+  } else {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) packed[c * 16 + j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+    for (int j = 0; j < BN / 2; ++j) packed[j] = 0u;
   }
   tc_fence_before();
   mbar_arrive(acce);

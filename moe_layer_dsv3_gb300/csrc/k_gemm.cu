@@ -81,7 +81,7 @@ int num_sms() {
 // Dispatch one grouped GEMM. Returns an MOE_* code.
 int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int K, int M, const GemmOperands& op,
                   const GemmEpilogue& ep, const int* counts, const int* poff, const int* lap_tiles,
-                  const int* row_src, int* status, cudaStream_t s, int bn_hint) {
+                  const int* row_src, int* status, cudaStream_t s, int bn_hint, const int* order) {
   if (!get_encode()) return MOE_ERR_CUDA;
   const bool bf16 = mode == kRouterMode;
   int BN;
@@ -121,6 +121,7 @@ int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int
   p.poff = poff;
   p.lap_tiles = lap_tiles;
   p.row_src = row_src;
+  p.order = order;
   p.E = m.E;
   p.Ep = m.Ep;
   p.C = m.C;

@@ -127,6 +127,19 @@ __global__ void sched_offsets_kernel(const int* __restrict__ counts, int E, int 
   }
 }
 
+// Experts ordered by descending count, ties to the lower index (order[rank] = e).
+__global__ void sched_order_kernel(const int* __restrict__ counts, int Ep, int* __restrict__ order) {
+  for (int e = threadIdx.x; e < Ep; e += blockDim.x) {
+    const int n = counts[e];
+    int r = 0;
+    for (int f = 0; f < Ep; ++f) {
+      const int m = counts[f];
+      r += (m > n || (m == n && f < e)) ? 1 : 0;
+    }
+    order[r] = e;
+  }
+}
+
 __global__ void sched_rank_kernel(const int32_t* __restrict__ idx, int T, int k, int kp, int E, int Ep, int64_t Ap,
                                   int units, const int* __restrict__ base, const int* __restrict__ offsets,
                                   const int* __restrict__ poff, int* __restrict__ rank, int* __restrict__ pos,
@@ -186,6 +199,8 @@ void launch_schedule(const Dims& m, const int32_t* idx, const Layout& L, void* w
   }
   { Prof prof("sched_offsets", s);
   sched_offsets_kernel<<<1, 256, 0, s>>>(counts, m.E, m.Ep, m.C, m.Lb, offsets, poff, lap_tiles, meta); }
+  { Prof prof("sched_order", s);
+  sched_order_kernel<<<1, 512, 0, s>>>(counts, m.Ep, ws_ptr<int>(L, ws, MOE_WS_ORDER)); }
   if (m.units > 0) {
     Prof prof("sched_rank", s);
     sched_rank_kernel<<<blocks, kWarps * 32, shm, s>>>(idx, m.T, m.k, m.kp, m.E, m.Ep, m.Ap, m.units, base, offsets,

@@ -130,6 +130,6 @@ struct GemmEpilogue {
 
 int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int K, int M, const GemmOperands& op,
                   const GemmEpilogue& ep, const int* counts, const int* poff, const int* lap_tiles,
-                  const int* row_src, int* status, cudaStream_t s, int bn_hint = 0);
+                  const int* row_src, int* status, cudaStream_t s, int bn_hint = 0, const int* order = nullptr);
 
 }  // namespace moe

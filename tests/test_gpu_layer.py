@@ -155,6 +155,10 @@ def test_schedule_bit_exact(run):
         assert np.all(rs[po[e] + len(a):po[e + 1]] == -1)
     meta = run.ws("META", torch.int32, (16,)).cpu().numpy()
     assert meta[0] == sch["n_laps"] and meta[1] == po[-1]
+    # experts by descending count, ties to the lower index (weight-gradient tile order)
+    order = run.ws("ORDER", torch.int32, (run.Ep,)).cpu().numpy()
+    allc = np.concatenate([sch["counts"], np.full(m.S, m.T)])
+    assert np.array_equal(order, np.lexsort((np.arange(run.Ep), -allc)))
 
 
 def test_quantised_activation_bytes(run):
