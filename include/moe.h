@@ -253,6 +253,14 @@ typedef struct moe_kernel_time {
 } moe_kernel_time_t;
 MOE_API int moe_profile_enable(int enable);
 MOE_API int moe_profile_read(moe_kernel_time_t* out, int max_entries, int* n_entries);
+/* Like moe_profile_read, but returns every recorded launch in issue order with
+ * its start and end in milliseconds after the first recorded start (launches
+ * on different streams may overlap), then clears the records. */
+typedef struct moe_kernel_span {
+  char name[32];
+  double start_ms, end_ms;
+} moe_kernel_span_t;
+MOE_API int moe_profile_trace(moe_kernel_span_t* out, int max_entries, int* n_entries);
 MOE_API long long moe_launch_count(void);
 
 #ifdef __cplusplus

@@ -74,6 +74,7 @@ _SIGS = {
     "moe_scales_to_tiled": [_P, _I, _I, _P, _P],
     "moe_profile_enable": [_I],
     "moe_profile_read": [ctypes.c_void_p, _I, ctypes.POINTER(_I)],
+    "moe_profile_trace": [ctypes.c_void_p, _I, ctypes.POINTER(_I)],
     "moe_launch_count": [],
 }
 for _name, _args in _SIGS.items():
@@ -188,6 +189,19 @@ def moe_profile_read(max_entries=64):
     n = ctypes.c_int()
     _check("moe_profile_read", _lib.moe_profile_read(ctypes.cast(buf, ctypes.c_void_p), max_entries, ctypes.byref(n)))
     return {buf[i].name.decode(): (buf[i].launches, buf[i].ms) for i in range(min(n.value, max_entries))}
+
+
+class MoeKernelSpan(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 32), ("start_ms", ctypes.c_double), ("end_ms", ctypes.c_double)]
+
+
+def moe_profile_trace(max_entries=4096):
+    """[(kernel name, start ms, end ms)] of the launches recorded since the last read, in issue order."""
+    buf = (MoeKernelSpan * max_entries)()
+    n = ctypes.c_int()
+    _check("moe_profile_trace", _lib.moe_profile_trace(ctypes.cast(buf, ctypes.c_void_p), max_entries,
+                                                       ctypes.byref(n)))
+    return [(buf[i].name.decode(), buf[i].start_ms, buf[i].end_ms) for i in range(min(n.value, max_entries))]
 
 
 def moe_launch_count():

@@ -111,6 +111,39 @@ int moe_profile_read(moe_kernel_time_t* out, int max_entries, int* n_entries) {
   return rc;
 }
 
+int moe_profile_trace(moe_kernel_span_t* out, int max_entries, int* n_entries) {
+  if (n_entries == nullptr || (max_entries > 0 && out == nullptr)) return MOE_ERR_INVALID_ARG;
+  std::vector<moe::Rec> recs;
+  {
+    std::lock_guard<std::mutex> lk(moe::g_mu);
+    recs.swap(moe::g_recs);
+  }
+  int rc = MOE_OK;
+  const int n = static_cast<int>(recs.size());
+  for (int i = 0; i < n; ++i) {
+    float t0 = 0.0f, t1 = 0.0f;
+    if (cudaEventSynchronize(recs[i].b) != cudaSuccess ||
+        cudaEventElapsedTime(&t0, recs[0].a, recs[i].a) != cudaSuccess ||
+        cudaEventElapsedTime(&t1, recs[0].a, recs[i].b) != cudaSuccess)
+      rc = MOE_ERR_CUDA;
+    if (i < max_entries) {
+      std::memset(out[i].name, 0, sizeof(out[i].name));
+      std::strncpy(out[i].name, recs[i].name, sizeof(out[i].name) - 1);
+      out[i].start_ms = t0;
+      out[i].end_ms = t1;
+    }
+  }
+  {
+    std::lock_guard<std::mutex> lk(moe::g_mu);
+    for (const auto& r : recs) {
+      moe::g_pool.push_back(r.a);
+      moe::g_pool.push_back(r.b);
+    }
+  }
+  *n_entries = n;
+  return rc;
+}
+
 long long moe_launch_count(void) { return moe::g_launches.load(); }
 
 }  // extern "C"
