@@ -263,6 +263,14 @@ typedef struct moe_kernel_span {
 MOE_API int moe_profile_trace(moe_kernel_span_t* out, int max_entries, int* n_entries);
 MOE_API long long moe_launch_count(void);
 
+/* Failure-detection self-test: launches one kernel that waits on a barrier
+ * nothing arrives on, through the same bounded wait every pipeline wait of
+ * the library uses. After limit_ns (at most 10 s) the wait gives up and
+ * writes MOE_ERR_TIMEOUT and site 900 into status[0..1] (a device int32[2]
+ * that the caller zeroes), and the kernel returns: no hang, no trap, and the
+ * context stays usable. */
+MOE_API int moe_selftest_wait_timeout(int* status, unsigned long long limit_ns, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

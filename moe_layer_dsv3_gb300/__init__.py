@@ -76,6 +76,7 @@ _SIGS = {
     "moe_profile_read": [ctypes.c_void_p, _I, ctypes.POINTER(_I)],
     "moe_profile_trace": [ctypes.c_void_p, _I, ctypes.POINTER(_I)],
     "moe_launch_count": [],
+    "moe_selftest_wait_timeout": [_P, ctypes.c_ulonglong, _P],
 }
 for _name, _args in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -202,6 +203,10 @@ def moe_profile_trace(max_entries=4096):
     _check("moe_profile_trace", _lib.moe_profile_trace(ctypes.cast(buf, ctypes.c_void_p), max_entries,
                                                        ctypes.byref(n)))
     return [(buf[i].name.decode(), buf[i].start_ms, buf[i].end_ms) for i in range(min(n.value, max_entries))]
+
+
+def moe_selftest_wait_timeout(status, limit_ns, stream=0):
+    _check("moe_selftest_wait_timeout", _lib.moe_selftest_wait_timeout(_p(status), limit_ns, _p(stream)))
 
 
 def moe_launch_count():

@@ -7,8 +7,21 @@
 
 #include "moe_internal.h"
 #include "prof.h"
+#include "ptx.cuh"
 
 namespace moe {
+
+// Self-test of the bounded waits: waits on an mbarrier that nothing ever
+// arrives on, so the wait must give up after limit_ns and record
+// (kErrTimeout, 900) in status, leaving the context usable.
+__global__ void wait_timeout_selftest_kernel(int* status, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+    mbar_wait(&bar, 0, status, 900, limit_ns);
+  }
+}
 
 namespace {
 
@@ -145,5 +158,11 @@ int moe_profile_trace(moe_kernel_span_t* out, int max_entries, int* n_entries) {
 }
 
 long long moe_launch_count(void) { return moe::g_launches.load(); }
+
+int moe_selftest_wait_timeout(int* status, unsigned long long limit_ns, moe_stream_t stream) {
+  if (status == nullptr || limit_ns == 0 || limit_ns > 10000000000ull) return MOE_ERR_INVALID_ARG;
+  moe::wait_timeout_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status, limit_ns);
+  return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
 
 }  // extern "C"
