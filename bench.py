@@ -279,7 +279,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     shape = gen.config(args.workload, T=args.T)
     inp = gen.make_inputs(shape, seed=rank, device="cuda")
-    L = MoELayer.from_shape(shape)
+    L = MoELayer.from_shape(shape, flags=M.MOE_FLAG_LAP_LAUNCHES if args.lap_launches else 0)
     L.quantize_weights(inp["w_gu"], inp["w_d"], inp["ws_gu"], inp["ws_d"])
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
@@ -450,7 +450,8 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "mxfp8", "data": "synthetic (seeded, random-init weights)",
-        "config": workload_config(shape),
+        "config": dict(workload_config(shape),
+                       ring_laps="per-lap launches" if args.lap_launches else "one launch, mover warps"),
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": shape.T * world / (ms_e2e / 1000.0), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
@@ -471,6 +472,8 @@ def main():
     ap.add_argument("--workload", default="dsv3_zipf")
     ap.add_argument("--T", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--lap-launches", action="store_true",
+                    help="one mover launch + one GEMM launch per ring lap instead of one all-laps launch")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

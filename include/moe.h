@@ -68,8 +68,17 @@ enum {
 typedef struct moe_config {
   int T, d, E, k, n_groups, topk_groups, I, n_shared;
   int capacity;
-  int flags; /* reserved, must be 0 */
+  int flags; /* 0 or MOE_FLAG_LAP_LAUNCHES; other bits are rejected */
 } moe_config_t;
+
+/* Ring-lap execution. By default each ring direction (forward GEMM1, backward
+ * dgrad of the down projection) is ONE persistent cooperative launch over all
+ * laps: two mover warps per CTA fill ring slots (lap L in buffer L % 2) while
+ * the other warps run the MMAs, and per-tile device counters order a slot's
+ * refill after its previous lap's tiles have read it. With this flag each lap
+ * is instead a mover launch followed by a GEMM launch, laps alternating
+ * between two streams. Both give bitwise-identical results. */
+#define MOE_FLAG_LAP_LAUNCHES 1
 
 /* Bytes of workspace the layer needs for this shape (schedule, saved
  * activations for backward, ring buffers, staging). */
@@ -170,7 +179,7 @@ MOE_API int moe_status(const moe_config_t* cfg, void* ws, int* code, int* site, 
 /* Named views into the workspace (for inspection and tests). */
 enum {
   MOE_WS_STATUS = 0,   /* int32[4] */
-  MOE_WS_META,         /* int32[16]: [0] laps used, [1] padded rows used */
+  MOE_WS_META,         /* int32[16]: [0] laps used, [1] padded rows used, [2] experts with tokens */
   MOE_WS_COUNTS,       /* int32[E+S]   per-expert assignment counts (shared last) */
   MOE_WS_OFFSETS,      /* int32[E+S+1] exclusive prefix sum of counts */
   MOE_WS_POFF,         /* int32[E+S+1] prefix sum of ceil128(counts) */
@@ -210,6 +219,10 @@ enum {
   MOE_WS_DXE,          /* bf16[T*(k+S)][d]  expert input gradients per assignment */
   MOE_WS_DWR_PART,     /* fp32[Rmax/32][d]  router weight-gradient partial sums */
   MOE_WS_ORDER,        /* int32[E+S]   experts by descending count (ties: lower index first) */
+  MOE_WS_LAPBASE,      /* int32[Lb+1]  prefix over laps of the lap tile counts */
+  MOE_WS_MOVED,        /* int32[...]   per lap m-tile: 8-row groups moved into the ring */
+  MOE_WS_CONSUMED,     /* int32[...]   per lap m-tile: GEMM tiles that finished reading it */
+  MOE_WS_DH,           /* f32[Rmax][I] dh = dO W_d at padded rank rows (input of the SwiGLU backward) */
   MOE_WS_COUNT
 };
 MOE_API int moe_ws_view(const moe_config_t* cfg, void* ws, int which, void** ptr, size_t* bytes);

@@ -35,7 +35,8 @@ MOE_ERR_SCRATCH = 7
 WS_NAMES = ["STATUS", "META", "COUNTS", "OFFSETS", "POFF", "RANK", "POS", "INV", "ROWSRC", "LAPTILES", "HIST",
             "BASE", "LOGITS", "SSEL", "XQ", "XQ_SF", "RING_X", "RING_X_SF", "GU", "HQ", "HQ_SF", "HTOK", "HTOK_SF",
             "O", "DW", "DL", "RING_DO", "RING_DO_SF", "DOS", "DOS_SF", "DOTOK", "DOTOK_SF", "DGU", "DGU_SF",
-            "DGUTOK", "DGUTOK_SF", "XTOK", "XTOK_SF", "DXE", "DWR_PART", "ORDER"]
+            "DGUTOK", "DGUTOK_SF", "XTOK", "XTOK_SF", "DXE", "DWR_PART", "ORDER",
+            "LAPBASE", "MOVED", "CONSUMED", "DH"]
 WS = {n: i for i, n in enumerate(WS_NAMES)}
 WQ_NAMES = ["W1F", "W1F_SF", "W2F", "W2F_SF", "W2B", "W2B_SF", "W1B", "W1B_SF"]
 WQ = {n: i for i, n in enumerate(WQ_NAMES)}
@@ -101,8 +102,11 @@ def _p(x):
     return None if x is None or x == 0 else ctypes.c_void_p(int(x))
 
 
-def config(T, d, E, k, n_groups=1, topk_groups=1, I=128, n_shared=0, capacity=0) -> MoeConfig:
-    return MoeConfig(T, d, E, k, n_groups, topk_groups, I, n_shared, capacity, 0)
+MOE_FLAG_LAP_LAUNCHES = 1   # one mover launch + one GEMM launch per ring lap instead of one launch for all laps
+
+
+def config(T, d, E, k, n_groups=1, topk_groups=1, I=128, n_shared=0, capacity=0, flags=0) -> MoeConfig:
+    return MoeConfig(T, d, E, k, n_groups, topk_groups, I, n_shared, capacity, flags)
 
 
 def moe_workspace_size(cfg: MoeConfig) -> int:

@@ -72,6 +72,17 @@ LapStreams* lap_streams() {
 
 int launch_status() { return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+// Counters of an all-laps ring launch, zeroed on the stream before it.
+RingMovers ring_movers(const Layout& L, void* ws, cudaStream_t s) {
+  RingMovers mv{};
+  mv.lapbase = ws_ptr<int>(L, ws, MOE_WS_LAPBASE);
+  mv.moved = ws_ptr<int>(L, ws, MOE_WS_MOVED);
+  mv.consumed = ws_ptr<int>(L, ws, MOE_WS_CONSUMED);
+  cudaMemsetAsync(mv.moved, 0, L.bytes[MOE_WS_MOVED], s);
+  cudaMemsetAsync(mv.consumed, 0, L.bytes[MOE_WS_CONSUMED], s);
+  return mv;
+}
+
 }  // namespace
 
 int validate(const moe_config_t* c) {
@@ -86,7 +97,7 @@ int validate(const moe_config_t* c) {
   if (c->n_groups > 1 && (c->E / c->n_groups < 2 || c->k > c->topk_groups * (c->E / c->n_groups)))
     return MOE_ERR_INVALID_ARG;
   if (c->capacity < 0 || c->capacity % 128) return MOE_ERR_INVALID_ARG;
-  if (c->flags != 0) return MOE_ERR_INVALID_ARG;
+  if (c->flags & ~MOE_FLAG_LAP_LAUNCHES) return MOE_ERR_INVALID_ARG;
   const int64_t Ap = static_cast<int64_t>(c->T) * (c->k + c->n_shared);
   if (Ap + 128LL * (c->E + c->n_shared) >= (1LL << 31)) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
@@ -163,6 +174,10 @@ Layout make_layout(const moe_config_t* c) {
   b.add(L.off, L.bytes, MOE_WS_DXE, 2 * Ap * d);
   b.add(L.off, L.bytes, MOE_WS_DWR_PART, 4 * (R / 32) * d);
   b.add(L.off, L.bytes, MOE_WS_ORDER, 4 * Ep);
+  b.add(L.off, L.bytes, MOE_WS_LAPBASE, 4 * static_cast<size_t>(m.Lb + 1));
+  b.add(L.off, L.bytes, MOE_WS_MOVED, 4 * static_cast<size_t>(lap_mtiles_max(m)));
+  b.add(L.off, L.bytes, MOE_WS_CONSUMED, 4 * static_cast<size_t>(lap_mtiles_max(m)));
+  b.add(L.off, L.bytes, MOE_WS_DH, 4 * static_cast<size_t>(m.Rmax) * m.I);
   L.total = b.cur;
   return L;
 }
@@ -344,7 +359,18 @@ int moe_forward(const moe_config_t* cfg, const void* x, const void* wq, const fl
   ep1.q_tok = ws_ptr<uint8_t>(L, ws, MOE_WS_HTOK);
   ep1.q_tok_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_HTOK_SF);
   ep1.q_tok_pitch = m.Rmax;
-  {
+  if (!(cfg->flags & MOE_FLAG_LAP_LAUNCHES)) {
+    // One persistent launch over all laps; its mover warps fill the ring.
+    RingMovers mv = ring_movers(L, ws, s);
+    mv.xq = xq;
+    mv.xq_sf = xq_sf;
+    mv.ring = ws_ptr<uint8_t>(L, ws, MOE_WS_RING_X);
+    mv.ring_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_RING_X_SF);
+    op1.a_rows = static_cast<int64_t>(kRingBufs) * m.E * m.C;
+    if (int r = gemm_dispatch("gemm1_fwd", kSwigluFwdRing, m, 0, 2 * m.I, m.d, 0, op1, ep1, counts, poff, lap_tiles,
+                              row_src, status, s, 0, nullptr, &mv))
+      return r;
+  } else {
     LapStreams* ls = lap_streams();
     if (ls == nullptr) return MOE_ERR_CUDA;
     std::lock_guard<std::mutex> lk(ls->mu);
@@ -446,14 +472,19 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
   opb2.b_cols = m.d;
   opb2.b_sf = wq_ptr<uint8_t>(W, wqm, MOE_WQ_W2B_SF);
   GemmEpilogue epb2{};
-  epb2.gu = ws_ptr<void>(L, ws, MOE_WS_GU);
-  epb2.q_rows = ws_ptr<uint8_t>(L, ws, MOE_WS_DGU);
-  epb2.q_rows_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_DGU_SF);
-  epb2.q_rows_ktiles = 2 * m.I / 128;
-  epb2.q_tok = ws_ptr<uint8_t>(L, ws, MOE_WS_DGUTOK);
-  epb2.q_tok_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_DGUTOK_SF);
-  epb2.q_tok_pitch = m.Rmax;
-  {
+  epb2.out = ws_ptr<void>(L, ws, MOE_WS_DH);
+  epb2.ldo = m.I;
+  if (!(cfg->flags & MOE_FLAG_LAP_LAUNCHES)) {
+    RingMovers mv = ring_movers(L, ws, s);
+    mv.dy = dy;
+    mv.topk_w = topk_w;
+    mv.ring = ws_ptr<uint8_t>(L, ws, MOE_WS_RING_DO);
+    mv.ring_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_RING_DO_SF);
+    opb2.a_rows = static_cast<int64_t>(kRingBufs) * m.E * m.C;
+    if (int r = gemm_dispatch("gemm_dgrad_down", kSwigluBwdRing, m, 0, m.I, m.d, 0, opb2, epb2, counts, poff,
+                              lap_tiles, row_src, status, s, 256, nullptr, &mv))
+      return r;
+  } else {
     LapStreams* ls = lap_streams();
     if (ls == nullptr) return MOE_ERR_CUDA;
     std::lock_guard<std::mutex> lk(ls->mu);
@@ -470,7 +501,7 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
       opb2.a_sf = ring_sf + rbuf * rb / 32;
       launch_rev_combine_lap(m, lap, dy, topk_w, L, ws, cs);
       rc = gemm_dispatch("gemm_dgrad_down", kSwigluBwd, m, lap, m.I, m.d, 0, opb2, epb2, counts, poff, lap_tiles,
-                         row_src, status, cs, 128);
+                         row_src, status, cs, 256);
     }
     for (int i = 0; i < kRingBufs - 1; ++i) {
       cudaEventRecord(ls->join[i], ls->aux[i]);
@@ -478,6 +509,8 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
     }
     if (rc) return rc;
   }
+  // SwiGLU backward on dh and the saved g,u; MX(dGU) along 2I and along ranks.
+  launch_swiglu_bwd_quant(m, L, ws, s);
   // dgrad of GEMM1: DX rows pushed to their assignment.
   GemmOperands opb4{};
   opb4.a = ws_ptr<uint8_t>(L, ws, MOE_WS_DGU);

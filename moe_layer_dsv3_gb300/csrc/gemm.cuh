@@ -13,6 +13,17 @@
 // owner, warps 2-5 = epilogue (each reads the TMEM lane quarter warp%4).
 // Work list: "tiles" of 128 rows x BN columns, decoded from the device-side
 // schedule, so the host never learns per-expert counts.
+//
+// The all-laps ring modes add two mover warps (256 threads) that fill the
+// ring token buffers while the other warps compute, so one persistent launch
+// covers every lap. Ordering goes through per-m-tile device counters:
+//   moved[gm]    8-row groups of m-tile gm written into its ring slot; the
+//                producer waits for all 16 before its first TMA load of gm;
+//   consumed[gm] tiles of gm whose A loads have landed; the movers of the
+//                same slot's next tenant (lap + 2) wait for all N / BN.
+// Both lists are walked in increasing (lap-major) order by every CTA and
+// every wait points to an earlier lap or to a move of the same lap, so the
+// waits cannot form a cycle once all CTAs are resident (cooperative launch).
 #pragma once
 #include <cuda_bf16.h>
 
@@ -23,6 +34,17 @@
 namespace moe {
 
 constexpr int kRouterMode = 5;   // bf16 x bf16 router logits
+
+// The epilogue / tile shape a mode shares with its per-lap form.
+__host__ __device__ constexpr int base_mode(int mode) {
+  return mode == kSwigluFwdRing ? kSwigluFwd : (mode == kSwigluBwdRing ? kSwigluBwd : mode);
+}
+__host__ __device__ constexpr bool ring_mode(int mode) { return mode == kSwigluFwdRing || mode == kSwigluBwdRing; }
+__host__ __device__ constexpr int gemm_threads(int mode) { return ring_mode(mode) ? 256 : 192; }
+
+constexpr int kMoverWarps = 2;
+constexpr int kMoveRows = 8;                    // ring rows per move item
+constexpr int kMoveItems = 128 / kMoveRows;     // move items per m-tile
 
 struct GemmParams {
   int N;                 // B rows per expert (output columns per expert)
@@ -39,6 +61,12 @@ struct GemmParams {
   uint8_t* q_tok; uint8_t* q_tok_sf; int64_t q_tok_pitch;
   __nv_bfloat16* gu; int I;
   int* status;
+  // all-laps ring modes
+  const int* lapbase; int Lb; int d;
+  int* moved; int* consumed;
+  const uint8_t* mv_xq; const uint8_t* mv_xq_sf;
+  const __nv_bfloat16* mv_dy; const float* mv_w;
+  uint8_t* ring; uint8_t* ring_sf;
 };
 
 template <int BN, int MODE>
@@ -62,7 +90,8 @@ struct GemmCfg {
   static constexpr int kNumAcc = (2 * BN <= kSfCol0) ? 2 : 1;
   static constexpr int kKElems = kBf16 ? 64 : 128;                  // K elements per stage
   static constexpr int kBarBytes = 256;
-  static constexpr int kScratchBytes = (MODE == kSwigluFwd || MODE == kSwigluBwd) ? 4 * 32 * 33 * 4 : 0;
+  static constexpr int kBase = base_mode(MODE);
+  static constexpr int kScratchBytes = kBase == kSwigluFwd ? 4 * 32 * 33 * 4 : 0;
   static constexpr int kSmem = 1024 + kStages * kStageBytes + kOutBytes + kBarBytes + kScratchBytes;
   static_assert(kSmem <= 232448, "shared memory budget");
   static_assert(kSfCol0 + kStages * kSfCols <= 512, "TMEM budget");
@@ -80,6 +109,7 @@ struct TileInfo {
   int n0;            // first output column
   int m0;            // first output row (wgrad / plain / router)
   bool use_a2;
+  int gm;            // all-laps ring modes: global m-tile of a ring tile, else -1
 };
 
 // Largest e in [0, n) with v[e] <= x < v[e+1] (v nondecreasing, v[0] <= x < v[n]).
@@ -94,45 +124,68 @@ __device__ __forceinline__ int seg_search(const int* v, int n, int64_t x) {
 
 template <int BN, int MODE>
 __device__ __forceinline__ int gemm_num_tiles(const GemmParams& p) {
-  if constexpr (MODE == kSwigluFwd || MODE == kSwigluBwd) {
+  if constexpr (ring_mode(MODE)) {
+    return p.lapbase[p.Lb] * (p.N / BN);
+  } else if constexpr (MODE == kSwigluFwd || MODE == kSwigluBwd) {
     return p.lap_tiles[p.lap * (p.Ep + 1) + p.Ep] * (p.N / BN);
   } else if constexpr (MODE == kPush) {
     return (p.poff[p.Ep] / 128) * (p.N / BN);
   } else if constexpr (MODE == kWgrad) {
     // positions of the two-ended schedule (see gemm_decode): enough rounds for the heavy half
+    const int N = p.static_tiles;
     const int g = gridDim.x;
-    if (g < 2 || (g & 1)) return p.static_tiles;
-    const int heavy = (p.static_tiles + 1) / 2;
+    if (g < 2 || (g & 1)) return N;
+    const int heavy = (N + 1) / 2;
     return ((heavy + g / 2 - 1) / (g / 2)) * g;
   } else {
     return p.static_tiles;
   }
 }
 
+// Tile (g, n) of ring lap L: g indexes the lap's m-tiles (experts in order;
+// the shared expert's tiles, read in place from A2, only in lap 0). The ring
+// rows of lap L start at ring_row0.
+template <int BN>
+__device__ __forceinline__ bool lap_decode(const GemmParams& p, int L, int g, int n, int64_t ring_row0,
+                                           TileInfo& t) {
+  const int* lt = p.lap_tiles + static_cast<int64_t>(L) * (p.Ep + 1);
+  const int e = seg_search(lt, p.Ep, g);
+  const int mt = g - lt[e];
+  const bool shared = e >= p.E;
+  const int64_t rank0 = shared ? static_cast<int64_t>(mt) * 128 : static_cast<int64_t>(L) * p.C + mt * 128;
+  const int cnt = p.counts[e];
+  t.e = e;
+  t.use_a2 = shared;
+  t.a_row = shared ? static_cast<int64_t>(mt) * 128 : ring_row0 + static_cast<int64_t>(e) * p.C + mt * 128;
+  t.b_row = static_cast<int64_t>(e) * p.N + static_cast<int64_t>(n) * BN;
+  t.k0 = 0;
+  t.nk = p.K / kTileK;
+  t.prow0 = p.poff[e] + rank0;
+  const int64_t v = cnt - rank0;
+  t.valid = v < 0 ? 0 : (v > 128 ? 128 : static_cast<int>(v));
+  t.n0 = n * BN;
+  t.m0 = 0;
+  t.gm = -1;
+  return t.prow0 + 128 <= p.poff[e + 1] && t.valid > 0;
+}
+
 template <int BN, int MODE>
 __device__ __forceinline__ bool gemm_decode(const GemmParams& p, int tile, TileInfo& t) {
   using Cf = GemmCfg<BN, MODE>;
-  if constexpr (MODE == kSwigluFwd || MODE == kSwigluBwd) {
+  t.gm = -1;
+  if constexpr (ring_mode(MODE)) {
+    // global m-tile gm (laps in order), n-tile n
+    const int nt = p.N / BN;
+    const int gm = tile / nt, n = tile - gm * nt;
+    const int L = seg_search(p.lapbase, p.Lb, gm);
+    const bool ok = lap_decode<BN>(p, L, gm - p.lapbase[L], n,
+                                   static_cast<int64_t>(L % kRingBufs) * p.E * p.C, t);
+    if (!t.use_a2) t.gm = gm;
+    return ok;
+  } else if constexpr (MODE == kSwigluFwd || MODE == kSwigluBwd) {
     const int nt = p.N / BN;
     const int g = tile / nt, n = tile - (tile / nt) * nt;
-    const int* lt = p.lap_tiles + p.lap * (p.Ep + 1);
-    const int e = seg_search(lt, p.Ep, g);
-    const int mt = g - lt[e];
-    const bool shared = e >= p.E;
-    const int64_t rank0 = shared ? static_cast<int64_t>(mt) * 128 : static_cast<int64_t>(p.lap) * p.C + mt * 128;
-    const int cnt = p.counts[e];
-    t.e = e;
-    t.use_a2 = shared;
-    t.a_row = shared ? static_cast<int64_t>(mt) * 128 : static_cast<int64_t>(e) * p.C + mt * 128;
-    t.b_row = static_cast<int64_t>(e) * p.N + static_cast<int64_t>(n) * BN;
-    t.k0 = 0;
-    t.nk = p.K / Cf::kKElems;
-    t.prow0 = p.poff[e] + rank0;
-    const int64_t v = cnt - rank0;
-    t.valid = v < 0 ? 0 : (v > 128 ? 128 : static_cast<int>(v));
-    t.n0 = n * BN;
-    t.m0 = 0;
-    return t.prow0 + 128 <= p.poff[e + 1] && t.valid > 0;
+    return lap_decode<BN>(p, p.lap, g, n, 0, t);
   } else if constexpr (MODE == kPush) {
     const int nt = p.N / BN;
     const int g = tile / nt, n = tile - (tile / nt) * nt;
@@ -203,35 +256,6 @@ __device__ __forceinline__ bool gemm_decode(const GemmParams& p, int tile, TileI
   }
 }
 
-// Row-wise MX of 32 values: codes to dst (16-byte aligned), scale byte to sf.
-__device__ __forceinline__ void emit_rowq(const float* v, uint8_t* dst, uint8_t* sf_byte) {
-  const int b = mx_scale_byte(amax32(v));
-  uint32_t w[8];
-  mx_pack32(v, mx_inv_scale(b), w);
-  store32(dst, w);
-  *sf_byte = static_cast<uint8_t>(b);
-}
-
-// Token-axis MX of a warp's 32x32 block (lane = row): transposes through
-// shared memory so that lane j owns column j, then writes 32 codes of that
-// column (32 consecutive ranks) and its scale.
-__device__ __forceinline__ void emit_tokq(const float* v, float* scr, int lane, uint8_t* q_tok, uint8_t* q_tok_sf,
-                                          int64_t pitch, int64_t col0, int64_t prow_base) {
-#pragma unroll
-  for (int j = 0; j < 32; ++j) scr[lane * 33 + j] = v[j];
-  __syncwarp();
-  float c[32];
-#pragma unroll
-  for (int r = 0; r < 32; ++r) c[r] = scr[r * 33 + lane];
-  __syncwarp();
-  const int b = mx_scale_byte(amax32(c));
-  uint32_t w[8];
-  mx_pack32(c, mx_inv_scale(b), w);
-  const int64_t col = col0 + lane;
-  store32(q_tok + col * pitch + prow_base, w);
-  q_tok_sf[sf_off(col, prow_base >> 5, pitch >> 7)] = static_cast<uint8_t>(b);
-}
-
 __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v) {
   uint4* p = reinterpret_cast<uint4*>(dst);
 #pragma unroll
@@ -274,33 +298,6 @@ __device__ __forceinline__ void drain_acc_bf16(uint32_t tacc, bool have_acc, uin
   mbar_arrive(acce);
 }
 
-// SwiGLU backward reads the saved bf16 g,u of its rows. The epilogue warps
-// issue those loads before waiting for the accumulator, so their latency
-// hides behind the tile's mainloop.
-template <int BN, int MODE>
-struct GuPrefetch {
-  static constexpr int kN = MODE == kSwigluBwd ? (BN / 32) * 8 : 1;
-  uint4 v[kN];
-};
-
-template <int BN, int MODE>
-__device__ __forceinline__ void prefetch_gu(const GemmParams& p, const TileInfo& t, int row, GuPrefetch<BN, MODE>& g) {
-  if constexpr (MODE == kSwigluBwd) {
-    const bool valid = row < t.valid;
-    const int64_t prow = t.prow0 + row;
-#pragma unroll
-    for (int c = 0; c < BN / 32; ++c) {
-      const uint4* pg = reinterpret_cast<const uint4*>(p.gu + prow * (2 * p.I) + t.n0 + c * 32);
-      const uint4* pu = reinterpret_cast<const uint4*>(p.gu + prow * (2 * p.I) + p.I + t.n0 + c * 32);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        g.v[c * 8 + i] = valid ? pg[i] : make_uint4(0, 0, 0, 0);
-        g.v[c * 8 + 4 + i] = valid ? pu[i] : make_uint4(0, 0, 0, 0);
-      }
-    }
-  }
-}
-
 __device__ __forceinline__ void unpack_bf16x32(const uint4* q, float* v) {
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
@@ -313,11 +310,165 @@ __device__ __forceinline__ void unpack_bf16x32(const uint4* q, float* v) {
   }
 }
 
+// ---------------------------------------------------------------- ring movers
+// One move item = kMoveRows consecutive ring rows of one m-tile. Lane r < 8
+// holds the assignment of row r (-1 past the expert's count: zero row).
+
+// A finished item becomes visible (to TMA reads too) before moved[gm] counts it.
+__device__ __forceinline__ void publish_move(int* ctr, int lane) {
+  fence_proxy_async_global();
+  __threadfence();
+  __syncwarp();
+  if (lane == 0) red_release_add(ctr, 1);
+}
+
+// Forward: ring row <- MX(x) row of its token, codes and tiled scales. The
+// item's 16-byte chunks are walked flat (consecutive lanes, consecutive
+// chunks) in rounds of kFwdU chunks a lane; the next round's loads are issued
+// before this round's stores, so two rounds are in flight.
+constexpr int kFwdU = 8;
+constexpr int kBwdU = 4;
+
+__device__ __forceinline__ void move_rows_fwd(const GemmParams& p, int lane, int a_lane, int64_t ring_row0) {
+  const int d = p.d;
+  const int chunks = d >> 4;
+  const int total = kMoveRows * chunks;
+  const int rounds = (total + 32 * kFwdU - 1) / (32 * kFwdU);
+  const int tok_l = a_lane >= 0 ? a_lane / p.k : -1;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  uint4 nxt[kFwdU];
+  auto load = [&](int rd, uint4* v) {
+#pragma unroll
+    for (int u = 0; u < kFwdU; ++u) {
+      const int f = (rd * kFwdU + u) * 32 + lane;
+      const int r = f / chunks, c = f - (f / chunks) * chunks;
+      const int t = __shfl_sync(0xffffffffu, tok_l, r < kMoveRows ? r : kMoveRows - 1);
+      v[u] = (f < total && t >= 0) ? __ldg(reinterpret_cast<const uint4*>(p.mv_xq + static_cast<int64_t>(t) * d) + c)
+                                   : zero;
+    }
+  };
+  load(0, nxt);
+  for (int rd = 0; rd < rounds; ++rd) {
+    uint4 cur[kFwdU];
+#pragma unroll
+    for (int u = 0; u < kFwdU; ++u) cur[u] = nxt[u];
+    if (rd + 1 < rounds) load(rd + 1, nxt);
+#pragma unroll
+    for (int u = 0; u < kFwdU; ++u) {
+      const int f = (rd * kFwdU + u) * 32 + lane;
+      const int r = f / chunks, c = f - (f / chunks) * chunks;
+      if (f < total) reinterpret_cast<uint4*>(p.ring + (ring_row0 + r) * d)[c] = cur[u];
+    }
+  }
+  const int ktiles = d >> 7;
+  int tok[kMoveRows];
+#pragma unroll
+  for (int r = 0; r < kMoveRows; ++r) tok[r] = __shfl_sync(0xffffffffu, tok_l, r);
+  for (int kt = lane; kt < ktiles; kt += 32) {
+    uint32_t sv[kMoveRows];
+#pragma unroll
+    for (int r = 0; r < kMoveRows; ++r)
+      sv[r] = tok[r] >= 0
+                  ? __ldg(reinterpret_cast<const uint32_t*>(p.mv_xq_sf + sf_tiled_offset(tok[r], kt * 4, ktiles)))
+                  : 0u;
+#pragma unroll
+    for (int r = 0; r < kMoveRows; ++r)
+      *reinterpret_cast<uint32_t*>(p.ring_sf + sf_tiled_offset(ring_row0 + r, kt * 4, ktiles)) = sv[r];
+  }
+}
+
+// Backward: ring row <- MX(fp32(w_a * dy[t_a])) along d (the reverse-combine
+// pull). Flat walk over the item's 32-element blocks, kBwdU blocks a lane per
+// round, next round's loads in flight while this round is quantised.
+__device__ __forceinline__ void move_rows_bwd(const GemmParams& p, int lane, int a_lane, int64_t ring_row0) {
+  const int d = p.d;
+  const int nb = d >> 5, ktiles = d >> 7;
+  const int total = kMoveRows * nb;
+  const int rounds = (total + 32 * kBwdU - 1) / (32 * kBwdU);
+  const int tok_l = a_lane >= 0 ? a_lane / p.k : -1;
+  const float w_l = a_lane >= 0 ? p.mv_w[a_lane] : 0.0f;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  uint4 nxt[kBwdU][4];
+  auto load = [&](int rd, uint4 (*v)[4]) {
+#pragma unroll
+    for (int u = 0; u < kBwdU; ++u) {
+      const int f = (rd * kBwdU + u) * 32 + lane;
+      const int r = f / nb, kb = f - (f / nb) * nb;
+      const int t = __shfl_sync(0xffffffffu, tok_l, r < kMoveRows ? r : kMoveRows - 1);
+      const uint4* src = reinterpret_cast<const uint4*>(p.mv_dy + static_cast<int64_t>(t < 0 ? 0 : t) * d + kb * 32);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[u][i] = (f < total && t >= 0) ? __ldg(src + i) : zero;
+    }
+  };
+  load(0, nxt);
+  for (int rd = 0; rd < rounds; ++rd) {
+    uint4 cur[kBwdU][4];
+#pragma unroll
+    for (int u = 0; u < kBwdU; ++u)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) cur[u][i] = nxt[u][i];
+    if (rd + 1 < rounds) load(rd + 1, nxt);
+#pragma unroll
+    for (int u = 0; u < kBwdU; ++u) {
+      const int f = (rd * kBwdU + u) * 32 + lane;
+      const int r = f / nb, kb = f - (f / nb) * nb;
+      const int rc = r < kMoveRows ? r : kMoveRows - 1;
+      const int t = __shfl_sync(0xffffffffu, tok_l, rc);
+      const float w = __shfl_sync(0xffffffffu, w_l, rc);
+      if (f < total) {
+        float v[32];
+        unpack_bf16x32(cur[u], v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = t >= 0 ? __fmul_rn(w, v[j]) : 0.0f;
+        const int b = mx_scale_byte(amax32(v));
+        uint32_t q[8];
+        mx_pack32(v, mx_inv_scale(b), q);
+        store32(p.ring + (ring_row0 + r) * d + kb * 32, q);
+        p.ring_sf[sf_tiled_offset(ring_row0 + r, kb, ktiles)] = static_cast<uint8_t>(b);
+      }
+    }
+  }
+}
+
+// Mover warp `wid` of this CTA: items j = blockIdx.x * kMoverWarps + wid,
+// then every gridDim.x * kMoverWarps, i.e. in increasing (lap-major) order.
+template <int BN, int MODE>
+__device__ void ring_mover(const GemmParams& p, int wid, int lane) {
+  const int nt = p.N / BN;
+  const int total = p.lapbase[p.Lb] * kMoveItems;
+  const int stride = gridDim.x * kMoverWarps;
+  for (int j = blockIdx.x * kMoverWarps + wid; j < total; j += stride) {
+    const int gm = j / kMoveItems, part = j - gm * kMoveItems;
+    const int L = seg_search(p.lapbase, p.Lb, gm);
+    const int g = gm - p.lapbase[L];
+    const int* lt = p.lap_tiles + static_cast<int64_t>(L) * (p.Ep + 1);
+    if (g >= lt[p.E]) continue;                 // shared-expert tile: A2 is read in place
+    const int e = seg_search(lt, p.E, g);
+    const int mt = g - lt[e];
+    if (L >= kRingBufs) {
+      // The slot's previous tenant is the same expert's m-tile mt of lap L - kRingBufs.
+      const int Lp = L - kRingBufs;
+      const int gp = p.lapbase[Lp] + p.lap_tiles[static_cast<int64_t>(Lp) * (p.Ep + 1) + e] + mt;
+      int ok = 1;
+      if (lane == 0) ok = wait_counter(p.consumed + gp, nt, p.status, 40) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      (void)ld_acquire_gpu(p.consumed + gp);   // every lane orders its writes after the reads
+    }
+    const int64_t rank0 = static_cast<int64_t>(L) * p.C + mt * 128 + part * kMoveRows;
+    const int64_t ring_row0 = (static_cast<int64_t>(L % kRingBufs) * p.E + e) * p.C + mt * 128 + part * kMoveRows;
+    const int cnt = p.counts[e];
+    const int a = (lane < kMoveRows && rank0 + lane < cnt) ? p.row_src[p.poff[e] + rank0 + lane] : -1;
+    if constexpr (base_mode(MODE) == kSwigluFwd) move_rows_fwd(p, lane, a, ring_row0);
+    else move_rows_bwd(p, lane, a, ring_row0);
+    publish_move(p.moved + gm, lane);
+  }
+}
+
 template <int BN, int MODE>
 __device__ __forceinline__ void gemm_epilogue_tile(const GemmParams& p, const TileInfo& t, uint32_t tacc, int q,
                                                    int lane, float* scr, uint8_t* out_smem, const CUtensorMap* tma_o,
-                                                   const CUtensorMap* tma_o2, uint64_t* acce,
-                                                   const GuPrefetch<BN, MODE>& gp) {
+                                                   const CUtensorMap* tma_o2, uint64_t* acce) {
   const int row = q * 32 + lane;
   const bool have_acc = t.nk > 0;
   const bool valid = row < t.valid;
@@ -351,31 +502,33 @@ __device__ __forceinline__ void gemm_epilogue_tile(const GemmParams& p, const Ti
       emit_tokq(&h[c * 32], scr, lane, p.q_tok, p.q_tok_sf, p.q_tok_pitch, icol, t.prow0 + q * 32);
     }
   } else if constexpr (MODE == kSwigluBwd) {
-    const int64_t prow = t.prow0 + row;
-    const int I = p.I;
+    // dh (fp32) to the tile's padded rank rows; the SwiGLU backward and the
+    // two MX quantisations of dGU run in their own kernel.
+    float* dst = static_cast<float*>(p.out) + (t.prow0 + row) * static_cast<int64_t>(p.ldo) + t.n0;
 #pragma unroll
-    for (int c = 0; c < BN / 32; ++c) {
-      float dh[32], g[32], u[32], dg[32], du[32];
-      tmem_ld32(tacc + c * 32, dh);
-      const int64_t icol = t.n0 + c * 32;
-      unpack_bf16x32(&gp.v[c * 8], g);
-      unpack_bf16x32(&gp.v[c * 8 + 4], u);
+    for (int c = 0; c < BN / 32; c += 2) {
+      uint32_t r0[32], r1[32];
+      tmem_ld32_async(tacc + c * 32, r0);
+      tmem_ld32_async(tacc + (c + 1) * 32, r1);
+      tmem_wait_ld();
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        if (valid) {
-          const float sg = 1.0f / (1.0f + __expf(-g[j]));
-          dg[j] = dh[j] * u[j] * sg * (1.0f + g[j] * (1.0f - sg));
-          du[j] = dh[j] * (g[j] * sg);
-        } else {
-          dg[j] = 0.0f;
-          du[j] = 0.0f;
-        }
+        reg_fence(r0[j]);
+        reg_fence(r1[j]);
       }
-      const int ktl = p.q_rows_ktiles;
-      emit_rowq(dg, p.q_rows + prow * (2 * I) + icol, p.q_rows_sf + sf_off(prow, icol >> 5, ktl));
-      emit_rowq(du, p.q_rows + prow * (2 * I) + I + icol, p.q_rows_sf + sf_off(prow, (I + icol) >> 5, ktl));
-      emit_tokq(dg, scr, lane, p.q_tok, p.q_tok_sf, p.q_tok_pitch, icol, t.prow0 + q * 32);
-      emit_tokq(du, scr, lane, p.q_tok, p.q_tok_sf, p.q_tok_pitch, I + icol, t.prow0 + q * 32);
+      if (c + 2 == BN / 32) {   // whole accumulator row read: hand TMEM back
+        tc_fence_before();
+        mbar_arrive(acce);
+      }
+      float4* d0 = reinterpret_cast<float4*>(dst + c * 32);
+      float4* d1 = reinterpret_cast<float4*>(dst + (c + 1) * 32);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        d0[i] = make_float4(__uint_as_float(r0[4 * i]), __uint_as_float(r0[4 * i + 1]), __uint_as_float(r0[4 * i + 2]),
+                            __uint_as_float(r0[4 * i + 3]));
+        d1[i] = make_float4(__uint_as_float(r1[4 * i]), __uint_as_float(r1[4 * i + 1]), __uint_as_float(r1[4 * i + 2]),
+                            __uint_as_float(r1[4 * i + 3]));
+      }
     }
   } else if constexpr (MODE == kPush) {
     const int64_t prow = t.prow0 + row;
@@ -434,11 +587,12 @@ __device__ __forceinline__ void gemm_epilogue_tile(const GemmParams& p, const Ti
 }
 
 template <int BN, int MODE>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(gemm_threads(MODE), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_a2,
                 const __grid_constant__ CUtensorMap tma_b, const __grid_constant__ CUtensorMap tma_o,
                 const __grid_constant__ CUtensorMap tma_o2, const __grid_constant__ GemmParams p) {
   using Cf = GemmCfg<BN, MODE>;
+  constexpr int BM = base_mode(MODE);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* out_smem = smem + Cf::kStages * Cf::kStageBytes;
@@ -464,7 +618,7 @@ __global__ void __launch_bounds__(192, 1)
     fence_proxy_async();
     tma_prefetch(&tma_a);
     tma_prefetch(&tma_b);
-    if (MODE == kSwigluFwd || MODE == kSwigluBwd) tma_prefetch(&tma_a2);
+    if (BM == kSwigluFwd || BM == kSwigluBwd) tma_prefetch(&tma_a2);
     if (Cf::kTmaOut) {
       tma_prefetch(&tma_o);
       tma_prefetch(&tma_o2);
@@ -489,6 +643,12 @@ __global__ void __launch_bounds__(192, 1)
       for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
         TileInfo t;
         if (!gemm_decode<BN, MODE>(p, tile, t)) continue;
+        if constexpr (ring_mode(MODE)) {
+          if (t.gm >= 0) {   // the movers have filled this m-tile's ring slot
+            if (!wait_counter(p.moved + t.gm, kMoveItems, p.status, 12)) { ok = false; break; }
+            fence_proxy_async_global();
+          }
+        }
         for (int ks = 0; ks < t.nk; ++ks) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, p.status, 10)) { ok = false; break; }
           uint8_t* sa = smem + stage * Cf::kStageBytes;
@@ -555,11 +715,17 @@ __global__ void __launch_bounds__(192, 1)
           tc_commit(&empty[stage]);
           if (++stage == Cf::kStages) { stage = 0; phase ^= 1u; }
         }
+        if constexpr (ring_mode(MODE)) {
+          if (ok && t.gm >= 0) {   // every A load of this tile has landed: its ring rows may be refilled
+            fence_proxy_async_global();
+            red_release_add(p.consumed + t.gm, 1);
+          }
+        }
         tc_commit(&accf[acc]);
         if (++acc == Cf::kNumAcc) { acc = 0; acc_phase ^= 1u; }
       }
     }
-  } else {
+  } else if (warp < 6) {
     const int q = warp & 3;
     float* scr = scratch + (warp - 2) * 32 * 33;
     uint32_t acc_phase = 0;
@@ -567,19 +733,19 @@ __global__ void __launch_bounds__(192, 1)
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
       TileInfo t;
       if (!gemm_decode<BN, MODE>(p, tile, t)) continue;
-      GuPrefetch<BN, MODE> gp;
-      prefetch_gu<BN, MODE>(p, t, q * 32 + lane, gp);
       if (!mbar_wait(&accf[acc], acc_phase, p.status, 30)) break;
       tc_fence_after();
-      gemm_epilogue_tile<BN, MODE>(p, t, tmem + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(q * 32) << 16),
-                                   q, lane, scr, out_smem, &tma_o, &tma_o2, &acce[acc], gp);
-      if constexpr (MODE != kPush && MODE != kWgrad && MODE != kSwigluFwd) {   // those release TMEM inside
+      gemm_epilogue_tile<BN, BM>(p, t, tmem + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(q * 32) << 16),
+                                   q, lane, scr, out_smem, &tma_o, &tma_o2, &acce[acc]);
+      if constexpr (BM != kPush && BM != kWgrad && BM != kSwigluFwd && BM != kSwigluBwd) {   // others release TMEM inside
         tc_fence_before();
         mbar_arrive(&acce[acc]);
       }
       if (++acc == Cf::kNumAcc) { acc = 0; acc_phase ^= 1u; }
     }
     if (Cf::kTmaOut && q == 2 && lane == 0) bulk_wait_all();
+  } else {
+    if constexpr (ring_mode(MODE)) ring_mover<BN, MODE>(p, warp - 6, lane);
   }
   tc_fence_before();
   __syncthreads();

@@ -61,8 +61,34 @@ int run(const char* name, const CUtensorMap& ta, const CUtensorMap& ta2, const C
   });
   if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
   if (grid <= 0) return MOE_OK;
+  if constexpr (ring_mode(MODE)) {
+    // CTAs wait on one another's counters: all of them must be resident, so
+    // the launch is cooperative and no larger than the co-resident limit.
+    static std::once_flag occ_once;
+    static int per_sm = 0;
+    std::call_once(occ_once, [] {
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_kernel<BN, MODE>, gemm_threads(MODE),
+                                                        Cf::kSmem) != cudaSuccess)
+        per_sm = 0;
+    });
+    if (per_sm < 1) return MOE_ERR_CUDA;
+    if (grid > per_sm * num_sms()) grid = per_sm * num_sms();
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(static_cast<unsigned>(grid));
+    lc.blockDim = dim3(gemm_threads(MODE));
+    lc.dynamicSmemBytes = Cf::kSmem;
+    lc.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    Prof prof(name, s);
+    if (cudaLaunchKernelEx(&lc, gemm_kernel<BN, MODE>, ta, ta2, tb, to, to2, p) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
   Prof prof(name, s);
-  gemm_kernel<BN, MODE><<<grid, 192, Cf::kSmem, s>>>(ta, ta2, tb, to, to2, p);
+  gemm_kernel<BN, MODE><<<grid, gemm_threads(MODE), Cf::kSmem, s>>>(ta, ta2, tb, to, to2, p);
   return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -81,11 +107,13 @@ int num_sms() {
 // Dispatch one grouped GEMM. Returns an MOE_* code.
 int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int K, int M, const GemmOperands& op,
                   const GemmEpilogue& ep, const int* counts, const int* poff, const int* lap_tiles,
-                  const int* row_src, int* status, cudaStream_t s, int bn_hint, const int* order) {
+                  const int* row_src, int* status, cudaStream_t s, int bn_hint, const int* order,
+                  const RingMovers* mv) {
   if (!get_encode()) return MOE_ERR_CUDA;
   const bool bf16 = mode == kRouterMode;
   int BN;
-  if (mode == kSwigluFwd) BN = kGemm1BN;
+  if (ring_mode(mode) && mv == nullptr) return MOE_ERR_INVALID_ARG;
+  if (base_mode(mode) == kSwigluFwd) BN = kGemm1BN;
   else if (mode == kRouterMode) BN = N <= 32 ? 32 : (N % 256 == 0 ? 256 : 128);
   else if ((bn_hint == 128 || bn_hint == 256) && N % bn_hint == 0) BN = bn_hint;
   else BN = (N % 256 == 0) ? 256 : 128;
@@ -141,10 +169,25 @@ int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int
   p.gu = static_cast<__nv_bfloat16*>(ep.gu);
   p.I = m.I;
   p.status = status;
+  if (mv != nullptr) {
+    p.lapbase = mv->lapbase;
+    p.Lb = m.Lb;
+    p.d = m.d;
+    p.moved = mv->moved;
+    p.consumed = mv->consumed;
+    p.mv_xq = mv->xq;
+    p.mv_xq_sf = mv->xq_sf;
+    p.mv_dy = static_cast<const __nv_bfloat16*>(mv->dy);
+    p.mv_w = mv->topk_w;
+    p.ring = mv->ring;
+    p.ring_sf = mv->ring_sf;
+  }
 
   const int nt = (N + BN - 1) / BN;
   int64_t upper;
-  if (mode == kSwigluFwd || mode == kSwigluBwd) {
+  if (ring_mode(mode)) {
+    upper = lap_mtiles_max(m) * nt;
+  } else if (mode == kSwigluFwd || mode == kSwigluBwd) {
     upper = (static_cast<int64_t>(m.E) * (m.C / 128) + (lap == 0 ? m.S * (m.Tpad / 128) : 0)) * nt;
   } else if (mode == kPush) {
     upper = (m.Rmax / 128) * nt;
@@ -161,6 +204,10 @@ int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int
     case kSwigluFwd:
       if (BN == 128) return run<128, kSwigluFwd>(name, ta, ta2, tb, to, to2, p, grid, s);
       return run<256, kSwigluFwd>(name, ta, ta2, tb, to, to2, p, grid, s);
+    case kSwigluFwdRing:
+      return run<kGemm1BN, kSwigluFwdRing>(name, ta, ta2, tb, to, to2, p, grid, s);
+    case kSwigluBwdRing:
+      return BN == 256 ? run<256, kSwigluBwdRing>(name, ta, ta2, tb, to, to2, p, grid, s) : run<128, kSwigluBwdRing>(name, ta, ta2, tb, to, to2, p, grid, s);
     case kSwigluBwd:
       return BN == 256 ? run<256, kSwigluBwd>(name, ta, ta2, tb, to, to2, p, grid, s) : run<128, kSwigluBwd>(name, ta, ta2, tb, to, to2, p, grid, s);
     case kPush:

@@ -147,6 +147,72 @@ __global__ void __launch_bounds__(kTokThreads, 2) tok_gather_kernel(
     *reinterpret_cast<float4*>(part + (r0 / 32) * d + c0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
 }
 
+// SwiGLU backward of padded rank rows and the two MX forms of dGU = [dg | du]:
+// along 2I per row (q_rows, tiled scales) and along ranks per column (q_tok,
+// [2I][Rmax], tiled scales). Row pr is an assignment iff row_src[pr] >= 0;
+// other rows of an expert's padded segment give zeros. CTA: 32 rows x 128
+// columns of I, one warp per 32 columns; lane = row.
+//   sg = sigmoid(g), dg = dh u sg (1 + g (1 - sg)), du = dh g sg   (fp32)
+__global__ void __launch_bounds__(128) swiglu_bwd_quant_kernel(
+    const float* __restrict__ dh, const __nv_bfloat16* __restrict__ gu, const int* __restrict__ row_src,
+    const int* __restrict__ poff_end, int I, int64_t Rmax, uint8_t* __restrict__ q_rows,
+    uint8_t* __restrict__ q_rows_sf, uint8_t* __restrict__ q_tok, uint8_t* __restrict__ q_tok_sf) {
+  __shared__ float scr[4][32 * 33];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 32;
+  if (r0 >= *poff_end) return;
+  const int c0 = (blockIdx.x * 4 + warp) * 32;
+  if (c0 >= I) return;
+  const int64_t prow = r0 + lane;
+  const bool valid = row_src[prow] >= 0;
+  float h[32];
+  uint4 graw[4], uraw[4];
+  {
+    const float4* pd = reinterpret_cast<const float4*>(dh + prow * I + c0);
+    const uint4* pg = reinterpret_cast<const uint4*>(gu + prow * (2 * I) + c0);
+    const uint4* pu = reinterpret_cast<const uint4*>(gu + prow * (2 * I) + I + c0);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 v = pd[i];
+      h[4 * i] = v.x; h[4 * i + 1] = v.y; h[4 * i + 2] = v.z; h[4 * i + 3] = v.w;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) { graw[i] = pg[i]; uraw[i] = pu[i]; }
+  }
+  float g[32], u[32], dg[32];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t wg[4] = {graw[k].x, graw[k].y, graw[k].z, graw[k].w};
+    const uint32_t wu[4] = {uraw[k].x, uraw[k].y, uraw[k].z, uraw[k].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      g[8 * k + 2 * i] = __uint_as_float(wg[i] << 16);
+      g[8 * k + 2 * i + 1] = __uint_as_float(wg[i] & 0xFFFF0000u);
+      u[8 * k + 2 * i] = __uint_as_float(wu[i] << 16);
+      u[8 * k + 2 * i + 1] = __uint_as_float(wu[i] & 0xFFFF0000u);
+    }
+  }
+  // du overwrites g (g * sg is kept in u's slot once u is used), dg its own array
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    if (valid) {
+      const float sg = 1.0f / (1.0f + __expf(-g[j]));
+      dg[j] = h[j] * u[j] * sg * (1.0f + g[j] * (1.0f - sg));
+      g[j] = h[j] * (g[j] * sg);
+    } else {
+      dg[j] = 0.0f;
+      g[j] = 0.0f;
+    }
+  }
+  const int ktl = 2 * I / 128;
+  uint8_t* qr = q_rows + prow * (2 * I);
+  float* sw = scr[warp];
+  emit_rowq(dg, qr + c0, q_rows_sf + sf_off(prow, c0 >> 5, ktl));
+  emit_tokq(dg, sw, lane, q_tok, q_tok_sf, Rmax, c0, r0);
+  emit_rowq(g, qr + I + c0, q_rows_sf + sf_off(prow, (I + c0) >> 5, ktl));
+  emit_tokq(g, sw, lane, q_tok, q_tok_sf, Rmax, I + c0, r0);
+}
+
 __global__ void scales_to_tiled_kernel(const uint8_t* __restrict__ canon, int64_t rows, int nb, uint8_t* tiled) {
   const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (gid >= rows * nb) return;
@@ -171,6 +237,17 @@ void launch_quant_cols(const void* src, int64_t rows, int K, int64_t ld, int64_t
   Prof prof("quant_cols", s);
   quant_cols_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(src), rows, K, ld, rows_pad, codes, sf,
                                          tiled ? 1 : 0);
+}
+
+void launch_swiglu_bwd_quant(const Dims& m, const Layout& L, void* ws, cudaStream_t s) {
+  if (m.Rmax == 0) return;
+  dim3 grid(static_cast<unsigned>(ceil_div(m.I, 128)), static_cast<unsigned>(m.Rmax / 32));
+  Prof prof("swiglu_bwd_quant", s);
+  swiglu_bwd_quant_kernel<<<grid, 128, 0, s>>>(
+      ws_ptr<float>(L, ws, MOE_WS_DH), ws_ptr<__nv_bfloat16>(L, ws, MOE_WS_GU), ws_ptr<int>(L, ws, MOE_WS_ROWSRC),
+      ws_ptr<int>(L, ws, MOE_WS_POFF) + m.Ep, m.I, m.Rmax, ws_ptr<uint8_t>(L, ws, MOE_WS_DGU),
+      ws_ptr<uint8_t>(L, ws, MOE_WS_DGU_SF), ws_ptr<uint8_t>(L, ws, MOE_WS_DGUTOK),
+      ws_ptr<uint8_t>(L, ws, MOE_WS_DGUTOK_SF));
 }
 
 void launch_tok_gather(const Dims& m, const void* src_rows, bool scale_by_gate, const float* topk_w,

@@ -92,7 +92,7 @@ __global__ void sched_scan_kernel(const int* __restrict__ hist, int Ep, int unit
 // processed whole in lap 0 (it is read in token order, not from the ring).
 __global__ void sched_offsets_kernel(const int* __restrict__ counts, int E, int Ep, int C, int Lb,
                                      int* __restrict__ offsets, int* __restrict__ poff, int* __restrict__ lap_tiles,
-                                     int* __restrict__ meta) {
+                                     int* __restrict__ meta, int* __restrict__ lapbase) {
   if (threadIdx.x == 0) {
     int o = 0, po = 0, laps = 0;
     for (int e = 0; e < Ep; ++e) {
@@ -107,6 +107,9 @@ __global__ void sched_offsets_kernel(const int* __restrict__ counts, int E, int 
     poff[Ep] = po;
     meta[0] = laps;
     meta[1] = po;
+    int active = 0;
+    for (int e = 0; e < Ep; ++e) active += counts[e] > 0 ? 1 : 0;
+    meta[2] = active;
   }
   for (int L = threadIdx.x; L < Lb; L += blockDim.x) {
     int run = 0;
@@ -124,6 +127,15 @@ __global__ void sched_offsets_kernel(const int* __restrict__ counts, int E, int 
       run += (len + 127) / 128;
     }
     lt[Ep] = run;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {       // lapbase[L] = sum over laps L' < L of their m-tiles
+    int run = 0;
+    for (int L = 0; L < Lb; ++L) {
+      lapbase[L] = run;
+      run += lap_tiles[static_cast<int64_t>(L) * (Ep + 1) + Ep];
+    }
+    lapbase[Lb] = run;
   }
 }
 
@@ -198,7 +210,8 @@ void launch_schedule(const Dims& m, const int32_t* idx, const Layout& L, void* w
     cudaMemsetAsync(counts, 0, sizeof(int) * m.Ep, s);
   }
   { Prof prof("sched_offsets", s);
-  sched_offsets_kernel<<<1, 256, 0, s>>>(counts, m.E, m.Ep, m.C, m.Lb, offsets, poff, lap_tiles, meta); }
+  sched_offsets_kernel<<<1, 256, 0, s>>>(counts, m.E, m.Ep, m.C, m.Lb, offsets, poff, lap_tiles, meta,
+                                         ws_ptr<int>(L, ws, MOE_WS_LAPBASE)); }
   { Prof prof("sched_order", s);
   sched_order_kernel<<<1, 512, 0, s>>>(counts, m.Ep, ws_ptr<int>(L, ws, MOE_WS_ORDER)); }
   if (m.units > 0) {

@@ -53,6 +53,10 @@ struct WLayout {
   size_t total;
 };
 
+// Upper bound on the m-tiles of all ring laps together: sum over experts of
+// (ceil(n_e / 128) + laps_e) <= Rmax / 128 + Ep * Lb.
+inline int64_t lap_mtiles_max(const Dims& m) { return m.Rmax / 128 + static_cast<int64_t>(m.Ep) * (m.Lb > 0 ? m.Lb : 1); }
+
 int validate(const moe_config_t* cfg);
 Dims make_dims(const moe_config_t* cfg);
 Layout make_layout(const moe_config_t* cfg);
@@ -97,6 +101,9 @@ void launch_rev_combine_dw(const Dims& m, const void* dy, const float* topk_w, c
                            cudaStream_t s);
 void launch_rev_combine_lap(const Dims& m, int lap, const void* dy, const float* topk_w, const Layout& L,
                             void* ws, cudaStream_t s);
+// SwiGLU backward of the padded rank rows and MX of dGU = [dg | du] two ways
+// (along 2I per row, and along ranks per column).
+void launch_swiglu_bwd_quant(const Dims& m, const Layout& L, void* ws, cudaStream_t s);
 void launch_tok_gather(const Dims& m, const void* src_rows, bool scale_by_gate, const float* topk_w,
                        bool router_partials, const Layout& L, void* ws, uint8_t* codes, uint8_t* sf,
                        cudaStream_t s);
@@ -108,9 +115,22 @@ void launch_router_dwr(const Dims& m, const Layout& L, void* ws, void* dw_router
 enum GemmMode : int {
   kSwigluFwd = 0,   // lap tiles, A = ring / x_q, epilogue SwiGLU + MX(h) two ways + saved g,u
   kPush = 1,        // padded tiles, epilogue bf16 rows pushed to their assignment
-  kSwigluBwd = 2,   // lap tiles, A = ring dO / dO_s, epilogue SwiGLU backward + MX(dGU) two ways
+  kSwigluBwd = 2,   // lap tiles, A = ring dO / dO_s, epilogue fp32 dh rows (SwiGLU backward follows)
   kWgrad = 3,       // per-expert K ranges, epilogue bf16 weight gradient
   kPlain = 4,       // single dense problem, fp32 output (unit test entry)
+  // 5 is the bf16 router-logit mode (gemm.cuh)
+  kSwigluFwdRing = 6,  // kSwigluFwd over all ring laps in one launch, mover warps fill the ring
+  kSwigluBwdRing = 7,  // kSwigluBwd over all ring laps in one launch, mover warps fill the dO ring
+};
+
+// Where the mover warps of the all-laps ring modes take each ring row from.
+struct RingMovers {
+  const int* lapbase;            // [Lb+1] first global m-tile of each lap
+  int* moved;                    // per global m-tile: 8-row groups written (target 16)
+  int* consumed;                 // per global m-tile: GEMM tiles whose A loads landed (target N / BN)
+  const uint8_t* xq; const uint8_t* xq_sf;   // forward: MX(x) rows along d, tiled scales
+  const void* dy; const float* topk_w;       // backward: bf16 dy rows and the gates
+  uint8_t* ring; uint8_t* ring_sf;           // [kRingBufs][E][C] rows, tiled scales
 };
 
 struct GemmOperands {
@@ -130,6 +150,7 @@ struct GemmEpilogue {
 
 int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int K, int M, const GemmOperands& op,
                   const GemmEpilogue& ep, const int* counts, const int* poff, const int* lap_tiles,
-                  const int* row_src, int* status, cudaStream_t s, int bn_hint = 0, const int* order = nullptr);
+                  const int* row_src, int* status, cudaStream_t s, int bn_hint = 0, const int* order = nullptr,
+                  const RingMovers* mv = nullptr);
 
 }  // namespace moe

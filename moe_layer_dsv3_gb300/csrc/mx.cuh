@@ -78,4 +78,33 @@ __device__ __forceinline__ int64_t sf_off(int64_t r, int64_t kb, int64_t k_tiles
   return ((r >> 7) * k_tiles + (kb >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (kb & 3);
 }
 
+// Row-wise MX of 32 values: codes to dst (16-byte aligned), scale byte to sf.
+__device__ __forceinline__ void emit_rowq(const float* v, uint8_t* dst, uint8_t* sf_byte) {
+  const int b = mx_scale_byte(amax32(v));
+  uint32_t w[8];
+  mx_pack32(v, mx_inv_scale(b), w);
+  store32(dst, w);
+  *sf_byte = static_cast<uint8_t>(b);
+}
+
+// Token-axis MX of a warp's 32x32 block (lane = row): transposes through
+// shared memory so that lane j owns column j, then writes 32 codes of that
+// column (32 consecutive ranks) and its scale.
+__device__ __forceinline__ void emit_tokq(const float* v, float* scr, int lane, uint8_t* q_tok, uint8_t* q_tok_sf,
+                                          int64_t pitch, int64_t col0, int64_t prow_base) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) scr[lane * 33 + j] = v[j];
+  __syncwarp();
+  float c[32];
+#pragma unroll
+  for (int r = 0; r < 32; ++r) c[r] = scr[r * 33 + lane];
+  __syncwarp();
+  const int b = mx_scale_byte(amax32(c));
+  uint32_t w[8];
+  mx_pack32(c, mx_inv_scale(b), w);
+  const int64_t col = col0 + lane;
+  store32(q_tok + col * pitch + prow_base, w);
+  q_tok_sf[sf_off(col, prow_base >> 5, pitch >> 7)] = static_cast<uint8_t>(b);
+}
+
 }  // namespace moe

@@ -84,6 +84,35 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
   }
 }
 
+// ----------------------------------------------------------------- cross-CTA flags
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Orders this thread's generic-proxy global accesses with its async-proxy (TMA) ones.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// Spin until *ctr >= target (acquire). Gives up after kWaitLimitNs and records (kErrTimeout, site).
+__device__ __forceinline__ bool wait_counter(const int* ctr, int target, int* status, int site) {
+  if (ld_acquire_gpu(ctr) >= target) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    for (int i = 0; i < 32; ++i) {
+      if (ld_acquire_gpu(ctr) >= target) return true;
+      __nanosleep(64);
+    }
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      report_error(status, kErrTimeout, site);
+      return false;
+    }
+  }
+}
+
 // ----------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");

@@ -391,3 +391,42 @@ def test_deterministic_rerun(run):
     for a, b in zip(outs1, outs2):
         assert torch.equal(a.view(torch.uint8) if a.dtype != torch.float32 else a.view(torch.int32),
                            b.view(torch.uint8) if b.dtype != torch.float32 else b.view(torch.int32))
+
+
+def test_lap_launch_path_bitwise(run):
+    """The per-lap launch form (a mover launch and a GEMM launch per ring lap, laps on two streams)
+    gives the same bytes as the single all-laps launch with mover warps: outputs, gradients and
+    both rings."""
+    from moe_layer_dsv3_gb300 import MOE_FLAG_LAP_LAUNCHES
+    from moe_layer_dsv3_gb300.layer import MoELayer
+    dev = run.dev
+    L2 = MoELayer.from_shape(run.shape, flags=MOE_FLAG_LAP_LAUNCHES)
+    L2.quantize_weights(dev["w_gu"], dev["w_d"], dev["ws_gu"], dev["ws_d"])
+    L2.forward(dev["x"], dev["w_router"], dev["bias"])
+    L2.backward(dev["dy"])
+    torch.cuda.synchronize()
+    assert L2.status() == (0, 0)
+    L = run.L
+    for name in ("y", "dx", "dw_router", "dw_gu", "dw_d", "dws_gu", "dws_d", "topk_w"):
+        a, b = getattr(L, name), getattr(L2, name)
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), name
+    for name in ("RING_X", "RING_X_SF", "RING_DO", "RING_DO_SF", "GU", "HQ", "DGU"):
+        assert torch.equal(L.ws_tensor(name), L2.ws_tensor(name)), name
+
+
+def test_idle_expert_weight_grads_zeroed(run):
+    """Experts that received no token get exactly zero weight gradients (their fill runs on a side
+    stream), whatever the output buffers held before; the other experts' gradients are unchanged."""
+    L, dev = run.L, run.dev
+    counts = run.f["sched"]["counts"]
+    ref_gu, ref_d = L.dw_gu.clone(), L.dw_d.clone()
+    L.dw_gu.view(torch.uint8).fill_(0xFF)          # NaN pattern
+    L.dw_d.view(torch.uint8).fill_(0xFF)
+    L.backward(dev["dy"])
+    torch.cuda.synchronize()
+    assert L.status() == (0, 0)
+    for e in range(run.shape.E):
+        if counts[e] == 0:
+            assert not L.dw_gu[e].view(torch.int16).any() and not L.dw_d[e].view(torch.int16).any(), e
+    assert torch.equal(L.dw_gu.view(torch.int16), ref_gu.view(torch.int16))
+    assert torch.equal(L.dw_d.view(torch.int16), ref_d.view(torch.int16))
