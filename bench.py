@@ -76,6 +76,8 @@ def hbm_bytes(shape):
         "tok_gather_x": R * d * 2.0 + R * row_q,
         "tok_gather_dO": R * d * 2.0 + R * row_q,
         "quant_rows": T * d * 2.0 * (1 + S) + T * row_q * (1 + S),
+        # dh fp32 and saved g|u bf16 in; dGU codes + scales out along 2I and along ranks
+        "swiglu_bwd_quant": R * (shape.I * 4.0 + 2 * shape.I * 2.0 + 2 * (2 * shape.I + 2 * shape.I / 32.0)),
     }
 
 
@@ -272,6 +274,47 @@ def run_reference(args, rank, world):
 
 
 # ---------------------------------------------------------------- our arm
+def standalone_movers(shape, L, inp, sp, hb):
+    """GB/s of the ring gather run as its own kernels: moe_dispatch (MX(x), then
+    one gather launch per lap) timed alone after the timed region. In the
+    default form the same moves run inside GEMM1's mover warps, overlapped
+    with the MMAs, and have no time of their own. The backward pull
+    (rev_combine_lap) is timed in one per-lap pass of a second layer."""
+    import moe_layer_dsv3_gb300 as M
+    from moe_layer_dsv3_gb300.layer import MoELayer
+    x, dy, wr, bias = inp["x"], inp["dy"], inp["w_router"], inp["bias"]
+    out = {}
+    for _ in range(2):
+        L.dispatch(x, sp)
+    torch.cuda.synchronize()
+    M.moe_profile_enable(True)
+    M.moe_profile_read()
+    for _ in range(3):
+        L.dispatch(x, sp)
+    torch.cuda.synchronize()
+    kern = M.moe_profile_read()
+    M.moe_profile_enable(False)
+    if "permute_lap" in kern and kern["permute_lap"][1] > 0:
+        out["permute_lap"] = 3 * hb["permute_lap"] / (kern["permute_lap"][1] / 1000.0) / 1e9
+    Lp = MoELayer.from_shape(shape, flags=M.MOE_FLAG_LAP_LAUNCHES)
+    Lp.wq = L.wq                                   # the same quantised weights
+    for _ in range(2):
+        Lp.forward(x, wr, bias, sp)
+        Lp.backward(dy, sp)
+    torch.cuda.synchronize()
+    M.moe_profile_enable(True)
+    M.moe_profile_read()
+    Lp.backward(dy, sp)
+    torch.cuda.synchronize()
+    kern = M.moe_profile_read()
+    M.moe_profile_enable(False)
+    if "rev_combine_lap" in kern and kern["rev_combine_lap"][1] > 0:
+        out["rev_combine_lap"] = hb["rev_combine_lap"] / (kern["rev_combine_lap"][1] / 1000.0) / 1e9
+    del Lp
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, rank, world, local_rank):
     import moe_layer_dsv3_gb300 as M
     from moe_layer_dsv3_gb300.layer import MoELayer
@@ -340,27 +383,60 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     stages = {n: ev[i].elapsed_time(ev[i + 1]) for i, n in enumerate(("route", "schedule", "forward", "backward"))}
 
-    # ---- end to end through the C ABI with host buffers (H2D of x, dy; D2H of y, dx)
+    # ---- end to end through the C ABI with host buffers (H2D of x, dy; D2H of y, dx).
+    # Every step copies its inputs from pinned host memory and its outputs back.
+    # The copies run on two copy streams, double-buffered on the device, so
+    # step i+1's upload and step i's download overlap step i's compute.
     xh = x.cpu().pin_memory()
     dyh = dy.cpu().pin_memory()
     yh = torch.empty_like(xh).pin_memory()
     dxh = torch.empty_like(xh).pin_memory()
-    xd, dyd = torch.empty_like(x), torch.empty_like(dy)
+    xd = [torch.empty_like(x) for _ in range(2)]
+    dyd = [torch.empty_like(dy) for _ in range(2)]
+    yd = [torch.empty_like(x) for _ in range(2)]
+    dxd = [torch.empty_like(x) for _ in range(2)]
+    h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
 
-    def e2e_step():
-        xd.copy_(xh, non_blocking=True)
-        dyd.copy_(dyh, non_blocking=True)
-        L.forward(xd, wr, bias, sp)
-        L.backward(dyd, sp)
-        yh.copy_(L.y, non_blocking=True)
-        dxh.copy_(L.dx, non_blocking=True)
+    def e2e_run(n, start_ev):
+        loaded = [torch.cuda.Event() for _ in range(2)]
+        done = [torch.cuda.Event() for _ in range(2)]
+        drained = [torch.cuda.Event() for _ in range(2)]
 
-    e2e_step()
+        def upload(b, after):
+            h2d_s.wait_event(after)
+            with torch.cuda.stream(h2d_s):
+                xd[b].copy_(xh, non_blocking=True)
+                dyd[b].copy_(dyh, non_blocking=True)
+            loaded[b].record(h2d_s)
+
+        upload(0, start_ev)
+        for i in range(n):
+            b = i % 2
+            if i + 1 < n:
+                upload(1 - b, done[1 - b] if i >= 1 else start_ev)
+            stream.wait_event(loaded[b])
+            if i >= 2:
+                stream.wait_event(drained[b])
+            L.forward(xd[b], wr, bias, sp)
+            L.backward(dyd[b], sp)
+            yd[b].copy_(L.y)
+            dxd[b].copy_(L.dx)
+            done[b].record(stream)
+            d2h_s.wait_event(done[b])
+            with torch.cuda.stream(d2h_s):
+                yh.copy_(yd[b], non_blocking=True)
+                dxh.copy_(dxd[b], non_blocking=True)
+            drained[b].record(d2h_s)
+        stream.wait_stream(d2h_s)
+        stream.wait_stream(h2d_s)
+
+    s0 = torch.cuda.Event()
+    s0.record(stream)
+    e2e_run(2, s0)
     torch.cuda.synchronize()
     barrier()
     e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    e2e_run(args.steps, e0)
     e1.record(stream)
     torch.cuda.synchronize()
     ms_e2e = e0.elapsed_time(e1) / args.steps
@@ -389,7 +465,7 @@ def run_ours(args, rank, world, local_rank):
     # Ring-lap kernels run on two streams and overlap one another, so their
     # event times are not additive; the dominant kernel is taken among the
     # kernels that run alone on the launch stream.
-    lap_kernels = {"gemm1_fwd", "gemm_dgrad_down", "permute_lap", "rev_combine_lap"}
+    lap_kernels = {"gemm1_fwd", "gemm_dgrad_down", "permute_lap", "rev_combine_lap"} if args.lap_launches else set()
     dom = max(((n, v) for n, v in kern.items() if n not in lap_kernels), key=lambda kv: kv[1][1])[0]
     fp8_peak = 2.0 * pk["bf16_sus"]
     if dom in fl:
@@ -414,11 +490,16 @@ def run_ours(args, rank, world, local_rank):
     gemm_ms = sum(kern[n][1] for n in gemm_names) / args.steps
     gemm_tflops = sum(fl[n] for n in gemm_names) / (gemm_ms / 1000.0) / 1e12 if gemm_ms else None
     perm = per_kernel.get("permute_lap", {}).get("gbs")
+    movers = None
+    if not args.lap_launches and not args.no_standalone_movers:
+        movers = standalone_movers(shape, L, inp, sp, hb)
+        perm = movers.get("permute_lap")
     extra = {
         "stages_ms": stages,
         "grouped_gemm_tflops": gemm_tflops,
         "grouped_gemm_frac_fp8_peak": gemm_tflops / fp8_peak if gemm_tflops else None,
         "permute_gbs": perm,
+        "standalone_movers_gbs": movers,
         "permute_frac_hbm": perm / pk["hbm_gbs"] if perm else None,
         "schedule_share": (stages["schedule"]) / sum(stages.values()),
         "lap_kernels_overlap": sorted(lap_kernels),
@@ -438,7 +519,7 @@ def run_ours(args, rank, world, local_rank):
     E_all = shape.E + shape.S
     extra["waves"] = {"sm_count": sms,
                       "gemm1_fwd": mt * (2 * shape.I // 256) / sms, "gemm2_fwd": mt * (shape.d // 256) / sms,
-                      "gemm_dgrad_down": mt * (shape.I // 128) / sms, "gemm_dgrad_gu": mt * (shape.d // 256) / sms,
+                      "gemm_dgrad_down": mt * (shape.I // 256) / sms, "gemm_dgrad_gu": mt * (shape.d // 256) / sms,
                       "gemm_wgrad_d": E_all * (shape.d // 128) * (shape.I // 256) / sms,
                       "gemm_wgrad_gu": E_all * (2 * shape.I // 128) * (shape.d // 256) / sms}
     extra["routing"] = {"max_count": int(counts.max()), "min_count": int(counts.min()),
@@ -472,6 +553,8 @@ def main():
     ap.add_argument("--workload", default="dsv3_zipf")
     ap.add_argument("--T", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-standalone-movers", action="store_true",
+                    help="skip the extra per-lap pass that times the ring movers as their own launches")
     ap.add_argument("--lap-launches", action="store_true",
                     help="one mover launch + one GEMM launch per ring lap instead of one all-laps launch")
     args = ap.parse_args()

@@ -161,6 +161,19 @@ MOE_API int moe_schedule(const moe_config_t* cfg, const int32_t* topk_idx, void*
 MOE_API int moe_forward(const moe_config_t* cfg, const void* x, const void* wq, const float* topk_w, void* y, void* ws,
                 moe_stream_t stream);
 
+/* Dispatch alone: MX(x) along d into the workspace, then every ring lap's
+ * rows gathered into the ring token buffers by the schedule of the last
+ * moe_schedule on this workspace (lap L of an expert into buffer L % 2; on
+ * return the buffers hold each expert's last two laps). This is the
+ * dispatch step the pages describe (tokens pulled into fixed-capacity ring
+ * buffers; techlab report, ring token buffer paragraph) run as its own
+ * kernels, one launch per lap on `stream`. moe_forward does the same moves
+ * inside its GEMM1 launch, so a forward needs no dispatch call; this entry
+ * serves callers that want the dispatched ring by itself.
+ * x: bf16 [T][d] (device). ws: the workspace. Errors: MOE_ERR_INVALID_ARG,
+ * MOE_ERR_UNSUPPORTED_ARCH, MOE_ERR_CUDA (launch failure). */
+MOE_API int moe_dispatch(const moe_config_t* cfg, const void* x, void* ws, moe_stream_t stream);
+
 /* Backward pass (write-ups: reverse-combine and reverse-dispatch on the
  * reused schedule, Cursor blog summary "method points").
  *   x, w_router, topk_idx, topk_w: the forward inputs / router outputs.

@@ -67,6 +67,7 @@ _SIGS = {
     "moe_route_noalloc": [_CFG, _P, _P, _P, _P, _P, _P],
     "moe_schedule": [_CFG, _P, _P, _P],
     "moe_forward": [_CFG, _P, _P, _P, _P, _P, _P],
+    "moe_dispatch": [_CFG, _P, _P, _P],
     "moe_backward": [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "moe_status": [_CFG, _P, ctypes.POINTER(_I), ctypes.POINTER(_I), _I, _P],
     "moe_ws_view": [_CFG, _P, _I, ctypes.POINTER(_P), _SZ],
@@ -147,6 +148,10 @@ def moe_schedule(cfg, topk_idx, ws, stream=0):
 
 def moe_forward(cfg, x, wq, topk_w, y, ws, stream=0):
     _check("moe_forward", _lib.moe_forward(ctypes.byref(cfg), _p(x), _p(wq), _p(topk_w), _p(y), _p(ws), _p(stream)))
+
+
+def moe_dispatch(cfg, x, ws, stream=0):
+    _check("moe_dispatch", _lib.moe_dispatch(ctypes.byref(cfg), _p(x), _p(ws), _p(stream)))
 
 
 def moe_backward(cfg, x, w_router, topk_idx, topk_w, dy, wq, dx, dw_router, dw_gu, dw_d, dws_gu, dws_d, ws, stream=0):

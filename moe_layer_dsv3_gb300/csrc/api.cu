@@ -315,6 +315,25 @@ int moe_schedule(const moe_config_t* cfg, const int32_t* topk_idx, void* ws, moe
   return launch_status();
 }
 
+int moe_dispatch(const moe_config_t* cfg, const void* x, void* ws, moe_stream_t stream) {
+  if (int r = validate(cfg)) return r;
+  if (!x || !ws) return MOE_ERR_INVALID_ARG;
+  if (!arch_ok()) return MOE_ERR_UNSUPPORTED_ARCH;
+  const Layout L = make_layout(cfg);
+  const Dims& m = L.m;
+  if (m.T == 0) return MOE_OK;
+  cudaStream_t s = S(stream);
+  uint8_t* xq = ws_ptr<uint8_t>(L, ws, MOE_WS_XQ);
+  uint8_t* xq_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_XQ_SF);
+  if (m.Tpad > m.T) {
+    cudaMemsetAsync(xq + m.T * m.d, 0, (m.Tpad - m.T) * m.d, s);
+    cudaMemsetAsync(xq_sf + (m.T / 128) * 128 * (m.d / 32), 0, (m.Tpad - m.T / 128 * 128) * (m.d / 32), s);
+  }
+  launch_quant_rows(x, m.T, m.d, m.d, xq, xq_sf, true, 0, s);
+  for (int lap = 0; lap < m.Lb; ++lap) launch_permute_lap(m, lap, L, ws, s);
+  return launch_status();
+}
+
 int moe_forward(const moe_config_t* cfg, const void* x, const void* wq, const float* topk_w, void* y, void* ws,
                 moe_stream_t stream) {
   if (int r = validate(cfg)) return r;

@@ -9,7 +9,7 @@ from __future__ import annotations
 
 import torch
 
-from . import (config, moe_backward, moe_forward, moe_quantize_weights, moe_route, moe_schedule, moe_status,
+from . import (config, moe_backward, moe_dispatch, moe_forward, moe_quantize_weights, moe_route, moe_schedule, moe_status,
                moe_weights_size, moe_workspace_size, moe_ws_view, moe_wq_view, MoeError)
 
 
@@ -63,6 +63,10 @@ class MoELayer:
 
     def schedule(self, stream=0):
         moe_schedule(self.cfg, self.topk_idx.data_ptr(), self.ws.data_ptr(), stream)
+
+    def dispatch(self, x, stream=0):
+        """MX(x) and the ring dispatch of every lap alone (moe_forward does this itself)."""
+        moe_dispatch(self.cfg, x.data_ptr(), self.ws.data_ptr(), stream)
 
     def forward_experts(self, x, stream=0):
         moe_forward(self.cfg, x.data_ptr(), self.wq.data_ptr(), self.topk_w.data_ptr(), self.y.data_ptr(),

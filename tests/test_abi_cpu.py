@@ -19,7 +19,7 @@ def _lib():
 
 def test_header_declares_entry_points():
     names = _declared()
-    for n in ("moe_route", "moe_schedule", "moe_forward", "moe_backward", "moe_quantize_mxfp8",
+    for n in ("moe_route", "moe_schedule", "moe_dispatch", "moe_forward", "moe_backward", "moe_quantize_mxfp8",
               "moe_quantize_weights", "moe_workspace_size", "moe_status"):
         assert n in names
 

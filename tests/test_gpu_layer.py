@@ -430,3 +430,21 @@ def test_idle_expert_weight_grads_zeroed(run):
             assert not L.dw_gu[e].view(torch.int16).any() and not L.dw_d[e].view(torch.int16).any(), e
     assert torch.equal(L.dw_gu.view(torch.int16), ref_gu.view(torch.int16))
     assert torch.equal(L.dw_d.view(torch.int16), ref_d.view(torch.int16))
+
+
+def test_dispatch_alone_fills_the_ring(run):
+    """moe_dispatch (MX(x) + the per-lap gather kernels) leaves the same ring bytes as the
+    forward's in-kernel movers."""
+    L, dev = run.L, run.dev
+    L.ws_tensor("RING_X").fill_(0x5A)              # rows no lap writes keep this in both runs
+    L.ws_tensor("RING_X_SF").fill_(0x5A)
+    L.forward(dev["x"], dev["w_router"], dev["bias"])
+    torch.cuda.synchronize()
+    ref = L.ws_tensor("RING_X").clone(), L.ws_tensor("RING_X_SF").clone()
+    L.ws_tensor("RING_X").fill_(0x5A)
+    L.ws_tensor("RING_X_SF").fill_(0x5A)
+    L.dispatch(dev["x"])
+    torch.cuda.synchronize()
+    assert L.status() == (0, 0)
+    assert torch.equal(L.ws_tensor("RING_X"), ref[0])
+    assert torch.equal(L.ws_tensor("RING_X_SF"), ref[1])
