@@ -275,8 +275,8 @@ def run_reference(args, rank, world):
 
 # ---------------------------------------------------------------- our arm
 def standalone_movers(shape, L, inp, sp, hb):
-    """GB/s of the ring gather run as its own kernels: moe_dispatch (MX(x), then
-    one gather launch per lap) timed alone after the timed region. In the
+    """GB/s of the ring gather run as its own kernel: moe_dispatch (MX(x), then
+    one gather launch over all laps) timed alone after the timed region. In the
     default form the same moves run inside GEMM1's mover warps, overlapped
     with the MMAs, and have no time of their own. The backward pull
     (rev_combine_lap) is timed in one per-lap pass of a second layer."""
@@ -294,8 +294,8 @@ def standalone_movers(shape, L, inp, sp, hb):
     torch.cuda.synchronize()
     kern = M.moe_profile_read()
     M.moe_profile_enable(False)
-    if "permute_lap" in kern and kern["permute_lap"][1] > 0:
-        out["permute_lap"] = 3 * hb["permute_lap"] / (kern["permute_lap"][1] / 1000.0) / 1e9
+    if "dispatch_all" in kern and kern["dispatch_all"][1] > 0:
+        out["permute_lap"] = 3 * hb["permute_lap"] / (kern["dispatch_all"][1] / 1000.0) / 1e9
     Lp = MoELayer.from_shape(shape, flags=M.MOE_FLAG_LAP_LAUNCHES)
     Lp.wq = L.wq                                   # the same quantised weights
     for _ in range(2):

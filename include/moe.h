@@ -167,9 +167,11 @@ MOE_API int moe_forward(const moe_config_t* cfg, const void* x, const void* wq, 
  * return the buffers hold each expert's last two laps). This is the
  * dispatch step the pages describe (tokens pulled into fixed-capacity ring
  * buffers; techlab report, ring token buffer paragraph) run as its own
- * kernels, one launch per lap on `stream`. moe_forward does the same moves
+ * kernel on `stream`. moe_forward does the same moves
  * inside its GEMM1 launch, so a forward needs no dispatch call; this entry
- * serves callers that want the dispatched ring by itself.
+ * serves callers that want the dispatched ring by itself. One launch covers
+ * all laps: a warp per (expert, buffer, 8 slots) writes that slot group's
+ * laps in lap order, so the final bytes equal those of lap-by-lap dispatch.
  * x: bf16 [T][d] (device). ws: the workspace. Errors: MOE_ERR_INVALID_ARG,
  * MOE_ERR_UNSUPPORTED_ARCH, MOE_ERR_CUDA (launch failure). */
 MOE_API int moe_dispatch(const moe_config_t* cfg, const void* x, void* ws, moe_stream_t stream);

@@ -330,7 +330,7 @@ int moe_dispatch(const moe_config_t* cfg, const void* x, void* ws, moe_stream_t 
     cudaMemsetAsync(xq_sf + (m.T / 128) * 128 * (m.d / 32), 0, (m.Tpad - m.T / 128 * 128) * (m.d / 32), s);
   }
   launch_quant_rows(x, m.T, m.d, m.d, xq, xq_sf, true, 0, s);
-  for (int lap = 0; lap < m.Lb; ++lap) launch_permute_lap(m, lap, L, ws, s);
+  launch_dispatch_all(m, L, ws, s);
   return launch_status();
 }
 

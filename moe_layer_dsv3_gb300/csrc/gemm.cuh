@@ -481,13 +481,19 @@ __device__ __forceinline__ void gemm_epilogue_tile(const GemmParams& p, const Ti
     float h[BN / 2];
 #pragma unroll
     for (int c = 0; c < BN / 64; ++c) {
+      uint32_t rg[32], ru[32];
+      tmem_ld32_async(tacc + c * 32, rg);
+      tmem_ld32_async(tacc + BN / 2 + c * 32, ru);
+      tmem_wait_ld();
       float g[32], u[32];
-      tmem_ld32(tacc + c * 32, g);
-      tmem_ld32(tacc + BN / 2 + c * 32, u);
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        if (!valid) { g[j] = 0.0f; u[j] = 0.0f; }
-        h[c * 32 + j] = g[j] / (1.0f + __expf(-g[j])) * u[j];
+        reg_fence(rg[j]);
+        reg_fence(ru[j]);
+        g[j] = valid ? __uint_as_float(rg[j]) : 0.0f;
+        u[j] = valid ? __uint_as_float(ru[j]) : 0.0f;
+        // silu(g) u with the fast reciprocal-based divide (about 2 ulp)
+        h[c * 32 + j] = __fdividef(g[j], 1.0f + __expf(-g[j])) * u[j];
       }
       const int64_t icol = i_base + c * 32;
       store_bf16x32(p.gu + prow * (2 * I) + icol, g);

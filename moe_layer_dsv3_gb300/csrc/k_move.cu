@@ -124,6 +124,76 @@ __global__ void __launch_bounds__(256) rev_combine_lap_kernel(
   }
 }
 
+// Dispatch of every ring lap in one launch (moe_dispatch). Item = (expert e,
+// ring buffer b, group of 8 slots). The item's warp writes, for each lap
+// L = b, b + 2, ... of e in that order, the lap's rows into those slots
+// (zeros past the lap's rows up to its last 128-row tile): the same writes,
+// in the same per-slot order, as the per-lap kernels. Rows are copied in
+// rounds of kDispU 16-byte chunks a lane, the next round's loads issued
+// before this round's stores.
+constexpr int kDispU = 8;
+
+__global__ void __launch_bounds__(256) dispatch_all_kernel(
+    const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xq_sf, const int* __restrict__ counts,
+    const int* __restrict__ poff, const int* __restrict__ row_src, int k, int d, int E, int C,
+    uint8_t* __restrict__ ring, uint8_t* __restrict__ ring_sf) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int groups = C / 8;
+  const int64_t item = static_cast<int64_t>(blockIdx.x) * 8 + warp;
+  if (item >= static_cast<int64_t>(E) * 2 * groups) return;
+  const int e = static_cast<int>(item / (2 * groups));
+  const int rem = static_cast<int>(item - static_cast<int64_t>(e) * 2 * groups);
+  const int b = rem / groups, s0 = (rem - b * groups) * 8;
+  const int n = counts[e];
+  const int chunks = d >> 4, ktiles = d >> 7;
+  const int total = 8 * chunks;
+  const int rounds = (total + 32 * kDispU - 1) / (32 * kDispU);
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  for (int L = b; static_cast<int64_t>(L) * C < n; L += 2) {
+    const int len = min(C, n - L * C);
+    if (s0 >= (len + 127) / 128 * 128) break;
+    const int64_t rank0 = static_cast<int64_t>(L) * C + s0;
+    const int64_t row0 = (static_cast<int64_t>(b) * E + e) * C + s0;
+    const int a_l = (lane < 8 && rank0 + lane < n) ? row_src[poff[e] + rank0 + lane] : -1;
+    const int tok_l = a_l >= 0 ? a_l / k : -1;
+    uint4 nxt[kDispU];
+    auto load = [&](int rd, uint4* v) {
+#pragma unroll
+      for (int u = 0; u < kDispU; ++u) {
+        const int f = (rd * kDispU + u) * 32 + lane;
+        const int r = f / chunks, c = f - (f / chunks) * chunks;
+        const int t = __shfl_sync(0xffffffffu, tok_l, r < 8 ? r : 7);
+        v[u] = (f < total && t >= 0) ? __ldg(reinterpret_cast<const uint4*>(xq + static_cast<int64_t>(t) * d) + c)
+                                     : zero;
+      }
+    };
+    load(0, nxt);
+    for (int rd = 0; rd < rounds; ++rd) {
+      uint4 cur[kDispU];
+#pragma unroll
+      for (int u = 0; u < kDispU; ++u) cur[u] = nxt[u];
+      if (rd + 1 < rounds) load(rd + 1, nxt);
+#pragma unroll
+      for (int u = 0; u < kDispU; ++u) {
+        const int f = (rd * kDispU + u) * 32 + lane;
+        const int r = f / chunks, c = f - (f / chunks) * chunks;
+        if (f < total) reinterpret_cast<uint4*>(ring + (row0 + r) * d)[c] = cur[u];
+      }
+    }
+    int tok[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) tok[r] = __shfl_sync(0xffffffffu, tok_l, r);
+    for (int kt = lane; kt < ktiles; kt += 32) {
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const uint32_t v = tok[r] >= 0 ? __ldg(reinterpret_cast<const uint32_t*>(xq_sf + sf_off(tok[r], kt * 4, ktiles)))
+                                       : 0u;
+        *reinterpret_cast<uint32_t*>(ring_sf + sf_off(row0 + r, kt * 4, ktiles)) = v;
+      }
+    }
+  }
+}
+
 // y[t] = bf16(sum_{j<k} w[t,j] O[t,j] + sum_s O_shared[s][t]), fp32 in slot order.
 __global__ void combine_kernel(const __nv_bfloat16* __restrict__ O, const float* __restrict__ topk_w, int T, int k,
                                int S, int d, __nv_bfloat16* __restrict__ y) {
@@ -168,24 +238,38 @@ __global__ void rev_combine_dw_kernel(const __nv_bfloat16* __restrict__ dy, cons
   const int t = blockIdx.x * (blockDim.x >> 5) + warp;
   if (t >= T) return;
   const int chunks = d / 8;
+  // One pass over the row: each dy chunk is loaded once and multiplied with
+  // the k output rows; every per-slot sum still runs over the chunks in
+  // increasing order, then a fixed xor-shuffle tree.
   float dws[8];
-  for (int j = 0; j < k; ++j) {
-    const int64_t a = static_cast<int64_t>(t) * k + j;
-    float acc = 0.0f;
-    for (int c = lane; c < chunks; c += 32) {
-      const uint4 u = reinterpret_cast<const uint4*>(dy + static_cast<int64_t>(t) * d)[c];
-      const uint4 o = reinterpret_cast<const uint4*>(O + a * d)[c];
-      const uint32_t qu[4] = {u.x, u.y, u.z, u.w};
-      const uint32_t qo[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        acc = fmaf(__uint_as_float(qu[i] << 16), __uint_as_float(qo[i] << 16), acc);
-        acc = fmaf(__uint_as_float(qu[i] & 0xFFFF0000u), __uint_as_float(qo[i] & 0xFFFF0000u), acc);
+  for (int j = 0; j < 8; ++j) dws[j] = 0.0f;
+  const uint4* pdy = reinterpret_cast<const uint4*>(dy + static_cast<int64_t>(t) * d);
+  const uint4* po = reinterpret_cast<const uint4*>(O + static_cast<int64_t>(t) * k * d);
+#pragma unroll 2
+  for (int c = lane; c < chunks; c += 32) {
+    const uint4 u = pdy[c];
+    uint4 o[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (j < k) o[j] = po[static_cast<int64_t>(j) * chunks + c];
+    const uint32_t qu[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < k) {
+        const uint32_t qo[4] = {o[j].x, o[j].y, o[j].z, o[j].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          dws[j] = fmaf(__uint_as_float(qu[i] << 16), __uint_as_float(qo[i] << 16), dws[j]);
+          dws[j] = fmaf(__uint_as_float(qu[i] & 0xFFFF0000u), __uint_as_float(qo[i] & 0xFFFF0000u), dws[j]);
+        }
       }
     }
+  }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    dws[j & 7] = acc;
+  for (int j = 0; j < 8; ++j) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dws[j] += __shfl_xor_sync(0xffffffffu, dws[j], o);
   }
   if (lane == 0) {
     const int64_t base = static_cast<int64_t>(t) * k;
@@ -278,6 +362,16 @@ static int lap_blocks(const Dims& m) {
   const int64_t groups = static_cast<int64_t>(m.E) * (m.C / 128) * 16;
   const int64_t cap = static_cast<int64_t>(num_sms()) * 16;
   return static_cast<int>(groups < cap ? groups : cap);
+}
+
+void launch_dispatch_all(const Dims& m, const Layout& L, void* ws, cudaStream_t s) {
+  const int64_t items = static_cast<int64_t>(m.E) * 2 * (m.C / 8);
+  if (items == 0) return;
+  Prof prof("dispatch_all", s);
+  dispatch_all_kernel<<<static_cast<unsigned>(ceil_div(items, 8)), 256, 0, s>>>(
+      ws_ptr<uint8_t>(L, ws, MOE_WS_XQ), ws_ptr<uint8_t>(L, ws, MOE_WS_XQ_SF), ws_ptr<int>(L, ws, MOE_WS_COUNTS),
+      ws_ptr<int>(L, ws, MOE_WS_POFF), ws_ptr<int>(L, ws, MOE_WS_ROWSRC), m.k, m.d, m.E, m.C,
+      ws_ptr<uint8_t>(L, ws, MOE_WS_RING_X), ws_ptr<uint8_t>(L, ws, MOE_WS_RING_X_SF));
 }
 
 void launch_permute_lap(const Dims& m, int lap, const Layout& L, void* ws, cudaStream_t s) {

@@ -96,6 +96,8 @@ void launch_schedule(const Dims& m, const int32_t* idx, const Layout& L, void* w
 
 // ---------------------------------------------------------------- data movement
 void launch_permute_lap(const Dims& m, int lap, const Layout& L, void* ws, cudaStream_t s);
+// Every lap of the ring dispatch in one launch (same writes, same per-slot lap order).
+void launch_dispatch_all(const Dims& m, const Layout& L, void* ws, cudaStream_t s);
 void launch_combine(const Dims& m, const float* topk_w, const Layout& L, void* ws, void* y, cudaStream_t s);
 void launch_rev_combine_dw(const Dims& m, const void* dy, const float* topk_w, const Layout& L, void* ws,
                            cudaStream_t s);
