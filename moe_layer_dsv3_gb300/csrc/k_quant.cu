@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(128) swiglu_bwd_quant_kernel(
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
     if (valid) {
-      const float sg = __fdividef(1.0f, 1.0f + __expf(-g[j]));   // fast reciprocal (about 2 ulp)
+      const float sg = 1.0f / (1.0f + __expf(-g[j]));
       dg[j] = h[j] * u[j] * sg * (1.0f + g[j] * (1.0f - sg));
       g[j] = h[j] * (g[j] * sg);
     } else {
