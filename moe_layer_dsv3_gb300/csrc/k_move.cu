@@ -125,7 +125,8 @@ __global__ void __launch_bounds__(256) rev_combine_lap_kernel(
 }
 
 // Dispatch of every ring lap in one launch (moe_dispatch). Item = (expert e,
-// ring buffer b, group of 8 slots). The item's warp writes, for each lap
+// ring buffer b, group of 8 slots), experts taken in descending-count order so
+// that the slot groups with the most laps start first. The item's warp writes, for each lap
 // L = b, b + 2, ... of e in that order, the lap's rows into those slots
 // (zeros past the lap's rows up to its last 128-row tile): the same writes,
 // in the same per-slot order, as the per-lap kernels. Rows are copied in
@@ -135,14 +136,16 @@ constexpr int kDispU = 8;
 
 __global__ void __launch_bounds__(256) dispatch_all_kernel(
     const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xq_sf, const int* __restrict__ counts,
-    const int* __restrict__ poff, const int* __restrict__ row_src, int k, int d, int E, int C,
-    uint8_t* __restrict__ ring, uint8_t* __restrict__ ring_sf) {
+    const int* __restrict__ poff, const int* __restrict__ row_src, const int* __restrict__ order, int k, int d,
+    int E, int Ep, int C, uint8_t* __restrict__ ring, uint8_t* __restrict__ ring_sf) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int groups = C / 8;
   const int64_t item = static_cast<int64_t>(blockIdx.x) * 8 + warp;
-  if (item >= static_cast<int64_t>(E) * 2 * groups) return;
-  const int e = static_cast<int>(item / (2 * groups));
-  const int rem = static_cast<int>(item - static_cast<int64_t>(e) * 2 * groups);
+  if (item >= static_cast<int64_t>(Ep) * 2 * groups) return;
+  const int ei = static_cast<int>(item / (2 * groups));
+  const int rem = static_cast<int>(item - static_cast<int64_t>(ei) * 2 * groups);
+  const int e = order[ei];              // every expert once; the shared one has no ring rows
+  if (e >= E) return;
   const int b = rem / groups, s0 = (rem - b * groups) * 8;
   const int n = counts[e];
   const int chunks = d >> 4, ktiles = d >> 7;
@@ -365,13 +368,13 @@ static int lap_blocks(const Dims& m) {
 }
 
 void launch_dispatch_all(const Dims& m, const Layout& L, void* ws, cudaStream_t s) {
-  const int64_t items = static_cast<int64_t>(m.E) * 2 * (m.C / 8);
+  const int64_t items = static_cast<int64_t>(m.Ep) * 2 * (m.C / 8);
   if (items == 0) return;
   Prof prof("dispatch_all", s);
   dispatch_all_kernel<<<static_cast<unsigned>(ceil_div(items, 8)), 256, 0, s>>>(
       ws_ptr<uint8_t>(L, ws, MOE_WS_XQ), ws_ptr<uint8_t>(L, ws, MOE_WS_XQ_SF), ws_ptr<int>(L, ws, MOE_WS_COUNTS),
-      ws_ptr<int>(L, ws, MOE_WS_POFF), ws_ptr<int>(L, ws, MOE_WS_ROWSRC), m.k, m.d, m.E, m.C,
-      ws_ptr<uint8_t>(L, ws, MOE_WS_RING_X), ws_ptr<uint8_t>(L, ws, MOE_WS_RING_X_SF));
+      ws_ptr<int>(L, ws, MOE_WS_POFF), ws_ptr<int>(L, ws, MOE_WS_ROWSRC), ws_ptr<int>(L, ws, MOE_WS_ORDER), m.k,
+      m.d, m.E, m.Ep, m.C, ws_ptr<uint8_t>(L, ws, MOE_WS_RING_X), ws_ptr<uint8_t>(L, ws, MOE_WS_RING_X_SF));
 }
 
 void launch_permute_lap(const Dims& m, int lap, const Layout& L, void* ws, cudaStream_t s) {
