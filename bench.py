@@ -383,6 +383,22 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     stages = {n: ev[i].elapsed_time(ev[i + 1]) for i, n in enumerate(("route", "schedule", "forward", "backward"))}
 
+    # ---- the same step replayed from a CUDA graph of its launches (launch-overhead check)
+    graph_ms = None
+    if not args.no_graph:
+        g = L.capture_step(x, wr, bias, dy)
+        for _ in range(2):
+            g.replay()
+        torch.cuda.synchronize()
+        ge0, ge1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ge0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        ge1.record(stream)
+        torch.cuda.synchronize()
+        graph_ms = ge0.elapsed_time(ge1) / args.steps
+        del g
+
     # ---- end to end through the C ABI with host buffers (H2D of x, dy; D2H of y, dx).
     # Every step copies its inputs from pinned host memory and its outputs back.
     # The copies run on two copy streams, double-buffered on the device, so
@@ -498,6 +514,7 @@ def run_ours(args, rank, world, local_rank):
         "stages_ms": stages,
         "grouped_gemm_tflops": gemm_tflops,
         "grouped_gemm_frac_fp8_peak": gemm_tflops / fp8_peak if gemm_tflops else None,
+        "graph_ms_per_step": graph_ms,
         "permute_gbs": perm,
         "standalone_movers_gbs": movers,
         "permute_frac_hbm": perm / pk["hbm_gbs"] if perm else None,
@@ -553,6 +570,7 @@ def main():
     ap.add_argument("--workload", default="dsv3_zipf")
     ap.add_argument("--T", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
     ap.add_argument("--no-standalone-movers", action="store_true",
                     help="skip the extra per-lap pass that times the ring movers as their own launches")
     ap.add_argument("--lap-launches", action="store_true",

@@ -86,6 +86,29 @@ class MoELayer:
                      self.dws_gu.data_ptr(), self.dws_d.data_ptr(), self.ws.data_ptr(), stream)
         return self.dx
 
+    def capture_step(self, x, w_router, bias, dy):
+        """Record one whole step (route, schedule, forward, backward) into a CUDA graph.
+
+        The library allocates nothing and never synchronises inside these calls,
+        so the step captures as-is: 21 kernel nodes (plus the counter memsets),
+        including the cooperative all-laps GEMM launches. Replaying the graph
+        re-runs the step on whatever x, dy, w_router and bias hold at that time
+        (the same device buffers). Returns the torch.cuda.CUDAGraph; call
+        .replay() on it.
+        """
+        s = torch.cuda.Stream(device=self.device)
+        s.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(s):                 # one eager step: one-time attribute setup happens outside capture
+            self.forward(x, w_router, bias, s.cuda_stream)
+            self.backward(dy, s.cuda_stream)
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s, capture_error_mode="thread_local"):
+            self.forward(x, w_router, bias, s.cuda_stream)
+            self.backward(dy, s.cuda_stream)
+        torch.cuda.current_stream(self.device).wait_stream(s)
+        return g
+
     def status(self, clear=True, stream=0):
         return moe_status(self.cfg, self.ws.data_ptr(), clear, stream)
 

@@ -448,3 +448,19 @@ def test_dispatch_alone_fills_the_ring(run):
     assert L.status() == (0, 0)
     assert torch.equal(L.ws_tensor("RING_X"), ref[0])
     assert torch.equal(L.ws_tensor("RING_X_SF"), ref[1])
+
+
+def test_graph_replay_bitwise(run):
+    """A CUDA graph of the whole step (captured through the C ABI) replays to the same bytes as eager
+    execution: outputs, gradients and the status word."""
+    L, dev = run.L, run.dev
+    outs = [L.y, L.dx, L.dw_router, L.dw_gu, L.dw_d] + ([L.dws_gu, L.dws_d] if run.shape.S else [])
+    eager = [t.clone() for t in outs]
+    g = L.capture_step(dev["x"], dev["w_router"], dev["bias"], dev["dy"])
+    for t in outs:
+        t.view(torch.uint8).fill_(0xFF)
+    g.replay()
+    torch.cuda.synchronize()
+    assert L.status() == (0, 0)
+    for a, b in zip(eager, outs):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
