@@ -273,6 +273,27 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- multi-rank timing
+def rank_barrier(world):
+    """Barrier over the ranks of a --gpus N run (no-op for one rank)."""
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(value, world, device):
+    """The slowest rank's value: the job's time is the max over ranks."""
+    if world > 1:
+        t = torch.tensor([value], device=device, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        value = float(t.item())
+    return value
+
+
+def job_tokens_per_s(tokens_per_rank, world, ms_step):
+    """Whole-job throughput: every rank processes its own tokens_per_rank each step."""
+    return tokens_per_rank * world / (ms_step / 1000.0)
+
+
 # ---------------------------------------------------------------- our arm
 def standalone_movers(shape, L, inp, sp, hb):
     """GB/s of the ring gather run as its own kernel: moe_dispatch (MX(x), then
@@ -340,8 +361,7 @@ def run_ours(args, rank, world, local_rank):
         raise RuntimeError("device status %d at site %d after warm-up" % (code, site))
 
     def barrier():
-        if world > 1:
-            torch.distributed.barrier()
+        rank_barrier(world)
 
     # ---- timed region: K steps, inputs resident in HBM
     clocks = ClockSampler(local_rank)
@@ -361,13 +381,9 @@ def run_ours(args, rank, world, local_rank):
     kern = M.moe_profile_read()
     M.moe_profile_enable(False)
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), world, "cuda")
     ms_step = ms / args.steps
-    value = shape.T * world / (ms_step / 1000.0)
+    value = job_tokens_per_s(shape.T, world, ms_step)
 
     # ---- per-stage split (one extra, separately timed step)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
@@ -455,11 +471,7 @@ def run_ours(args, rank, world, local_rank):
     e2e_run(args.steps, e0)
     e1.record(stream)
     torch.cuda.synchronize()
-    ms_e2e = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms_e2e], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_e2e = float(t.item())
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, "cuda")
     code, site = L.status()
     if code:
         raise RuntimeError("device status %d at site %d" % (code, site))
@@ -552,7 +564,7 @@ def run_ours(args, rank, world, local_rank):
                        ring_laps="per-lap launches" if args.lap_launches else "one launch, mover warps"),
         "roofline": roof,
         "cpu_baseline": cpu,
-        "e2e": {"value": shape.T * world / (ms_e2e / 1000.0), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_tokens_per_s(shape.T, world, ms_e2e), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "clocks": clk,

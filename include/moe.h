@@ -64,7 +64,9 @@ enum {
  *   capacity: ring capacity per routed expert (rows); 0 = default
  *   ceil128(2*T*k/E). Constraints: d, I, capacity multiples of 128;
  *   E a multiple of n_groups with at least 2 experts per group when
- *   n_groups > 1; 1 <= k <= 8 and k <= E; E <= 512. */
+ *   n_groups > 1; 1 <= k <= 8 and k <= E; E <= 512. T = 0 is valid: every
+ *   call then succeeds, moe_backward writes zero weight gradients, and the
+ *   per-token arrays (x, topk_idx, topk_w, y, dy, dx) may be null. */
 typedef struct moe_config {
   int T, d, E, k, n_groups, topk_groups, I, n_shared;
   int capacity;

@@ -72,6 +72,9 @@ LapStreams* lap_streams() {
 
 int launch_status() { return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+// A per-token array (x, topk_idx, topk_w, y, dy, dx) may be null only when there are no tokens.
+inline bool tok_ok(const void* p, const moe_config_t* c) { return p != nullptr || c->T == 0; }
+
 // Counters of an all-laps ring launch, zeroed on the stream before it.
 RingMovers ring_movers(const Layout& L, void* ws, cudaStream_t s) {
   RingMovers mv{};
@@ -295,7 +298,8 @@ int moe_quantize_weights(const moe_config_t* cfg, const void* w_gu, const void* 
 int moe_route(const moe_config_t* cfg, const void* x, const void* w_router, const float* bias, int32_t* topk_idx,
               float* topk_w, void* ws, moe_stream_t stream) {
   if (int r = validate(cfg)) return r;
-  if (!x || !w_router || !bias || !topk_idx || !topk_w || !ws) return MOE_ERR_INVALID_ARG;
+  if (!tok_ok(x, cfg) || !w_router || !bias || !tok_ok(topk_idx, cfg) || !tok_ok(topk_w, cfg) || !ws)
+    return MOE_ERR_INVALID_ARG;
   if (!arch_ok()) return MOE_ERR_UNSUPPORTED_ARCH;
   const Layout L = make_layout(cfg);
   const Dims& m = L.m;
@@ -308,7 +312,7 @@ int moe_route(const moe_config_t* cfg, const void* x, const void* w_router, cons
 
 int moe_schedule(const moe_config_t* cfg, const int32_t* topk_idx, void* ws, moe_stream_t stream) {
   if (int r = validate(cfg)) return r;
-  if (!topk_idx || !ws) return MOE_ERR_INVALID_ARG;
+  if (!tok_ok(topk_idx, cfg) || !ws) return MOE_ERR_INVALID_ARG;
   if (!arch_ok()) return MOE_ERR_UNSUPPORTED_ARCH;
   const Layout L = make_layout(cfg);
   launch_schedule(L.m, topk_idx, L, ws, S(stream));
@@ -317,7 +321,7 @@ int moe_schedule(const moe_config_t* cfg, const int32_t* topk_idx, void* ws, moe
 
 int moe_dispatch(const moe_config_t* cfg, const void* x, void* ws, moe_stream_t stream) {
   if (int r = validate(cfg)) return r;
-  if (!x || !ws) return MOE_ERR_INVALID_ARG;
+  if (!tok_ok(x, cfg) || !ws) return MOE_ERR_INVALID_ARG;
   if (!arch_ok()) return MOE_ERR_UNSUPPORTED_ARCH;
   const Layout L = make_layout(cfg);
   const Dims& m = L.m;
@@ -337,7 +341,7 @@ int moe_dispatch(const moe_config_t* cfg, const void* x, void* ws, moe_stream_t 
 int moe_forward(const moe_config_t* cfg, const void* x, const void* wq, const float* topk_w, void* y, void* ws,
                 moe_stream_t stream) {
   if (int r = validate(cfg)) return r;
-  if (!x || !wq || !topk_w || !y || !ws) return MOE_ERR_INVALID_ARG;
+  if (!tok_ok(x, cfg) || !wq || !tok_ok(topk_w, cfg) || !tok_ok(y, cfg) || !ws) return MOE_ERR_INVALID_ARG;
   if (!arch_ok()) return MOE_ERR_UNSUPPORTED_ARCH;
   const Layout L = make_layout(cfg);
   const WLayout W = make_wlayout(cfg);
@@ -435,7 +439,8 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
                  const float* topk_w, const void* dy, const void* wq, void* dx, void* dw_router, void* dw_gu,
                  void* dw_d, void* dws_gu, void* dws_d, void* ws, moe_stream_t stream) {
   if (int r = validate(cfg)) return r;
-  if (!x || !w_router || !topk_idx || !topk_w || !dy || !wq || !dx || !dw_router || !dw_gu || !dw_d || !ws)
+  if (!tok_ok(x, cfg) || !w_router || !tok_ok(topk_idx, cfg) || !tok_ok(topk_w, cfg) || !tok_ok(dy, cfg) || !wq ||
+      !tok_ok(dx, cfg) || !dw_router || !dw_gu || !dw_d || !ws)
     return MOE_ERR_INVALID_ARG;
   if (cfg->n_shared > 0 && (!dws_gu || !dws_d)) return MOE_ERR_INVALID_ARG;
   if (!arch_ok()) return MOE_ERR_UNSUPPORTED_ARCH;

@@ -195,7 +195,9 @@ int route_scratch(float** out) {
 extern "C" int moe_route_noalloc(const moe_config_t* cfg, const void* x, const void* w_router, const float* bias,
                                  int32_t* topk_idx, float* topk_w, moe_stream_t stream) {
   if (int r = moe::validate(cfg)) return r;
-  if (!x || !w_router || !bias || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+  const bool no_tokens = cfg->T == 0;   // per-token arrays may be null then
+  if ((!x && !no_tokens) || !w_router || !bias || (!topk_idx && !no_tokens) || (!topk_w && !no_tokens))
+    return MOE_ERR_INVALID_ARG;
   if (static_cast<int64_t>(cfg->T) * cfg->E > moe::kRouteScratchFloats) return MOE_ERR_SCRATCH;
   if (!moe::arch_ok()) return MOE_ERR_UNSUPPORTED_ARCH;
   if (cfg->T == 0) return MOE_OK;

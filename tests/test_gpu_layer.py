@@ -464,3 +464,23 @@ def test_graph_replay_bitwise(run):
     assert L.status() == (0, 0)
     for a, b in zip(eager, outs):
         assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+
+
+@pytest.mark.parametrize("S", [0, 1])
+def test_no_tokens(S):
+    """T = 0: every call succeeds, nothing is routed, and every gradient is zero."""
+    _need_gpu()
+    from moe_layer_dsv3_gb300.layer import MoELayer
+    L = MoELayer(0, 256, 8, 2, 2, 1, 128, S, 128)
+    x = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    wr = torch.randn((8, 256), device="cuda").to(torch.bfloat16)
+    bias = torch.zeros(8, device="cuda")
+    for t in (L.dw_router, L.dw_gu, L.dw_d, L.dws_gu, L.dws_d):
+        t.view(torch.uint8).fill_(0xFF)
+    L.forward(x, wr, bias)
+    L.backward(torch.empty_like(x))
+    torch.cuda.synchronize()
+    assert L.status() == (0, 0)
+    assert not L.ws_tensor("COUNTS", torch.int32, (8 + S,)).any()
+    for t in (L.dw_router, L.dw_gu, L.dw_d) + ((L.dws_gu, L.dws_d) if S else ()):
+        assert not t.view(torch.int16).any()
