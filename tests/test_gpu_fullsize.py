@@ -312,15 +312,46 @@ def test_router_backward(full):
         assert rel_frob(_f64(full.L.dw_router[e]), ref) < TOL, e
 
 
+def _checksum(t):
+    """Position-weighted int64 checksum of a tensor's 16-bit words, a few experts at a time."""
+    total = 0
+    for c in t.view(torch.int16).split(8):
+        w = c.reshape(c.shape[0], -1).to(torch.int64)
+        total += int((w * torch.arange(1, w.shape[1] + 1, device=w.device) % 65521).sum().item())
+        total += int(w.sum().item())
+    return total
+
+
 def test_bitwise_rerun(full):
     L, i = full.L, full.inp
     before = [t.clone() for t in (L.y, L.dx, L.dw_router, L.topk_w)]
-    h_gu = torch.sum(L.dw_gu.view(torch.int16).to(torch.int64)).item()
-    h_d = torch.sum(L.dw_d.view(torch.int16).to(torch.int64)).item()
+    h_gu, h_d = _checksum(L.dw_gu), _checksum(L.dw_d)
     L.forward(i["x"], i["w_router"], i["bias"])
     L.backward(i["dy"])
     torch.cuda.synchronize()
     for a_, b_ in zip(before, (L.y, L.dx, L.dw_router, L.topk_w)):
         assert torch.equal(a_.view(torch.uint8), b_.view(torch.uint8))
-    assert torch.sum(L.dw_gu.view(torch.int16).to(torch.int64)).item() == h_gu
-    assert torch.sum(L.dw_d.view(torch.int16).to(torch.int64)).item() == h_d
+    assert _checksum(L.dw_gu) == h_gu
+    assert _checksum(L.dw_d) == h_d
+
+
+def test_lap_launch_form_bitwise(full):
+    """At full size, with ring wrap-around (17 laps at dsv3_zipf), the per-lap launch form
+    (MOE_FLAG_LAP_LAUNCHES: a mover launch and a GEMM launch per lap, laps on two streams)
+    gives the same bytes as the default all-laps launch with mover warps."""
+    if full.shape.name != "dsv3_zipf" and not (full.shape.name == "e384" and full.shape.T == 2368):
+        pytest.skip("the wrap-around workload and one wide one (a second layer at T=65536 does not fit beside this one)")
+    import moe_layer_dsv3_gb300 as M
+    from moe_layer_dsv3_gb300.layer import MoELayer
+    s, i = full.shape, full.inp
+    Lp = MoELayer.from_shape(s, flags=M.MOE_FLAG_LAP_LAUNCHES)
+    Lp.wq = full.L.wq
+    Lp.forward(i["x"], i["w_router"], i["bias"])
+    Lp.backward(i["dy"])
+    torch.cuda.synchronize()
+    assert Lp.status() == (0, 0)
+    L = full.L
+    for name in ("y", "dx", "dw_router", "dw_gu", "dw_d", "dws_gu", "dws_d"):
+        assert torch.equal(getattr(L, name).view(torch.int16), getattr(Lp, name).view(torch.int16)), name
+    del Lp
+    torch.cuda.empty_cache()
