@@ -449,10 +449,8 @@ def run_ours(args, rank, world, local_rank):
             stream.wait_event(loaded[b])
             if i >= 2:
                 stream.wait_event(drained[b])
-            L.forward(xd[b], wr, bias, sp)
-            L.backward(dyd[b], sp)
-            yd[b].copy_(L.y)
-            dxd[b].copy_(L.dx)
+            L.forward(xd[b], wr, bias, sp, y=yd[b])          # outputs go straight to this step's buffers
+            L.backward(dyd[b], sp, dx=dxd[b])
             done[b].record(stream)
             d2h_s.wait_event(done[b])
             with torch.cuda.stream(d2h_s):

@@ -68,23 +68,27 @@ class MoELayer:
         """MX(x) and the ring dispatch of every lap alone (moe_forward does this itself)."""
         moe_dispatch(self.cfg, x.data_ptr(), self.ws.data_ptr(), stream)
 
-    def forward_experts(self, x, stream=0):
-        moe_forward(self.cfg, x.data_ptr(), self.wq.data_ptr(), self.topk_w.data_ptr(), self.y.data_ptr(),
+    def forward_experts(self, x, stream=0, y=None):
+        y = self.y if y is None else y
+        moe_forward(self.cfg, x.data_ptr(), self.wq.data_ptr(), self.topk_w.data_ptr(), y.data_ptr(),
                     self.ws.data_ptr(), stream)
+        return y
 
-    def forward(self, x, w_router, bias, stream=0):
+    def forward(self, x, w_router, bias, stream=0, y=None):
+        """Route, schedule and run the experts; writes y (default: self.y) and returns it."""
         self._x, self._w_router = x, w_router
         self.route(x, w_router, bias, stream)
         self.schedule(stream)
-        self.forward_experts(x, stream)
-        return self.y
+        return self.forward_experts(x, stream, y)
 
-    def backward(self, dy, stream=0):
+    def backward(self, dy, stream=0, dx=None):
+        """Gradients of the last forward; writes dx (default: self.dx) and the weight gradients."""
+        dx = self.dx if dx is None else dx
         moe_backward(self.cfg, self._x.data_ptr(), self._w_router.data_ptr(), self.topk_idx.data_ptr(),
-                     self.topk_w.data_ptr(), dy.data_ptr(), self.wq.data_ptr(), self.dx.data_ptr(),
+                     self.topk_w.data_ptr(), dy.data_ptr(), self.wq.data_ptr(), dx.data_ptr(),
                      self.dw_router.data_ptr(), self.dw_gu.data_ptr(), self.dw_d.data_ptr(),
                      self.dws_gu.data_ptr(), self.dws_d.data_ptr(), self.ws.data_ptr(), stream)
-        return self.dx
+        return dx
 
     def capture_step(self, x, w_router, bias, dy):
         """Record one whole step (route, schedule, forward, backward) into a CUDA graph.
