@@ -159,7 +159,14 @@ MOE_API int moe_schedule(const moe_config_t* cfg, const int32_t* topk_idx, void*
  *   x [T][d] bf16, wq from moe_quantize_weights, topk_w [T][k] fp32 (from
  *   moe_route). y [T][d] bf16 = sum_j w[t,j] expert_{idx[t,j]}(x_t) +
  *   shared(x_t), each expert a SwiGLU FFN on MXFP8 operands. Saves what
- *   backward needs in ws. */
+ *   backward needs in ws.
+ * All pointers are device memory owned by the caller (the library allocates
+ * nothing); ws must hold the schedule of moe_schedule for the same topk_idx.
+ * Asynchronous on `stream`; the two ring GEMMs are cooperative launches, so
+ * they start once all their CTAs can be resident. Errors (returned before
+ * any launch): MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED_ARCH; MOE_ERR_CUDA
+ * for a launch failure. A bounded device wait that gives up is reported
+ * through moe_status (MOE_ERR_TIMEOUT), not by the return value. */
 MOE_API int moe_forward(const moe_config_t* cfg, const void* x, const void* wq, const float* topk_w, void* y, void* ws,
                 moe_stream_t stream);
 
@@ -183,7 +190,10 @@ MOE_API int moe_dispatch(const moe_config_t* cfg, const void* x, void* ws, moe_s
  *   x, w_router, topk_idx, topk_w: the forward inputs / router outputs.
  *   dy [T][d] bf16. Outputs (bf16): dx [T][d], dw_router [E][d],
  *   dw_gu [E][2I][d], dw_d [E][d][I], dws_gu [n_shared][2I][d],
- *   dws_d [n_shared][d][I]. The router bias receives no gradient. */
+ *   dws_d [n_shared][d][I]. The router bias receives no gradient.
+ * ws must be the workspace of the matching moe_forward (its saved g,u, MX(h)
+ * and schedule are read). Ownership, stream and error behaviour as for
+ * moe_forward; dws_gu / dws_d may be null when n_shared = 0. */
 MOE_API int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, const int32_t* topk_idx,
                  const float* topk_w, const void* dy, const void* wq, void* dx, void* dw_router, void* dw_gu,
                  void* dw_d, void* dws_gu, void* dws_d, void* ws, moe_stream_t stream);
