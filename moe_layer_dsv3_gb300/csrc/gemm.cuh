@@ -91,7 +91,9 @@ struct GemmCfg {
   static constexpr int kKElems = kBf16 ? 64 : 128;                  // K elements per stage
   static constexpr int kBarBytes = 256;
   static constexpr int kBase = base_mode(MODE);
-  static constexpr int kScratchBytes = kBase == kSwigluFwd ? 4 * 32 * 33 * 4 : 0;
+  // Per epilogue warp, 32 x 33 fp32: the SwiGLU forward's transpose tile, or
+  // the push epilogue's 32-row x 128-byte store-coalescing tile.
+  static constexpr int kScratchBytes = (kBase == kSwigluFwd || kBase == kPush) ? 4 * 32 * 33 * 4 : 0;
   static constexpr int kSmem = 1024 + kStages * kStageBytes + kOutBytes + kBarBytes + kScratchBytes;
   static_assert(kSmem <= 232448, "shared memory budget");
   static_assert(kSfCol0 + kStages * kSfCols <= 512, "TMEM budget");
@@ -541,11 +543,28 @@ __device__ __forceinline__ void gemm_epilogue_tile(const GemmParams& p, const Ti
     const int a = valid ? p.row_src[prow] : -1;
     uint32_t packed[BN / 2];
     drain_acc_bf16<BN>(tacc, true, packed, acce);
-    if (a >= 0) {
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(a) * p.ldo + t.n0);
+    // Each lane holds one row; rows go to scattered assignments. Per 64-column
+    // chunk the warp swaps the tile through shared memory so that each store
+    // instruction writes 4 rows x 128 contiguous bytes instead of 32 x 16.
+    uint8_t* buf = reinterpret_cast<uint8_t*>(scr);
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
 #pragma unroll
-      for (int i = 0; i < BN / 8; ++i)
-        dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+    for (int c = 0; c < BN / 64; ++c) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int w = (c * 8 + i) * 4;
+        *reinterpret_cast<uint4*>(buf + lane * 128 + ((i ^ (lane & 7)) << 4)) =
+            make_uint4(packed[w], packed[w + 1], packed[w + 2], packed[w + 3]);
+      }
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int r = 4 * j + (lane >> 3), ch = lane & 7;
+        const int ar = __shfl_sync(0xffffffffu, a, r);
+        const uint4 v = *reinterpret_cast<const uint4*>(buf + r * 128 + ((ch ^ (r & 7)) << 4));
+        if (ar >= 0) reinterpret_cast<uint4*>(out + static_cast<int64_t>(ar) * p.ldo + t.n0 + c * 64)[ch] = v;
+      }
+      __syncwarp();
     }
   } else if constexpr (MODE == kWgrad) {
     // bf16 tile -> shared staging (boxes of 128 rows x 64 columns, 128-byte
