@@ -92,8 +92,8 @@ struct GemmCfg {
   static constexpr int kBarBytes = 256;
   static constexpr int kBase = base_mode(MODE);
   // Per epilogue warp, 32 x 33 fp32: the SwiGLU forward's transpose tile, or
-  // the push epilogue's 32-row x 128-byte store-coalescing tile.
-  static constexpr int kScratchBytes = (kBase == kSwigluFwd || kBase == kPush) ? 4 * 32 * 33 * 4 : 0;
+  // the 32-row x 128-byte store-coalescing tile of the push and dh epilogues.
+  static constexpr int kScratchBytes = (kBase == kSwigluFwd || kBase == kPush || kBase == kSwigluBwd) ? 4 * 32 * 33 * 4 : 0;
   static constexpr int kSmem = 1024 + kStages * kStageBytes + kOutBytes + kBarBytes + kScratchBytes;
   static_assert(kSmem <= 232448, "shared memory budget");
   static_assert(kSfCol0 + kStages * kSfCols <= 512, "TMEM budget");
@@ -467,6 +467,25 @@ __device__ void ring_mover(const GemmParams& p, int wid, int lane) {
   }
 }
 
+// Stores 32 rows x 128 bytes that a warp holds one row per lane (8 uint4 in
+// v) so that each store instruction writes 4 whole 128-byte row segments
+// instead of 32 scattered 16-byte pieces: the rows pass through a swizzled
+// 4 KB shared tile. dst(r) gives row r's destination (null: skip the row).
+template <typename DstOf>
+__device__ __forceinline__ void warp_store_rows128(uint8_t* buf, int lane, const uint4* v, DstOf dst) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) *reinterpret_cast<uint4*>(buf + lane * 128 + ((i ^ (lane & 7)) << 4)) = v[i];
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int r = 4 * j + (lane >> 3), ch = lane & 7;
+    const uint4 val = *reinterpret_cast<const uint4*>(buf + r * 128 + ((ch ^ (r & 7)) << 4));
+    uint4* d = dst(r);
+    if (d != nullptr) d[ch] = val;
+  }
+  __syncwarp();
+}
+
 template <int BN, int MODE>
 __device__ __forceinline__ void gemm_epilogue_tile(const GemmParams& p, const TileInfo& t, uint32_t tacc, int q,
                                                    int lane, float* scr, uint8_t* out_smem, const CUtensorMap* tma_o,
@@ -512,7 +531,8 @@ __device__ __forceinline__ void gemm_epilogue_tile(const GemmParams& p, const Ti
   } else if constexpr (MODE == kSwigluBwd) {
     // dh (fp32) to the tile's padded rank rows; the SwiGLU backward and the
     // two MX quantisations of dGU run in their own kernel.
-    float* dst = static_cast<float*>(p.out) + (t.prow0 + row) * static_cast<int64_t>(p.ldo) + t.n0;
+    uint8_t* buf = reinterpret_cast<uint8_t*>(scr);
+    float* rows0 = static_cast<float*>(p.out) + (t.prow0 + q * 32) * static_cast<int64_t>(p.ldo) + t.n0;
 #pragma unroll
     for (int c = 0; c < BN / 32; c += 2) {
       uint32_t r0[32], r1[32];
@@ -528,15 +548,18 @@ __device__ __forceinline__ void gemm_epilogue_tile(const GemmParams& p, const Ti
         tc_fence_before();
         mbar_arrive(acce);
       }
-      float4* d0 = reinterpret_cast<float4*>(dst + c * 32);
-      float4* d1 = reinterpret_cast<float4*>(dst + (c + 1) * 32);
+      uint4 v0[8], v1[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        d0[i] = make_float4(__uint_as_float(r0[4 * i]), __uint_as_float(r0[4 * i + 1]), __uint_as_float(r0[4 * i + 2]),
-                            __uint_as_float(r0[4 * i + 3]));
-        d1[i] = make_float4(__uint_as_float(r1[4 * i]), __uint_as_float(r1[4 * i + 1]), __uint_as_float(r1[4 * i + 2]),
-                            __uint_as_float(r1[4 * i + 3]));
+        v0[i] = make_uint4(r0[4 * i], r0[4 * i + 1], r0[4 * i + 2], r0[4 * i + 3]);
+        v1[i] = make_uint4(r1[4 * i], r1[4 * i + 1], r1[4 * i + 2], r1[4 * i + 3]);
       }
+      warp_store_rows128(buf, lane, v0, [&](int r) {
+        return reinterpret_cast<uint4*>(rows0 + static_cast<int64_t>(r) * p.ldo + c * 32);
+      });
+      warp_store_rows128(buf, lane, v1, [&](int r) {
+        return reinterpret_cast<uint4*>(rows0 + static_cast<int64_t>(r) * p.ldo + (c + 1) * 32);
+      });
     }
   } else if constexpr (MODE == kPush) {
     const int64_t prow = t.prow0 + row;
@@ -550,21 +573,16 @@ __device__ __forceinline__ void gemm_epilogue_tile(const GemmParams& p, const Ti
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
 #pragma unroll
     for (int c = 0; c < BN / 64; ++c) {
+      uint4 v[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int w = (c * 8 + i) * 4;
-        *reinterpret_cast<uint4*>(buf + lane * 128 + ((i ^ (lane & 7)) << 4)) =
-            make_uint4(packed[w], packed[w + 1], packed[w + 2], packed[w + 3]);
+        v[i] = make_uint4(packed[w], packed[w + 1], packed[w + 2], packed[w + 3]);
       }
-      __syncwarp();
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int r = 4 * j + (lane >> 3), ch = lane & 7;
+      warp_store_rows128(buf, lane, v, [&](int r) {
         const int ar = __shfl_sync(0xffffffffu, a, r);
-        const uint4 v = *reinterpret_cast<const uint4*>(buf + r * 128 + ((ch ^ (r & 7)) << 4));
-        if (ar >= 0) reinterpret_cast<uint4*>(out + static_cast<int64_t>(ar) * p.ldo + t.n0 + c * 64)[ch] = v;
-      }
-      __syncwarp();
+        return ar >= 0 ? reinterpret_cast<uint4*>(out + static_cast<int64_t>(ar) * p.ldo + t.n0 + c * 64) : nullptr;
+      });
     }
   } else if constexpr (MODE == kWgrad) {
     // bf16 tile -> shared staging (boxes of 128 rows x 64 columns, 128-byte
