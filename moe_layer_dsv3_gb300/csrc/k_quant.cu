@@ -150,20 +150,23 @@ __global__ void __launch_bounds__(kTokThreads, 2) tok_gather_kernel(
 // SwiGLU backward of padded rank rows and the two MX forms of dGU = [dg | du]:
 // along 2I per row (q_rows, tiled scales) and along ranks per column (q_tok,
 // [2I][Rmax], tiled scales). Row pr is an assignment iff row_src[pr] >= 0;
-// other rows of an expert's padded segment give zeros. CTA: 32 rows x 128
-// columns of I, one warp per 32 columns; lane = row.
+// other rows of an expert's padded segment give zeros. CTA: 128 rows x 32
+// columns of I, warp q on rows 32q..32q+31 (lane = row). The token-axis
+// codes of the 4 warps meet in shared memory, so each column's 128 rows are
+// stored as one 128-byte run.
 //   sg = sigmoid(g), dg = dh u sg (1 + g (1 - sg)), du = dh g sg   (fp32)
 __global__ void __launch_bounds__(128) swiglu_bwd_quant_kernel(
     const float* __restrict__ dh, const __nv_bfloat16* __restrict__ gu, const int* __restrict__ row_src,
     const int* __restrict__ poff_end, int I, int64_t Rmax, uint8_t* __restrict__ q_rows,
     uint8_t* __restrict__ q_rows_sf, uint8_t* __restrict__ q_tok, uint8_t* __restrict__ q_tok_sf) {
   __shared__ float scr[4][32 * 33];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 32;
+  __shared__ __align__(16) uint8_t tst[2][32 * 128];   // [dg|du][column][128 rows], 16-byte chunks swizzled
+  __shared__ uint32_t tsf[2][32];                        // [dg|du][column]: 4 scale bytes (row blocks)
+  const int q = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128;
   if (r0 >= *poff_end) return;
-  const int c0 = (blockIdx.x * 4 + warp) * 32;
-  if (c0 >= I) return;
-  const int64_t prow = r0 + lane;
+  const int c0 = blockIdx.x * 32;
+  const int64_t prow = r0 + q * 32 + lane;
   const bool valid = row_src[prow] >= 0;
   float h[32];
   uint4 graw[4], uraw[4];
@@ -206,11 +209,41 @@ __global__ void __launch_bounds__(128) swiglu_bwd_quant_kernel(
   }
   const int ktl = 2 * I / 128;
   uint8_t* qr = q_rows + prow * (2 * I);
-  float* sw = scr[warp];
   emit_rowq(dg, qr + c0, q_rows_sf + sf_off(prow, c0 >> 5, ktl));
-  emit_tokq(dg, sw, lane, q_tok, q_tok_sf, Rmax, c0, r0);
   emit_rowq(g, qr + I + c0, q_rows_sf + sf_off(prow, (I + c0) >> 5, ktl));
-  emit_tokq(g, sw, lane, q_tok, q_tok_sf, Rmax, I + c0, r0);
+  // Token-axis codes: transpose this warp's 32 x 32 block (lane = column), quantise the column's 32 rows.
+  float* sw = scr[q];
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    const float* v = x == 0 ? dg : g;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) sw[lane * 33 + j] = v[j];
+    __syncwarp();
+    float cv[32];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) cv[r] = sw[r * 33 + lane];
+    __syncwarp();
+    const int b = mx_scale_byte(amax32(cv));
+    uint32_t w[8];
+    mx_pack32(cv, mx_inv_scale(b), w);
+    uint8_t* col_run = tst[x] + lane * 128;
+    *reinterpret_cast<uint4*>(col_run + (((2 * q) ^ (lane & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(col_run + (((2 * q + 1) ^ (lane & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+    reinterpret_cast<uint8_t*>(tsf[x])[lane * 4 + q] = static_cast<uint8_t>(b);
+  }
+  __syncthreads();
+  // 2 x 32 columns x 128 rows of codes: 8 threads per 128-byte column run.
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int idx = threadIdx.x + 128 * i;
+    const int x = idx >> 8, col = (idx >> 3) & 31, ch = idx & 7;
+    const uint4 v = *reinterpret_cast<const uint4*>(tst[x] + col * 128 + ((ch ^ (col & 7)) << 4));
+    *reinterpret_cast<uint4*>(q_tok + static_cast<int64_t>(x * I + c0 + col) * Rmax + r0 + ch * 16) = v;
+  }
+  if (threadIdx.x < 64) {
+    const int x = threadIdx.x >> 5, col = threadIdx.x & 31;
+    *reinterpret_cast<uint32_t*>(q_tok_sf + sf_off(x * I + c0 + col, r0 >> 5, Rmax >> 7)) = tsf[x][col];
+  }
 }
 
 __global__ void scales_to_tiled_kernel(const uint8_t* __restrict__ canon, int64_t rows, int nb, uint8_t* tiled) {
@@ -241,7 +274,7 @@ void launch_quant_cols(const void* src, int64_t rows, int K, int64_t ld, int64_t
 
 void launch_swiglu_bwd_quant(const Dims& m, const Layout& L, void* ws, cudaStream_t s) {
   if (m.Rmax == 0) return;
-  dim3 grid(static_cast<unsigned>(ceil_div(m.I, 128)), static_cast<unsigned>(m.Rmax / 32));
+  dim3 grid(static_cast<unsigned>(m.I / 32), static_cast<unsigned>(m.Rmax / 128));
   Prof prof("swiglu_bwd_quant", s);
   swiglu_bwd_quant_kernel<<<grid, 128, 0, s>>>(
       ws_ptr<float>(L, ws, MOE_WS_DH), ws_ptr<__nv_bfloat16>(L, ws, MOE_WS_GU), ws_ptr<int>(L, ws, MOE_WS_ROWSRC),
