@@ -72,43 +72,52 @@ __device__ __forceinline__ int token_of(int a, int T, int k) {
 // (shared-expert assignments have gate 1). Optionally also accumulates the
 // router weight-gradient partial sums part[pr/32][c] = sum_r dl_a x[t_a][c]
 // over the routed rows of the 32-row block, in rank order.
-// CTA: 32 rows x 1024 columns; each thread loads 8 bytes (4 columns) of each
-// of the 32 rows, then owns those 4 columns.
+// CTA: 128 rows x 128 columns, warp g on rows 32g..32g+31; lane l loads 8
+// bytes (columns 4l..4l+3) of each of its 32 rows and owns those 4 columns.
+// The 4 warps' codes meet in shared memory, so each column's 128 rows are
+// stored as one 128-byte run.
 constexpr int kTokCols = 4;
-constexpr int kTokThreads = 256;
+constexpr int kTokThreads = 128;
 
 __device__ __forceinline__ float bf16_lane(const uint2& u, int j) {
   const uint32_t w = j < 2 ? u.x : u.y;
   return (j & 1) ? __uint_as_float(w & 0xFFFF0000u) : __uint_as_float(w << 16);
 }
 
-__global__ void __launch_bounds__(kTokThreads, 2) tok_gather_kernel(
+template <bool kGate, bool kPart>
+__global__ void __launch_bounds__(kTokThreads, 4) tok_gather_kernel(
     const __nv_bfloat16* __restrict__ src, const int* __restrict__ row_src, const int* __restrict__ poff_end, int T,
-    int k, int d, int64_t Rmax, const float* __restrict__ topk_w, int scale_by_gate, const float* __restrict__ dl,
+    int k, int d, int64_t Rmax, const float* __restrict__ topk_w, const float* __restrict__ dl,
     float* __restrict__ part, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 32;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128;
   if (r0 >= *poff_end) return;
-  __shared__ int s_tok[32];
-  __shared__ float s_w[32];
-  __shared__ float s_dl[32];
-  if (threadIdx.x < 32) {
+  __shared__ int s_tok[128];
+  __shared__ float s_w[128];
+  __shared__ float s_dl[128];
+  __shared__ __align__(16) uint8_t st[128 * 128];   // [column][128 rows], 16-byte chunks swizzled
+  __shared__ uint32_t ssf[128];                      // [column]: scale bytes of the 4 row blocks
+  {
     const int a = row_src[r0 + threadIdx.x];
     float w = 1.0f, g = 0.0f;
     if (a >= 0 && a < T * k) {
-      if (scale_by_gate) w = topk_w[a];
-      if (dl != nullptr) g = dl[a];
+      if (kGate) w = topk_w[a];
+      if (kPart) g = dl[a];
     }
     s_tok[threadIdx.x] = a >= 0 ? token_of(a, T, k) : -1;
     s_w[threadIdx.x] = w;
     s_dl[threadIdx.x] = g;
   }
   __syncthreads();
-  const int c0 = (blockIdx.x * kTokThreads + threadIdx.x) * kTokCols;
-  if (c0 >= d) return;
+  const int q = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cb = blockIdx.x * 128;
+  const int c0 = cb + lane * kTokCols;
+  const int* tok = s_tok + 32 * q;
+  const float* wr = s_w + 32 * q;
+  const float* dr = s_dl + 32 * q;
   uint2 raw[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
-    const int t = s_tok[i];
+    const int t = tok[i];
     raw[i] = t >= 0 ? *reinterpret_cast<const uint2*>(src + static_cast<int64_t>(t) * d + c0) : make_uint2(0, 0);
   }
   float amax[kTokCols], acc[kTokCols];
@@ -119,8 +128,8 @@ __global__ void __launch_bounds__(kTokThreads, 2) tok_gather_kernel(
 #pragma unroll
     for (int j = 0; j < kTokCols; ++j) {
       float x = bf16_lane(raw[i], j);
-      acc[j] = fmaf(s_dl[i], x, acc[j]);
-      if (scale_by_gate) x = s_w[i] * x;
+      if (kPart) acc[j] = fmaf(dr[i], x, acc[j]);
+      if (kGate) x = wr[i] * x;
       amax[j] = fmaxf(amax[j], fabsf(x));
     }
   }
@@ -130,21 +139,34 @@ __global__ void __launch_bounds__(kTokThreads, 2) tok_gather_kernel(
     const float inv = mx_inv_scale(b);
     uint32_t w[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
+    for (int h = 0; h < 8; ++h) {
       float v4[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        float x = bf16_lane(raw[4 * q + u], j);
-        if (scale_by_gate) x = s_w[4 * q + u] * x;
+        float x = bf16_lane(raw[4 * h + u], j);
+        if (kGate) x = wr[4 * h + u] * x;
         v4[u] = x * inv;
       }
-      w[q] = e4m3x2(v4[0], v4[1]) | (e4m3x2(v4[2], v4[3]) << 16);
+      w[h] = e4m3x2(v4[0], v4[1]) | (e4m3x2(v4[2], v4[3]) << 16);
     }
-    store32(codes + static_cast<int64_t>(c0 + j) * Rmax + r0, w);
-    sf[sf_off(c0 + j, r0 / 32, Rmax / 128)] = static_cast<uint8_t>(b);
+    const int col = lane * kTokCols + j;
+    uint8_t* run = st + col * 128;
+    *reinterpret_cast<uint4*>(run + (((2 * q) ^ (lane & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(run + (((2 * q + 1) ^ (lane & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+    reinterpret_cast<uint8_t*>(ssf)[col * 4 + q] = static_cast<uint8_t>(b);
   }
-  if (part != nullptr)
-    *reinterpret_cast<float4*>(part + (r0 / 32) * d + c0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  if (kPart)
+    *reinterpret_cast<float4*>(part + (r0 / 32 + q) * d + c0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  __syncthreads();
+  // 128 columns x 128 rows of codes: 8 threads per 128-byte column run.
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int idx = threadIdx.x + kTokThreads * i;
+    const int col = idx >> 3, ch = idx & 7;
+    const uint4 v = *reinterpret_cast<const uint4*>(st + col * 128 + ((ch ^ ((col >> 2) & 7)) << 4));
+    *reinterpret_cast<uint4*>(codes + static_cast<int64_t>(cb + col) * Rmax + r0 + ch * 16) = v;
+  }
+  *reinterpret_cast<uint32_t*>(sf + sf_off(cb + threadIdx.x, r0 >> 5, Rmax >> 7)) = ssf[threadIdx.x];
 }
 
 // SwiGLU backward of padded rank rows and the two MX forms of dGU = [dg | du]:
@@ -286,13 +308,16 @@ void launch_swiglu_bwd_quant(const Dims& m, const Layout& L, void* ws, cudaStrea
 void launch_tok_gather(const Dims& m, const void* src_rows, bool scale_by_gate, const float* topk_w,
                        bool router_partials, const Layout& L, void* ws, uint8_t* codes, uint8_t* sf,
                        cudaStream_t s) {
-  dim3 grid(static_cast<unsigned>(ceil_div(m.d, kTokThreads * kTokCols)), static_cast<unsigned>(m.Rmax / 32));
+  dim3 grid(static_cast<unsigned>(m.d / 128), static_cast<unsigned>(m.Rmax / 128));
   const int* poff = ws_ptr<int>(L, ws, MOE_WS_POFF);
   Prof prof(scale_by_gate ? "tok_gather_dO" : "tok_gather_x", s);
-  tok_gather_kernel<<<grid, kTokThreads, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(src_rows), ws_ptr<int>(L, ws, MOE_WS_ROWSRC), poff + m.Ep, m.T, m.k, m.d,
-      m.Rmax, topk_w, scale_by_gate ? 1 : 0, router_partials ? ws_ptr<float>(L, ws, MOE_WS_DL) : nullptr,
-      router_partials ? ws_ptr<float>(L, ws, MOE_WS_DWR_PART) : nullptr, codes, sf);
+  const auto* sp = static_cast<const __nv_bfloat16*>(src_rows);
+  const int* rs = ws_ptr<int>(L, ws, MOE_WS_ROWSRC);
+  const float* dl = router_partials ? ws_ptr<float>(L, ws, MOE_WS_DL) : nullptr;
+  float* part = router_partials ? ws_ptr<float>(L, ws, MOE_WS_DWR_PART) : nullptr;
+  auto kern = scale_by_gate ? (router_partials ? tok_gather_kernel<true, true> : tok_gather_kernel<true, false>)
+                            : (router_partials ? tok_gather_kernel<false, true> : tok_gather_kernel<false, false>);
+  kern<<<grid, kTokThreads, 0, s>>>(sp, rs, poff + m.Ep, m.T, m.k, m.d, m.Rmax, topk_w, dl, part, codes, sf);
 }
 
 }  // namespace moe
