@@ -16,6 +16,7 @@ sample of the same workload on the host cores.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -71,11 +72,11 @@ def hbm_bytes(shape):
         "permute_lap": 2.0 * Rr * row_q,
         "combine": T * (k + S) * d * 2.0 + T * k * 4.0 + T * d * 2.0,
         "rev_combine_dw": T * k * d * 2.0 + T * d * 2.0 + T * k * 12.0,
-        "rev_combine_lap": Rr * d * 2.0 + Rr * row_q,
+        "permute_lap_dO": 2.0 * Rr * row_q,
         "reverse_dispatch": T * (k + S) * d * 2.0 + T * k * 12.0 + T * d * 2.0,
         "tok_gather_x": R * d * 2.0 + R * row_q,
         "tok_gather_dO": R * d * 2.0 + R * row_q,
-        "quant_rows": T * d * 2.0 * (1 + S) + T * row_q * (1 + S),
+        "quant_rows": 2 * (T * d * 2.0 + T * row_q),          # MX(x) forward, MX(dy) backward
         # dh fp32 and saved g|u bf16 in; dGU codes + scales out along 2I and along ranks
         "swiglu_bwd_quant": R * (shape.I * 4.0 + 2 * shape.I * 2.0 + 2 * (2 * shape.I + 2 * shape.I / 32.0)),
     }
@@ -240,7 +241,7 @@ def workload_config(shape, extra=None):
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    shape = gen.config(args.workload, T=args.T)
+    shape = _shape(args)
     inp = gen.make_inputs(shape, seed=0, device="cpu", weights=False)
     host = {
         "x": inp["x"].double().numpy(), "dy": inp["dy"].double().numpy(),
@@ -299,8 +300,9 @@ def standalone_movers(shape, L, inp, sp, hb):
     """GB/s of the ring gather run as its own kernel: moe_dispatch (MX(x), then
     one gather launch over all laps) timed alone after the timed region. In the
     default form the same moves run inside GEMM1's mover warps, overlapped
-    with the MMAs, and have no time of their own. The backward pull
-    (rev_combine_lap) is timed in one per-lap pass of a second layer."""
+    with the MMAs, and have no time of their own. The backward pull of the
+    MX(dy) rows into the dO ring (permute_lap_dO) is timed in one per-lap pass
+    of a second layer."""
     import moe_layer_dsv3_gb300 as M
     from moe_layer_dsv3_gb300.layer import MoELayer
     x, dy, wr, bias = inp["x"], inp["dy"], inp["w_router"], inp["bias"]
@@ -329,8 +331,8 @@ def standalone_movers(shape, L, inp, sp, hb):
     torch.cuda.synchronize()
     kern = M.moe_profile_read()
     M.moe_profile_enable(False)
-    if "rev_combine_lap" in kern and kern["rev_combine_lap"][1] > 0:
-        out["rev_combine_lap"] = hb["rev_combine_lap"] / (kern["rev_combine_lap"][1] / 1000.0) / 1e9
+    if "permute_lap_dO" in kern and kern["permute_lap_dO"][1] > 0:
+        out["permute_lap_dO"] = hb["permute_lap_dO"] / (kern["permute_lap_dO"][1] / 1000.0) / 1e9
     del Lp
     torch.cuda.empty_cache()
     return out
@@ -341,7 +343,7 @@ def run_ours(args, rank, world, local_rank):
     from moe_layer_dsv3_gb300.layer import MoELayer
 
     torch.cuda.set_device(local_rank)
-    shape = gen.config(args.workload, T=args.T)
+    shape = _shape(args)
     inp = gen.make_inputs(shape, seed=rank, device="cuda")
     L = MoELayer.from_shape(shape, flags=M.MOE_FLAG_LAP_LAUNCHES if args.lap_launches else 0)
     L.quantize_weights(inp["w_gu"], inp["w_d"], inp["ws_gu"], inp["ws_d"])
@@ -491,7 +493,7 @@ def run_ours(args, rank, world, local_rank):
     # Ring-lap kernels run on two streams and overlap one another, so their
     # event times are not additive; the dominant kernel is taken among the
     # kernels that run alone on the launch stream.
-    lap_kernels = {"gemm1_fwd", "gemm_dgrad_down", "permute_lap", "rev_combine_lap"} if args.lap_launches else set()
+    lap_kernels = {"gemm1_fwd", "gemm_dgrad_down", "permute_lap", "permute_lap_dO"} if args.lap_launches else set()
     dom = max(((n, v) for n, v in kern.items() if n not in lap_kernels), key=lambda kv: kv[1][1])[0]
     fp8_peak = 2.0 * pk["bf16_sus"]
     if dom in fl:
@@ -571,6 +573,15 @@ def run_ours(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def _shape(args):
+    shape = gen.config(args.workload, T=args.T)
+    if args.capacity is not None:
+        if args.capacity <= 0 or args.capacity % 128:
+            raise SystemExit("--capacity must be a positive multiple of 128")
+        shape = dataclasses.replace(shape, C=args.capacity)
+    return shape
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -579,6 +590,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="dsv3_zipf")
     ap.add_argument("--T", type=int, default=None)
+    ap.add_argument("--capacity", type=int, default=None,
+                    help="ring capacity per expert (multiple of 128) instead of the workload's")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
     ap.add_argument("--no-standalone-movers", action="store_true",

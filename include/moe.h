@@ -191,6 +191,10 @@ MOE_API int moe_dispatch(const moe_config_t* cfg, const void* x, void* ws, moe_s
  *   dy [T][d] bf16. Outputs (bf16): dx [T][d], dw_router [E][d],
  *   dw_gu [E][2I][d], dw_d [E][d][I], dws_gu [n_shared][2I][d],
  *   dws_d [n_shared][d][I]. The router bias receives no gradient.
+ * Rounding points of the expert dgrad: each token's dy is quantised once,
+ * MX along d; a routed row's gate w multiplies its down-projection gradient
+ * dh = w (MX(dy) . W_d) in fp32, the same quantity as (w dy) . W_d. The
+ * weight gradient of W_d quantises w dy along tokens.
  * ws must be the workspace of the matching moe_forward (its saved g,u, MX(h)
  * and schedule are read). Ownership, stream and error behaviour as for
  * moe_forward; dws_gu / dws_d may be null when n_shared = 0. */
@@ -231,9 +235,9 @@ enum {
   MOE_WS_O,            /* bf16[T*(k+S)][d]  expert outputs per assignment */
   MOE_WS_DW,           /* fp32[T][k]        gate gradients */
   MOE_WS_DL,           /* fp32[T][k]        router logit gradients */
-  MOE_WS_RING_DO,      /* u8[2][E][C][d]    two ring buffers of MX(w dy) (reverse-combine), as RING_X */
+  MOE_WS_RING_DO,      /* u8[2][E][C][d]    two ring buffers of the MX(dy) rows (reverse-combine), as RING_X */
   MOE_WS_RING_DO_SF,
-  MOE_WS_DOS,          /* u8[Tpad][d]       MX(dy) along d (shared expert) */
+  MOE_WS_DOS,          /* u8[Tpad][d]       MX(dy) along d: the dO ring source and the shared expert A */
   MOE_WS_DOS_SF,
   MOE_WS_DOTOK,        /* u8[d][Rmax]       MX(w dy) along tokens */
   MOE_WS_DOTOK_SF,

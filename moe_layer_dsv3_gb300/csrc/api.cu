@@ -408,7 +408,7 @@ int moe_forward(const moe_config_t* cfg, const void* x, const void* wq, const fl
       cudaStream_t cs = rbuf ? ls->aux[rbuf - 1] : s;
       op1.a = ring + rbuf * rb;
       op1.a_sf = ring_sf + rbuf * rb / 32;
-      launch_permute_lap(m, lap, L, ws, cs);
+      launch_permute_lap(m, lap, false, L, ws, cs);
       rc = gemm_dispatch("gemm1_fwd", kSwigluFwd, m, lap, 2 * m.I, m.d, 0, op1, ep1, counts, poff, lap_tiles, row_src,
                          status, cs);
     }
@@ -467,16 +467,16 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
   }
   // Reverse-combine: gate gradients, router logit gradients.
   launch_rev_combine_dw(m, dy, topk_w, L, ws, s);
-  // Shared-expert dgrad input MX(dy) along d (token order; rows past T zero).
+  // MX(dy) along d, once per token (token order; rows past T zero): the rows
+  // the dO ring is filled from, and the shared expert's dgrad input in place.
+  // The gate of a routed row scales its dh in the dgrad-down epilogue.
   uint8_t* dos = ws_ptr<uint8_t>(L, ws, MOE_WS_DOS);
   uint8_t* dos_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_DOS_SF);
-  if (m.S) {
-    if (m.Tpad > m.T) {
-      cudaMemsetAsync(dos + m.T * m.d, 0, (m.Tpad - m.T) * m.d, s);
-      cudaMemsetAsync(dos_sf + (m.T / 128) * 128 * (m.d / 32), 0, (m.Tpad - m.T / 128 * 128) * (m.d / 32), s);
-    }
-    launch_quant_rows(dy, m.T, m.d, m.d, dos, dos_sf, true, 0, s);
+  if (m.Tpad > m.T) {
+    cudaMemsetAsync(dos + m.T * m.d, 0, (m.Tpad - m.T) * m.d, s);
+    cudaMemsetAsync(dos_sf + (m.T / 128) * 128 * (m.d / 32), 0, (m.Tpad - m.T / 128 * 128) * (m.d / 32), s);
   }
+  launch_quant_rows(dy, m.T, m.d, m.d, dos, dos_sf, true, 0, s);
   // Token-axis operands of the weight gradients (and router dW partial sums).
   launch_tok_gather(m, x, false, topk_w, true, L, ws, ws_ptr<uint8_t>(L, ws, MOE_WS_XTOK),
                     ws_ptr<uint8_t>(L, ws, MOE_WS_XTOK_SF), s);
@@ -497,11 +497,12 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
   opb2.b_sf = wq_ptr<uint8_t>(W, wqm, MOE_WQ_W2B_SF);
   GemmEpilogue epb2{};
   epb2.out = ws_ptr<void>(L, ws, MOE_WS_DH);
+  epb2.gate = topk_w;
   epb2.ldo = m.I;
   if (!(cfg->flags & MOE_FLAG_LAP_LAUNCHES)) {
     RingMovers mv = ring_movers(L, ws, s);
-    mv.dy = dy;
-    mv.topk_w = topk_w;
+    mv.xq = dos;
+    mv.xq_sf = dos_sf;
     mv.ring = ws_ptr<uint8_t>(L, ws, MOE_WS_RING_DO);
     mv.ring_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_RING_DO_SF);
     opb2.a_rows = static_cast<int64_t>(kRingBufs) * m.E * m.C;
@@ -523,7 +524,7 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
       cudaStream_t cs = rbuf ? ls->aux[rbuf - 1] : s;
       opb2.a = ring + rbuf * rb;
       opb2.a_sf = ring_sf + rbuf * rb / 32;
-      launch_rev_combine_lap(m, lap, dy, topk_w, L, ws, cs);
+      launch_permute_lap(m, lap, true, L, ws, cs);
       rc = gemm_dispatch("gemm_dgrad_down", kSwigluBwd, m, lap, m.I, m.d, 0, opb2, epb2, counts, poff, lap_tiles,
                          row_src, status, cs, 256);
     }

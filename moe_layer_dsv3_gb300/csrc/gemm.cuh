@@ -60,12 +60,12 @@ struct GemmParams {
   uint8_t* q_rows; uint8_t* q_rows_sf; int q_rows_ktiles;
   uint8_t* q_tok; uint8_t* q_tok_sf; int64_t q_tok_pitch;
   __nv_bfloat16* gu; int I;
+  const float* gate;
   int* status;
   // all-laps ring modes
   const int* lapbase; int Lb; int d;
   int* moved; int* consumed;
   const uint8_t* mv_xq; const uint8_t* mv_xq_sf;
-  const __nv_bfloat16* mv_dy; const float* mv_w;
   uint8_t* ring; uint8_t* ring_sf;
 };
 
@@ -324,14 +324,13 @@ __device__ __forceinline__ void publish_move(int* ctr, int lane) {
   if (lane == 0) red_release_add(ctr, 1);
 }
 
-// Forward: ring row <- MX(x) row of its token, codes and tiled scales. The
-// item's 16-byte chunks are walked flat (consecutive lanes, consecutive
+// Ring row <- the MX row of its token (x in the forward, dy in the backward),
+// codes and tiled scales. The item's 16-byte chunks are walked flat (consecutive lanes, consecutive
 // chunks) in rounds of kFwdU chunks a lane; the next round's loads are issued
 // before this round's stores, so two rounds are in flight.
 constexpr int kFwdU = 8;
-constexpr int kBwdU = 4;
 
-__device__ __forceinline__ void move_rows_fwd(const GemmParams& p, int lane, int a_lane, int64_t ring_row0) {
+__device__ __forceinline__ void move_rows(const GemmParams& p, int lane, int a_lane, int64_t ring_row0) {
   const int d = p.d;
   const int chunks = d >> 4;
   const int total = kMoveRows * chunks;
@@ -379,59 +378,6 @@ __device__ __forceinline__ void move_rows_fwd(const GemmParams& p, int lane, int
   }
 }
 
-// Backward: ring row <- MX(fp32(w_a * dy[t_a])) along d (the reverse-combine
-// pull). Flat walk over the item's 32-element blocks, kBwdU blocks a lane per
-// round, next round's loads in flight while this round is quantised.
-__device__ __forceinline__ void move_rows_bwd(const GemmParams& p, int lane, int a_lane, int64_t ring_row0) {
-  const int d = p.d;
-  const int nb = d >> 5, ktiles = d >> 7;
-  const int total = kMoveRows * nb;
-  const int rounds = (total + 32 * kBwdU - 1) / (32 * kBwdU);
-  const int tok_l = a_lane >= 0 ? a_lane / p.k : -1;
-  const float w_l = a_lane >= 0 ? p.mv_w[a_lane] : 0.0f;
-  const uint4 zero = make_uint4(0, 0, 0, 0);
-  uint4 nxt[kBwdU][4];
-  auto load = [&](int rd, uint4 (*v)[4]) {
-#pragma unroll
-    for (int u = 0; u < kBwdU; ++u) {
-      const int f = (rd * kBwdU + u) * 32 + lane;
-      const int r = f / nb, kb = f - (f / nb) * nb;
-      const int t = __shfl_sync(0xffffffffu, tok_l, r < kMoveRows ? r : kMoveRows - 1);
-      const uint4* src = reinterpret_cast<const uint4*>(p.mv_dy + static_cast<int64_t>(t < 0 ? 0 : t) * d + kb * 32);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) v[u][i] = (f < total && t >= 0) ? __ldg(src + i) : zero;
-    }
-  };
-  load(0, nxt);
-  for (int rd = 0; rd < rounds; ++rd) {
-    uint4 cur[kBwdU][4];
-#pragma unroll
-    for (int u = 0; u < kBwdU; ++u)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) cur[u][i] = nxt[u][i];
-    if (rd + 1 < rounds) load(rd + 1, nxt);
-#pragma unroll
-    for (int u = 0; u < kBwdU; ++u) {
-      const int f = (rd * kBwdU + u) * 32 + lane;
-      const int r = f / nb, kb = f - (f / nb) * nb;
-      const int rc = r < kMoveRows ? r : kMoveRows - 1;
-      const int t = __shfl_sync(0xffffffffu, tok_l, rc);
-      const float w = __shfl_sync(0xffffffffu, w_l, rc);
-      if (f < total) {
-        float v[32];
-        unpack_bf16x32(cur[u], v);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = t >= 0 ? __fmul_rn(w, v[j]) : 0.0f;
-        const int b = mx_scale_byte(amax32(v));
-        uint32_t q[8];
-        mx_pack32(v, mx_inv_scale(b), q);
-        store32(p.ring + (ring_row0 + r) * d + kb * 32, q);
-        p.ring_sf[sf_tiled_offset(ring_row0 + r, kb, ktiles)] = static_cast<uint8_t>(b);
-      }
-    }
-  }
-}
-
 // Mover warp `wid` of this CTA: items j = blockIdx.x * kMoverWarps + wid,
 // then every gridDim.x * kMoverWarps, i.e. in increasing (lap-major) order.
 template <int BN, int MODE>
@@ -461,8 +407,7 @@ __device__ void ring_mover(const GemmParams& p, int wid, int lane) {
     const int64_t ring_row0 = (static_cast<int64_t>(L % kRingBufs) * p.E + e) * p.C + mt * 128 + part * kMoveRows;
     const int cnt = p.counts[e];
     const int a = (lane < kMoveRows && rank0 + lane < cnt) ? p.row_src[p.poff[e] + rank0 + lane] : -1;
-    if constexpr (base_mode(MODE) == kSwigluFwd) move_rows_fwd(p, lane, a, ring_row0);
-    else move_rows_bwd(p, lane, a, ring_row0);
+    move_rows(p, lane, a, ring_row0);
     publish_move(p.moved + gm, lane);
   }
 }
@@ -529,10 +474,13 @@ __device__ __forceinline__ void gemm_epilogue_tile(const GemmParams& p, const Ti
       emit_tokq(&h[c * 32], scr, lane, p.q_tok, p.q_tok_sf, p.q_tok_pitch, icol, t.prow0 + q * 32);
     }
   } else if constexpr (MODE == kSwigluBwd) {
-    // dh (fp32) to the tile's padded rank rows; the SwiGLU backward and the
-    // two MX quantisations of dGU run in their own kernel.
+    // dh (fp32) to the tile's padded rank rows, each routed row times its
+    // assignment's gate (the A rows are the token's MX(dy); the gate is a
+    // per-row scalar of the down projection's gradient). The SwiGLU backward
+    // and the two MX quantisations of dGU run in their own kernel.
     uint8_t* buf = reinterpret_cast<uint8_t*>(scr);
     float* rows0 = static_cast<float*>(p.out) + (t.prow0 + q * 32) * static_cast<int64_t>(p.ldo) + t.n0;
+    const float gw = (valid && t.e < p.E) ? p.gate[p.row_src[t.prow0 + row]] : 1.0f;
 #pragma unroll
     for (int c = 0; c < BN / 32; c += 2) {
       uint32_t r0[32], r1[32];
@@ -543,6 +491,8 @@ __device__ __forceinline__ void gemm_epilogue_tile(const GemmParams& p, const Ti
       for (int j = 0; j < 32; ++j) {
         reg_fence(r0[j]);
         reg_fence(r1[j]);
+        r0[j] = __float_as_uint(__fmul_rn(__uint_as_float(r0[j]), gw));
+        r1[j] = __float_as_uint(__fmul_rn(__uint_as_float(r1[j]), gw));
       }
       if (c + 2 == BN / 32) {   // whole accumulator row read: hand TMEM back
         tc_fence_before();

@@ -167,6 +167,7 @@ int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int
   p.q_tok_sf = ep.q_tok_sf;
   p.q_tok_pitch = ep.q_tok_pitch;
   p.gu = static_cast<__nv_bfloat16*>(ep.gu);
+  p.gate = ep.gate;
   p.I = m.I;
   p.status = status;
   if (mv != nullptr) {
@@ -177,8 +178,6 @@ int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int
     p.consumed = mv->consumed;
     p.mv_xq = mv->xq;
     p.mv_xq_sf = mv->xq_sf;
-    p.mv_dy = static_cast<const __nv_bfloat16*>(mv->dy);
-    p.mv_w = mv->topk_w;
     p.ring = mv->ring;
     p.ring_sf = mv->ring_sf;
   }

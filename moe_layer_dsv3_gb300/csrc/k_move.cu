@@ -69,7 +69,8 @@ __device__ __forceinline__ bool lap_row(const int* lap_tiles, const int* counts,
   return true;
 }
 
-// ring[e*C + slot] <- x_q[t] (codes and scales) for the rows of lap L.
+// ring[e*C + slot] <- the MX row of token t (codes and scales) for the rows of lap L:
+// x_q into the x ring in the forward, MX(dy) into the dO ring in the backward.
 __global__ void __launch_bounds__(256) permute_lap_kernel(
     const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xq_sf, const int* __restrict__ lap_tiles,
     const int* __restrict__ counts, const int* __restrict__ poff, const int* __restrict__ row_src, int T, int k,
@@ -88,38 +89,6 @@ __global__ void __launch_bounds__(256) permute_lap_kernel(
     for (int kt = lane; kt < ktiles; kt += 32) {
       const uint32_t v = t >= 0 ? *reinterpret_cast<const uint32_t*>(xq_sf + sf_off(t, kt * 4, ktiles)) : 0u;
       *reinterpret_cast<uint32_t*>(ring_sf + sf_off(row, kt * 4, ktiles)) = v;
-    }
-  }
-}
-
-// ring_dO[e*C + slot] <- MX(fp32(w_a * dy[t])) along d for the rows of lap L.
-__global__ void __launch_bounds__(256) rev_combine_lap_kernel(
-    const __nv_bfloat16* __restrict__ dy, const float* __restrict__ topk_w, const int* __restrict__ lap_tiles,
-    const int* __restrict__ counts, const int* __restrict__ poff, const int* __restrict__ row_src, int T, int k,
-    int d, int E, int Ep, int C, int L, uint8_t* __restrict__ ring, uint8_t* __restrict__ ring_sf) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_groups = lap_tiles[static_cast<int64_t>(L) * (Ep + 1) + E] * 16;
-  const int nb = d / 32, ktiles = d / 128;
-  for (int gid = blockIdx.x; gid < n_groups; gid += gridDim.x) {
-    int64_t row;
-    int t, a;
-    if (!lap_row(lap_tiles, counts, poff, row_src, T, k, E, Ep, C, L, gid, warp, row, t, a)) continue;
-    const float w = t >= 0 ? topk_w[a] : 0.0f;
-    for (int kb = lane; kb < nb; kb += 32) {
-      float v[32];
-      if (t >= 0) {
-        load_bf16x32(dy + static_cast<int64_t>(t) * d + kb * 32, v);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(w, v[j]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = 0.0f;
-      }
-      const int b = mx_scale_byte(amax32(v));
-      uint32_t wq[8];
-      mx_pack32(v, mx_inv_scale(b), wq);
-      store32(ring + row * d + kb * 32, wq);
-      ring_sf[sf_off(row, kb, ktiles)] = static_cast<uint8_t>(b);
     }
   }
 }
@@ -377,27 +346,16 @@ void launch_dispatch_all(const Dims& m, const Layout& L, void* ws, cudaStream_t 
       m.d, m.E, m.Ep, m.C, ws_ptr<uint8_t>(L, ws, MOE_WS_RING_X), ws_ptr<uint8_t>(L, ws, MOE_WS_RING_X_SF));
 }
 
-void launch_permute_lap(const Dims& m, int lap, const Layout& L, void* ws, cudaStream_t s) {
+void launch_permute_lap(const Dims& m, int lap, bool dO, const Layout& L, void* ws, cudaStream_t s) {
   const int blocks = lap_blocks(m);
   if (blocks == 0) return;
-  Prof prof("permute_lap", s);
+  Prof prof(dO ? "permute_lap_dO" : "permute_lap", s);
   permute_lap_kernel<<<blocks, 256, 0, s>>>(
-      ws_ptr<uint8_t>(L, ws, MOE_WS_XQ), ws_ptr<uint8_t>(L, ws, MOE_WS_XQ_SF), ws_ptr<int>(L, ws, MOE_WS_LAPTILES),
-      ws_ptr<int>(L, ws, MOE_WS_COUNTS), ws_ptr<int>(L, ws, MOE_WS_POFF), ws_ptr<int>(L, ws, MOE_WS_ROWSRC), m.T, m.k,
-      m.d, m.E, m.Ep, m.C, lap, ws_ptr<uint8_t>(L, ws, MOE_WS_RING_X) + (lap % kRingBufs) * ring_bytes(m),
-      ws_ptr<uint8_t>(L, ws, MOE_WS_RING_X_SF) + (lap % kRingBufs) * ring_bytes(m) / 32);
-}
-
-void launch_rev_combine_lap(const Dims& m, int lap, const void* dy, const float* topk_w, const Layout& L, void* ws,
-                            cudaStream_t s) {
-  const int blocks = lap_blocks(m);
-  if (blocks == 0) return;
-  Prof prof("rev_combine_lap", s);
-  rev_combine_lap_kernel<<<blocks, 256, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(dy), topk_w, ws_ptr<int>(L, ws, MOE_WS_LAPTILES),
-      ws_ptr<int>(L, ws, MOE_WS_COUNTS), ws_ptr<int>(L, ws, MOE_WS_POFF), ws_ptr<int>(L, ws, MOE_WS_ROWSRC), m.T, m.k,
-      m.d, m.E, m.Ep, m.C, lap, ws_ptr<uint8_t>(L, ws, MOE_WS_RING_DO) + (lap % kRingBufs) * ring_bytes(m),
-      ws_ptr<uint8_t>(L, ws, MOE_WS_RING_DO_SF) + (lap % kRingBufs) * ring_bytes(m) / 32);
+      ws_ptr<uint8_t>(L, ws, dO ? MOE_WS_DOS : MOE_WS_XQ), ws_ptr<uint8_t>(L, ws, dO ? MOE_WS_DOS_SF : MOE_WS_XQ_SF),
+      ws_ptr<int>(L, ws, MOE_WS_LAPTILES), ws_ptr<int>(L, ws, MOE_WS_COUNTS), ws_ptr<int>(L, ws, MOE_WS_POFF),
+      ws_ptr<int>(L, ws, MOE_WS_ROWSRC), m.T, m.k, m.d, m.E, m.Ep, m.C, lap,
+      ws_ptr<uint8_t>(L, ws, dO ? MOE_WS_RING_DO : MOE_WS_RING_X) + (lap % kRingBufs) * ring_bytes(m),
+      ws_ptr<uint8_t>(L, ws, dO ? MOE_WS_RING_DO_SF : MOE_WS_RING_X_SF) + (lap % kRingBufs) * ring_bytes(m) / 32);
 }
 
 void launch_combine(const Dims& m, const float* topk_w, const Layout& L, void* ws, void* y, cudaStream_t s) {

@@ -95,14 +95,12 @@ void launch_router_topk(const Dims& m, const float* logits, const float* bias, i
 void launch_schedule(const Dims& m, const int32_t* idx, const Layout& L, void* ws, cudaStream_t s);
 
 // ---------------------------------------------------------------- data movement
-void launch_permute_lap(const Dims& m, int lap, const Layout& L, void* ws, cudaStream_t s);
+void launch_permute_lap(const Dims& m, int lap, bool dO, const Layout& L, void* ws, cudaStream_t s);
 // Every lap of the ring dispatch in one launch (same writes, same per-slot lap order).
 void launch_dispatch_all(const Dims& m, const Layout& L, void* ws, cudaStream_t s);
 void launch_combine(const Dims& m, const float* topk_w, const Layout& L, void* ws, void* y, cudaStream_t s);
 void launch_rev_combine_dw(const Dims& m, const void* dy, const float* topk_w, const Layout& L, void* ws,
                            cudaStream_t s);
-void launch_rev_combine_lap(const Dims& m, int lap, const void* dy, const float* topk_w, const Layout& L,
-                            void* ws, cudaStream_t s);
 // SwiGLU backward of the padded rank rows and MX of dGU = [dg | du] two ways
 // (along 2I per row, and along ranks per column).
 void launch_swiglu_bwd_quant(const Dims& m, const Layout& L, void* ws, cudaStream_t s);
@@ -130,8 +128,7 @@ struct RingMovers {
   const int* lapbase;            // [Lb+1] first global m-tile of each lap
   int* moved;                    // per global m-tile: 8-row groups written (target 16)
   int* consumed;                 // per global m-tile: GEMM tiles whose A loads landed (target N / BN)
-  const uint8_t* xq; const uint8_t* xq_sf;   // forward: MX(x) rows along d, tiled scales
-  const void* dy; const float* topk_w;       // backward: bf16 dy rows and the gates
+  const uint8_t* xq; const uint8_t* xq_sf;   // MX rows along d (x forward, dy backward), tiled scales
   uint8_t* ring; uint8_t* ring_sf;           // [kRingBufs][E][C] rows, tiled scales
 };
 
@@ -147,6 +144,7 @@ struct GemmEpilogue {
   uint8_t* q_rows; uint8_t* q_rows_sf; int q_rows_ktiles;     // MX along the N axis
   uint8_t* q_tok;  uint8_t* q_tok_sf;  int64_t q_tok_pitch;   // MX along tokens (transposed)
   void* gu;             // saved bf16 g|u rows
+  const float* gate;    // dh epilogue: per-assignment gate that scales each routed row
   int ldo;              // output row pitch (elements)
 };
 

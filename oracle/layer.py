@@ -20,8 +20,12 @@ Forward, per assignment a = (t, j) routed to expert e = idx[t, j]:
 
 Backward with upstream gradient dy:
   dw[t,j]  = <dy[t], O[t,j]>                        (fp32 result)
-  dO[a]    = fp32(w[t,j] * dy[t]) ; MX along d and along tokens
-  dh       = dO_q . W_d[e]   (W_d MX along d)
+  dy_q     = MX(dy[t]) along d                      (once per token)
+  dh       = w[t,j] * (dy_q . W_d[e])   (W_d MX along d; the gate is a per-row
+             scalar of the gradient of O[t,j], so it is applied to dh rather
+             than quantised into k copies of dy; the write-ups leave the
+             rounding point open)
+  dO[a]    = fp32(w[t,j] * dy[t]) ; MX along tokens (for dW_d)
   dg       = dh * u * sig(g) * (1 + g (1 - sig(g))),  du = dh * silu(g)
              (g, u the saved bf16 values)
   dGU      = fp32([dg | du]) ; MX along 2I and along tokens
@@ -129,9 +133,14 @@ def swiglu_bwd(dh, g, u):
     return np.concatenate([dg, du], axis=1)
 
 
-def expert_backward(dOv, gu_saved, W: ExpertWeights, exact: bool = False) -> dict:
-    """dgrad part of one expert: dO values [n, d] -> dh, dGU, dX."""
+def expert_backward(dOv, gu_saved, W: ExpertWeights, exact: bool = False, row_gate=None) -> dict:
+    """dgrad part of one expert: dO values [n, d] -> dh, dGU, dX.
+
+    ``row_gate`` [n], when given, multiplies each row of dh (the routed rows'
+    gates; ``dOv`` then holds the token's dy rather than w * dy)."""
     dh = dOv @ W.d_bwd.val.T                         # [n, I]
+    if row_gate is not None:
+        dh = dh * np.asarray(row_gate, dtype=np.float64)[:, None]
     I = W.I
     dgu = swiglu_bwd(dh, gu_saved[:, :I], gu_saved[:, I:])
     if not exact:
@@ -223,6 +232,8 @@ def layer_backward(fwd: dict, inp: dict, shape, exact: bool = False) -> dict:
     else:
         dO = (np.asarray(w, dtype=np.float32)[:, :, None] * dy.astype(np.float32)[:, None, :]).astype(np.float64)
     dO = dO.reshape(T * k, d)
+    gates = (np.asarray(w, dtype=np.float64) if exact else
+             np.asarray(w, dtype=np.float32).astype(np.float64)).reshape(T * k)
     DX = np.zeros((T * k, d))
     dW_gu = np.zeros((E, 2 * I, d))
     dW_d = np.zeros((E, d, I))
@@ -231,8 +242,8 @@ def layer_backward(fwd: dict, inp: dict, shape, exact: bool = False) -> dict:
         a = expert_rows(sch, e)
         W = fwd["weights"][e]
         r = fwd["experts"][e]
-        dOq = Q(dO[a], 1, exact)
-        b = expert_backward(dOq.val, r["gu_saved"], W, exact)
+        dOq = Q(dy[a // k], 1, exact)               # the tokens' MX(dy) rows
+        b = expert_backward(dOq.val, r["gu_saved"], W, exact, row_gate=gates[a])
         DX[a] = b["dx"]
         dO_tok = tokq(dO[a], exact)
         h_tok = tokq(r["h"], exact)

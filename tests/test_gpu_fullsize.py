@@ -216,12 +216,11 @@ def test_expert_stages(full):
         # GEMM2 on the GPU's MX h
         O = _f64(full.ws("O", torch.bfloat16, (full.Ap, d))[torch.as_tensor(a[sel], device="cuda")])
         assert rel_frob(O, OL.expert_gemm2(hq, W)) < TOL, e
-        # backward: dO = fp32(w * dy), dgrad-down + SwiGLU bwd on the GPU's saved g,u, dgrad gate/up
+        # backward: MX(dy) rows, dh scaled by the gate, SwiGLU bwd on the GPU's saved g,u, dgrad gate/up
         wa = np.where(a[sel] < full.A, topk_w[np.minimum(a[sel], full.A - 1)], 1.0).astype(np.float32)
-        dyr = dy[torch.as_tensor(tok, device="cuda")].float().cpu().numpy()
-        dO = (wa[:, None] * dyr).astype(np.float64)
-        dOq = OL.Q(dO, 1, False)
-        rb = OL.expert_backward(dOq.val, gu, W)
+        dyr = dy[torch.as_tensor(tok, device="cuda")].float().cpu().numpy().astype(np.float64)
+        dOq = OL.Q(dyr, 1, False)
+        rb = OL.expert_backward(dOq.val, gu, W, row_gate=wa)
         dgu = mxfp8.dequantize(full.rows_u8("DGU", full.Rmax, 2 * I, prow),
                                full.rows_sf("DGU_SF", full.Rmax, 2 * I, prow), 1)
         assert rel_frob(dgu, mxfp8.roundtrip(rb["dgu"], 1)) < TOL, e

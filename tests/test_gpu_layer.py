@@ -270,7 +270,7 @@ def test_reverse_combine(run):
     dw = run.ws("DW", torch.float32, (m.T, m.k)).cpu().numpy()
     ref = np.einsum("tc,tjc->tj", dy, O[:run.A].reshape(m.T, m.k, m.d))
     assert rel_frob(dw, ref) < 1e-6
-    # dO = fp32(w * dy): token-axis bytes bit-exact
+    # dO = fp32(w * dy) along tokens: bytes bit-exact
     dtok = run.u8("DOTOK", m.d, run.Rmax)
     dtsf = run.sf("DOTOK_SF", m.d, run.Rmax)
     xtok = run.u8("XTOK", m.d, run.Rmax)
@@ -318,7 +318,8 @@ def test_dgrad_down_swiglu_stage(run):
             continue
         W, _, be = _expert_weights(run, e)
         dOv = be["dOq"].val                        # identical bytes on both sides (bit-exact checks above)
-        r = OL.expert_backward(dOv, gu[rows], W)
+        gate = np.asarray(run.f["w"], dtype=np.float32).reshape(-1)[a] if e < m.E else None
+        r = OL.expert_backward(dOv, gu[rows], W, row_gate=gate)
         got = mxfp8.dequantize(dq[rows], dsf[rows], 1)
         assert rel_frob(got, mxfp8.roundtrip(r["dgu"], 1)) < TOL, e
 

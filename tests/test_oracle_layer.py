@@ -137,3 +137,34 @@ def test_quantized_backward_structure():
     for key in ("dx", "dW_gu", "dW_d"):
         rel = np.linalg.norm(b[key] - be[key]) / np.linalg.norm(be[key])
         assert rel < 0.1, (key, rel)
+
+
+def test_gate_on_dh_equals_gate_on_dy_for_power_of_two_gates():
+    # The expert dgrad quantises each token's dy once and scales dh by the
+    # gate. A power-of-two gate moves only the E8M0 scale of MX(w dy), so then
+    # MX(w dy) = w MX(dy) exactly and dh must equal the product of the
+    # independently quantised w dy rows with W_d, row for row.
+    shape = _tiny_shape(T=40, d=64, E=4, k=2, G=1, g_top=1, I=32, S=0)
+    inp = _inputs(shape, seed=6)
+    f = L.layer_forward(inp, shape)
+    rng = np.random.default_rng(8)
+    f = dict(f)
+    f["w"] = 2.0 ** rng.integers(-3, 2, size=f["w"].shape).astype(np.float64)
+    b = L.layer_backward(f, inp, shape)
+    sch = f["sched"]
+    k = shape.k
+    for e in range(shape.E):
+        a = sch["inv"][sch["offsets"][e]:sch["offsets"][e + 1]]
+        if len(a) == 0:
+            continue
+        wdy = f["w"].reshape(-1)[a][:, None] * inp["dy"][a // k]
+        dh = mxfp8.roundtrip(wdy, 1) @ mxfp8.roundtrip(inp["w_d"][e].T, 1).T    # W_d MX along d
+        assert np.allclose(b["experts"][e]["dh"], dh, rtol=1e-12, atol=1e-300), e
+    # a gate that is not a power of two moves the codes: the two rounding points differ
+    f["w"] = f["w"] * 1.37
+    b2 = L.layer_backward(f, inp, shape)
+    e = int(np.argmax(sch["counts"]))
+    a = sch["inv"][sch["offsets"][e]:sch["offsets"][e + 1]]
+    wdy = f["w"].reshape(-1)[a][:, None] * inp["dy"][a // k]
+    dh_other = mxfp8.roundtrip(wdy, 1) @ mxfp8.roundtrip(inp["w_d"][e].T, 1).T
+    assert not np.allclose(b2["experts"][e]["dh"], dh_other, rtol=1e-9, atol=0)
