@@ -266,8 +266,6 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v
                       pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
 }
 
-__device__ __forceinline__ void load_bf16x32_g(const __nv_bfloat16* src, float* v) { load_bf16x32(src, v); }
-
 // Read this thread's whole accumulator row (BN fp32 columns) into packed bf16
 // pairs, then hand the TMEM buffer back to the MMA warp at once, so the next
 // tile's MMAs start while the row is still being written out.
@@ -298,18 +296,6 @@ __device__ __forceinline__ void drain_acc_bf16(uint32_t tacc, bool have_acc, uin
   }
   tc_fence_before();
   mbar_arrive(acce);
-}
-
-__device__ __forceinline__ void unpack_bf16x32(const uint4* q, float* v) {
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const uint32_t w[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      v[8 * k + 2 * i] = __uint_as_float(w[i] << 16);
-      v[8 * k + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-  }
 }
 
 // ---------------------------------------------------------------- ring movers
