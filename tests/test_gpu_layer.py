@@ -2,7 +2,7 @@
 against the oracle, element by element, at sizes the oracle finishes in
 seconds that still span several tiles, ring laps and ragged tails.
 
-Bars (spec reading): route indices, counts, ranks, permutation and
+Bars: route indices, counts, ranks, permutation and
 quantised bytes bit-exact; bf16 outputs and gradients within relative
 Frobenius error 1e-3 of the oracle on identical quantised operands
 ("stage-wise"), and end to end.
