@@ -565,7 +565,18 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
   epw.out = dw_d;
   epw.out2 = dws_d;
   epw.ldo = m.I;
+  // Reverse-dispatch (+ router input gradient) and the router weight gradient
+  // depend on no weight gradient: they run on a side stream beside them, in
+  // the SM resources the persistent weight-gradient CTAs leave free.
+  LapStreams* ls = lap_streams();
+  if (ls == nullptr) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(ls->mu);
+  cudaEventRecord(ls->fork, s);
   if (int r = gemm_dispatch("gemm_wgrad_d", kWgrad, m, 0, m.I, 0, m.d, opw, epw, counts, poff, lap_tiles, row_src, status, s, 256, ws_ptr<int>(L, ws, MOE_WS_ORDER))) return r;
+  cudaStreamWaitEvent(ls->aux[0], ls->fork, 0);
+  launch_reverse_dispatch(m, topk_idx, w_router, L, ws, dx, ls->aux[0]);
+  launch_router_dwr(m, L, ws, dw_router, ls->aux[0]);
+  cudaEventRecord(ls->join[0], ls->aux[0]);
   opw.a = ws_ptr<uint8_t>(L, ws, MOE_WS_DGUTOK);
   opw.a_rows = 2 * m.I;
   opw.a_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_DGUTOK_SF);
@@ -575,11 +586,10 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
   epw.out = dw_gu;
   epw.out2 = dws_gu;
   epw.ldo = m.d;
-  if (int r = gemm_dispatch("gemm_wgrad_gu", kWgrad, m, 0, m.d, 0, 2 * m.I, opw, epw, counts, poff, lap_tiles, row_src, status, s, 256, ws_ptr<int>(L, ws, MOE_WS_ORDER)))
-    return r;
-  // Reverse-dispatch (+ router input gradient) and the router weight gradient.
-  launch_reverse_dispatch(m, topk_idx, w_router, L, ws, dx, s);
-  launch_router_dwr(m, L, ws, dw_router, s);
+  const int r = gemm_dispatch("gemm_wgrad_gu", kWgrad, m, 0, m.d, 0, 2 * m.I, opw, epw, counts, poff, lap_tiles,
+                              row_src, status, s, 256, ws_ptr<int>(L, ws, MOE_WS_ORDER));
+  cudaStreamWaitEvent(s, ls->join[0], 0);
+  if (r) return r;
   return launch_status();
 }
 
