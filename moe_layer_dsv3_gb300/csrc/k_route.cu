@@ -58,9 +58,10 @@ __device__ __forceinline__ void warp_best(float& v, int& e) {
   }
 }
 
-constexpr int kMaxPerLane = 16;   // E <= 512
-
-// One warp per token. Lane l owns experts e = l + 32 i.
+// One warp per token. Lane l owns experts e = l + 32 i, i < kMaxPerLane
+// (a compile-time bound on ceil(E / 32), so the per-lane loops have no dead
+// iterations at the common expert counts).
+template <int kMaxPerLane>
 __global__ void router_topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E,
                                    int k, int G, int gtop, int32_t* __restrict__ idx_out,
                                    float* __restrict__ w_out, float* __restrict__ s_out) {
@@ -157,7 +158,10 @@ void launch_router_topk(const Dims& m, const float* logits, const float* bias, i
   if (m.T == 0) return;
   const int warps = 4;
   Prof prof("router_topk", s);
-  router_topk_kernel<<<static_cast<unsigned>(ceil_div(m.T, warps)), warps * 32, warps * m.E * sizeof(float), s>>>(
+  const int per = (m.E + 31) / 32;   // E <= 512
+  auto kern = per <= 4 ? router_topk_kernel<4> : per <= 8 ? router_topk_kernel<8> : per <= 12 ? router_topk_kernel<12>
+                                                                                    : router_topk_kernel<16>;
+  kern<<<static_cast<unsigned>(ceil_div(m.T, warps)), warps * 32, warps * m.E * sizeof(float), s>>>(
       logits, bias, m.T, m.E, m.k, m.G, m.gtop, idx, w, s_sel);
 }
 

@@ -90,9 +90,13 @@ __global__ void sched_scan_kernel(const int* __restrict__ hist, int Ep, int unit
 // lap_tiles[L][e] = sum_{e' < e} ceil(len(e', L) / 128), where a routed
 // expert's lap L holds ranks [L*C, min(n, (L+1)*C)) and a shared expert is
 // processed whole in lap 0 (it is read in token order, not from the ring).
-__global__ void sched_offsets_kernel(const int* __restrict__ counts, int E, int Ep, int C, int Lb,
+__global__ void sched_offsets_kernel(const int* counts, int E, int Ep, int C, int Lb,
                                      int* __restrict__ offsets, int* __restrict__ poff, int* __restrict__ lap_tiles,
                                      int* __restrict__ meta, int* __restrict__ lapbase) {
+  __shared__ int sc[1024];   // counts, Ep <= 513
+  for (int e = threadIdx.x; e < Ep; e += blockDim.x) sc[e] = counts[e];
+  __syncthreads();
+  counts = sc;
   if (threadIdx.x == 0) {
     int o = 0, po = 0, laps = 0;
     for (int e = 0; e < Ep; ++e) {
