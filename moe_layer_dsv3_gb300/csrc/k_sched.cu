@@ -98,21 +98,20 @@ __global__ void sched_offsets_kernel(const int* counts, int E, int Ep, int C, in
   __syncthreads();
   counts = sc;
   if (threadIdx.x == 0) {
-    int o = 0, po = 0, laps = 0;
+    int o = 0, po = 0, nmax = 0, active = 0;
     for (int e = 0; e < Ep; ++e) {
       offsets[e] = o;
       poff[e] = po;
       const int n = counts[e];
       o += n;
-      po += (n + 127) / 128 * 128;
-      if (e < E) laps = max(laps, (n + C - 1) / C);
+      po += (n + 127) & ~127;
+      if (e < E) nmax = max(nmax, n);
+      active += n > 0 ? 1 : 0;
     }
     offsets[Ep] = o;
     poff[Ep] = po;
-    meta[0] = laps;
+    meta[0] = (nmax + C - 1) / C;   // laps of the busiest routed expert
     meta[1] = po;
-    int active = 0;
-    for (int e = 0; e < Ep; ++e) active += counts[e] > 0 ? 1 : 0;
     meta[2] = active;
   }
   for (int L = threadIdx.x; L < Lb; L += blockDim.x) {
