@@ -115,7 +115,7 @@ void launch_router_dwr(const Dims& m, const Layout& L, void* ws, void* dw_router
 enum GemmMode : int {
   kSwigluFwd = 0,   // lap tiles, A = ring / x_q, epilogue SwiGLU + MX(h) two ways + saved g,u
   kPush = 1,        // padded tiles, epilogue bf16 rows pushed to their assignment
-  kSwigluBwd = 2,   // lap tiles, A = ring dO / dO_s, epilogue fp32 dh rows (SwiGLU backward follows)
+  kSwigluBwd = 2,   // lap tiles, A = ring of MX(dy) rows / MX(dy) in place, epilogue fp32 dh rows times the gate
   kWgrad = 3,       // per-expert K ranges, epilogue bf16 weight gradient
   kPlain = 4,       // single dense problem, fp32 output (unit test entry)
   // 5 is the bf16 router-logit mode (gemm.cuh)
