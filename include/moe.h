@@ -13,7 +13,10 @@
  *
  * Conventions for every entry point
  *   - Pointers named in the signature are DEVICE pointers unless stated.
- *     bf16 tensors are row-major, dense (row pitch = row length).
+ *     bf16 tensors are row-major, dense (row pitch = row length). Tensor,
+ *     weight, gradient and workspace buffers must start on a 16-byte boundary
+ *     (MOE_ERR_INVALID_ARG otherwise); topk_idx, topk_w and bias only need
+ *     their element alignment.
  *   - The caller allocates and frees every buffer, including the workspace
  *     (moe_workspace_size) and the quantised-weight blob (moe_weights_size).
  *     The library never allocates device memory and never synchronises the

@@ -75,6 +75,12 @@ int launch_status() { return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE
 // A per-token array (x, topk_idx, topk_w, y, dy, dx) may be null only when there are no tokens.
 inline bool tok_ok(const void* p, const moe_config_t* c) { return p != nullptr || c->T == 0; }
 
+// Device buffers read or written with 16-byte vectors or by TMA must start on
+// a 16-byte boundary; null (allowed where tok_ok allows it) passes.
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+template <typename... P>
+inline bool all_al16(const P*... p) { return (al16(p) && ...); }
+
 // Counters of an all-laps ring launch, zeroed on the stream before it.
 RingMovers ring_movers(const Layout& L, void* ws, cudaStream_t s) {
   RingMovers mv{};
@@ -261,6 +267,7 @@ int moe_quantize_weights(const moe_config_t* cfg, const void* w_gu, const void* 
   if (int r = validate(cfg)) return r;
   if (w_gu == nullptr || w_d == nullptr || wq == nullptr) return MOE_ERR_INVALID_ARG;
   if (cfg->n_shared > 0 && (ws_gu == nullptr || ws_d == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (!all_al16(w_gu, w_d, ws_gu, ws_d, wq)) return MOE_ERR_INVALID_ARG;
   if (!arch_ok()) return MOE_ERR_UNSUPPORTED_ARCH;
   const Dims m = make_dims(cfg);
   const WLayout W = make_wlayout(cfg);
@@ -300,6 +307,7 @@ int moe_route(const moe_config_t* cfg, const void* x, const void* w_router, cons
   if (int r = validate(cfg)) return r;
   if (!tok_ok(x, cfg) || !w_router || !bias || !tok_ok(topk_idx, cfg) || !tok_ok(topk_w, cfg) || !ws)
     return MOE_ERR_INVALID_ARG;
+  if (!all_al16(x, w_router, ws)) return MOE_ERR_INVALID_ARG;
   if (!arch_ok()) return MOE_ERR_UNSUPPORTED_ARCH;
   const Layout L = make_layout(cfg);
   const Dims& m = L.m;
@@ -313,6 +321,7 @@ int moe_route(const moe_config_t* cfg, const void* x, const void* w_router, cons
 int moe_schedule(const moe_config_t* cfg, const int32_t* topk_idx, void* ws, moe_stream_t stream) {
   if (int r = validate(cfg)) return r;
   if (!tok_ok(topk_idx, cfg) || !ws) return MOE_ERR_INVALID_ARG;
+  if (!all_al16(ws)) return MOE_ERR_INVALID_ARG;
   if (!arch_ok()) return MOE_ERR_UNSUPPORTED_ARCH;
   const Layout L = make_layout(cfg);
   launch_schedule(L.m, topk_idx, L, ws, S(stream));
@@ -322,6 +331,7 @@ int moe_schedule(const moe_config_t* cfg, const int32_t* topk_idx, void* ws, moe
 int moe_dispatch(const moe_config_t* cfg, const void* x, void* ws, moe_stream_t stream) {
   if (int r = validate(cfg)) return r;
   if (!tok_ok(x, cfg) || !ws) return MOE_ERR_INVALID_ARG;
+  if (!all_al16(x, ws)) return MOE_ERR_INVALID_ARG;
   if (!arch_ok()) return MOE_ERR_UNSUPPORTED_ARCH;
   const Layout L = make_layout(cfg);
   const Dims& m = L.m;
@@ -342,6 +352,7 @@ int moe_forward(const moe_config_t* cfg, const void* x, const void* wq, const fl
                 moe_stream_t stream) {
   if (int r = validate(cfg)) return r;
   if (!tok_ok(x, cfg) || !wq || !tok_ok(topk_w, cfg) || !tok_ok(y, cfg) || !ws) return MOE_ERR_INVALID_ARG;
+  if (!all_al16(x, wq, y, ws)) return MOE_ERR_INVALID_ARG;
   if (!arch_ok()) return MOE_ERR_UNSUPPORTED_ARCH;
   const Layout L = make_layout(cfg);
   const WLayout W = make_wlayout(cfg);
@@ -443,6 +454,7 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
       !tok_ok(dx, cfg) || !dw_router || !dw_gu || !dw_d || !ws)
     return MOE_ERR_INVALID_ARG;
   if (cfg->n_shared > 0 && (!dws_gu || !dws_d)) return MOE_ERR_INVALID_ARG;
+  if (!all_al16(x, w_router, dy, wq, dx, dw_router, dw_gu, dw_d, dws_gu, dws_d, ws)) return MOE_ERR_INVALID_ARG;
   if (!arch_ok()) return MOE_ERR_UNSUPPORTED_ARCH;
   const Layout L = make_layout(cfg);
   const WLayout W = make_wlayout(cfg);

@@ -202,6 +202,7 @@ extern "C" int moe_route_noalloc(const moe_config_t* cfg, const void* x, const v
   const bool no_tokens = cfg->T == 0;   // per-token arrays may be null then
   if ((!x && !no_tokens) || !w_router || !bias || (!topk_idx && !no_tokens) || (!topk_w && !no_tokens))
     return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w_router)) & 15u) return MOE_ERR_INVALID_ARG;
   if (static_cast<int64_t>(cfg->T) * cfg->E > moe::kRouteScratchFloats) return MOE_ERR_SCRATCH;
   if (!moe::arch_ok()) return MOE_ERR_UNSUPPORTED_ARCH;
   if (cfg->T == 0) return MOE_OK;

@@ -77,3 +77,30 @@ def test_views_are_disjoint_and_inside_workspace():
     spans.sort()
     for (a0, a1), (b0, b1) in zip(spans, spans[1:]):
         assert a1 <= b0
+
+
+def test_misaligned_buffers_are_rejected_before_any_launch():
+    # Argument checks run before the device check, so on a host without a GPU a
+    # misaligned buffer gives MOE_ERR_INVALID_ARG and an aligned one gets as
+    # far as MOE_ERR_UNSUPPORTED_ARCH; nothing is launched or dereferenced.
+    m = _lib()
+    cfg = m.config(256, 256, 8, 2, 1, 1, 128, 1)
+    A, B = 1 << 20, (1 << 20) + 8           # 16-byte aligned and misaligned fake device addresses
+
+    def rc(call):
+        try:
+            call()
+            return m.MOE_OK
+        except m.MoeError as e:
+            return e.code
+
+    calls = {
+        "forward": lambda x: m.moe_forward(cfg, x, A, A, A, A),
+        "backward": lambda x: m.moe_backward(cfg, A, A, A, A, x, A, A, A, A, A, A, A, A),
+        "route": lambda x: m.moe_route(cfg, x, A, A, A, A, A),
+        "dispatch": lambda x: m.moe_dispatch(cfg, A, x),
+        "quantize_weights": lambda x: m.moe_quantize_weights(cfg, A, x, A, A, A),
+    }
+    for name, call in calls.items():
+        assert rc(lambda: call(B)) == m.MOE_ERR_INVALID_ARG, name
+        assert rc(lambda: call(A)) != m.MOE_ERR_INVALID_ARG, name
