@@ -37,14 +37,102 @@ METRIC = "MoE-layer tokens/s fwd+bwd MXFP8 (1xGB300)"
 
 
 # ---------------------------------------------------------------- helpers
+PEAK_FILE = os.path.join(ROOT, "profiles", "mxfp8_peak.json")
+
+
 def peaks():
+    """Roofline denominators: HBM and bf16 from MEASURED_PEAKS.json (else the
+    recipe's fallback); dense MXFP8 from the library GEMM measured by
+    `bench.py --probe-peak` (profiles/mxfp8_peak.json) when present, else
+    2 x the sustained bf16 figure (the nominal fp8/bf16 ratio)."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return {"hbm_gbs": d["hbm_gbs"], "bf16": d["bf16_tflops"], "bf16_sus": d["bf16_tflops_sustained"],
-                "src": "measured"}
-    return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sus": 1700.0, "src": "fallback"}
+        pk = {"hbm_gbs": d["hbm_gbs"], "bf16": d["bf16_tflops"], "bf16_sus": d["bf16_tflops_sustained"],
+              "src": "measured"}
+    else:
+        pk = {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sus": 1700.0, "src": "fallback"}
+    pk["fp8"] = 2.0 * pk["bf16_sus"]
+    pk["fp8_note"] = ("dense MXFP8 = 2 x %s sustained bf16 (%s TFLOP/s), the nominal fp8/bf16 ratio"
+                      % ("measured" if pk["src"] == "measured" else "fallback", pk["bf16_sus"]))
+    if os.path.exists(PEAK_FILE):
+        with open(PEAK_FILE) as f:
+            m = json.load(f)
+        lib = m.get("library") or {}
+        if lib.get("tflops_sustained"):
+            pk["fp8"] = lib["tflops_sustained"]
+            pk["fp8_note"] = ("measured MXFP8: %s, %s, sustained (profiles/mxfp8_peak.json)"
+                              % (lib.get("name"), lib.get("shape")))
+    return pk
+
+
+def probe_peak(args):
+    """Dense MXFP8 GEMM throughput on this GPU: a library GEMM (cuBLASLt through
+    torch._scaled_mm with E8M0 block scales, 32 elements per scale) and this
+    repo's own plain tcgen05 GEMM (moe_gemm_mxfp8), at M = N = K = n. Burst =
+    best of 10 launches; sustained = back-to-back launches for ~4 s."""
+    import moe_layer_dsv3_gb300 as M
+    n = args.probe_n
+    dev = "cuda"
+    torch.manual_seed(0)
+    a8 = (torch.randn(n, n, device=dev) * 0.5).to(torch.float8_e4m3fn)
+    b8 = (torch.randn(n, n, device=dev) * 0.5).to(torch.float8_e4m3fn)
+    flop = 2.0 * n ** 3
+
+    def timeit(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        best = None
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            t = e0.elapsed_time(e1)
+            best = t if best is None else min(best, t)
+        reps = max(1, int(4000.0 / best))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        sus = e0.elapsed_time(e1) / reps
+        return flop / (best / 1e3) / 1e12, flop / (sus / 1e3) / 1e12
+
+    out = {"n": n, "gpu": torch.cuda.get_device_name(0), "torch": torch.__version__}
+    clocks = ClockSampler(0)
+    # library: MX block scales, all 2^0 (E8M0 byte 127), one per 32 elements along K
+    lib = {"name": "cuBLASLt via torch._scaled_mm (E4M3 x E4M3, E8M0 scale per 32 along K)",
+           "shape": "M=N=K=%d" % n}
+    try:
+        sa = torch.full((n, n // 32), 127, dtype=torch.uint8, device=dev).view(torch.float8_e8m0fnu)
+        sb = torch.full((n, n // 32), 127, dtype=torch.uint8, device=dev).view(torch.float8_e8m0fnu)
+        fn = lambda: torch._scaled_mm(a8, b8.t(), sa, sb, out_dtype=torch.bfloat16)  # noqa: E731
+        ref = fn().float()
+        chk = (a8.float() @ b8.float().t())
+        lib["rel_err"] = float((ref - chk).norm() / chk.norm())
+        lib["tflops_burst"], lib["tflops_sustained"] = timeit(fn)
+    except Exception as e:   # record why the library path is unavailable
+        lib["error"] = "%s: %s" % (type(e).__name__, str(e)[:300])
+    out["library"] = lib
+    # this repo's plain MXFP8 GEMM (fp32 output)
+    ours = {"name": "moe_gemm_mxfp8 (tcgen05 kind::mxf8f6f4.block_scale, fp32 out)", "shape": "M=N=K=%d" % n}
+    sf = torch.full((n * n // 32,), 127, dtype=torch.uint8, device=dev)
+    c = torch.empty((n, n), dtype=torch.float32, device=dev)
+    sp = torch.cuda.current_stream().cuda_stream
+    fn = lambda: M.moe_gemm_mxfp8(n, n, n, a8.data_ptr(), sf.data_ptr(), b8.data_ptr(), sf.data_ptr(),  # noqa: E731
+                                  c.data_ptr(), sp)
+    fn()
+    torch.cuda.synchronize()
+    ours["rel_err"] = float((c - a8.float() @ b8.float().t()).norm() / (a8.float() @ b8.float().t()).norm())
+    ours["tflops_burst"], ours["tflops_sustained"] = timeit(fn)
+    out["ours"] = ours
+    out["clocks"] = clocks.stop()
+    print(json.dumps(out), flush=True)
 
 
 def gemm_flops(shape):
@@ -495,13 +583,11 @@ def run_ours(args, rank, world, local_rank):
     # kernels that run alone on the launch stream.
     lap_kernels = {"gemm1_fwd", "gemm_dgrad_down", "permute_lap", "permute_lap_dO"} if args.lap_launches else set()
     dom = max(((n, v) for n, v in kern.items() if n not in lap_kernels), key=lambda kv: kv[1][1])[0]
-    fp8_peak = 2.0 * pk["bf16_sus"]
+    fp8_peak = pk["fp8"]
     if dom in fl:
         achieved = per_kernel[dom]["tflops"]
         roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
-                "frac": achieved / fp8_peak, "traffic": None,
-                "peak_note": "dense MXFP8 = 2 x %s sustained bf16 (%s TFLOP/s), the nominal fp8/bf16 ratio"
-                             % ("measured" if pk["src"] == "measured" else "fallback", pk["bf16_sus"]),
+                "frac": achieved / fp8_peak, "traffic": None, "peak_note": pk["fp8_note"],
                 "flop_per_step": fl[dom]}
     else:
         achieved = per_kernel[dom].get("gbs", 0.0)
@@ -598,7 +684,13 @@ def main():
                     help="skip the extra per-lap pass that times the ring movers as their own launches")
     ap.add_argument("--lap-launches", action="store_true",
                     help="one mover launch + one GEMM launch per ring lap instead of one all-laps launch")
+    ap.add_argument("--probe-peak", action="store_true",
+                    help="measure dense MXFP8 GEMM throughput (library and this repo's plain GEMM) and exit")
+    ap.add_argument("--probe-n", type=int, default=8192)
     args = ap.parse_args()
+    if args.probe_peak:
+        probe_peak(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -25,9 +25,17 @@
  *     stream) and runs asynchronously.
  *   - Return value: MOE_OK, or an MOE_ERR_* code for argument, architecture
  *     or launch errors, in which case nothing further was enqueued.
+ *     MOE_ERR_CUDA reflects the entry point's own launches and stream
+ *     operations only: an error that other code left in the CUDA runtime's
+ *     last-error state is neither reported nor cleared.
  *     Device-side failures (a bounded wait that ran out, a bounds check)
  *     are recorded in a status word in the workspace; read it with
  *     moe_status after synchronising.
+ *   - Streams: moe_forward (with MOE_FLAG_LAP_LAUNCHES) and moe_backward fork
+ *     part of their work onto an auxiliary stream and join it back before
+ *     returning. The library creates one auxiliary stream per (device,
+ *     caller stream) on first use and keeps it until the process exits, so
+ *     layers driven from different streams do not wait on each other.
  *   - Results are bitwise deterministic: no floating-point atomics, every
  *     reduction has a fixed order.
  */
@@ -138,12 +146,16 @@ MOE_API int moe_route(const moe_config_t* cfg, const void* x, const void* w_rout
  *   T * E must be at most 4,194,304 (T = 16384 at E = 256), otherwise the
  *   call returns MOE_ERR_SCRATCH and enqueues nothing.
  *   It calls no cudaMalloc, cudaFree or other allocating routine. Its first
- *   call on a device looks up the array's device address (once per device,
- *   with that device current); make that first call before any stream
- *   capture. Every call shares the one array and overwrites the logits it
- *   reads, so nothing needs clearing between calls; calls that overlap on
- *   the GPU (different streams, or different host threads, on one device)
- *   race on it and must be ordered by the caller. */
+ *   call in each CUDA context of a device looks up the array's device
+ *   address (with that device current); make that first call before any
+ *   stream capture. Under lazy module loading (the CUDA default) the device
+ *   also reserves the array's 16 MiB at that first call, or at an earlier
+ *   moe_route on the device, whichever comes first: so make one of them
+ *   before another allocator reserves the GPU's memory. Every call shares
+ *   the one array and overwrites the logits it reads, so nothing needs
+ *   clearing between calls; calls that overlap on the GPU (different
+ *   streams, or different host threads, on one device) race on it and must
+ *   be ordered by the caller. */
 MOE_API int moe_route_noalloc(const moe_config_t* cfg, const void* x, const void* w_router, const float* bias,
                               int32_t* topk_idx, float* topk_w, moe_stream_t stream);
 

@@ -1,6 +1,8 @@
 // C ABI: argument checks, workspace layout, and the launch sequence of the
 // forward and backward passes. Every step runs in this library's kernels.
+#include <atomic>
 #include <cstring>
+#include <map>
 #include <mutex>
 
 #include "moe_internal.h"
@@ -22,19 +24,31 @@ struct Builder {
 
 }  // namespace
 
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return -1;
+  return dev;
+}
+
+cudaError_t& call_error() {
+  thread_local cudaError_t e = cudaSuccess;
+  return e;
+}
+
 bool arch_ok() {
-  static int ok = -1;
-  if (ok < 0) {
-    int dev = 0, major = 0, minor = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
-      ok = 0;
-    } else {
-      ok = (major == 10 && minor == 3) ? 1 : 0;
-    }
+  static std::atomic<int> cache[kMaxDev];   // 0 unknown, 1 sm_103, 2 other
+  const int dev = current_device();
+  if (dev < 0) return false;
+  int v = cache[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return false;
+    v = (major == 10 && minor == 3) ? 1 : 2;
+    cache[dev].store(v, std::memory_order_relaxed);
   }
-  return ok == 1;
+  return v == 1;
 }
 
 namespace {
@@ -42,35 +56,41 @@ namespace {
 inline cudaStream_t S(moe_stream_t s) { return static_cast<cudaStream_t>(s); }
 
 // Ring lap L runs on lap stream L % kRingBufs (stream 0 is the caller's, the
-// others are auxiliary streams of this device) and uses ring buffer
-// L % kRingBufs, so up to kRingBufs laps are in flight: a lap waits only for
-// the lap that used its ring buffer before. Fork and join are event record /
-// wait pairs on the caller's stream.
+// others are auxiliary streams) and uses ring buffer L % kRingBufs, so up to
+// kRingBufs laps are in flight: a lap waits only for the lap that used its
+// ring buffer before. The backward's side work (reverse-dispatch, router
+// weight gradient) runs on the first auxiliary stream. Each caller stream of
+// each device gets auxiliary streams and fork / join events of its own, so
+// layers driven from different streams do not serialise on a shared one;
+// they are created on first use and kept until the process exits. Fork and
+// join are event record / wait pairs on the caller's stream.
 struct LapStreams {
   std::mutex mu;
   cudaStream_t aux[kRingBufs - 1] = {};
   cudaEvent_t fork = nullptr;
   cudaEvent_t join[kRingBufs - 1] = {};
 };
-constexpr int kMaxDev = 64;
-LapStreams g_lap[kMaxDev];
+std::mutex g_lap_mu;
+std::map<cudaStream_t, LapStreams> g_lap[kMaxDev];
 
-LapStreams* lap_streams() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
-  LapStreams& l = g_lap[dev];
-  std::lock_guard<std::mutex> lk(l.mu);
-  if (l.fork == nullptr) {
-    for (int i = 0; i < kRingBufs - 1; ++i)
-      if (cudaStreamCreateWithFlags(&l.aux[i], cudaStreamNonBlocking) != cudaSuccess ||
-          cudaEventCreateWithFlags(&l.join[i], cudaEventDisableTiming) != cudaSuccess)
-        return nullptr;
-    if (cudaEventCreateWithFlags(&l.fork, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+LapStreams* lap_streams(cudaStream_t caller) {
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  LapStreams* l;
+  {
+    std::lock_guard<std::mutex> lk(g_lap_mu);
+    l = &g_lap[dev][caller];   // std::map nodes stay put while others are added
   }
-  return &l;
+  std::lock_guard<std::mutex> lk(l->mu);
+  if (l->fork == nullptr) {
+    for (int i = 0; i < kRingBufs - 1; ++i)
+      if (cudaStreamCreateWithFlags(&l->aux[i], cudaStreamNonBlocking) != cudaSuccess ||
+          cudaEventCreateWithFlags(&l->join[i], cudaEventDisableTiming) != cudaSuccess)
+        return nullptr;
+    if (cudaEventCreateWithFlags(&l->fork, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+  }
+  return l;
 }
-
-int launch_status() { return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 // A per-token array (x, topk_idx, topk_w, y, dy, dx) may be null only when there are no tokens.
 inline bool tok_ok(const void* p, const moe_config_t* c) { return p != nullptr || c->T == 0; }
@@ -87,8 +107,8 @@ RingMovers ring_movers(const Layout& L, void* ws, cudaStream_t s) {
   mv.lapbase = ws_ptr<int>(L, ws, MOE_WS_LAPBASE);
   mv.moved = ws_ptr<int>(L, ws, MOE_WS_MOVED);
   mv.consumed = ws_ptr<int>(L, ws, MOE_WS_CONSUMED);
-  cudaMemsetAsync(mv.moved, 0, L.bytes[MOE_WS_MOVED], s);
-  cudaMemsetAsync(mv.consumed, 0, L.bytes[MOE_WS_CONSUMED], s);
+  note(cudaMemsetAsync(mv.moved, 0, L.bytes[MOE_WS_MOVED], s));
+  note(cudaMemsetAsync(mv.consumed, 0, L.bytes[MOE_WS_CONSUMED], s));
   return mv;
 }
 
@@ -252,6 +272,7 @@ int moe_quantize_mxfp8(const void* src, int rows, int K, int axis, void* codes, 
   if (axis != 0 && axis != 1) return MOE_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(src) % 16 || reinterpret_cast<uintptr_t>(codes) % 16) return MOE_ERR_INVALID_ARG;
   if (!arch_ok()) return MOE_ERR_UNSUPPORTED_ARCH;
+  CallScope call;
   if (rows == 0) return MOE_OK;
   if (axis == 1) {
     launch_quant_rows(src, rows, K, K, static_cast<uint8_t*>(codes), static_cast<uint8_t*>(scales), false, 0, S(stream));
@@ -259,7 +280,7 @@ int moe_quantize_mxfp8(const void* src, int rows, int K, int axis, void* codes, 
     launch_quant_cols(src, rows, K, K, round_up(rows, 32), static_cast<uint8_t*>(codes), static_cast<uint8_t*>(scales),
                       false, 1, S(stream));
   }
-  return launch_status();
+  return call.status();
 }
 
 int moe_quantize_weights(const moe_config_t* cfg, const void* w_gu, const void* w_d, const void* ws_gu,
@@ -269,6 +290,7 @@ int moe_quantize_weights(const moe_config_t* cfg, const void* w_gu, const void* 
   if (cfg->n_shared > 0 && (ws_gu == nullptr || ws_d == nullptr)) return MOE_ERR_INVALID_ARG;
   if (!all_al16(w_gu, w_d, ws_gu, ws_d, wq)) return MOE_ERR_INVALID_ARG;
   if (!arch_ok()) return MOE_ERR_UNSUPPORTED_ARCH;
+  CallScope call;
   const Dims m = make_dims(cfg);
   const WLayout W = make_wlayout(cfg);
   cudaStream_t s = S(stream);
@@ -299,7 +321,7 @@ int moe_quantize_weights(const moe_config_t* cfg, const void* w_gu, const void* 
     launch_quant_cols(gu, 2 * I, static_cast<int>(d), d, 2 * I, w1b + e0 * d * 2 * I, w1b_sf + e0 * d * 2 * I / 32,
                       true, static_cast<int>(n), s);
   }
-  return launch_status();
+  return call.status();
 }
 
 int moe_route(const moe_config_t* cfg, const void* x, const void* w_router, const float* bias, int32_t* topk_idx,
@@ -309,13 +331,14 @@ int moe_route(const moe_config_t* cfg, const void* x, const void* w_router, cons
     return MOE_ERR_INVALID_ARG;
   if (!all_al16(x, w_router, ws)) return MOE_ERR_INVALID_ARG;
   if (!arch_ok()) return MOE_ERR_UNSUPPORTED_ARCH;
+  CallScope call;
   const Layout L = make_layout(cfg);
   const Dims& m = L.m;
   if (m.T == 0) return MOE_OK;
   float* logits = ws_ptr<float>(L, ws, MOE_WS_LOGITS);
-  launch_router_logits(m, x, w_router, logits, S(stream));
+  if (int r = launch_router_logits(m, x, w_router, logits, S(stream))) return r;
   launch_router_topk(m, logits, bias, topk_idx, topk_w, ws_ptr<float>(L, ws, MOE_WS_SSEL), S(stream));
-  return launch_status();
+  return call.status();
 }
 
 int moe_schedule(const moe_config_t* cfg, const int32_t* topk_idx, void* ws, moe_stream_t stream) {
@@ -323,9 +346,10 @@ int moe_schedule(const moe_config_t* cfg, const int32_t* topk_idx, void* ws, moe
   if (!tok_ok(topk_idx, cfg) || !ws) return MOE_ERR_INVALID_ARG;
   if (!all_al16(ws)) return MOE_ERR_INVALID_ARG;
   if (!arch_ok()) return MOE_ERR_UNSUPPORTED_ARCH;
+  CallScope call;
   const Layout L = make_layout(cfg);
   launch_schedule(L.m, topk_idx, L, ws, S(stream));
-  return launch_status();
+  return call.status();
 }
 
 int moe_dispatch(const moe_config_t* cfg, const void* x, void* ws, moe_stream_t stream) {
@@ -333,6 +357,7 @@ int moe_dispatch(const moe_config_t* cfg, const void* x, void* ws, moe_stream_t 
   if (!tok_ok(x, cfg) || !ws) return MOE_ERR_INVALID_ARG;
   if (!all_al16(x, ws)) return MOE_ERR_INVALID_ARG;
   if (!arch_ok()) return MOE_ERR_UNSUPPORTED_ARCH;
+  CallScope call;
   const Layout L = make_layout(cfg);
   const Dims& m = L.m;
   if (m.T == 0) return MOE_OK;
@@ -340,12 +365,12 @@ int moe_dispatch(const moe_config_t* cfg, const void* x, void* ws, moe_stream_t 
   uint8_t* xq = ws_ptr<uint8_t>(L, ws, MOE_WS_XQ);
   uint8_t* xq_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_XQ_SF);
   if (m.Tpad > m.T) {
-    cudaMemsetAsync(xq + m.T * m.d, 0, (m.Tpad - m.T) * m.d, s);
-    cudaMemsetAsync(xq_sf + (m.T / 128) * 128 * (m.d / 32), 0, (m.Tpad - m.T / 128 * 128) * (m.d / 32), s);
+    note(cudaMemsetAsync(xq + m.T * m.d, 0, (m.Tpad - m.T) * m.d, s));
+    note(cudaMemsetAsync(xq_sf + (m.T / 128) * 128 * (m.d / 32), 0, (m.Tpad - m.T / 128 * 128) * (m.d / 32), s));
   }
   launch_quant_rows(x, m.T, m.d, m.d, xq, xq_sf, true, 0, s);
   launch_dispatch_all(m, L, ws, s);
-  return launch_status();
+  return call.status();
 }
 
 int moe_forward(const moe_config_t* cfg, const void* x, const void* wq, const float* topk_w, void* y, void* ws,
@@ -354,6 +379,7 @@ int moe_forward(const moe_config_t* cfg, const void* x, const void* wq, const fl
   if (!tok_ok(x, cfg) || !wq || !tok_ok(topk_w, cfg) || !tok_ok(y, cfg) || !ws) return MOE_ERR_INVALID_ARG;
   if (!all_al16(x, wq, y, ws)) return MOE_ERR_INVALID_ARG;
   if (!arch_ok()) return MOE_ERR_UNSUPPORTED_ARCH;
+  CallScope call;
   const Layout L = make_layout(cfg);
   const WLayout W = make_wlayout(cfg);
   const Dims& m = L.m;
@@ -363,8 +389,8 @@ int moe_forward(const moe_config_t* cfg, const void* x, const void* wq, const fl
   uint8_t* xq = ws_ptr<uint8_t>(L, ws, MOE_WS_XQ);
   uint8_t* xq_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_XQ_SF);
   if (m.Tpad > m.T) {
-    cudaMemsetAsync(xq + m.T * m.d, 0, (m.Tpad - m.T) * m.d, s);
-    cudaMemsetAsync(xq_sf + (m.T / 128) * 128 * (m.d / 32), 0, (m.Tpad - m.T / 128 * 128) * (m.d / 32), s);
+    note(cudaMemsetAsync(xq + m.T * m.d, 0, (m.Tpad - m.T) * m.d, s));
+    note(cudaMemsetAsync(xq_sf + (m.T / 128) * 128 * (m.d / 32), 0, (m.Tpad - m.T / 128 * 128) * (m.d / 32), s));
   }
   launch_quant_rows(x, m.T, m.d, m.d, xq, xq_sf, true, 0, s);
   int* counts = ws_ptr<int>(L, ws, MOE_WS_COUNTS);
@@ -405,11 +431,11 @@ int moe_forward(const moe_config_t* cfg, const void* x, const void* wq, const fl
                               row_src, status, s, 0, nullptr, &mv))
       return r;
   } else {
-    LapStreams* ls = lap_streams();
+    LapStreams* ls = lap_streams(s);
     if (ls == nullptr) return MOE_ERR_CUDA;
     std::lock_guard<std::mutex> lk(ls->mu);
-    cudaEventRecord(ls->fork, s);
-    for (int i = 0; i < kRingBufs - 1; ++i) cudaStreamWaitEvent(ls->aux[i], ls->fork, 0);
+    note(cudaEventRecord(ls->fork, s));
+    for (int i = 0; i < kRingBufs - 1; ++i) note(cudaStreamWaitEvent(ls->aux[i], ls->fork, 0));
     const uint8_t* ring = op1.a;
     const uint8_t* ring_sf = op1.a_sf;
     const size_t rb = static_cast<size_t>(m.E) * m.C * m.d;
@@ -424,8 +450,8 @@ int moe_forward(const moe_config_t* cfg, const void* x, const void* wq, const fl
                          status, cs);
     }
     for (int i = 0; i < kRingBufs - 1; ++i) {
-      cudaEventRecord(ls->join[i], ls->aux[i]);
-      cudaStreamWaitEvent(s, ls->join[i], 0);
+      note(cudaEventRecord(ls->join[i], ls->aux[i]));
+      note(cudaStreamWaitEvent(s, ls->join[i], 0));
     }
     if (rc) return rc;
   }
@@ -443,7 +469,7 @@ int moe_forward(const moe_config_t* cfg, const void* x, const void* wq, const fl
   ep2.ldo = m.d;
   if (int r = gemm_dispatch("gemm2_fwd", kPush, m, 0, m.d, m.I, 0, op2, ep2, counts, poff, lap_tiles, row_src, status, s)) return r;
   launch_combine(m, topk_w, L, ws, y, s);
-  return launch_status();
+  return call.status();
 }
 
 int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, const int32_t* topk_idx,
@@ -456,6 +482,7 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
   if (cfg->n_shared > 0 && (!dws_gu || !dws_d)) return MOE_ERR_INVALID_ARG;
   if (!all_al16(x, w_router, dy, wq, dx, dw_router, dw_gu, dw_d, dws_gu, dws_d, ws)) return MOE_ERR_INVALID_ARG;
   if (!arch_ok()) return MOE_ERR_UNSUPPORTED_ARCH;
+  CallScope call;
   const Layout L = make_layout(cfg);
   const WLayout W = make_wlayout(cfg);
   const Dims& m = L.m;
@@ -468,14 +495,14 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
   int* status = ws_ptr<int>(L, ws, MOE_WS_STATUS);
   if (m.T == 0) {
     // No tokens: every gradient is zero.
-    cudaMemsetAsync(dw_router, 0, static_cast<size_t>(m.E) * m.d * 2, s);
-    cudaMemsetAsync(dw_gu, 0, static_cast<size_t>(m.E) * 2 * m.I * m.d * 2, s);
-    cudaMemsetAsync(dw_d, 0, static_cast<size_t>(m.E) * m.d * m.I * 2, s);
+    note(cudaMemsetAsync(dw_router, 0, static_cast<size_t>(m.E) * m.d * 2, s));
+    note(cudaMemsetAsync(dw_gu, 0, static_cast<size_t>(m.E) * 2 * m.I * m.d * 2, s));
+    note(cudaMemsetAsync(dw_d, 0, static_cast<size_t>(m.E) * m.d * m.I * 2, s));
     if (m.S) {
-      cudaMemsetAsync(dws_gu, 0, static_cast<size_t>(m.S) * 2 * m.I * m.d * 2, s);
-      cudaMemsetAsync(dws_d, 0, static_cast<size_t>(m.S) * m.d * m.I * 2, s);
+      note(cudaMemsetAsync(dws_gu, 0, static_cast<size_t>(m.S) * 2 * m.I * m.d * 2, s));
+      note(cudaMemsetAsync(dws_d, 0, static_cast<size_t>(m.S) * m.d * m.I * 2, s));
     }
-    return launch_status();
+    return call.status();
   }
   // Reverse-combine: gate gradients, router logit gradients.
   launch_rev_combine_dw(m, dy, topk_w, L, ws, s);
@@ -485,8 +512,8 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
   uint8_t* dos = ws_ptr<uint8_t>(L, ws, MOE_WS_DOS);
   uint8_t* dos_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_DOS_SF);
   if (m.Tpad > m.T) {
-    cudaMemsetAsync(dos + m.T * m.d, 0, (m.Tpad - m.T) * m.d, s);
-    cudaMemsetAsync(dos_sf + (m.T / 128) * 128 * (m.d / 32), 0, (m.Tpad - m.T / 128 * 128) * (m.d / 32), s);
+    note(cudaMemsetAsync(dos + m.T * m.d, 0, (m.Tpad - m.T) * m.d, s));
+    note(cudaMemsetAsync(dos_sf + (m.T / 128) * 128 * (m.d / 32), 0, (m.Tpad - m.T / 128 * 128) * (m.d / 32), s));
   }
   launch_quant_rows(dy, m.T, m.d, m.d, dos, dos_sf, true, 0, s);
   // Token-axis operands of the weight gradients (and router dW partial sums).
@@ -522,11 +549,11 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
                               lap_tiles, row_src, status, s, 256, nullptr, &mv))
       return r;
   } else {
-    LapStreams* ls = lap_streams();
+    LapStreams* ls = lap_streams(s);
     if (ls == nullptr) return MOE_ERR_CUDA;
     std::lock_guard<std::mutex> lk(ls->mu);
-    cudaEventRecord(ls->fork, s);
-    for (int i = 0; i < kRingBufs - 1; ++i) cudaStreamWaitEvent(ls->aux[i], ls->fork, 0);
+    note(cudaEventRecord(ls->fork, s));
+    for (int i = 0; i < kRingBufs - 1; ++i) note(cudaStreamWaitEvent(ls->aux[i], ls->fork, 0));
     const uint8_t* ring = opb2.a;
     const uint8_t* ring_sf = opb2.a_sf;
     const size_t rb = static_cast<size_t>(m.E) * m.C * m.d;
@@ -541,8 +568,8 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
                          row_src, status, cs, 256);
     }
     for (int i = 0; i < kRingBufs - 1; ++i) {
-      cudaEventRecord(ls->join[i], ls->aux[i]);
-      cudaStreamWaitEvent(s, ls->join[i], 0);
+      note(cudaEventRecord(ls->join[i], ls->aux[i]));
+      note(cudaStreamWaitEvent(s, ls->join[i], 0));
     }
     if (rc) return rc;
   }
@@ -580,15 +607,15 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
   // Reverse-dispatch (+ router input gradient) and the router weight gradient
   // depend on no weight gradient: they run on a side stream beside them, in
   // the SM resources the persistent weight-gradient CTAs leave free.
-  LapStreams* ls = lap_streams();
+  LapStreams* ls = lap_streams(s);
   if (ls == nullptr) return MOE_ERR_CUDA;
   std::lock_guard<std::mutex> lk(ls->mu);
-  cudaEventRecord(ls->fork, s);
+  note(cudaEventRecord(ls->fork, s));
   if (int r = gemm_dispatch("gemm_wgrad_d", kWgrad, m, 0, m.I, 0, m.d, opw, epw, counts, poff, lap_tiles, row_src, status, s, 256, ws_ptr<int>(L, ws, MOE_WS_ORDER))) return r;
-  cudaStreamWaitEvent(ls->aux[0], ls->fork, 0);
+  note(cudaStreamWaitEvent(ls->aux[0], ls->fork, 0));
   launch_reverse_dispatch(m, topk_idx, w_router, L, ws, dx, ls->aux[0]);
   launch_router_dwr(m, L, ws, dw_router, ls->aux[0]);
-  cudaEventRecord(ls->join[0], ls->aux[0]);
+  note(cudaEventRecord(ls->join[0], ls->aux[0]));
   opw.a = ws_ptr<uint8_t>(L, ws, MOE_WS_DGUTOK);
   opw.a_rows = 2 * m.I;
   opw.a_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_DGUTOK_SF);
@@ -600,9 +627,9 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
   epw.ldo = m.d;
   const int r = gemm_dispatch("gemm_wgrad_gu", kWgrad, m, 0, m.d, 0, 2 * m.I, opw, epw, counts, poff, lap_tiles,
                               row_src, status, s, 256, ws_ptr<int>(L, ws, MOE_WS_ORDER));
-  cudaStreamWaitEvent(s, ls->join[0], 0);
+  note(cudaStreamWaitEvent(s, ls->join[0], 0));
   if (r) return r;
-  return launch_status();
+  return call.status();
 }
 
 int moe_status(const moe_config_t* cfg, void* ws, int* code, int* site, int clear, moe_stream_t stream) {

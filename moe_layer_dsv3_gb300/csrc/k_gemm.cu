@@ -1,6 +1,7 @@
 // Host side of the tcgen05 grouped GEMM: tensor maps, grid sizing, dispatch.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "gemm.cuh"
@@ -50,56 +51,69 @@ bool make_tmap_out(CUtensorMap* m, void* base, int64_t rows, int64_t cols) {
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Per device: 0 = not yet set up, 1 = ready, 2 = set-up failed.
+struct DevOnce {
+  std::mutex mu;
+  int state[kMaxDev] = {};
+  int per_sm[kMaxDev] = {};
+};
+
 template <int BN, int MODE>
 int run(const char* name, const CUtensorMap& ta, const CUtensorMap& ta2, const CUtensorMap& tb, const CUtensorMap& to,
         const CUtensorMap& to2, const GemmParams& p, int grid, cudaStream_t s) {
   using Cf = GemmCfg<BN, MODE>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_kernel<BN, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmem);
-  });
-  if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
+  // The shared-memory opt-in (and, for cooperative launches, the resident
+  // limit) belongs to the current device: set up once per device.
+  static DevOnce once;
+  const int dev = current_device();
+  if (dev < 0) return MOE_ERR_CUDA;
+  int per_sm = 0;
+  {
+    std::lock_guard<std::mutex> lk(once.mu);
+    if (once.state[dev] == 0) {
+      bool ok = cudaFuncSetAttribute(gemm_kernel<BN, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmem) ==
+                cudaSuccess;
+      if (ok && ring_mode(MODE))
+        ok = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&once.per_sm[dev], gemm_kernel<BN, MODE>,
+                                                           gemm_threads(MODE), Cf::kSmem) == cudaSuccess &&
+             once.per_sm[dev] >= 1;
+      once.state[dev] = ok ? 1 : 2;
+    }
+    if (once.state[dev] != 1) return MOE_ERR_CUDA;
+    per_sm = once.per_sm[dev];
+  }
   if (grid <= 0) return MOE_OK;
+  cudaLaunchConfig_t lc = {};
+  cudaLaunchAttribute attr[1];
   if constexpr (ring_mode(MODE)) {
     // CTAs wait on one another's counters: all of them must be resident, so
     // the launch is cooperative and no larger than the co-resident limit.
-    static std::once_flag occ_once;
-    static int per_sm = 0;
-    std::call_once(occ_once, [] {
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_kernel<BN, MODE>, gemm_threads(MODE),
-                                                        Cf::kSmem) != cudaSuccess)
-        per_sm = 0;
-    });
-    if (per_sm < 1) return MOE_ERR_CUDA;
     if (grid > per_sm * num_sms()) grid = per_sm * num_sms();
-    cudaLaunchConfig_t lc = {};
-    lc.gridDim = dim3(static_cast<unsigned>(grid));
-    lc.blockDim = dim3(gemm_threads(MODE));
-    lc.dynamicSmemBytes = Cf::kSmem;
-    lc.stream = s;
-    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
     lc.attrs = attr;
     lc.numAttrs = 1;
-    Prof prof(name, s);
-    if (cudaLaunchKernelEx(&lc, gemm_kernel<BN, MODE>, ta, ta2, tb, to, to2, p) != cudaSuccess) return MOE_ERR_CUDA;
-    return MOE_OK;
   }
+  lc.gridDim = dim3(static_cast<unsigned>(grid));
+  lc.blockDim = dim3(gemm_threads(MODE));
+  lc.dynamicSmemBytes = Cf::kSmem;
+  lc.stream = s;
   Prof prof(name, s);
-  gemm_kernel<BN, MODE><<<grid, gemm_threads(MODE), Cf::kSmem, s>>>(ta, ta2, tb, to, to2, p);
-  return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  const cudaError_t e = cudaLaunchKernelEx(&lc, gemm_kernel<BN, MODE>, ta, ta2, tb, to, to2, p);
+  note(e);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // namespace
 
 int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  static std::atomic<int> cache[kMaxDev];
+  const int dev = current_device();
+  if (dev < 0) return 1;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 1;
+    cache[dev].store(n, std::memory_order_relaxed);
   }
   return n;
 }

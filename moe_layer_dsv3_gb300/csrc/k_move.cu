@@ -339,8 +339,7 @@ static int lap_blocks(const Dims& m) {
 void launch_dispatch_all(const Dims& m, const Layout& L, void* ws, cudaStream_t s) {
   const int64_t items = static_cast<int64_t>(m.Ep) * 2 * (m.C / 8);
   if (items == 0) return;
-  Prof prof("dispatch_all", s);
-  dispatch_all_kernel<<<static_cast<unsigned>(ceil_div(items, 8)), 256, 0, s>>>(
+  launch_kernel("dispatch_all", dispatch_all_kernel, dim3(static_cast<unsigned>(ceil_div(items, 8))), dim3(256), 0, s,
       ws_ptr<uint8_t>(L, ws, MOE_WS_XQ), ws_ptr<uint8_t>(L, ws, MOE_WS_XQ_SF), ws_ptr<int>(L, ws, MOE_WS_COUNTS),
       ws_ptr<int>(L, ws, MOE_WS_POFF), ws_ptr<int>(L, ws, MOE_WS_ROWSRC), ws_ptr<int>(L, ws, MOE_WS_ORDER), m.k,
       m.d, m.E, m.Ep, m.C, ws_ptr<uint8_t>(L, ws, MOE_WS_RING_X), ws_ptr<uint8_t>(L, ws, MOE_WS_RING_X_SF));
@@ -349,8 +348,7 @@ void launch_dispatch_all(const Dims& m, const Layout& L, void* ws, cudaStream_t 
 void launch_permute_lap(const Dims& m, int lap, bool dO, const Layout& L, void* ws, cudaStream_t s) {
   const int blocks = lap_blocks(m);
   if (blocks == 0) return;
-  Prof prof(dO ? "permute_lap_dO" : "permute_lap", s);
-  permute_lap_kernel<<<blocks, 256, 0, s>>>(
+  launch_kernel(dO ? "permute_lap_dO" : "permute_lap", permute_lap_kernel, dim3(blocks), dim3(256), 0, s,
       ws_ptr<uint8_t>(L, ws, dO ? MOE_WS_DOS : MOE_WS_XQ), ws_ptr<uint8_t>(L, ws, dO ? MOE_WS_DOS_SF : MOE_WS_XQ_SF),
       ws_ptr<int>(L, ws, MOE_WS_LAPTILES), ws_ptr<int>(L, ws, MOE_WS_COUNTS), ws_ptr<int>(L, ws, MOE_WS_POFF),
       ws_ptr<int>(L, ws, MOE_WS_ROWSRC), m.T, m.k, m.d, m.E, m.Ep, m.C, lap,
@@ -361,16 +359,14 @@ void launch_permute_lap(const Dims& m, int lap, bool dO, const Layout& L, void* 
 void launch_combine(const Dims& m, const float* topk_w, const Layout& L, void* ws, void* y, cudaStream_t s) {
   const int64_t n = static_cast<int64_t>(m.T) * (m.d / 8);
   if (n == 0) return;
-  Prof prof("combine", s);
-  combine_kernel<<<static_cast<unsigned>(ceil_div(n, 256)), 256, 0, s>>>(
+  launch_kernel("combine", combine_kernel, dim3(static_cast<unsigned>(ceil_div(n, 256))), dim3(256), 0, s,
       ws_ptr<__nv_bfloat16>(L, ws, MOE_WS_O), topk_w, m.T, m.k, m.S, m.d, static_cast<__nv_bfloat16*>(y));
 }
 
 void launch_rev_combine_dw(const Dims& m, const void* dy, const float* topk_w, const Layout& L, void* ws,
                            cudaStream_t s) {
   if (m.T == 0) return;
-  Prof prof("rev_combine_dw", s);
-  rev_combine_dw_kernel<<<static_cast<unsigned>(ceil_div(m.T, 8)), 256, 0, s>>>(
+  launch_kernel("rev_combine_dw", rev_combine_dw_kernel, dim3(static_cast<unsigned>(ceil_div(m.T, 8))), dim3(256), 0, s,
       static_cast<const __nv_bfloat16*>(dy), ws_ptr<__nv_bfloat16>(L, ws, MOE_WS_O), topk_w,
       ws_ptr<float>(L, ws, MOE_WS_SSEL), m.T, m.k, m.d, ws_ptr<float>(L, ws, MOE_WS_DW),
       ws_ptr<float>(L, ws, MOE_WS_DL));
@@ -380,17 +376,15 @@ void launch_reverse_dispatch(const Dims& m, const int32_t* idx, const void* w_ro
                              void* dx, cudaStream_t s) {
   const int64_t n = static_cast<int64_t>(m.T) * (m.d / 8);
   if (n == 0) return;
-  Prof prof("reverse_dispatch", s);
-  reverse_dispatch_kernel<<<static_cast<unsigned>(ceil_div(n, 256)), 256, 0, s>>>(
-      ws_ptr<__nv_bfloat16>(L, ws, MOE_WS_DXE), ws_ptr<float>(L, ws, MOE_WS_DL), idx,
+  launch_kernel("reverse_dispatch", reverse_dispatch_kernel, dim3(static_cast<unsigned>(ceil_div(n, 256))), dim3(256), 0,
+                s, ws_ptr<__nv_bfloat16>(L, ws, MOE_WS_DXE), ws_ptr<float>(L, ws, MOE_WS_DL), idx,
       static_cast<const __nv_bfloat16*>(w_router), m.T, m.k, m.S, m.d, static_cast<__nv_bfloat16*>(dx));
 }
 
 void launch_router_dwr(const Dims& m, const Layout& L, void* ws, void* dw_router, cudaStream_t s) {
   dim3 grid(static_cast<unsigned>(ceil_div(m.d, 128)), static_cast<unsigned>(m.E));
-  Prof prof("router_dwr", s);
-  router_dwr_kernel<<<grid, 256, 0, s>>>(ws_ptr<float>(L, ws, MOE_WS_DWR_PART), ws_ptr<int>(L, ws, MOE_WS_POFF), m.d,
-                                         static_cast<__nv_bfloat16*>(dw_router));
+  launch_kernel("router_dwr", router_dwr_kernel, grid, dim3(256), 0, s, ws_ptr<float>(L, ws, MOE_WS_DWR_PART),
+                ws_ptr<int>(L, ws, MOE_WS_POFF), m.d, static_cast<__nv_bfloat16*>(dw_router));
 }
 
 }  // namespace moe

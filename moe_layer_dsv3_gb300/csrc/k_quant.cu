@@ -280,8 +280,7 @@ void launch_quant_rows(const void* src, int64_t rows, int K, int64_t ld, uint8_t
   const int64_t n = rows * (K / 32);
   if (n == 0) return;
   const int threads = 256;
-  Prof prof("quant_rows", s);
-  quant_rows_kernel<<<static_cast<unsigned>(ceil_div(n, threads)), threads, 0, s>>>(
+  launch_kernel("quant_rows", quant_rows_kernel, dim3(static_cast<unsigned>(ceil_div(n, threads))), dim3(threads), 0, s,
       static_cast<const __nv_bfloat16*>(src), rows, K, ld, codes, sf, tiled ? 1 : 0, interleave_I);
 }
 
@@ -289,16 +288,14 @@ void launch_quant_cols(const void* src, int64_t rows, int K, int64_t ld, int64_t
                        uint8_t* sf, bool tiled, int batch, cudaStream_t s) {
   if (rows_pad == 0 || K == 0 || batch == 0) return;
   dim3 grid(static_cast<unsigned>(ceil_div(K, 256)), static_cast<unsigned>(rows_pad / 32), static_cast<unsigned>(batch));
-  Prof prof("quant_cols", s);
-  quant_cols_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(src), rows, K, ld, rows_pad, codes, sf,
-                                         tiled ? 1 : 0);
+  launch_kernel("quant_cols", quant_cols_kernel, grid, dim3(256), 0, s, static_cast<const __nv_bfloat16*>(src), rows, K,
+                ld, rows_pad, codes, sf, tiled ? 1 : 0);
 }
 
 void launch_swiglu_bwd_quant(const Dims& m, const Layout& L, void* ws, cudaStream_t s) {
   if (m.Rmax == 0) return;
   dim3 grid(static_cast<unsigned>(m.I / 32), static_cast<unsigned>(m.Rmax / 128));
-  Prof prof("swiglu_bwd_quant", s);
-  swiglu_bwd_quant_kernel<<<grid, 128, 0, s>>>(
+  launch_kernel("swiglu_bwd_quant", swiglu_bwd_quant_kernel, grid, dim3(128), 0, s,
       ws_ptr<float>(L, ws, MOE_WS_DH), ws_ptr<__nv_bfloat16>(L, ws, MOE_WS_GU), ws_ptr<int>(L, ws, MOE_WS_ROWSRC),
       ws_ptr<int>(L, ws, MOE_WS_POFF) + m.Ep, m.I, m.Rmax, ws_ptr<uint8_t>(L, ws, MOE_WS_DGU),
       ws_ptr<uint8_t>(L, ws, MOE_WS_DGU_SF), ws_ptr<uint8_t>(L, ws, MOE_WS_DGUTOK),
@@ -310,14 +307,14 @@ void launch_tok_gather(const Dims& m, const void* src_rows, bool scale_by_gate, 
                        cudaStream_t s) {
   dim3 grid(static_cast<unsigned>(m.d / 128), static_cast<unsigned>(m.Rmax / 128));
   const int* poff = ws_ptr<int>(L, ws, MOE_WS_POFF);
-  Prof prof(scale_by_gate ? "tok_gather_dO" : "tok_gather_x", s);
   const auto* sp = static_cast<const __nv_bfloat16*>(src_rows);
   const int* rs = ws_ptr<int>(L, ws, MOE_WS_ROWSRC);
   const float* dl = router_partials ? ws_ptr<float>(L, ws, MOE_WS_DL) : nullptr;
   float* part = router_partials ? ws_ptr<float>(L, ws, MOE_WS_DWR_PART) : nullptr;
   auto kern = scale_by_gate ? (router_partials ? tok_gather_kernel<true, true> : tok_gather_kernel<true, false>)
                             : (router_partials ? tok_gather_kernel<false, true> : tok_gather_kernel<false, false>);
-  kern<<<grid, kTokThreads, 0, s>>>(sp, rs, poff + m.Ep, m.T, m.k, m.d, m.Rmax, topk_w, dl, part, codes, sf);
+  launch_kernel(scale_by_gate ? "tok_gather_dO" : "tok_gather_x", kern, grid, dim3(kTokThreads), 0, s, sp, rs,
+                poff + m.Ep, m.T, m.k, m.d, m.Rmax, topk_w, dl, part, codes, sf);
 }
 
 }  // namespace moe
@@ -326,9 +323,9 @@ extern "C" int moe_scales_to_tiled(const void* canon, int rows, int K, void* til
   if (canon == nullptr || tiled == nullptr || rows <= 0 || K <= 0 || rows % 128 || K % 128) return MOE_ERR_INVALID_ARG;
   const int nb = K / 32;
   const int64_t n = static_cast<int64_t>(rows) * nb;
-  moe::Prof prof("scales_to_tiled", static_cast<cudaStream_t>(stream));
-  moe::scales_to_tiled_kernel<<<static_cast<unsigned>(moe::ceil_div(n, 256)), 256, 0,
-                                static_cast<cudaStream_t>(stream)>>>(static_cast<const uint8_t*>(canon), rows, nb,
-                                                                      static_cast<uint8_t*>(tiled));
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  moe::CallScope call;
+  moe::launch_kernel("scales_to_tiled", moe::scales_to_tiled_kernel, dim3(static_cast<unsigned>(moe::ceil_div(n, 256))),
+                     dim3(256), 0, static_cast<cudaStream_t>(stream), static_cast<const uint8_t*>(canon),
+                     static_cast<int64_t>(rows), nb, static_cast<uint8_t*>(tiled));
+  return call.status();
 }

@@ -7,6 +7,8 @@
 // best groups (ties to the lower group), take the k best v among kept
 // experts (ties to the lower expert), slots in descending-v order, gates
 // w = s / sum(s) summed in slot order.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "moe_internal.h"
@@ -139,7 +141,7 @@ __global__ void router_topk_kernel(const float* __restrict__ logits, const float
   }
 }
 
-void launch_router_logits(const Dims& m, const void* x, const void* w_router, float* logits, cudaStream_t s) {
+int launch_router_logits(const Dims& m, const void* x, const void* w_router, float* logits, cudaStream_t s) {
   GemmOperands op{};
   op.a = static_cast<const uint8_t*>(x);
   op.a_rows = m.T;
@@ -150,19 +152,19 @@ void launch_router_logits(const Dims& m, const void* x, const void* w_router, fl
   GemmEpilogue ep{};
   ep.out = logits;
   ep.ldo = m.E;
-  gemm_dispatch("router_gemm", kRouterMode, m, 0, m.E, m.d, m.T, op, ep, nullptr, nullptr, nullptr, nullptr, nullptr, s);
+  return gemm_dispatch("router_gemm", kRouterMode, m, 0, m.E, m.d, m.T, op, ep, nullptr, nullptr, nullptr, nullptr,
+                       nullptr, s);
 }
 
 void launch_router_topk(const Dims& m, const float* logits, const float* bias, int32_t* idx, float* w, float* s_sel,
                         cudaStream_t s) {
   if (m.T == 0) return;
   const int warps = 4;
-  Prof prof("router_topk", s);
   const int per = (m.E + 31) / 32;   // E <= 512
   auto kern = per <= 4 ? router_topk_kernel<4> : per <= 8 ? router_topk_kernel<8> : per <= 12 ? router_topk_kernel<12>
                                                                                     : router_topk_kernel<16>;
-  kern<<<static_cast<unsigned>(ceil_div(m.T, warps)), warps * 32, warps * m.E * sizeof(float), s>>>(
-      logits, bias, m.T, m.E, m.k, m.G, m.gtop, idx, w, s_sel);
+  launch_kernel("router_topk", kern, dim3(static_cast<unsigned>(ceil_div(m.T, warps))), dim3(warps * 32),
+                warps * m.E * sizeof(float), s, logits, bias, m.T, m.E, m.k, m.G, m.gtop, idx, w, s_sel);
 }
 
 // ---------------------------------------------------------------- router without allocation
@@ -170,26 +172,63 @@ void launch_router_topk(const Dims& m, const float* logits, const float* bias, i
 // file-scope device array (every GPU that loads the library holds it until
 // the process exits). Host code must not pass the array's name to a kernel:
 // on the host it is only a stand-in symbol, so its device address is looked
-// up once per device with cudaGetSymbolAddress.
+// up with cudaGetSymbolAddress, once per CUDA context of a device.
 constexpr int64_t kRouteScratchFloats = int64_t(1) << 22;   // 16 MiB: T * E <= 4,194,304
 static __device__ __align__(256) float g_route_scratch[kRouteScratchFloats];
 
 namespace {
-constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
-float* g_scratch_addr[kMaxDevices] = {};
+struct ScratchSlot {
+  unsigned long long ctx_id = 0;   // context the address belongs to (0 = none yet)
+  float* addr = nullptr;
+};
+ScratchSlot g_scratch[kMaxDev];
 
-// Device address of the scratch on the current device (set up on first use).
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+
+// Unique id of the calling thread's current context (ids are never reused in a
+// process, so a context created after cudaDeviceReset gets a new one); 0 if
+// it cannot be read.
+unsigned long long current_ctx_id() {
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+  });
+  if (g_ctx_current == nullptr || g_ctx_id == nullptr) return 0;
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (g_ctx_current(&c) != CUDA_SUCCESS || c == nullptr || g_ctx_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of the scratch in the current context (looked up on the
+// first call in each context).
 int route_scratch(float** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  const int dev = current_device();
+  if (dev < 0) return MOE_ERR_CUDA;
+  const unsigned long long id = current_ctx_id();
+  if (id == 0) return MOE_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  ScratchSlot& slot = g_scratch[dev];
+  if (slot.ctx_id != id) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
-    g_scratch_addr[dev] = static_cast<float*>(p);
+    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr) {
+      (void)cudaGetLastError();   // the failed lookup's own error: not left for the caller to find
+      return MOE_ERR_CUDA;
+    }
+    slot.addr = static_cast<float*>(p);
+    slot.ctx_id = id;
   }
-  *out = g_scratch_addr[dev];
+  *out = slot.addr;
   return MOE_OK;
 }
 }  // namespace
@@ -210,7 +249,8 @@ extern "C" int moe_route_noalloc(const moe_config_t* cfg, const void* x, const v
   if (int r = moe::route_scratch(&logits)) return r;
   const moe::Dims m = moe::make_dims(cfg);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  moe::launch_router_logits(m, x, w_router, logits, s);
+  moe::CallScope call;
+  if (int r = moe::launch_router_logits(m, x, w_router, logits, s)) return r;
   moe::launch_router_topk(m, logits, bias, topk_idx, topk_w, nullptr, s);
-  return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return call.status();
 }

@@ -203,26 +203,21 @@ void launch_schedule(const Dims& m, const int32_t* idx, const Layout& L, void* w
   int* status = ws_ptr<int>(L, ws, MOE_WS_STATUS);
   const unsigned blocks = static_cast<unsigned>(ceil_div(m.units, kWarps));
   const size_t shm = static_cast<size_t>(kWarps) * m.Ep * sizeof(int);
-  cudaMemsetAsync(ws_ptr<int>(L, ws, MOE_WS_ROWSRC), 0xFF, L.bytes[MOE_WS_ROWSRC], s);
+  note(cudaMemsetAsync(ws_ptr<int>(L, ws, MOE_WS_ROWSRC), 0xFF, L.bytes[MOE_WS_ROWSRC], s));
   if (m.units > 0) {
-    { Prof prof("sched_hist", s);
-    sched_hist_kernel<<<blocks, kWarps * 32, shm, s>>>(idx, m.k, m.kp, m.E, m.Ep, m.Ap, m.units, hist, status); }
-    { Prof prof("sched_scan", s);
-    sched_scan_kernel<<<m.Ep, 256, 0, s>>>(hist, m.Ep, m.units, base, counts); }
+    launch_kernel("sched_hist", sched_hist_kernel, dim3(blocks), dim3(kWarps * 32), shm, s, idx, m.k, m.kp, m.E, m.Ep,
+                  m.Ap, m.units, hist, status);
+    launch_kernel("sched_scan", sched_scan_kernel, dim3(m.Ep), dim3(256), 0, s, hist, m.Ep, m.units, base, counts);
   } else {
-    cudaMemsetAsync(counts, 0, sizeof(int) * m.Ep, s);
+    note(cudaMemsetAsync(counts, 0, sizeof(int) * m.Ep, s));
   }
-  { Prof prof("sched_offsets", s);
-  sched_offsets_kernel<<<1, 256, 0, s>>>(counts, m.E, m.Ep, m.C, m.Lb, offsets, poff, lap_tiles, meta,
-                                         ws_ptr<int>(L, ws, MOE_WS_LAPBASE)); }
-  { Prof prof("sched_order", s);
-  sched_order_kernel<<<1, 512, 0, s>>>(counts, m.Ep, ws_ptr<int>(L, ws, MOE_WS_ORDER)); }
+  launch_kernel("sched_offsets", sched_offsets_kernel, dim3(1), dim3(256), 0, s, counts, m.E, m.Ep, m.C, m.Lb, offsets,
+                poff, lap_tiles, meta, ws_ptr<int>(L, ws, MOE_WS_LAPBASE));
+  launch_kernel("sched_order", sched_order_kernel, dim3(1), dim3(512), 0, s, counts, m.Ep, ws_ptr<int>(L, ws, MOE_WS_ORDER));
   if (m.units > 0) {
-    Prof prof("sched_rank", s);
-    sched_rank_kernel<<<blocks, kWarps * 32, shm, s>>>(idx, m.T, m.k, m.kp, m.E, m.Ep, m.Ap, m.units, base, offsets,
-                                                       poff, ws_ptr<int>(L, ws, MOE_WS_RANK),
-                                                       ws_ptr<int>(L, ws, MOE_WS_POS), ws_ptr<int>(L, ws, MOE_WS_INV),
-                                                       ws_ptr<int>(L, ws, MOE_WS_ROWSRC));
+    launch_kernel("sched_rank", sched_rank_kernel, dim3(blocks), dim3(kWarps * 32), shm, s, idx, m.T, m.k, m.kp, m.E,
+                  m.Ep, m.Ap, m.units, base, offsets, poff, ws_ptr<int>(L, ws, MOE_WS_RANK),
+                  ws_ptr<int>(L, ws, MOE_WS_POS), ws_ptr<int>(L, ws, MOE_WS_INV), ws_ptr<int>(L, ws, MOE_WS_ROWSRC));
   }
 }
 

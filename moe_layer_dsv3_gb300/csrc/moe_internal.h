@@ -71,9 +71,29 @@ inline T* wq_ptr(const WLayout& L, void* wq, int which) {
   return reinterpret_cast<T*>(static_cast<char*>(wq) + L.off[which]);
 }
 
+// Per-device caches are indexed by the device ordinal, below this bound.
+constexpr int kMaxDev = 64;
+// Current device ordinal, or -1 when it cannot be read or is past kMaxDev.
+int current_device();
+// SM count of the current device (cached per device).
 int num_sms();
-// Current device is compute capability 10.3 (GB300).
+// Current device is compute capability 10.3 (GB300) (cached per device).
 bool arch_ok();
+
+// ---------------------------------------------------------------- call errors
+// An entry point collects the return codes of its own kernel launches and
+// stream operations in a slot of the calling host thread, so its result
+// reflects only those calls: an error that other code left in the CUDA
+// runtime's last-error state is neither read nor cleared by the library.
+cudaError_t& call_error();
+inline void note(cudaError_t e) {
+  if (e != cudaSuccess && call_error() == cudaSuccess) call_error() = e;
+}
+// Opened at the top of an entry point: clears the slot; status() reads it.
+struct CallScope {
+  CallScope() { call_error() = cudaSuccess; }
+  int status() const { return call_error() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+};
 
 // ---------------------------------------------------------------- quantisers
 // Row-wise MX quantisation of bf16 src[rows][K] (row pitch ld elements).
@@ -87,7 +107,9 @@ void launch_quant_cols(const void* src, int64_t rows, int K, int64_t ld, int64_t
                        uint8_t* sf, bool tiled, int batch, cudaStream_t s);
 
 // ---------------------------------------------------------------- router
-void launch_router_logits(const Dims& m, const void* x, const void* w_router, float* logits, cudaStream_t s);
+// Returns an MOE_* code: host-side failures (tensor-map encoding, launch
+// attributes) come back here, since they launch nothing.
+int launch_router_logits(const Dims& m, const void* x, const void* w_router, float* logits, cudaStream_t s);
 void launch_router_topk(const Dims& m, const float* logits, const float* bias, int32_t* idx, float* w,
                         float* s_sel, cudaStream_t s);
 

@@ -161,8 +161,10 @@ long long moe_launch_count(void) { return moe::g_launches.load(); }
 
 int moe_selftest_wait_timeout(int* status, unsigned long long limit_ns, moe_stream_t stream) {
   if (status == nullptr || limit_ns == 0 || limit_ns > 10000000000ull) return MOE_ERR_INVALID_ARG;
-  moe::wait_timeout_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status, limit_ns);
-  return cudaPeekAtLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  moe::CallScope call;
+  moe::launch_kernel("selftest_wait", moe::wait_timeout_selftest_kernel, dim3(1), dim3(32), 0,
+                     static_cast<cudaStream_t>(stream), status, limit_ns);
+  return call.status();
 }
 
 }  // extern "C"

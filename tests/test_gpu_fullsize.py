@@ -22,7 +22,10 @@ from tests.helpers import np_f64, np_u8, rel_frob, untile_scales
 pytestmark = pytest.mark.gpu
 TOL = 1e-3
 
-WORKLOADS = [("small", None), ("dsv3_fwd", None), ("dsv3_zipf", None), ("e384", 2368), ("e384", 65536)]
+# Every configuration of the workload set, the 384-expert shape at each token count of
+# its sweep (a few rows per expert at T = 512 up to 1.5K per expert at T = 65536).
+WORKLOADS = [("small", None), ("dsv3_fwd", None), ("dsv3_zipf", None)] + \
+    [("e384", T) for T in (512, 1024, 2368, 4096, 16384, 65536)]
 
 
 def _f64(t):

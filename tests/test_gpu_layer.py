@@ -16,10 +16,20 @@ from oracle import layer as OL
 from oracle import mxfp8
 from oracle import route as OR
 from oracle import schedule as OS
+from oracle.sigmoid import sigmoid_spec
 from tests.helpers import np_f64, np_u8, rel_frob, untile_scales
 
 pytestmark = pytest.mark.gpu
+# Tolerances (relative Frobenius error against the oracle rounded to bf16):
+#   TOL = 1e-3 for every stage fed identical quantised operands on both sides (the
+#   target's bar), and for the forward output y;
+#   5 * TOL for gradients taken end to end, where each side quantises its own
+#   intermediates (h, dGU): MX codes then differ in about 1e-5 of the elements, where
+#   GEMM rounding moves a value across an E4M3 rounding point, and each flip is worth
+#   up to one E4M3 step (1/16 relative); the flips compound through two dgrad GEMMs
+#   and the token-axis weight-gradient operands.
 TOL = 1e-3
+TOL_E2E_GRAD = 5 * TOL
 
 
 def _need_gpu():
@@ -123,12 +133,19 @@ def test_route_bit_exact(run):
     assert np.array_equal(w.view(np.uint32), run.f["w"].view(np.uint32))
     ssel = run.ws("SSEL", torch.float32, (m.T, m.k)).cpu().numpy()
     assert np.array_equal(ssel.view(np.uint32), run.f["s_sel"].view(np.uint32))
-    # end to end against the oracle's own (correctly rounded) logits: only near-ties may differ
+    # end to end against the oracle's own (correctly rounded) logits: a token may differ only
+    # where the oracle's selection boundary lies inside the GPU's own score perturbation, i.e.
+    # the margin between its k-th chosen and best unchosen v is at most twice the largest
+    # |v_gpu - v_oracle| of that token (a few ulp of v for logits within 1e-5)
     idx2, _, _, lg2 = OR.route(run.host["x"], run.host["w_router"], run.host["bias"], m.k, m.G, m.g_top)
     bad = np.flatnonzero((idx2 != idx).any(axis=1))
     if len(bad):
+        b32 = np.asarray(run.host["bias"], dtype=np.float32)[None, :]
+        v_gpu = (sigmoid_spec(run.logits[bad]) + b32).astype(np.float32).astype(np.float64)
+        v_orc = (sigmoid_spec(lg2[bad]) + b32).astype(np.float32).astype(np.float64)
+        delta = np.abs(v_gpu - v_orc).max(axis=1)
         margin = OR.selection_margin(lg2[bad], run.host["bias"], idx2[bad], m.G, m.g_top)
-        assert np.all(margin < 1e-5), margin
+        assert np.all(margin <= 2 * delta), (margin, delta)
 
 
 def test_schedule_bit_exact(run):
@@ -360,16 +377,34 @@ def test_wgrad_stage(run):
         assert rel_frob(ggu, ref_gu) < TOL, e
 
 
-def test_backward_end_to_end(run):
+def _assert_grads_end_to_end(run, b):
+    """Every gradient against an oracle backward, at the end-to-end bar (see TOL_E2E_GRAD)."""
     m = run.shape
-    b = run.b
-    assert rel_frob(np_f64(run.L.dx), b["dx"]) < TOL * 5
-    assert rel_frob(np_f64(run.L.dw_router), b["dw_router"]) < TOL * 5
-    assert rel_frob(np_f64(run.L.dw_d), b["dW_d"]) < TOL * 5
-    assert rel_frob(np_f64(run.L.dw_gu), b["dW_gu"]) < TOL * 5
+    assert rel_frob(np_f64(run.L.dx), b["dx"]) < TOL_E2E_GRAD
+    assert rel_frob(np_f64(run.L.dw_router), b["dw_router"]) < TOL_E2E_GRAD
+    assert rel_frob(np_f64(run.L.dw_d), b["dW_d"]) < TOL_E2E_GRAD
+    assert rel_frob(np_f64(run.L.dw_gu), b["dW_gu"]) < TOL_E2E_GRAD
     if m.S:
-        assert rel_frob(np_f64(run.L.dws_d[:m.S]), b["dWs_d"]) < TOL * 5
-        assert rel_frob(np_f64(run.L.dws_gu[:m.S]), b["dWs_gu"]) < TOL * 5
+        assert rel_frob(np_f64(run.L.dws_d[:m.S]), b["dWs_d"]) < TOL_E2E_GRAD
+        assert rel_frob(np_f64(run.L.dws_gu[:m.S]), b["dWs_gu"]) < TOL_E2E_GRAD
+
+
+def test_backward_end_to_end(run):
+    _assert_grads_end_to_end(run, run.b)
+
+
+def test_end_to_end_on_oracle_own_logits(run):
+    """The whole chain against an oracle that routes from its own correctly rounded fp64
+    logits, so no value the GPU computed enters the reference: identical expert indices,
+    gates within the logit difference, y within TOL and every gradient within the
+    end-to-end bar."""
+    m = run.shape
+    f = OL.layer_forward(run.host, m)
+    b = OL.layer_backward(f, run.host, m)
+    assert np.array_equal(run.L.topk_idx.cpu().numpy(), f["idx"])
+    assert rel_frob(run.L.topk_w.cpu().numpy(), f["w"]) < 1e-5
+    assert rel_frob(np_f64(run.L.y), f["y"]) < TOL
+    _assert_grads_end_to_end(run, b)
 
 
 def test_router_backward_stage(run):

@@ -139,3 +139,42 @@ def test_token_axis_zero_padding():
 def test_rejects_ragged_axis():
     with pytest.raises(ValueError):
         mxfp8.quantize(np.ones((2, 33)))
+
+
+def _block_closed_form(col):
+    """One 32-element block by the format's closed form, element by element in
+    Python scalars: scale byte from the exponent of amax, codes by nearest search."""
+    import math
+    amax = max(abs(float(v)) for v in col)
+    if amax == 0.0:
+        return np.zeros(32, np.uint8), 0
+    e = math.frexp(amax)[1] - 1                     # floor(log2 amax)
+    byte = min(max(e - 8 + 127, 0), 254)
+    X = 2.0 ** (byte - 127)
+    return _brute_encode(np.array([float(v) / X for v in col])), byte
+
+
+@pytest.mark.parametrize("n", [1, 31, 32, 33, 45, 96])
+def test_layer_token_axis_quantiser_against_closed_form(n):
+    """oracle.layer.tokq -- the token-axis MX of one expert's rank-ordered rows that
+    every weight-gradient reference uses -- against blocks of 32 consecutive ranks of
+    one column, zero-padded past the last rank, each quantised by the closed form."""
+    from oracle import layer as OL
+    rng = np.random.default_rng(n)
+    rows = rng.normal(size=(n, 64)) * np.exp2(rng.integers(-12, 12, (1, 64)))
+    rows[:, 5] = 0.0                                 # an all-zero column
+    q = OL.tokq(rows, exact=False)
+    n_pad = -(-n // 32) * 32
+    assert q.codes.shape == (64, n_pad) and q.scales.shape == (64, n_pad // 32)
+    for c in range(64):
+        col = np.zeros(n_pad)
+        col[:n] = rows[:, c]
+        for b in range(n_pad // 32):
+            codes, byte = _block_closed_form(col[32 * b:32 * b + 32])
+            assert np.array_equal(q.codes[c, 32 * b:32 * b + 32], codes), (c, b)
+            assert q.scales[c, b] == byte, (c, b)
+    assert not q.codes[:, n:].any()                  # padding ranks quantise to +0
+    deq = mxfp8.e4m3_decode(q.codes) * np.exp2(np.repeat(q.scales.astype(np.float64), 32, axis=1) - 127)
+    assert np.array_equal(q.val, deq)
+    ex = OL.tokq(rows, exact=True)                   # exact mode: the padded transpose itself
+    assert np.array_equal(ex.val[:, :n], rows.T) and not ex.val[:, n:].any()

@@ -3,6 +3,7 @@ import itertools
 import math
 
 import numpy as np
+import pytest
 
 from oracle import route as R
 from oracle import sigmoid as SG
@@ -137,3 +138,38 @@ def test_selection_margin_positive_for_strict_choice():
     b = np.zeros(16, np.float32)
     idx, _, _ = R.select(lg, b, 2)
     assert np.all(R.selection_margin(lg, b, idx) >= 0)
+
+
+def _brute_select_f64(v, k, G, g_top):
+    """Dominance search as in _brute_select, with fp64 group scores."""
+    E = v.shape[0]
+    per = E // G
+    allowed = list(range(E))
+    if G > 1:
+        gs = [max(v[g * per + a] + v[g * per + b] for a, b in itertools.combinations(range(per), 2))
+              for g in range(G)]
+        kept = next(c for c in itertools.combinations(range(G), g_top)
+                    if all(_dominates(gs[a], a, gs[b], b) for a in c for b in range(G) if b not in c))
+        allowed = [e for e in range(E) if e // per in kept]
+    chosen = next(c for c in itertools.combinations(allowed, k)
+                  if all(_dominates(v[a], a, v[b], b) for a in c for b in allowed if b not in c))
+    return sorted(chosen, key=lambda e: (-float(v[e]), e))
+
+
+@pytest.mark.parametrize("E,G,g_top,k", [(8, 1, 1, 2), (16, 4, 2, 4), (12, 3, 1, 3)])
+def test_select_f64_brute_force(E, G, g_top, k):
+    """The exact-mode (fp64, textbook sigmoid) selection used by the finite-difference
+    pins, against an exhaustive dominance search over expert and group subsets, with the
+    scores and gates checked against their definitions element by element."""
+    rng = np.random.default_rng(E + G)
+    lg = rng.normal(0, 2, (120, E))
+    lg[:10, 1] = lg[:10, 2]                           # exact score ties
+    b = rng.normal(0, 0.1, E)
+    b[1] = b[2]
+    idx, w, s = R.select_f64(lg, b, k, G, g_top)
+    for t in range(120):
+        v = np.array([1.0 / (1.0 + math.exp(-lg[t, e])) + b[e] for e in range(E)])
+        assert list(idx[t]) == _brute_select_f64(v, k, G, g_top), t
+        ssel = [1.0 / (1.0 + math.exp(-lg[t, e])) for e in idx[t]]
+        assert np.allclose(s[t], ssel, rtol=1e-15, atol=0)
+        assert np.allclose(w[t], np.array(ssel) / math.fsum(ssel), rtol=1e-15, atol=0)
