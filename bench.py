@@ -10,8 +10,8 @@ One step = route -> schedule -> forward -> backward of one synthetic batch
 N > 1 runs under torch.distributed.run, one rank per GPU, each rank an
 independent replica of the layer on its own batch ("replicas only": the
 layer has no exchange step on one GPU, so no collective is on the data path;
-scaling is weak). `--impl reference` times the CPU oracle on a bounded
-sample of the same workload on the host cores.
+scaling is weak). `--impl reference` times the C++ fp64 CPU oracle on a
+bounded sample of the same workload on all host cores.
 """
 from __future__ import annotations
 
@@ -151,19 +151,22 @@ def gemm_flops(shape):
 
 
 def hbm_bytes(shape):
-    """Algorithmic bytes per step of the memory-bound kernels (read + write, once)."""
+    """Algorithmic bytes per step of the memory-bound kernels: every tensor a
+    kernel needs read once and every output written once. A gather reads each
+    source row once however many rows it is copied to (the repeats come from
+    L2), so its bytes are the source once plus the gathered rows written."""
     T, d, k, S, E = shape.T, shape.d, shape.k, shape.S, shape.E
     Rr = T * k                    # routed rows (ring traffic)
     R = T * (k + S)
     row_q = d + d // 32           # one MX row (codes + scales)
     return {
-        "permute_lap": 2.0 * Rr * row_q,
+        "permute_lap": T * row_q + Rr * row_q,
         "combine": T * (k + S) * d * 2.0 + T * k * 4.0 + T * d * 2.0,
         "rev_combine_dw": T * k * d * 2.0 + T * d * 2.0 + T * k * 12.0,
-        "permute_lap_dO": 2.0 * Rr * row_q,
+        "permute_lap_dO": T * row_q + Rr * row_q,
         "reverse_dispatch": T * (k + S) * d * 2.0 + T * k * 12.0 + T * d * 2.0,
-        "tok_gather_x": R * d * 2.0 + R * row_q,
-        "tok_gather_dO": R * d * 2.0 + R * row_q,
+        "tok_gather_x": T * d * 2.0 + R * row_q,
+        "tok_gather_dO": T * d * 2.0 + R * row_q,
         "quant_rows": 2 * (T * d * 2.0 + T * row_q),          # MX(x) forward, MX(dy) backward
         # dh fp32 and saved g|u bf16 in; dGU codes + scales out along 2I and along ranks
         "swiglu_bwd_quant": R * (shape.I * 4.0 + 2 * shape.I * 2.0 + 2 * (2 * shape.I + 2 * shape.I / 32.0)),
@@ -217,8 +220,9 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- CPU oracle sample
-def oracle_sample(shape, host, idx_full=None, n_experts=2, shared_rows=256, seed=0):
-    """Time the CPU oracle on a bounded sample of one layer step and extrapolate.
+def oracle_sample(shape, host, idx_full=None, w_full=None, n_experts=2, shared_rows=256, seed=0, nthreads=0):
+    """Time the C++ fp64 oracle (oracle/cpp, std::thread over `nthreads` host
+    cores) on a bounded sample of one layer step and extrapolate.
 
     Sample: router logits + selection for 1024 tokens, the schedule of all
     tokens, the full forward+backward of `n_experts` routed experts of
@@ -228,66 +232,57 @@ def oracle_sample(shape, host, idx_full=None, n_experts=2, shared_rows=256, seed
     MX quantisation is done before timing (it is not part of a layer step).
     Returns (tokens/s, description).
     """
-    from oracle import layer as OL
-    from oracle import mxfp8
-    from oracle import route as OR
-    from oracle import schedule as OS
+    from oracle import cxx
 
     T, d, E, k, I, S = shape.T, shape.d, shape.E, shape.k, shape.I, shape.S
-    x = host["x"]
+    x, dy = host["x"], host["dy"]
     nt = min(1024, T)
     t0 = time.perf_counter()
-    idx_s, w_s, s_s, lg = OR.route(x[:nt], host["w_router"], host["bias"], k, shape.G, shape.g_top)
+    idx_s, w_s, s_s, _ = cxx.route(x[:nt], host["w_router"], host["bias"], k, shape.G, shape.g_top, nthreads)
     t_route = (time.perf_counter() - t0) * T / nt
     if idx_full is None:
-        idx_full, _, _, _ = OR.route(x, host["w_router"], host["bias"], k, shape.G, shape.g_top)
+        idx_full, w_full, _, _ = cxx.route(x, host["w_router"], host["bias"], k, shape.G, shape.g_top, nthreads)
     t0 = time.perf_counter()
-    sch = OS.schedule(idx_full, E, shape.C)
+    sch = cxx.schedule(idx_full, E, shape.C)
     t_sched = time.perf_counter() - t0
     counts = sch["counts"]
     order = np.argsort(np.abs(counts - counts.mean()), kind="stable")
     experts = [int(e) for e in order[:n_experts] if counts[e] > 0]
     rng = np.random.default_rng(seed)
-    wcache = host.setdefault("_weights", {})      # MX weights are prepared once, outside the timing
+    wcache = host.setdefault("_cxx_weights", {})     # MX weights are prepared once, outside the timing
 
     def expert_weights(e):
         if e not in wcache:
             if e < E:
-                wcache[e] = OL.ExpertWeights(host["w_gu_of"](e), host["w_d_of"](e))
+                wcache[e] = cxx.ExpertWeights(host["w_gu_of"](e), host["w_d_of"](e), nthreads)
             else:
-                wcache[e] = OL.ExpertWeights(host["ws_gu_of"](e - E), host["ws_d_of"](e - E))
+                wcache[e] = cxx.ExpertWeights(host["ws_gu_of"](e - E), host["ws_d_of"](e - E), nthreads)
         return wcache[e]
 
+    wflat = np.asarray(w_full, dtype=np.float32).reshape(-1)
     prepared = []
     for e in experts:
-        prepared.append(("routed", e, expert_weights(e), OS.expert_rows(sch, e) // k))
+        a = sch["inv"][sch["offsets"][e]:sch["offsets"][e + 1]]
+        prepared.append((e, expert_weights(e), a // k, wflat[a]))
     if S:
         toks = np.sort(rng.choice(T, min(shared_rows, T), replace=False))
-        prepared.append(("shared", E, expert_weights(E), toks))
-    dy = host["dy"]
+        prepared.append((E, expert_weights(E), toks, None))
     rows_done = 0
     t0 = time.perf_counter()
-    for kind, e, W, toks in prepared:
-        xq = OL.Q(x[toks], 1, False)
-        r = OL.expert_forward(xq.val, W)
-        dO = dy[toks].astype(np.float32).astype(np.float64)
-        dOq = OL.Q(dO, 1, False)
-        b = OL.expert_backward(dOq.val, r["gu_saved"], W)
-        OL.wgrad(OL.tokq(dO, False), OL.tokq(r["h"], False))
-        OL.wgrad(OL.tokq(b["dgu"], False), OL.tokq(x[toks], False))
+    for e, W, toks, gate in prepared:
+        cxx.expert_q(x[toks], dy[toks], gate, W, nthreads)
         rows_done += len(toks)
     t_exp = time.perf_counter() - t0
     R = T * (k + S)
     t0 = time.perf_counter()
-    O = np.zeros((nt, k, d))
-    OL.combine(w_s, O, np.zeros((nt, d)))
-    OL.router_backward(np.zeros((nt, k)), w_s, s_s, idx_s, x[:nt], host["w_router"], E)
+    cxx.combine(w_s, np.zeros((nt, k, d)), np.zeros((nt, d)) if S else None)
+    cxx.router_backward(np.zeros((nt, k)), w_s, s_s, idx_s, x[:nt], host["w_router"], E)
     t_comb = (time.perf_counter() - t0) * T / nt
     total = t_route + t_sched + t_exp * R / max(rows_done, 1) + t_comb
-    desc = ("router on %d tokens, schedule of all %d tokens, fwd+bwd of %d routed experts (%d rows) and the "
-            "shared expert on %d tokens, combine/router-bwd on %d tokens; extrapolated to the %d-row step"
-            % (nt, T, len(experts), rows_done - (len(prepared[-1][3]) if S else 0), len(prepared[-1][3]) if S else 0,
-               nt, R))
+    n_shared_rows = len(prepared[-1][2]) if S else 0
+    desc = ("C++ fp64 oracle, %d threads: router on %d tokens, schedule of all %d tokens, fwd+bwd of %d routed "
+            "experts (%d rows) and the shared expert on %d tokens, combine/router-bwd on %d tokens; extrapolated to "
+            "the %d-row step" % (nthreads, nt, T, len(experts), rows_done - n_shared_rows, n_shared_rows, nt, R))
     return T / total, desc
 
 
@@ -344,12 +339,15 @@ def run_reference(args, rank, world):
     host["w_d_of"] = lambda e: wgen(e + 5000, (shape.d, shape.I))
     host["ws_gu_of"] = lambda e: wgen(e, (2 * shape.I, shape.d), True)
     host["ws_d_of"] = lambda e: wgen(e + 5000, (shape.d, shape.I), True)
-    from oracle import route as OR
-    idx_full, _, _, _ = OR.route(host["x"], host["w_router"], host["bias"], shape.k, shape.G, shape.g_top)
+    from oracle import cxx
+    nthreads = cores()
+    idx_full, w_full, _, _ = cxx.route(host["x"], host["w_router"], host["bias"], shape.k, shape.G, shape.g_top,
+                                       nthreads)
     vals = []
     desc = ""
     for i in range(args.warmup + args.steps):
-        v, desc = oracle_sample(shape, host, idx_full=idx_full, n_experts=1, shared_rows=128, seed=i)
+        v, desc = oracle_sample(shape, host, idx_full=idx_full, w_full=w_full, n_experts=1, shared_rows=128, seed=i,
+                                nthreads=nthreads)
         if i >= args.warmup:
             vals.append(v)
     val = statistics.median(vals)
@@ -357,7 +355,7 @@ def run_reference(args, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * shape.T / val,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(shape),
-            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores(), "kind": "oracle", "sample": desc},
+            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": nthreads, "kind": "oracle", "sample": desc},
             "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -433,7 +431,8 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     shape = _shape(args)
     inp = gen.make_inputs(shape, seed=rank, device="cuda")
-    L = MoELayer.from_shape(shape, flags=M.MOE_FLAG_LAP_LAUNCHES if args.lap_launches else 0)
+    flags = (M.MOE_FLAG_LAP_LAUNCHES if args.lap_launches else 0) | (M.MOE_FLAG_WGRAD_PAIR if args.wgrad_pair else 0)
+    L = MoELayer.from_shape(shape, flags=flags)
     L.quantize_weights(inp["w_gu"], inp["w_d"], inp["ws_gu"], inp["ws_d"])
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
@@ -624,7 +623,7 @@ def run_ours(args, rank, world, local_rank):
     if world == 1 and not args.no_cpu_baseline:
         host = host_inputs_for_oracle(shape, inp)
         idx = L.topk_idx.cpu().numpy()
-        v, desc = oracle_sample(shape, host, idx_full=idx)
+        v, desc = oracle_sample(shape, host, idx_full=idx, w_full=L.topk_w.cpu().numpy(), nthreads=cores())
         cpu = {"value": v, "unit": "tokens/s", "cores": cores(), "kind": "oracle", "sample": desc}
     counts = L.ws_tensor("COUNTS", torch.int32, (shape.E + shape.S,)).cpu().numpy()[:shape.E]
     # Waves of each grouped GEMM: output tiles / SM count (the commentary's rule asks for >= 2).
@@ -647,7 +646,8 @@ def run_ours(args, rank, world, local_rank):
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "mxfp8", "data": "synthetic (seeded, random-init weights)",
         "config": dict(workload_config(shape),
-                       ring_laps="per-lap launches" if args.lap_launches else "one launch, mover warps"),
+                       ring_laps="per-lap launches" if args.lap_launches else "one launch, mover warps",
+                       wgrad_tiles="CTA pairs 256-row" if args.wgrad_pair else "single CTA 128x256"),
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": job_tokens_per_s(shape.T, world, ms_e2e), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
@@ -684,6 +684,8 @@ def main():
                     help="skip the extra per-lap pass that times the ring movers as their own launches")
     ap.add_argument("--lap-launches", action="store_true",
                     help="one mover launch + one GEMM launch per ring lap instead of one all-laps launch")
+    ap.add_argument("--wgrad-pair", action="store_true",
+                    help="weight gradients on CTA pairs (256-row tiles) instead of single-CTA tiles (for comparison)")
     ap.add_argument("--probe-peak", action="store_true",
                     help="measure dense MXFP8 GEMM throughput (library and this repo's plain GEMM) and exit")
     ap.add_argument("--probe-n", type=int, default=8192)

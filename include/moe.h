@@ -81,7 +81,7 @@ enum {
 typedef struct moe_config {
   int T, d, E, k, n_groups, topk_groups, I, n_shared;
   int capacity;
-  int flags; /* 0 or MOE_FLAG_LAP_LAUNCHES; other bits are rejected */
+  int flags; /* MOE_FLAG_* bits below; other bits are rejected */
 } moe_config_t;
 
 /* Ring-lap execution. By default each ring direction (forward GEMM1, backward
@@ -92,6 +92,16 @@ typedef struct moe_config {
  * is instead a mover launch followed by a GEMM launch, laps alternating
  * between two streams. Both give bitwise-identical results. */
 #define MOE_FLAG_LAP_LAUNCHES 1
+
+/* Weight gradients. By default each weight-gradient GEMM runs on single-CTA
+ * 128 x 256 tiles (one persistent CTA per SM). With this flag they run on CTA
+ * pairs instead, wherever the gradient's row count (d for dW_d, 2I for dW_gu)
+ * is a multiple of 256: clusters of two CTAs on two SMs compute 256 x 256
+ * (or 256 x 128) output tiles with tcgen05 .cta_group::2 MMAs, each SM
+ * staging half of the tile's B rows. Both forms give the same bytes (the same
+ * products summed in the same K order). The pair form is the faster product
+ * on long K but the slower weight gradient at this layer's per-expert K. */
+#define MOE_FLAG_WGRAD_PAIR 2
 
 /* Bytes of workspace the layer needs for this shape (schedule, saved
  * activations for backward, ring buffers, staging). */
@@ -291,6 +301,16 @@ MOE_API int moe_wq_view(const moe_config_t* cfg, void* wq, int which, void** ptr
  *   (moe_scales_to_tiled). M, N, K multiples of 128. */
 MOE_API int moe_gemm_mxfp8(int M, int N, int K, const void* a, const void* a_sf, const void* b, const void* b_sf, float* c,
                    moe_stream_t stream);
+
+/* moe_gemm_mxfp8 on CTA pairs (exposed for testing; the kernel of the
+ * MOE_FLAG_WGRAD_PAIR weight gradients). Clusters of two CTAs on two SMs
+ * compute 256 x 256 tiles (256 x 128 when N is not a multiple of 256) with
+ * tcgen05 .cta_group::2 MMAs issued by the even CTA; each CTA stages its 128
+ * rows of A and half of the tile's rows of B, two 128-element K atoms per
+ * pipeline stage. Same operands and result as moe_gemm_mxfp8; M a multiple
+ * of 256, N and K of 128. */
+MOE_API int moe_gemm_mxfp8_pair(int M, int N, int K, const void* a, const void* a_sf, const void* b,
+                                const void* b_sf, float* c, moe_stream_t stream);
 
 /* Re-lay canonical scales [rows][K/32] into the tiled layout the tensor
  * cores read: 512-byte atoms of 128 rows x 4 blocks, atom (r/128, kb/4) at

@@ -73,6 +73,7 @@ _SIGS = {
     "moe_ws_view": [_CFG, _P, _I, ctypes.POINTER(_P), _SZ],
     "moe_wq_view": [_CFG, _P, _I, ctypes.POINTER(_P), _SZ],
     "moe_gemm_mxfp8": [_I, _I, _I, _P, _P, _P, _P, _P, _P],
+    "moe_gemm_mxfp8_pair": [_I, _I, _I, _P, _P, _P, _P, _P, _P],
     "moe_scales_to_tiled": [_P, _I, _I, _P, _P],
     "moe_profile_enable": [_I],
     "moe_profile_read": [ctypes.c_void_p, _I, ctypes.POINTER(_I)],
@@ -104,6 +105,7 @@ def _p(x):
 
 
 MOE_FLAG_LAP_LAUNCHES = 1   # one mover launch + one GEMM launch per ring lap instead of one launch for all laps
+MOE_FLAG_WGRAD_PAIR = 2     # weight gradients on CTA pairs (256-row tiles) instead of single-CTA 128 x 256 tiles
 
 
 def config(T, d, E, k, n_groups=1, topk_groups=1, I=128, n_shared=0, capacity=0, flags=0) -> MoeConfig:
@@ -183,6 +185,11 @@ def moe_wq_view(cfg, wq, which):
 
 def moe_gemm_mxfp8(M, N, K, a, a_sf, b, b_sf, c, stream=0):
     _check("moe_gemm_mxfp8", _lib.moe_gemm_mxfp8(M, N, K, _p(a), _p(a_sf), _p(b), _p(b_sf), _p(c), _p(stream)))
+
+
+def moe_gemm_mxfp8_pair(M, N, K, a, a_sf, b, b_sf, c, stream=0):
+    _check("moe_gemm_mxfp8_pair",
+           _lib.moe_gemm_mxfp8_pair(M, N, K, _p(a), _p(a_sf), _p(b), _p(b_sf), _p(c), _p(stream)))
 
 
 def moe_scales_to_tiled(canon, rows, K, tiled, stream=0):

@@ -126,7 +126,7 @@ int validate(const moe_config_t* c) {
   if (c->n_groups > 1 && (c->E / c->n_groups < 2 || c->k > c->topk_groups * (c->E / c->n_groups)))
     return MOE_ERR_INVALID_ARG;
   if (c->capacity < 0 || c->capacity % 128) return MOE_ERR_INVALID_ARG;
-  if (c->flags & ~MOE_FLAG_LAP_LAUNCHES) return MOE_ERR_INVALID_ARG;
+  if (c->flags & ~(MOE_FLAG_LAP_LAUNCHES | MOE_FLAG_WGRAD_PAIR)) return MOE_ERR_INVALID_ARG;
   const int64_t Ap = static_cast<int64_t>(c->T) * (c->k + c->n_shared);
   if (Ap + 128LL * (c->E + c->n_shared) >= (1LL << 31)) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
@@ -611,7 +611,15 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
   if (ls == nullptr) return MOE_ERR_CUDA;
   std::lock_guard<std::mutex> lk(ls->mu);
   note(cudaEventRecord(ls->fork, s));
-  if (int r = gemm_dispatch("gemm_wgrad_d", kWgrad, m, 0, m.I, 0, m.d, opw, epw, counts, poff, lap_tiles, row_src, status, s, 256, ws_ptr<int>(L, ws, MOE_WS_ORDER))) return r;
+  // Weight gradients on single-CTA 128 x 256 tiles, or on CTA pairs (256-row
+  // tiles) when asked for and the output rows allow it.
+  const bool pair_d = (cfg->flags & MOE_FLAG_WGRAD_PAIR) && m.d % kPairRows == 0;
+  const bool pair_gu = (cfg->flags & MOE_FLAG_WGRAD_PAIR) && (2 * m.I) % kPairRows == 0;
+  const int* order = ws_ptr<int>(L, ws, MOE_WS_ORDER);
+  if (int r = pair_d ? gemm_pair_dispatch("gemm_wgrad_d", kWgrad, m, m.I, m.d, 0, opw, epw, poff, order, status, s)
+                     : gemm_dispatch("gemm_wgrad_d", kWgrad, m, 0, m.I, 0, m.d, opw, epw, counts, poff, lap_tiles,
+                                     row_src, status, s, 256, order))
+    return r;
   note(cudaStreamWaitEvent(ls->aux[0], ls->fork, 0));
   launch_reverse_dispatch(m, topk_idx, w_router, L, ws, dx, ls->aux[0]);
   launch_router_dwr(m, L, ws, dw_router, ls->aux[0]);
@@ -625,8 +633,10 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
   epw.out = dw_gu;
   epw.out2 = dws_gu;
   epw.ldo = m.d;
-  const int r = gemm_dispatch("gemm_wgrad_gu", kWgrad, m, 0, m.d, 0, 2 * m.I, opw, epw, counts, poff, lap_tiles,
-                              row_src, status, s, 256, ws_ptr<int>(L, ws, MOE_WS_ORDER));
+  const int r = pair_gu ? gemm_pair_dispatch("gemm_wgrad_gu", kWgrad, m, m.d, 2 * m.I, 0, opw, epw, poff, order,
+                                             status, s)
+                        : gemm_dispatch("gemm_wgrad_gu", kWgrad, m, 0, m.d, 0, 2 * m.I, opw, epw, counts, poff,
+                                        lap_tiles, row_src, status, s, 256, order);
   note(cudaStreamWaitEvent(s, ls->join[0], 0));
   if (r) return r;
   return call.status();

@@ -35,6 +35,15 @@ namespace moe {
 
 constexpr int kRouterMode = 5;   // bf16 x bf16 router logits
 
+// Host-side tensor-map helpers (k_gemm.cu).
+bool get_encode();
+// 2-D K-major operand [rows][cols] (1- or 2-byte elements), box 128 bytes x box_rows, 128-byte swizzle.
+bool make_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows, bool bf16);
+// 2-D bf16 output [rows][cols] written by TMA stores, box 64 columns x 128 rows, 128-byte swizzle.
+bool make_tmap_out(CUtensorMap* m, void* base, int64_t rows, int64_t cols);
+// Tiled scale array as uint32 [atoms][128]: one box = one 512-byte scale atom.
+bool make_tmap_sf(CUtensorMap* m, const void* base, int64_t atoms);
+
 // The epilogue / tile shape a mode shares with its per-lap form.
 __host__ __device__ constexpr int base_mode(int mode) {
   return mode == kSwigluFwdRing ? kSwigluFwd : (mode == kSwigluBwdRing ? kSwigluBwd : mode);

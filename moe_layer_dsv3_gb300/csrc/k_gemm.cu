@@ -10,9 +10,9 @@
 namespace moe {
 
 namespace {
-
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
+}  // namespace
 
 bool get_encode() {
   std::call_once(g_encode_once, [] {
@@ -50,6 +50,20 @@ bool make_tmap_out(CUtensorMap* m, void* base, int64_t rows, int64_t cols) {
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+// Scale atoms of a tiled-scale array as a 2-D map of uint32 [atoms][128]: one
+// box = one 512-byte atom (128 rows x 4 blocks), selected by its row coordinate.
+bool make_tmap_sf(CUtensorMap* m, const void* base, int64_t atoms) {
+  cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(atoms)};
+  cuuint64_t strides[1] = {512};
+  cuuint32_t box[2] = {128, 1};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
 
 // Per device: 0 = not yet set up, 1 = ready, 2 = set-up failed.
 struct DevOnce {

@@ -17,6 +17,8 @@ constexpr int kRingBufs = 2;    // ring token buffers; lap L uses buffer L % kRi
 // tile holds matching g and u columns.
 constexpr int kGemm1BN = 256;
 constexpr int kGuBlock = kGemm1BN / 2;
+// Output rows of a CTA-pair GEMM tile (gemm_pair.cuh).
+constexpr int kPairRows = 256;
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
@@ -174,5 +176,11 @@ int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int
                   const GemmEpilogue& ep, const int* counts, const int* poff, const int* lap_tiles,
                   const int* row_src, int* status, cudaStream_t s, int bn_hint = 0, const int* order = nullptr,
                   const RingMovers* mv = nullptr);
+
+// The weight-gradient (kWgrad) or plain (kPlain, fp32 out) GEMM on CTA pairs:
+// 256 x 128 output tiles, tcgen05 MMAs issued for both SMs of a cluster of two
+// (gemm_pair.cuh). M a multiple of 256, N of 128; operands as for gemm_dispatch.
+int gemm_pair_dispatch(const char* name, int mode, const Dims& m, int N, int M, int K, const GemmOperands& op,
+                       const GemmEpilogue& ep, const int* poff, const int* order, int* status, cudaStream_t s);
 
 }  // namespace moe

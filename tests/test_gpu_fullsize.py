@@ -8,6 +8,8 @@ the GPU's own quantised operands: sampled tokens, and the rows, token-axis
 operands and weight-gradient rows of sampled experts (the busiest one, whose
 rows wrap the ring many times, a median one, and the shared expert).
 """
+import gc
+
 import numpy as np
 import pytest
 import torch
@@ -113,21 +115,24 @@ class Full:
         return self._w[e]
 
 
-_CACHE = {}
+def _release_device_memory():
+    gc.collect()
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
 
 
 @pytest.fixture(scope="module", params=WORKLOADS, ids=lambda p: "%s-%s" % p)
 def full(request):
+    """One workload on the device at a time: the previous one is released before this
+    one is built (a 384-expert layer holds about 100 GB: weights, MX weights, gradients)."""
     if not torch.cuda.is_available():
         pytest.skip("no GPU")
-    key = request.param
-    for k in list(_CACHE):           # keep one workload on the device at a time
-        if k != key:
-            del _CACHE[k]
-    torch.cuda.empty_cache()
-    if key not in _CACHE:
-        _CACHE[key] = Full(*key)
-    return _CACHE[key]
+    _release_device_memory()
+    f = Full(*request.param)
+    yield f
+    f.L = f.inp = f._w = None
+    del f
+    _release_device_memory()
 
 
 def test_status_and_route(full):
@@ -356,4 +361,25 @@ def test_lap_launch_form_bitwise(full):
     for name in ("y", "dx", "dw_router", "dw_gu", "dw_d", "dws_gu", "dws_d"):
         assert torch.equal(getattr(L, name).view(torch.int16), getattr(Lp, name).view(torch.int16)), name
     del Lp
+    torch.cuda.empty_cache()
+
+
+def test_wgrad_pair_form_bitwise(full):
+    """At the benchmark workload, the CTA-pair weight-gradient form (MOE_FLAG_WGRAD_PAIR)
+    gives the same gradient bytes as the default single-CTA form."""
+    if full.shape.name != "dsv3_zipf":
+        pytest.skip("the benchmark workload only (a second layer's gradients are 22.5 GB)")
+    import moe_layer_dsv3_gb300 as M
+    from moe_layer_dsv3_gb300.layer import MoELayer
+    s, i = full.shape, full.inp
+    L2 = MoELayer.from_shape(s, flags=M.MOE_FLAG_WGRAD_PAIR)
+    L2.wq = full.L.wq
+    L2.forward(i["x"], i["w_router"], i["bias"])
+    L2.backward(i["dy"])
+    torch.cuda.synchronize()
+    assert L2.status() == (0, 0)
+    L = full.L
+    for name in ("dw_gu", "dw_d", "dws_gu", "dws_d"):
+        assert torch.equal(getattr(L, name).view(torch.int16), getattr(L2, name).view(torch.int16)), name
+    del L2
     torch.cuda.empty_cache()

@@ -70,7 +70,7 @@ def test_scales_to_tiled(lib):
     assert np.array_equal(untile_scales(got, 256, 512), canon)
 
 
-def _gemm_case(lib, M, N, K, seed, unit_scales=False):
+def _gemm_case(lib, M, N, K, seed, unit_scales=False, pair=False):
     rng = np.random.default_rng(seed)
     a = rng.normal(0, 1, (M, K)) * np.exp2(rng.integers(-3, 4, (M, 1)))
     b = rng.normal(0, 1, (N, K)) * np.exp2(rng.integers(-3, 4, (N, 1)))
@@ -90,7 +90,8 @@ def _gemm_case(lib, M, N, K, seed, unit_scales=False):
     A, B = dev(aq), dev(bq)
     Asf, Bsf = dev(tile_scales(asf, M, K)), dev(tile_scales(bsf, N, K))
     C = torch.zeros((M, N), dtype=torch.float32, device="cuda")
-    lib.moe_gemm_mxfp8(M, N, K, A.data_ptr(), Asf.data_ptr(), B.data_ptr(), Bsf.data_ptr(), C.data_ptr())
+    fn = lib.moe_gemm_mxfp8_pair if pair else lib.moe_gemm_mxfp8
+    fn(M, N, K, A.data_ptr(), Asf.data_ptr(), B.data_ptr(), Bsf.data_ptr(), C.data_ptr())
     torch.cuda.synchronize()
     return C.cpu().numpy().astype(np.float64), ref
 
@@ -104,3 +105,30 @@ def test_gemm_unit_scales_single_tile(lib):
 def test_gemm_block_scaled(lib, M, N, K):
     got, ref = _gemm_case(lib, M, N, K, M + N + K)
     assert rel_frob(got, ref) < 1e-5, rel_frob(got, ref)
+
+
+def _block_errors(got, ref):
+    """Relative error per (128-row, 64-column) block: locates a wrong operand half."""
+    M, N = ref.shape
+    out = {}
+    for i in range(0, M, 128):
+        for j in range(0, N, 64):
+            out[(i, j)] = rel_frob(got[i:i + 128, j:j + 64], ref[i:i + 128, j:j + 64])
+    return out
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 128, 128), (512, 256, 384), (768, 384, 1024), (512, 512, 640)])
+def test_gemm_pair_block_scaled(lib, M, N, K):
+    """The CTA-pair GEMM (256-row tiles over two SMs, 256 or 128 columns, scales per row and
+    per 32-block, an odd number of K atoms so the last stage is partial) against the fp64
+    product of the dequantised operands, and against the one-CTA GEMM."""
+    got, ref = _gemm_case(lib, M, N, K, M + N + K, pair=True)
+    err = rel_frob(got, ref)
+    assert err < 1e-5, (err, {k: v for k, v in _block_errors(got, ref).items() if v > 1e-5})
+    one, _ = _gemm_case(lib, M, N, K, M + N + K)
+    assert rel_frob(got, one) < 1e-6
+
+
+def test_gemm_pair_unit_scales(lib):
+    got, ref = _gemm_case(lib, 256, 128, 128, 0, unit_scales=True, pair=True)
+    assert rel_frob(got, ref) < 1e-6, rel_frob(got, ref)

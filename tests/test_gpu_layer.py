@@ -450,6 +450,23 @@ def test_lap_launch_path_bitwise(run):
         assert torch.equal(L.ws_tensor(name), L2.ws_tensor(name)), name
 
 
+def test_wgrad_pair_matches_single_cta(run):
+    """Weight gradients on CTA pairs (MOE_FLAG_WGRAD_PAIR, where the gradient's row count is a
+    multiple of 256) and on single-CTA tiles (the default) give the same bytes: both sum the
+    same block-scaled products in the same K order."""
+    from moe_layer_dsv3_gb300 import MOE_FLAG_WGRAD_PAIR
+    from moe_layer_dsv3_gb300.layer import MoELayer
+    dev = run.dev
+    L2 = MoELayer.from_shape(run.shape, flags=MOE_FLAG_WGRAD_PAIR)
+    L2.wq = run.L.wq
+    L2.forward(dev["x"], dev["w_router"], dev["bias"])
+    L2.backward(dev["dy"])
+    torch.cuda.synchronize()
+    assert L2.status() == (0, 0)
+    for name in ("dw_gu", "dw_d", "dws_gu", "dws_d", "dx", "dw_router"):
+        assert torch.equal(getattr(run.L, name).view(torch.int16), getattr(L2, name).view(torch.int16)), name
+
+
 def test_idle_expert_weight_grads_zeroed(run):
     """Experts that received no token get exactly zero weight gradients (their fill runs on a side
     stream), whatever the output buffers held before; the other experts' gradients are unchanged."""
