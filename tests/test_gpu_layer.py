@@ -393,6 +393,20 @@ def test_backward_end_to_end(run):
     _assert_grads_end_to_end(run, run.b)
 
 
+def test_end_to_end_on_cxx_oracle(run):
+    """The whole chain against the C++ fp64 oracle routing from its own logits (nothing the
+    GPU computed enters it): identical expert indices, y within TOL, every gradient within
+    the end-to-end bar."""
+    from oracle import cxx
+    m = run.shape
+    c = cxx.layer(run.host, m)
+    assert np.array_equal(run.L.topk_idx.cpu().numpy(), c["idx"])
+    assert rel_frob(run.L.topk_w.cpu().numpy(), c["w"]) < 1e-5
+    assert rel_frob(np_f64(run.L.y), c["y"]) < TOL
+    _assert_grads_end_to_end(run, {"dx": c["dx"], "dw_router": c["dw_router"], "dW_d": c["dW_d"],
+                                   "dW_gu": c["dW_gu"], "dWs_d": c["dWs_d"], "dWs_gu": c["dWs_gu"]})
+
+
 def test_end_to_end_on_oracle_own_logits(run):
     """The whole chain against an oracle that routes from its own correctly rounded fp64
     logits, so no value the GPU computed enters the reference: identical expert indices,
