@@ -131,6 +131,16 @@ def probe_peak(args):
     ours["rel_err"] = float((c - a8.float() @ b8.float().t()).norm() / (a8.float() @ b8.float().t()).norm())
     ours["tflops_burst"], ours["tflops_sustained"] = timeit(fn)
     out["ours"] = ours
+    # this repo's NVFP4 GEMM (E2M1 codes, E4M3 scale per 16; all scales 1, alpha 1)
+    nv = {"name": "moe_gemm_nvfp4 (tcgen05 kind::mxf4nvf4.block_scale.scale_vec::4X, fp32 out)",
+          "shape": "M=N=K=%d" % n}
+    a4 = torch.randint(0, 256, (n, n // 2), dtype=torch.uint8, device=dev)
+    b4 = torch.randint(0, 256, (n, n // 2), dtype=torch.uint8, device=dev)
+    sf4 = torch.full((n * n // 16,), 0x38, dtype=torch.uint8, device=dev)     # E4M3 1.0
+    fn = lambda: M.moe_gemm_nvfp4(n, n, n, a4.data_ptr(), sf4.data_ptr(), b4.data_ptr(), sf4.data_ptr(),  # noqa: E731
+                                  1.0, c.data_ptr(), sp)
+    nv["tflops_burst"], nv["tflops_sustained"] = timeit(fn)
+    out["ours_nvfp4"] = nv
     out["clocks"] = clocks.stop()
     print(json.dumps(out), flush=True)
 

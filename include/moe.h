@@ -312,6 +312,31 @@ MOE_API int moe_gemm_mxfp8(int M, int N, int K, const void* a, const void* a_sf,
 MOE_API int moe_gemm_mxfp8_pair(int M, int N, int K, const void* a, const void* a_sf, const void* b,
                                 const void* b_sf, float* c, moe_stream_t stream);
 
+/* NVFP4 (exposed as a stand-alone quantiser and GEMM; the write-ups name
+ * NVFP4 training kernels beside the MXFP8 ones, Cursor blog summary, opening
+ * paragraph, and give no detail). Read as NVIDIA's 4-bit format: E2M1
+ * elements (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6), one E4M3 scale per 16
+ * elements along K, one fp32 scale g per tensor (g = amax / (6 * 448) is the
+ * usual choice; the caller supplies it). Every step is an IEEE binary32
+ * operation: sb = E4M3_RNE_satfinite(amax(block) / (6 g)),
+ * X = decode(sb) g, q = E2M1_RNE_satfinite(v / X) (0 when X = 0).
+ *   src: bf16 [rows][K], K a multiple of 16. codes: [rows][K/2] bytes, element
+ *   2i in the low nibble (8-byte aligned). scales: canonical [rows][K/16]
+ *   (tiled = 0) or the tiled layout of 512-byte atoms of 128 rows x 4 blocks
+ *   of 16 (tiled = 1; rows a multiple of 128, K of 64), byte offset
+ *   ((r/128)*(K/64) + kb/4)*512 + (r%32)*16 + (r/32%4)*4 + kb%4.
+ * Errors: MOE_ERR_INVALID_ARG (shapes, g <= 0, alignment), MOE_ERR_UNSUPPORTED_ARCH. */
+MOE_API int moe_quantize_nvfp4(const void* src_bf16, int rows, int K, float g, void* codes, void* scales, int tiled,
+                               moe_stream_t stream);
+
+/* NVFP4 GEMM on the tensor cores (tcgen05 kind::mxf4nvf4, scale_vec::4X):
+ * c[M][N] (fp32) = alpha * dequant(a)[M][K] . dequant(b)[N][K]^T, where a, b are
+ * packed E2M1 codes [rows][K/2] and a_sf, b_sf their E4M3 block scales in the
+ * tiled layout of moe_quantize_nvfp4; alpha is the product of the two tensor
+ * scales. M, N multiples of 128, K of 256; 16-byte aligned pointers. */
+MOE_API int moe_gemm_nvfp4(int M, int N, int K, const void* a, const void* a_sf, const void* b, const void* b_sf,
+                           float alpha, float* c, moe_stream_t stream);
+
 /* Re-lay canonical scales [rows][K/32] into the tiled layout the tensor
  * cores read: 512-byte atoms of 128 rows x 4 blocks, atom (r/128, kb/4) at
  * ((r/128)*(K/128) + kb/4)*512, byte (r%32)*16 + (r/32%4)*4 + kb%4.

@@ -74,6 +74,8 @@ _SIGS = {
     "moe_wq_view": [_CFG, _P, _I, ctypes.POINTER(_P), _SZ],
     "moe_gemm_mxfp8": [_I, _I, _I, _P, _P, _P, _P, _P, _P],
     "moe_gemm_mxfp8_pair": [_I, _I, _I, _P, _P, _P, _P, _P, _P],
+    "moe_quantize_nvfp4": [_P, _I, _I, ctypes.c_float, _P, _P, _I, _P],
+    "moe_gemm_nvfp4": [_I, _I, _I, _P, _P, _P, _P, ctypes.c_float, _P, _P],
     "moe_scales_to_tiled": [_P, _I, _I, _P, _P],
     "moe_profile_enable": [_I],
     "moe_profile_read": [ctypes.c_void_p, _I, ctypes.POINTER(_I)],
@@ -190,6 +192,16 @@ def moe_gemm_mxfp8(M, N, K, a, a_sf, b, b_sf, c, stream=0):
 def moe_gemm_mxfp8_pair(M, N, K, a, a_sf, b, b_sf, c, stream=0):
     _check("moe_gemm_mxfp8_pair",
            _lib.moe_gemm_mxfp8_pair(M, N, K, _p(a), _p(a_sf), _p(b), _p(b_sf), _p(c), _p(stream)))
+
+
+def moe_quantize_nvfp4(src, rows, K, g, codes, scales, tiled=True, stream=0):
+    _check("moe_quantize_nvfp4",
+           _lib.moe_quantize_nvfp4(_p(src), rows, K, float(g), _p(codes), _p(scales), int(bool(tiled)), _p(stream)))
+
+
+def moe_gemm_nvfp4(M, N, K, a, a_sf, b, b_sf, alpha, c, stream=0):
+    _check("moe_gemm_nvfp4",
+           _lib.moe_gemm_nvfp4(M, N, K, _p(a), _p(a_sf), _p(b), _p(b_sf), float(alpha), _p(c), _p(stream)))
 
 
 def moe_scales_to_tiled(canon, rows, K, tiled, stream=0):

@@ -66,6 +66,7 @@ struct GemmParams {
   int M;                 // plain / router / wgrad output rows per expert
   int static_tiles;      // tile count when it does not depend on the schedule
   void* out; void* out2; int ldo;
+  float alpha;           // NVFP4 plain mode: product of the operands' tensor scales
   uint8_t* q_rows; uint8_t* q_rows_sf; int q_rows_ktiles;
   uint8_t* q_tok; uint8_t* q_tok_sf; int64_t q_tok_pitch;
   __nv_bfloat16* gu; int I;
@@ -81,6 +82,9 @@ struct GemmParams {
 template <int BN, int MODE>
 struct GemmCfg {
   static constexpr bool kBf16 = MODE == kRouterMode;
+  // NVFP4: a 128-byte stage row holds 256 E2M1 values; the scales (one E4M3
+  // per 16) of a stage are 4 atoms per 128 rows, one atom per K = 64 MMA.
+  static constexpr bool kNv4 = MODE == kPlainNv4;
   // Weight gradients stage their bf16 output tile in shared memory and write
   // it with TMA stores, so the tile's DRAM write overlaps the next mainloop.
   static constexpr bool kTmaOut = MODE == kWgrad;
@@ -88,16 +92,18 @@ struct GemmCfg {
   static constexpr int kOutBytes = kTmaOut ? 128 * BN * 2 : 0;
   static constexpr int kABytes = 128 * 128;
   static constexpr int kBBytes = BN * 128;
-  static constexpr int kSfaBytes = kBf16 ? 0 : 512;
-  static constexpr int kSfbBytes = kBf16 ? 0 : (BN / 128) * 512;
+  static constexpr int kSfAtoms = kNv4 ? 4 : 1;                    // scale atoms per 128 rows per stage
+  static constexpr int kSfaBytes = kBf16 ? 0 : 512 * kSfAtoms;
+  static constexpr int kSfbBytes = kBf16 ? 0 : (BN / 128) * 512 * kSfAtoms;
   static constexpr int kTx = kABytes + kBBytes + kSfaBytes + kSfbBytes;
   static constexpr int kStageBytes = ((kTx + 1023) / 1024) * 1024;
-  static constexpr int kSfCols = kBf16 ? 0 : 4 + (BN / 128) * 4;   // TMEM columns of scales per stage
+  static constexpr int kSfCols = kBf16 ? 0 : kSfAtoms * (4 + (BN / 128) * 4);   // TMEM columns of scales per stage
   static constexpr int kSfCol0 = 256;
   // Accumulator buffers in TMEM: two when they fit below the scale columns, so
   // the epilogue of one tile overlaps the mainloop of the next.
   static constexpr int kNumAcc = (2 * BN <= kSfCol0) ? 2 : 1;
-  static constexpr int kKElems = kBf16 ? 64 : 128;                  // K elements per stage
+  static constexpr int kKElems = kBf16 ? 64 : (kNv4 ? 256 : 128);   // K elements per stage
+  static constexpr int kTmaX = kBf16 ? 64 : 128;                     // tensor-map x extent per stage (elements / bytes)
   static constexpr int kBarBytes = 256;
   static constexpr int kBase = base_mode(MODE);
   // Per epilogue warp, 32 x 33 fp32: the SwiGLU forward's transpose tile, or
@@ -559,6 +565,10 @@ __device__ __forceinline__ void gemm_epilogue_tile(const GemmParams& p, const Ti
     for (int c = 0; c < BN / 32; ++c) {
       float v[32];
       tmem_ld32(tacc + c * 32, v);
+      if constexpr (MODE == kPlainNv4) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(v[j], p.alpha);
+      }
       if (orow < p.M) {
         const int col0 = t.n0 + c * 32;
         if (col0 + 32 <= p.N && (p.ldo % 4) == 0) {
@@ -643,10 +653,18 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
           uint8_t* sb = sa + Cf::kABytes;
           mbar_arrive_expect_tx(&full[stage], Cf::kTx);
           const int kt = t.k0 + ks;
-          const int kx = kt * Cf::kKElems;
+          const int kx = kt * Cf::kTmaX;
           tma_load_2d(sa, t.use_a2 ? &tma_a2 : &tma_a, kx, static_cast<int>(t.a_row), &full[stage]);
           tma_load_2d(sb, &tma_b, kx, static_cast<int>(t.b_row), &full[stage]);
-          if constexpr (!Cf::kBf16) {
+          if constexpr (Cf::kNv4) {
+            // a stage's 4 atoms of one 128-row tile are contiguous (a_ktiles = atoms per row tile)
+            uint8_t* ssfa = sb + Cf::kBBytes;
+            bulk_load(ssfa, p.a_sf + ((t.a_row >> 7) * p.a_ktiles + kt * 4) * 512, 2048, &full[stage]);
+#pragma unroll
+            for (int j = 0; j < BN / 128; ++j)
+              bulk_load(ssfa + 2048 + 2048 * j, p.b_sf + (((t.b_row >> 7) + j) * p.b_ktiles + kt * 4) * 512, 2048,
+                        &full[stage]);
+          } else if constexpr (!Cf::kBf16) {
             uint8_t* ssfa = sb + Cf::kBBytes;
             const uint8_t* asf = (t.use_a2 ? p.a2_sf : p.a_sf) + ((t.a_row >> 7) * p.a_ktiles + kt) * 512;
             bulk_load(ssfa, asf, 512, &full[stage]);
@@ -671,7 +689,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      constexpr uint32_t idesc0 = Cf::kBf16 ? idesc_bf16(128, BN) : idesc_mxf8(128, BN);
+      constexpr uint32_t idesc0 = Cf::kBf16 ? idesc_bf16(128, BN) : (Cf::kNv4 ? idesc_nvf4(128, BN) : idesc_mxf8(128, BN));
       for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
         TileInfo t;
         if (!gemm_decode<BN, MODE>(p, tile, t)) continue;
@@ -688,6 +706,23 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
             for (int kk = 0; kk < 4; ++kk)
               tc_mma_bf16(dacc, desc_kmajor_sw128(sa + kk * 32), desc_kmajor_sw128(sb + kk * 32), idesc0,
                           (ks | kk) != 0);
+          } else if constexpr (Cf::kNv4) {
+            // per K = 64 step kk: A's atom kk at columns sfa_t + 4 kk; B's atoms (kk, row tile j)
+            // side by side at sfb_t + (BN / 128) 4 kk + 4 j
+            const uint32_t sfa_t = tmem + Cf::kSfCol0 + stage * Cf::kSfCols;
+            const uint32_t sfb_t = sfa_t + 16;
+            const uint32_t ssf = sb + Cf::kBBytes;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              tc_cp_sf(sfa_t + 4 * kk, desc_sf_chunk(ssf + 512 * kk));
+#pragma unroll
+              for (int j = 0; j < BN / 128; ++j)
+                tc_cp_sf(sfb_t + (BN / 128) * 4 * kk + 4 * j, desc_sf_chunk(ssf + 2048 + 2048 * j + 512 * kk));
+            }
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma_nvf4(dacc, desc_kmajor_sw128(sa + kk * 32), desc_kmajor_sw128(sb + kk * 32), idesc0,
+                          sfa_t + 4 * kk, sfb_t + (BN / 128) * 4 * kk, (ks | kk) != 0);
           } else {
             const uint32_t sfa_t = tmem + Cf::kSfCol0 + stage * Cf::kSfCols;
             const uint32_t sfb_t = sfa_t + 4;

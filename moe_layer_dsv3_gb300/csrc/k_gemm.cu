@@ -188,6 +188,8 @@ int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int
   p.out = ep.out;
   p.out2 = ep.out2;
   p.ldo = ep.ldo;
+  p.alpha = ep.alpha;
+  if (mode == kPlainNv4) p.a_ktiles = p.b_ktiles = K / 64;   // scale atoms (64 elements) per 128-row tile
   p.q_rows = ep.q_rows;
   p.q_rows_sf = ep.q_rows_sf;
   p.q_rows_ktiles = ep.q_rows_ktiles;
@@ -243,6 +245,8 @@ int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int
       return BN == 256 ? run<256, kWgrad>(name, ta, ta2, tb, to, to2, p, grid, s) : run<128, kWgrad>(name, ta, ta2, tb, to, to2, p, grid, s);
     case kPlain:
       return BN == 256 ? run<256, kPlain>(name, ta, ta2, tb, to, to2, p, grid, s) : run<128, kPlain>(name, ta, ta2, tb, to, to2, p, grid, s);
+    case kPlainNv4:
+      return BN == 256 ? run<256, kPlainNv4>(name, ta, ta2, tb, to, to2, p, grid, s) : run<128, kPlainNv4>(name, ta, ta2, tb, to, to2, p, grid, s);
     case kRouterMode:
       if (BN == 32) return run<32, kRouterMode>(name, ta, ta2, tb, to, to2, p, grid, s);
       return BN == 256 ? run<256, kRouterMode>(name, ta, ta2, tb, to, to2, p, grid, s) : run<128, kRouterMode>(name, ta, ta2, tb, to, to2, p, grid, s);

@@ -108,6 +108,13 @@ void launch_quant_rows(const void* src, int64_t rows, int K, int64_t ld, uint8_t
 void launch_quant_cols(const void* src, int64_t rows, int K, int64_t ld, int64_t rows_pad, uint8_t* codes,
                        uint8_t* sf, bool tiled, int batch, cudaStream_t s);
 
+// NVFP4 quantisation of bf16 src[rows][K] along K with tensor scale g: packed
+// E2M1 codes [rows][K/2] (element 2i in the low nibble), E4M3 block scales
+// (16 elements) canonical [rows][K/16] or, when tiled, in the 512-byte atoms
+// of 128 rows x 4 blocks the tensor cores read.
+void launch_quant_nvfp4(const void* src, int64_t rows, int K, float g, uint8_t* codes, uint8_t* sf, bool tiled,
+                        cudaStream_t s);
+
 // ---------------------------------------------------------------- router
 // Returns an MOE_* code: host-side failures (tensor-map encoding, launch
 // attributes) come back here, since they launch nothing.
@@ -145,6 +152,7 @@ enum GemmMode : int {
   // 5 is the bf16 router-logit mode (gemm.cuh)
   kSwigluFwdRing = 6,  // kSwigluFwd over all ring laps in one launch, mover warps fill the ring
   kSwigluBwdRing = 7,  // kSwigluBwd over all ring laps in one launch, mover warps fill the dO ring
+  kPlainNv4 = 8,       // single dense NVFP4 problem (E2M1, E4M3 scale per 16), fp32 output times alpha
 };
 
 // Where the mover warps of the all-laps ring modes take each ring row from.
@@ -170,6 +178,7 @@ struct GemmEpilogue {
   void* gu;             // saved bf16 g|u rows
   const float* gate;    // dh epilogue: per-assignment gate that scales each routed row
   int ldo;              // output row pitch (elements)
+  float alpha = 1.0f;   // NVFP4 plain mode: scale of the fp32 product
 };
 
 int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int K, int M, const GemmOperands& op,

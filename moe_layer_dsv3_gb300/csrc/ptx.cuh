@@ -216,6 +216,19 @@ __device__ __forceinline__ void tc_mma_mxf8(uint32_t d_tmem, uint64_t adesc, uin
       : "memory");
 }
 
+// D[tmem] (+)= A[smem] x B[smem]^T, NVFP4: E2M1 operands (two per byte), one
+// E4M3 scale per 16 elements from TMEM (four per row per K = 64 step).
+__device__ __forceinline__ void tc_mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t"
+      "}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= A[smem] x B[smem]^T for bf16 inputs, fp32 accumulate.
 __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                             uint32_t accumulate) {
@@ -235,6 +248,11 @@ __host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N) {
 }
 __device__ __forceinline__ uint32_t idesc_mxf8_sf(uint32_t base, uint32_t sfa_id, uint32_t sfb_id) {
   return base | (sfb_id << 4) | (sfa_id << 29);
+}
+// Instruction descriptor, block-scaled E2M1 x E2M1 (formats 1), both K-major,
+// UE4M3 scales (scale-format bit 0), scale-factor ids 0.
+__host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
+  return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 // Instruction descriptor, bf16 x bf16 -> fp32, both K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {

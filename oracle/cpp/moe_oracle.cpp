@@ -216,9 +216,45 @@ std::vector<double> transpose(const double* a, int64_t rows, int64_t cols) {
 
 double silu(double g) { return g / (1.0 + std::exp(-g)); }
 
+// ---------------------------------------------------------------- NVFP4
+// E2M1 magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6: the nearest (ties to the even
+// code), saturating at 6; the sign bit follows the sign of v.
+uint8_t e2m1_encode(double v) {
+  static const double mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+  const double a = std::min(std::fabs(v), 6.0);
+  int best = 0;
+  for (int c = 1; c < 8; ++c) {
+    const double dc = std::fabs(a - mag[c]), db = std::fabs(a - mag[best]);
+    if (dc < db || (dc == db && (c & 1) == 0)) best = c;
+  }
+  return static_cast<uint8_t>(best | (std::signbit(v) ? 8 : 0));
+}
+
 }  // namespace
 
 extern "C" {
+
+// NVFP4 along K of fp32 v [rows][K] (K a multiple of 16) with tensor scale g:
+// codes [rows][K] (one 4-bit code per byte), E4M3 block scales [rows][K/16].
+//   denom = fp32(6 g); sb = E4M3(fp32(amax / denom)); X = fp32(decode(sb) g);
+//   q = E2M1(fp32(v / X)), or 0 when X = 0.
+void orc_nvfp4_quantize(const float* v, int64_t rows, int64_t K, float g, uint8_t* codes, uint8_t* scales) {
+  const float denom = 6.0f * g;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t b = 0; b < K / 16; ++b) {
+      const float* blk = v + r * K + b * 16;
+      float amax = 0.0f;
+      for (int i = 0; i < 16; ++i) amax = std::max(amax, std::fabs(blk[i]));
+      const uint8_t sb = e4m3_encode(static_cast<double>(amax / denom));
+      scales[r * (K / 16) + b] = sb;
+      const float X = static_cast<float>(e4m3_decode(sb)) * g;
+      for (int i = 0; i < 16; ++i)
+        codes[r * K + b * 16 + i] = X > 0.0f ? e2m1_encode(static_cast<double>(blk[i] / X)) : 0;
+    }
+}
+void orc_e2m1_encode(const double* v, int64_t n, uint8_t* codes) {
+  for (int64_t i = 0; i < n; ++i) codes[i] = e2m1_encode(v[i]);
+}
 
 // ---------------------------------------------------------------- codec and router pieces (pins)
 void orc_e4m3_encode(const double* v, int64_t n, uint8_t* codes) {

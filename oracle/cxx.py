@@ -41,6 +41,7 @@ for _name, _args in {
     "orc_combine": [_P, _P, _P, _I, _I, _I, _P],
     "orc_router_backward": [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P],
     "orc_layer": [_I] * 8 + [_P] * 9 + [_I] + [_P] * 10,
+    "orc_nvfp4_quantize": [_P, _L, _L, ctypes.c_float, _P, _P], "orc_e2m1_encode": [_P, _L, _P],
 }.items():
     getattr(_lib, _name).argtypes = _args
     getattr(_lib, _name).restype = None
@@ -100,6 +101,27 @@ def quantize_tokens(rows):
     scales = np.empty((K, n_pad // 32), np.uint8)
     _lib.orc_mx_quantize_tokens(_p(r), n, K, _p(codes), _p(scales))
     return codes, scales
+
+
+def e2m1_encode(v) -> np.ndarray:
+    v = _c(v, np.float64)
+    out = np.empty(v.shape, np.uint8)
+    _lib.orc_e2m1_encode(_p(v), v.size, _p(out))
+    return out
+
+
+def nvfp4_quantize(v, g=None):
+    """NVFP4 along the last axis: (4-bit codes, E4M3 block scales, tensor scale g)."""
+    v = np.asarray(v, dtype=np.float32)
+    if g is None:
+        amax = np.float32(np.abs(v).max()) if v.size else np.float32(0)
+        g = np.float32(amax / np.float32(6 * 448.0)) if amax > 0 else np.float32(1.0)
+    flat = _c(v.reshape(-1, v.shape[-1]), np.float32)
+    rows, K = flat.shape
+    codes = np.empty((rows, K), np.uint8)
+    sb = np.empty((rows, K // 16), np.uint8)
+    _lib.orc_nvfp4_quantize(_p(flat), rows, K, float(g), _p(codes), _p(sb))
+    return codes.reshape(v.shape), sb.reshape(v.shape[:-1] + (K // 16,)), np.float32(g)
 
 
 # ---------------------------------------------------------------- router
