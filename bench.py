@@ -442,7 +442,7 @@ def run_ours(args, rank, world, local_rank):
     shape = _shape(args)
     inp = gen.make_inputs(shape, seed=rank, device="cuda")
     flags = (M.MOE_FLAG_LAP_LAUNCHES if args.lap_launches else 0) | (M.MOE_FLAG_WGRAD_PAIR if args.wgrad_pair else 0)
-    L = MoELayer.from_shape(shape, flags=flags)
+    L = MoELayer.from_shape(shape, flags=flags, n_mover_warps=args.mover_warps)
     L.quantize_weights(inp["w_gu"], inp["w_d"], inp["ws_gu"], inp["ws_d"])
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
@@ -657,7 +657,8 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None, "dtype": "mxfp8", "data": "synthetic (seeded, random-init weights)",
         "config": dict(workload_config(shape),
                        ring_laps="per-lap launches" if args.lap_launches else "one launch, mover warps",
-                       wgrad_tiles="CTA pairs 256-row" if args.wgrad_pair else "single CTA 128x256"),
+                       wgrad_tiles="CTA pairs 256-row" if args.wgrad_pair else "single CTA 128x256",
+                       mover_warps=args.mover_warps or 2),
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": job_tokens_per_s(shape.T, world, ms_e2e), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
@@ -694,6 +695,8 @@ def main():
                     help="skip the extra per-lap pass that times the ring movers as their own launches")
     ap.add_argument("--lap-launches", action="store_true",
                     help="one mover launch + one GEMM launch per ring lap instead of one all-laps launch")
+    ap.add_argument("--mover-warps", type=int, default=0, choices=[0, 1, 2, 4],
+                    help="mover warps per CTA of the all-laps ring GEMMs (0 = library default)")
     ap.add_argument("--wgrad-pair", action="store_true",
                     help="weight gradients on CTA pairs (256-row tiles) instead of single-CTA tiles (for comparison)")
     ap.add_argument("--probe-peak", action="store_true",

@@ -82,6 +82,13 @@ typedef struct moe_config {
   int T, d, E, k, n_groups, topk_groups, I, n_shared;
   int capacity;
   int flags; /* MOE_FLAG_* bits below; other bits are rejected */
+  /* Mover warps per CTA of the all-laps ring GEMMs (the counterpart, on one
+   * GPU, of the write-ups' "communication SM count" tuning knob: techlab
+   * report, section on the two scorecards): 0 = default (2), 1, 2 or 4. The
+   * forward GEMM1 takes at most 2 (its SwiGLU epilogue needs the register
+   * file of 8 warps); the backward dgrad GEMM takes any of the three. Results
+   * do not depend on it. */
+  int n_mover_warps;
 } moe_config_t;
 
 /* Ring-lap execution. By default each ring direction (forward GEMM1, backward

@@ -44,7 +44,8 @@ WQ = {n: i for i, n in enumerate(WQ_NAMES)}
 
 class MoeConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
-                ("T", "d", "E", "k", "n_groups", "topk_groups", "I", "n_shared", "capacity", "flags")]
+                ("T", "d", "E", "k", "n_groups", "topk_groups", "I", "n_shared", "capacity", "flags",
+                 "n_mover_warps")]
 
 
 class MoeError(RuntimeError):
@@ -110,8 +111,9 @@ MOE_FLAG_LAP_LAUNCHES = 1   # one mover launch + one GEMM launch per ring lap in
 MOE_FLAG_WGRAD_PAIR = 2     # weight gradients on CTA pairs (256-row tiles) instead of single-CTA 128 x 256 tiles
 
 
-def config(T, d, E, k, n_groups=1, topk_groups=1, I=128, n_shared=0, capacity=0, flags=0) -> MoeConfig:
-    return MoeConfig(T, d, E, k, n_groups, topk_groups, I, n_shared, capacity, flags)
+def config(T, d, E, k, n_groups=1, topk_groups=1, I=128, n_shared=0, capacity=0, flags=0,
+           n_mover_warps=0) -> MoeConfig:
+    return MoeConfig(T, d, E, k, n_groups, topk_groups, I, n_shared, capacity, flags, n_mover_warps)
 
 
 def moe_workspace_size(cfg: MoeConfig) -> int:

@@ -127,6 +127,8 @@ int validate(const moe_config_t* c) {
     return MOE_ERR_INVALID_ARG;
   if (c->capacity < 0 || c->capacity % 128) return MOE_ERR_INVALID_ARG;
   if (c->flags & ~(MOE_FLAG_LAP_LAUNCHES | MOE_FLAG_WGRAD_PAIR)) return MOE_ERR_INVALID_ARG;
+  if (c->n_mover_warps != 0 && c->n_mover_warps != 1 && c->n_mover_warps != 2 && c->n_mover_warps != 4)
+    return MOE_ERR_INVALID_ARG;
   const int64_t Ap = static_cast<int64_t>(c->T) * (c->k + c->n_shared);
   if (Ap + 128LL * (c->E + c->n_shared) >= (1LL << 31)) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
@@ -152,6 +154,7 @@ Dims make_dims(const moe_config_t* c) {
   m.Rmax = round_up(m.Ap, 128) + 128LL * m.Ep;
   m.Lb = m.T > 0 ? static_cast<int>(ceil_div(m.T, m.C)) : 0;
   m.units = static_cast<int>(ceil_div(m.Ap, kSchedUnit));
+  m.MV = c->n_mover_warps > 0 ? c->n_mover_warps : 2;
   return m;
 }
 

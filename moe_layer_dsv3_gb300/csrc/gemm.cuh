@@ -49,9 +49,14 @@ __host__ __device__ constexpr int base_mode(int mode) {
   return mode == kSwigluFwdRing ? kSwigluFwd : (mode == kSwigluBwdRing ? kSwigluBwd : mode);
 }
 __host__ __device__ constexpr bool ring_mode(int mode) { return mode == kSwigluFwdRing || mode == kSwigluBwdRing; }
-__host__ __device__ constexpr int gemm_threads(int mode) { return ring_mode(mode) ? 256 : 192; }
+// 192 threads (producer, MMA, 4 epilogue warps), plus MV mover warps in the all-laps ring modes.
+__host__ __device__ constexpr int gemm_threads(int mode, int mv) { return ring_mode(mode) ? 192 + 32 * mv : 192; }
 
-constexpr int kMoverWarps = 2;
+// Mover warps per CTA of the all-laps ring modes: the library default, and
+// the largest count GEMM1 can take (its SwiGLU epilogue warps hold 255
+// registers, so 8 warps already fill the register file).
+constexpr int kMoverWarpsDefault = 2;
+constexpr int kMoverWarpsGemm1Max = 2;
 constexpr int kMoveRows = 8;                    // ring rows per move item
 constexpr int kMoveItems = 128 / kMoveRows;     // move items per m-tile
 
@@ -379,14 +384,14 @@ __device__ __forceinline__ void move_rows(const GemmParams& p, int lane, int a_l
   }
 }
 
-// Mover warp `wid` of this CTA: items j = blockIdx.x * kMoverWarps + wid,
-// then every gridDim.x * kMoverWarps, i.e. in increasing (lap-major) order.
-template <int BN, int MODE>
+// Mover warp `wid` of this CTA (MV per CTA): items j = blockIdx.x * MV + wid,
+// then every gridDim.x * MV, i.e. in increasing (lap-major) order.
+template <int BN, int MODE, int MV>
 __device__ void ring_mover(const GemmParams& p, int wid, int lane) {
   const int nt = p.N / BN;
   const int total = p.lapbase[p.Lb] * kMoveItems;
-  const int stride = gridDim.x * kMoverWarps;
-  for (int j = blockIdx.x * kMoverWarps + wid; j < total; j += stride) {
+  const int stride = gridDim.x * MV;
+  for (int j = blockIdx.x * MV + wid; j < total; j += stride) {
     const int gm = j / kMoveItems, part = j - gm * kMoveItems;
     const int L = seg_search(p.lapbase, p.Lb, gm);
     const int g = gm - p.lapbase[L];
@@ -584,8 +589,8 @@ __device__ __forceinline__ void gemm_epilogue_tile(const GemmParams& p, const Ti
   }
 }
 
-template <int BN, int MODE>
-__global__ void __launch_bounds__(gemm_threads(MODE), 1)
+template <int BN, int MODE, int MV = kMoverWarpsDefault>
+__global__ void __launch_bounds__(gemm_threads(MODE, MV), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_a2,
                 const __grid_constant__ CUtensorMap tma_b, const __grid_constant__ CUtensorMap tma_o,
                 const __grid_constant__ CUtensorMap tma_o2, const __grid_constant__ GemmParams p) {
@@ -768,7 +773,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
     }
     if (Cf::kTmaOut && q == 2 && lane == 0) bulk_wait_all();
   } else {
-    if constexpr (ring_mode(MODE)) ring_mover<BN, MODE>(p, warp - 6, lane);
+    if constexpr (ring_mode(MODE)) ring_mover<BN, MODE, MV>(p, warp - 6, lane);
   }
   tc_fence_before();
   __syncthreads();

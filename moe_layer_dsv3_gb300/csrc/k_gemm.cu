@@ -72,7 +72,7 @@ struct DevOnce {
   int per_sm[kMaxDev] = {};
 };
 
-template <int BN, int MODE>
+template <int BN, int MODE, int MV = kMoverWarpsDefault>
 int run(const char* name, const CUtensorMap& ta, const CUtensorMap& ta2, const CUtensorMap& tb, const CUtensorMap& to,
         const CUtensorMap& to2, const GemmParams& p, int grid, cudaStream_t s) {
   using Cf = GemmCfg<BN, MODE>;
@@ -85,11 +85,11 @@ int run(const char* name, const CUtensorMap& ta, const CUtensorMap& ta2, const C
   {
     std::lock_guard<std::mutex> lk(once.mu);
     if (once.state[dev] == 0) {
-      bool ok = cudaFuncSetAttribute(gemm_kernel<BN, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmem) ==
+      bool ok = cudaFuncSetAttribute(gemm_kernel<BN, MODE, MV>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmem) ==
                 cudaSuccess;
       if (ok && ring_mode(MODE))
-        ok = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&once.per_sm[dev], gemm_kernel<BN, MODE>,
-                                                           gemm_threads(MODE), Cf::kSmem) == cudaSuccess &&
+        ok = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&once.per_sm[dev], gemm_kernel<BN, MODE, MV>,
+                                                           gemm_threads(MODE, MV), Cf::kSmem) == cudaSuccess &&
              once.per_sm[dev] >= 1;
       once.state[dev] = ok ? 1 : 2;
     }
@@ -109,11 +109,11 @@ int run(const char* name, const CUtensorMap& ta, const CUtensorMap& ta2, const C
     lc.numAttrs = 1;
   }
   lc.gridDim = dim3(static_cast<unsigned>(grid));
-  lc.blockDim = dim3(gemm_threads(MODE));
+  lc.blockDim = dim3(gemm_threads(MODE, MV));
   lc.dynamicSmemBytes = Cf::kSmem;
   lc.stream = s;
   Prof prof(name, s);
-  const cudaError_t e = cudaLaunchKernelEx(&lc, gemm_kernel<BN, MODE>, ta, ta2, tb, to, to2, p);
+  const cudaError_t e = cudaLaunchKernelEx(&lc, gemm_kernel<BN, MODE, MV>, ta, ta2, tb, to, to2, p);
   note(e);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -234,9 +234,17 @@ int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int
       if (BN == 128) return run<128, kSwigluFwd>(name, ta, ta2, tb, to, to2, p, grid, s);
       return run<256, kSwigluFwd>(name, ta, ta2, tb, to, to2, p, grid, s);
     case kSwigluFwdRing:
-      return run<kGemm1BN, kSwigluFwdRing>(name, ta, ta2, tb, to, to2, p, grid, s);
+      return m.MV == 1 ? run<kGemm1BN, kSwigluFwdRing, 1>(name, ta, ta2, tb, to, to2, p, grid, s)
+                       : run<kGemm1BN, kSwigluFwdRing, kMoverWarpsGemm1Max>(name, ta, ta2, tb, to, to2, p, grid, s);
     case kSwigluBwdRing:
-      return BN == 256 ? run<256, kSwigluBwdRing>(name, ta, ta2, tb, to, to2, p, grid, s) : run<128, kSwigluBwdRing>(name, ta, ta2, tb, to, to2, p, grid, s);
+      if (BN == 256) {
+        return m.MV == 1   ? run<256, kSwigluBwdRing, 1>(name, ta, ta2, tb, to, to2, p, grid, s)
+               : m.MV == 4 ? run<256, kSwigluBwdRing, 4>(name, ta, ta2, tb, to, to2, p, grid, s)
+                           : run<256, kSwigluBwdRing, 2>(name, ta, ta2, tb, to, to2, p, grid, s);
+      }
+      return m.MV == 1   ? run<128, kSwigluBwdRing, 1>(name, ta, ta2, tb, to, to2, p, grid, s)
+             : m.MV == 4 ? run<128, kSwigluBwdRing, 4>(name, ta, ta2, tb, to, to2, p, grid, s)
+                         : run<128, kSwigluBwdRing, 2>(name, ta, ta2, tb, to, to2, p, grid, s);
     case kSwigluBwd:
       return BN == 256 ? run<256, kSwigluBwd>(name, ta, ta2, tb, to, to2, p, grid, s) : run<128, kSwigluBwd>(name, ta, ta2, tb, to, to2, p, grid, s);
     case kPush:

@@ -40,6 +40,7 @@ struct Dims {
   int64_t Rmax;    // padded-row capacity of rank-ordered buffers
   int Lb;          // upper bound on ring laps: ceil(T / C)
   int units;       // schedule units
+  int MV;          // mover warps per CTA of the all-laps ring GEMMs (1, 2 or 4)
 };
 
 struct Layout {

@@ -15,8 +15,8 @@ from . import (config, moe_backward, moe_dispatch, moe_forward, moe_quantize_wei
 
 class MoELayer:
     def __init__(self, T, d, E, k, n_groups=1, topk_groups=1, I=128, n_shared=0, capacity=0, device="cuda",
-                 flags=0):
-        self.cfg = config(T, d, E, k, n_groups, topk_groups, I, n_shared, capacity, flags)
+                 flags=0, n_mover_warps=0):
+        self.cfg = config(T, d, E, k, n_groups, topk_groups, I, n_shared, capacity, flags, n_mover_warps)
         self.T, self.d, self.E, self.k, self.I, self.S = T, d, E, k, I, n_shared
         dev = torch.device(device)
         self.device = dev
@@ -34,9 +34,9 @@ class MoELayer:
         self._x = self._w_router = None
 
     @classmethod
-    def from_shape(cls, shape, device="cuda", flags=0):
+    def from_shape(cls, shape, device="cuda", flags=0, n_mover_warps=0):
         return cls(shape.T, shape.d, shape.E, shape.k, shape.G, shape.g_top, shape.I, shape.S, shape.C, device,
-                   flags)
+                   flags, n_mover_warps)
 
     # ------------------------------------------------------------ views
     def ws_tensor(self, name, dtype=torch.uint8, shape=None) -> torch.Tensor:

@@ -464,6 +464,24 @@ def test_lap_launch_path_bitwise(run):
         assert torch.equal(L.ws_tensor(name), L2.ws_tensor(name)), name
 
 
+@pytest.mark.parametrize("mv", [1, 4])
+def test_mover_warp_count_bitwise(run, mv):
+    """The mover-warp count of the all-laps ring GEMMs is a tuning knob only: 1 and 4 movers per
+    CTA give the same bytes as the default 2 (outputs, gradients, both rings)."""
+    from moe_layer_dsv3_gb300.layer import MoELayer
+    dev = run.dev
+    L2 = MoELayer.from_shape(run.shape, n_mover_warps=mv)
+    L2.wq = run.L.wq
+    L2.forward(dev["x"], dev["w_router"], dev["bias"])
+    L2.backward(dev["dy"])
+    torch.cuda.synchronize()
+    assert L2.status() == (0, 0)
+    for name in ("y", "dx", "dw_router", "dw_gu", "dw_d", "dws_gu", "dws_d"):
+        assert torch.equal(getattr(run.L, name).view(torch.int16), getattr(L2, name).view(torch.int16)), name
+    for name in ("RING_X", "RING_DO", "GU", "HQ", "DGU"):
+        assert torch.equal(run.L.ws_tensor(name), L2.ws_tensor(name)), name
+
+
 def test_wgrad_pair_matches_single_cta(run):
     """Weight gradients on CTA pairs (MOE_FLAG_WGRAD_PAIR, where the gradient's row count is a
     multiple of 256) and on single-CTA tiles (the default) give the same bytes: both sum the

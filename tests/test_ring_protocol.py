@@ -7,7 +7,7 @@ slot's previous tenant (lap L - 2). This model replays that protocol on
 concrete schedules with every CTA walking its tiles and move items in the
 kernel's order, and checks that it always makes progress (no wait cycle),
 that the previous tenant is the same (expert, m-tile), and that every index
-stays inside the buffers the host sizes.
+stays inside the buffers the host sizes, for 1, 2 and 4 mover warps per CTA.
 """
 import numpy as np
 import pytest
@@ -48,7 +48,7 @@ def seg(v, n, x):
     return lo
 
 
-def replay(counts, E, S, T, C, grid, nt):
+def replay(counts, E, S, T, C, grid, nt, mv=2):
     Ep = E + S
     lt, lapbase, Lb = lap_schedule(counts, E, S, C, T)
     A = int(sum(counts[:E]))
@@ -65,7 +65,7 @@ def replay(counts, E, S, T, C, grid, nt):
     moved = np.zeros(ntot, int)
     consumed = np.zeros(ntot, int)
     prod = [list(range(c, ntot * nt, grid)) for c in range(grid)]
-    movers = [list(range(2 * c + w, ntot * MOVE_ITEMS, 2 * grid)) for c in range(grid) for w in range(2)]
+    movers = [list(range(mv * c + w, ntot * MOVE_ITEMS, mv * grid)) for c in range(grid) for w in range(mv)]
     pi = [0] * len(prod)
     mi = [0] * len(movers)
     while True:
@@ -112,16 +112,18 @@ def zipf_counts(E, T, k, s, seed):
     return [int(c) for c in np.minimum(rng.multinomial(T * k, rng.permutation(p)), T)]
 
 
+@pytest.mark.parametrize("mv", [1, 2, 4])
 @pytest.mark.parametrize("grid", [1, 3, 16, 152])
-def test_zipf_wrap_schedule_progresses(grid):
+def test_zipf_wrap_schedule_progresses(grid, mv):
     counts = zipf_counts(64, 2048, 8, 1.1, 0) + [2048]
     assert max(counts[:64]) > 3 * 128                    # several laps of C=128
-    replay(counts, 64, 1, 2048, 128, grid, 16)
+    replay(counts, 64, 1, 2048, 128, grid, 16, mv)
 
 
-def test_benchmark_shape_schedule_progresses():
+@pytest.mark.parametrize("mv", [1, 2, 4])
+def test_benchmark_shape_schedule_progresses(mv):
     counts = zipf_counts(256, 16384, 8, 1.1, 1) + [16384]
-    replay(counts, 256, 1, 16384, 640, 152, 16)
+    replay(counts, 256, 1, 16384, 640, 152, 16, mv)
 
 
 @pytest.mark.parametrize("counts,E,S,T,C,nt", [
@@ -132,4 +134,5 @@ def test_benchmark_shape_schedule_progresses():
 ])
 def test_edge_schedules_progress(counts, E, S, T, C, nt):
     for grid in (1, 2, 7):
-        replay(counts, E, S, T, C, grid, nt)
+        for mv in (1, 2, 4):
+            replay(counts, E, S, T, C, grid, nt, mv)
