@@ -69,9 +69,11 @@ __device__ __forceinline__ bool lap_row(const int* lap_tiles, const int* counts,
   return true;
 }
 
+constexpr int kPermChunks = 14;   // 16-byte chunks a lane keeps in flight (a whole 7168-byte row per warp)
+
 // ring[e*C + slot] <- the MX row of token t (codes and scales) for the rows of lap L:
 // x_q into the x ring in the forward, MX(dy) into the dO ring in the backward.
-__global__ void __launch_bounds__(256) permute_lap_kernel(
+__global__ void __launch_bounds__(256, 3) permute_lap_kernel(
     const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xq_sf, const int* __restrict__ lap_tiles,
     const int* __restrict__ counts, const int* __restrict__ poff, const int* __restrict__ row_src, int T, int k,
     int d, int E, int Ep, int C, int L, uint8_t* __restrict__ ring, uint8_t* __restrict__ ring_sf) {
@@ -84,8 +86,19 @@ __global__ void __launch_bounds__(256) permute_lap_kernel(
     if (!lap_row(lap_tiles, counts, poff, row_src, T, k, E, Ep, C, L, gid, warp, row, t, a)) continue;
     const uint4* src = reinterpret_cast<const uint4*>(xq + static_cast<int64_t>(t < 0 ? 0 : t) * d);
     uint4* dst = reinterpret_cast<uint4*>(ring + row * d);
-#pragma unroll 4
-    for (int c = lane; c < chunks; c += 32) dst[c] = t >= 0 ? src[c] : make_uint4(0, 0, 0, 0);
+    for (int c0 = 0; c0 < chunks; c0 += 32 * kPermChunks) {   // all of a lane's chunks in flight
+      uint4 v[kPermChunks];
+#pragma unroll
+      for (int u = 0; u < kPermChunks; ++u) {
+        const int c = c0 + u * 32 + lane;
+        v[u] = (t >= 0 && c < chunks) ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < kPermChunks; ++u) {
+        const int c = c0 + u * 32 + lane;
+        if (c < chunks) dst[c] = v[u];
+      }
+    }
     for (int kt = lane; kt < ktiles; kt += 32) {
       const uint32_t v = t >= 0 ? *reinterpret_cast<const uint32_t*>(xq_sf + sf_off(t, kt * 4, ktiles)) : 0u;
       *reinterpret_cast<uint32_t*>(ring_sf + sf_off(row, kt * 4, ktiles)) = v;
@@ -94,74 +107,53 @@ __global__ void __launch_bounds__(256) permute_lap_kernel(
 }
 
 // Dispatch of every ring lap in one launch (moe_dispatch). Item = (expert e,
-// ring buffer b, group of 8 slots), experts taken in descending-count order so
-// that the slot groups with the most laps start first. The item's warp writes, for each lap
-// L = b, b + 2, ... of e in that order, the lap's rows into those slots
-// (zeros past the lap's rows up to its last 128-row tile): the same writes,
-// in the same per-slot order, as the per-lap kernels. Rows are copied in
-// rounds of kDispU 16-byte chunks a lane, the next round's loads issued
-// before this round's stores.
-constexpr int kDispU = 8;
+// ring buffer b, one ring slot), experts taken in descending-count order so
+// that the slots with the most laps start first. The item's warp writes, for
+// each lap L = b, b + 2, ... of e in that order, the lap's row for that slot
+// (zero past the lap's rows up to its last 128-row tile): the same writes, in
+// the same per-slot order, as the per-lap kernels. A slot's chain is at most
+// ceil(laps / 2) rows long; each lane keeps kDispChunks 16-byte chunks of the
+// row in flight (all of a 7168-byte row).
+constexpr int kDispChunks = 14;
 
-__global__ void __launch_bounds__(256) dispatch_all_kernel(
+__global__ void __launch_bounds__(256, 3) dispatch_all_kernel(
     const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xq_sf, const int* __restrict__ counts,
     const int* __restrict__ poff, const int* __restrict__ row_src, const int* __restrict__ order, int k, int d,
     int E, int Ep, int C, uint8_t* __restrict__ ring, uint8_t* __restrict__ ring_sf) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int groups = C / 8;
   const int64_t item = static_cast<int64_t>(blockIdx.x) * 8 + warp;
-  if (item >= static_cast<int64_t>(Ep) * 2 * groups) return;
-  const int ei = static_cast<int>(item / (2 * groups));
-  const int rem = static_cast<int>(item - static_cast<int64_t>(ei) * 2 * groups);
+  if (item >= static_cast<int64_t>(Ep) * 2 * C) return;
+  const int ei = static_cast<int>(item / (2 * C));
+  const int rem = static_cast<int>(item - static_cast<int64_t>(ei) * 2 * C);
   const int e = order[ei];              // every expert once; the shared one has no ring rows
   if (e >= E) return;
-  const int b = rem / groups, s0 = (rem - b * groups) * 8;
+  const int b = rem / C, slot = rem - b * C;
   const int n = counts[e];
   const int chunks = d >> 4, ktiles = d >> 7;
-  const int total = 8 * chunks;
-  const int rounds = (total + 32 * kDispU - 1) / (32 * kDispU);
-  const uint4 zero = make_uint4(0, 0, 0, 0);
+  const int64_t row = (static_cast<int64_t>(b) * E + e) * C + slot;
+  uint4* dst = reinterpret_cast<uint4*>(ring + row * d);
   for (int L = b; static_cast<int64_t>(L) * C < n; L += 2) {
     const int len = min(C, n - L * C);
-    if (s0 >= (len + 127) / 128 * 128) break;
-    const int64_t rank0 = static_cast<int64_t>(L) * C + s0;
-    const int64_t row0 = (static_cast<int64_t>(b) * E + e) * C + s0;
-    const int a_l = (lane < 8 && rank0 + lane < n) ? row_src[poff[e] + rank0 + lane] : -1;
-    const int tok_l = a_l >= 0 ? a_l / k : -1;
-    uint4 nxt[kDispU];
-    auto load = [&](int rd, uint4* v) {
+    if (slot >= (len + 127) / 128 * 128) break;
+    const int64_t rank = static_cast<int64_t>(L) * C + slot;
+    const int t = rank < n ? row_src[poff[e] + rank] / k : -1;
+    const uint4* src = reinterpret_cast<const uint4*>(xq + static_cast<int64_t>(t < 0 ? 0 : t) * d);
+    for (int c0 = 0; c0 < chunks; c0 += 32 * kDispChunks) {
+      uint4 v[kDispChunks];
 #pragma unroll
-      for (int u = 0; u < kDispU; ++u) {
-        const int f = (rd * kDispU + u) * 32 + lane;
-        const int r = f / chunks, c = f - (f / chunks) * chunks;
-        const int t = __shfl_sync(0xffffffffu, tok_l, r < 8 ? r : 7);
-        v[u] = (f < total && t >= 0) ? __ldg(reinterpret_cast<const uint4*>(xq + static_cast<int64_t>(t) * d) + c)
-                                     : zero;
+      for (int u = 0; u < kDispChunks; ++u) {
+        const int c = c0 + u * 32 + lane;
+        v[u] = (t >= 0 && c < chunks) ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
       }
-    };
-    load(0, nxt);
-    for (int rd = 0; rd < rounds; ++rd) {
-      uint4 cur[kDispU];
 #pragma unroll
-      for (int u = 0; u < kDispU; ++u) cur[u] = nxt[u];
-      if (rd + 1 < rounds) load(rd + 1, nxt);
-#pragma unroll
-      for (int u = 0; u < kDispU; ++u) {
-        const int f = (rd * kDispU + u) * 32 + lane;
-        const int r = f / chunks, c = f - (f / chunks) * chunks;
-        if (f < total) reinterpret_cast<uint4*>(ring + (row0 + r) * d)[c] = cur[u];
+      for (int u = 0; u < kDispChunks; ++u) {
+        const int c = c0 + u * 32 + lane;
+        if (c < chunks) dst[c] = v[u];
       }
     }
-    int tok[8];
-#pragma unroll
-    for (int r = 0; r < 8; ++r) tok[r] = __shfl_sync(0xffffffffu, tok_l, r);
     for (int kt = lane; kt < ktiles; kt += 32) {
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const uint32_t v = tok[r] >= 0 ? __ldg(reinterpret_cast<const uint32_t*>(xq_sf + sf_off(tok[r], kt * 4, ktiles)))
-                                       : 0u;
-        *reinterpret_cast<uint32_t*>(ring_sf + sf_off(row0 + r, kt * 4, ktiles)) = v;
-      }
+      const uint32_t sv = t >= 0 ? __ldg(reinterpret_cast<const uint32_t*>(xq_sf + sf_off(t, kt * 4, ktiles))) : 0u;
+      *reinterpret_cast<uint32_t*>(ring_sf + sf_off(row, kt * 4, ktiles)) = sv;
     }
   }
 }
@@ -337,7 +329,7 @@ static int lap_blocks(const Dims& m) {
 }
 
 void launch_dispatch_all(const Dims& m, const Layout& L, void* ws, cudaStream_t s) {
-  const int64_t items = static_cast<int64_t>(m.Ep) * 2 * (m.C / 8);
+  const int64_t items = static_cast<int64_t>(m.Ep) * 2 * m.C;
   if (items == 0) return;
   launch_kernel("dispatch_all", dispatch_all_kernel, dim3(static_cast<unsigned>(ceil_div(items, 8))), dim3(256), 0, s,
       ws_ptr<uint8_t>(L, ws, MOE_WS_XQ), ws_ptr<uint8_t>(L, ws, MOE_WS_XQ_SF), ws_ptr<int>(L, ws, MOE_WS_COUNTS),
