@@ -107,53 +107,78 @@ __global__ void __launch_bounds__(256, 3) permute_lap_kernel(
 }
 
 // Dispatch of every ring lap in one launch (moe_dispatch). Item = (expert e,
-// ring buffer b, one ring slot), experts taken in descending-count order so
-// that the slots with the most laps start first. The item's warp writes, for
-// each lap L = b, b + 2, ... of e in that order, the lap's row for that slot
-// (zero past the lap's rows up to its last 128-row tile): the same writes, in
-// the same per-slot order, as the per-lap kernels. A slot's chain is at most
-// ceil(laps / 2) rows long; each lane keeps kDispChunks 16-byte chunks of the
-// row in flight (all of a 7168-byte row).
-constexpr int kDispChunks = 14;
+// ring buffer b, kDispSlots consecutive ring slots), experts taken in
+// descending-count order so that the slots with the most laps start first.
+// The item's warp writes, for each lap L = b, b + 2, ... of e in that order,
+// the lap's rows for those slots (zero past the lap's rows up to its last
+// 128-row tile): the same writes, in the same per-slot order, as the per-lap
+// kernels; one thread's stores to a row are ordered, so the last lap wins.
+// Lane l looks up the token of slot l % kDispSlots in lap l / kDispSlots of a
+// batch of 32 / kDispSlots laps, so one dependent chain of index loads serves
+// many rows; each row is then copied with kDispChunks 16-byte chunks a lane
+// in flight. Measured (one GB300, dsv3_zipf): 2 slots per item beat 1, 4 and
+// 8, and a TMA bulk-copy form through shared memory.
+constexpr int kDispSlots = 2;
+constexpr int kDispChunks = 7;
 
-__global__ void __launch_bounds__(256, 3) dispatch_all_kernel(
+__global__ void __launch_bounds__(256, 4) dispatch_all_kernel(
     const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xq_sf, const int* __restrict__ counts,
     const int* __restrict__ poff, const int* __restrict__ row_src, const int* __restrict__ order, int k, int d,
     int E, int Ep, int C, uint8_t* __restrict__ ring, uint8_t* __restrict__ ring_sf) {
+  constexpr int kLapsPerBatch = 32 / kDispSlots;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int groups = C / kDispSlots;
   const int64_t item = static_cast<int64_t>(blockIdx.x) * 8 + warp;
-  if (item >= static_cast<int64_t>(Ep) * 2 * C) return;
-  const int ei = static_cast<int>(item / (2 * C));
-  const int rem = static_cast<int>(item - static_cast<int64_t>(ei) * 2 * C);
+  if (item >= static_cast<int64_t>(Ep) * 2 * groups) return;
+  const int ei = static_cast<int>(item / (2 * groups));
+  const int rem = static_cast<int>(item - static_cast<int64_t>(ei) * 2 * groups);
   const int e = order[ei];              // every expert once; the shared one has no ring rows
   if (e >= E) return;
-  const int b = rem / C, slot = rem - b * C;
+  const int b = rem / groups, s0 = (rem - b * groups) * kDispSlots;
   const int n = counts[e];
+  if (static_cast<int64_t>(b) * C >= n) return;
+  const int laps = static_cast<int>((n - static_cast<int64_t>(b) * C + 2LL * C - 1) / (2LL * C));   // laps b, b+2, ...
+  const int p0 = poff[e];
   const int chunks = d >> 4, ktiles = d >> 7;
-  const int64_t row = (static_cast<int64_t>(b) * E + e) * C + slot;
-  uint4* dst = reinterpret_cast<uint4*>(ring + row * d);
-  for (int L = b; static_cast<int64_t>(L) * C < n; L += 2) {
-    const int len = min(C, n - L * C);
-    if (slot >= (len + 127) / 128 * 128) break;
-    const int64_t rank = static_cast<int64_t>(L) * C + slot;
-    const int t = rank < n ? row_src[poff[e] + rank] / k : -1;
-    const uint4* src = reinterpret_cast<const uint4*>(xq + static_cast<int64_t>(t < 0 ? 0 : t) * d);
-    for (int c0 = 0; c0 < chunks; c0 += 32 * kDispChunks) {
-      uint4 v[kDispChunks];
-#pragma unroll
-      for (int u = 0; u < kDispChunks; ++u) {
-        const int c = c0 + u * 32 + lane;
-        v[u] = (t >= 0 && c < chunks) ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int u = 0; u < kDispChunks; ++u) {
-        const int c = c0 + u * 32 + lane;
-        if (c < chunks) dst[c] = v[u];
+  for (int jb = 0; jb < laps; jb += kLapsPerBatch) {
+    // lane: lap jb + lane / kDispSlots, slot s0 + lane % kDispSlots -> token, -1 (zero row) or -2 (no row)
+    int tok = -2;
+    {
+      const int j = jb + lane / kDispSlots, slot = s0 + lane % kDispSlots;
+      if (j < laps) {
+        const int64_t L = b + 2LL * j;
+        const int len = static_cast<int>(min(static_cast<int64_t>(C), n - L * C));
+        if (slot < len) tok = row_src[p0 + L * C + slot] / k;
+        else if (slot < (len + 127) / 128 * 128) tok = -1;
       }
     }
-    for (int kt = lane; kt < ktiles; kt += 32) {
-      const uint32_t sv = t >= 0 ? __ldg(reinterpret_cast<const uint32_t*>(xq_sf + sf_off(t, kt * 4, ktiles))) : 0u;
-      *reinterpret_cast<uint32_t*>(ring_sf + sf_off(row, kt * 4, ktiles)) = sv;
+    const int nj = min(kLapsPerBatch, laps - jb);
+    for (int jj = 0; jj < nj; ++jj) {
+#pragma unroll 1
+      for (int ss = 0; ss < kDispSlots; ++ss) {
+        const int t = __shfl_sync(0xffffffffu, tok, jj * kDispSlots + ss);
+        if (t == -2) continue;
+        const int64_t row = (static_cast<int64_t>(b) * E + e) * C + s0 + ss;
+        const uint4* src = reinterpret_cast<const uint4*>(xq + static_cast<int64_t>(t < 0 ? 0 : t) * d);
+        uint4* dst = reinterpret_cast<uint4*>(ring + row * d);
+        for (int c0 = 0; c0 < chunks; c0 += 32 * kDispChunks) {
+          uint4 v[kDispChunks];
+#pragma unroll
+          for (int u = 0; u < kDispChunks; ++u) {
+            const int c = c0 + u * 32 + lane;
+            v[u] = (t >= 0 && c < chunks) ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+          for (int u = 0; u < kDispChunks; ++u) {
+            const int c = c0 + u * 32 + lane;
+            if (c < chunks) dst[c] = v[u];
+          }
+        }
+        for (int kt = lane; kt < ktiles; kt += 32) {
+          const uint32_t sv = t >= 0 ? __ldg(reinterpret_cast<const uint32_t*>(xq_sf + sf_off(t, kt * 4, ktiles))) : 0u;
+          *reinterpret_cast<uint32_t*>(ring_sf + sf_off(row, kt * 4, ktiles)) = sv;
+        }
+      }
     }
   }
 }
@@ -329,7 +354,7 @@ static int lap_blocks(const Dims& m) {
 }
 
 void launch_dispatch_all(const Dims& m, const Layout& L, void* ws, cudaStream_t s) {
-  const int64_t items = static_cast<int64_t>(m.Ep) * 2 * m.C;
+  const int64_t items = static_cast<int64_t>(m.Ep) * 2 * (m.C / kDispSlots);
   if (items == 0) return;
   launch_kernel("dispatch_all", dispatch_all_kernel, dim3(static_cast<unsigned>(ceil_div(items, 8))), dim3(256), 0, s,
       ws_ptr<uint8_t>(L, ws, MOE_WS_XQ), ws_ptr<uint8_t>(L, ws, MOE_WS_XQ_SF), ws_ptr<int>(L, ws, MOE_WS_COUNTS),

@@ -383,3 +383,25 @@ def test_wgrad_pair_form_bitwise(full):
         assert torch.equal(getattr(L, name).view(torch.int16), getattr(L2, name).view(torch.int16)), name
     del L2
     torch.cuda.empty_cache()
+
+
+def test_dispatch_alone_fills_the_ring_full_size(full):
+    """moe_dispatch (one launch over all laps) leaves the same ring bytes as the forward's mover
+    warps, at the workloads with ring wrap-around and at the widest expert count."""
+    if full.shape.name not in ("dsv3_zipf", "small") and not (full.shape.name == "e384" and full.shape.T == 2368):
+        pytest.skip("the wrap-around workload and two without wrap")
+    L, i = full.L, full.inp
+    L.ws_tensor("RING_X").fill_(0x5A)
+    L.ws_tensor("RING_X_SF").fill_(0x5A)
+    L.forward(i["x"], i["w_router"], i["bias"])
+    torch.cuda.synchronize()
+    ref = L.ws_tensor("RING_X").clone(), L.ws_tensor("RING_X_SF").clone()
+    L.ws_tensor("RING_X").fill_(0x5A)
+    L.ws_tensor("RING_X_SF").fill_(0x5A)
+    L.dispatch(i["x"])
+    torch.cuda.synchronize()
+    assert L.status() == (0, 0)
+    assert torch.equal(L.ws_tensor("RING_X"), ref[0])
+    assert torch.equal(L.ws_tensor("RING_X_SF"), ref[1])
+    del ref
+    torch.cuda.empty_cache()
