@@ -342,6 +342,25 @@ def test_bitwise_rerun(full):
     assert _checksum(L.dw_d) == h_d
 
 
+def test_idle_expert_weight_grads_full_size(full):
+    """Experts without tokens get all-zero weight gradients whatever the buffers held (their
+    tiles are stored by the weight-gradient kernels' zero-fill warp), and rewriting the buffers
+    from a NaN pattern leaves the other experts' gradient bytes unchanged."""
+    L, i = full.L, full.inp
+    s = full.shape
+    idle = np.flatnonzero(full.sched["counts"][:s.E] == 0)
+    h_gu, h_d = _checksum(L.dw_gu), _checksum(L.dw_d)
+    L.dw_gu.view(torch.uint8).fill_(0xFF)
+    L.dw_d.view(torch.uint8).fill_(0xFF)
+    L.backward(i["dy"])
+    torch.cuda.synchronize()
+    assert L.status() == (0, 0)
+    for e in idle:
+        assert not L.dw_gu[int(e)].view(torch.int16).any() and not L.dw_d[int(e)].view(torch.int16).any(), e
+    assert _checksum(L.dw_gu) == h_gu
+    assert _checksum(L.dw_d) == h_d
+
+
 def test_lap_launch_form_bitwise(full):
     """At full size, with ring wrap-around (17 laps at dsv3_zipf), the per-lap launch form
     (MOE_FLAG_LAP_LAUNCHES: a mover launch and a GEMM launch per lap, laps on two streams)

@@ -500,8 +500,9 @@ def test_wgrad_pair_matches_single_cta(run):
 
 
 def test_idle_expert_weight_grads_zeroed(run):
-    """Experts that received no token get exactly zero weight gradients (their fill runs on a side
-    stream), whatever the output buffers held before; the other experts' gradients are unchanged."""
+    """Experts that received no token get exactly zero weight gradients (stored by the
+    weight-gradient kernels' zero-fill warp), whatever the output buffers held before; the other
+    experts' gradients are unchanged."""
     L, dev = run.L, run.dev
     counts = run.f["sched"]["counts"]
     ref_gu, ref_d = L.dw_gu.clone(), L.dw_d.clone()
