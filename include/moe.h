@@ -382,6 +382,14 @@ MOE_API long long moe_launch_count(void);
  * context stays usable. */
 MOE_API int moe_selftest_wait_timeout(int* status, unsigned long long limit_ns, moe_stream_t stream);
 
+/* Host-side fault injection, for tests of the error paths. The next `count`
+ * TMA tensor-map encodings made by this process fail as a failed
+ * cuTensorMapEncodeTiled would: the GEMM that needed the map is not launched,
+ * nothing that depends on it is launched, and the entry point returns
+ * MOE_ERR_CUDA. count <= 0 clears a pending injection. Nothing reaches the
+ * GPU. Returns MOE_OK. */
+MOE_API int moe_debug_fail_tensor_maps(int count);
+
 #ifdef __cplusplus
 }
 #endif

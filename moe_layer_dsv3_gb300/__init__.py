@@ -83,6 +83,7 @@ _SIGS = {
     "moe_profile_trace": [ctypes.c_void_p, _I, ctypes.POINTER(_I)],
     "moe_launch_count": [],
     "moe_selftest_wait_timeout": [_P, ctypes.c_ulonglong, _P],
+    "moe_debug_fail_tensor_maps": [_I],
 }
 for _name, _args in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -237,6 +238,11 @@ def moe_profile_trace(max_entries=4096):
 
 def moe_selftest_wait_timeout(status, limit_ns, stream=0):
     _check("moe_selftest_wait_timeout", _lib.moe_selftest_wait_timeout(_p(status), limit_ns, _p(stream)))
+
+
+def moe_debug_fail_tensor_maps(count):
+    """Make the next `count` tensor-map encodings fail on the host (0 clears); tests only."""
+    _check("moe_debug_fail_tensor_maps", _lib.moe_debug_fail_tensor_maps(int(count)))
 
 
 def moe_launch_count():

@@ -12,6 +12,15 @@ namespace moe {
 namespace {
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
+std::atomic<int> g_fail_tmaps{0};   // injected encode failures still to hand out
+
+// Takes one injected failure, if any is pending.
+bool injected_failure() {
+  int n = g_fail_tmaps.load(std::memory_order_relaxed);
+  while (n > 0)
+    if (g_fail_tmaps.compare_exchange_weak(n, n - 1, std::memory_order_relaxed)) return true;
+  return false;
+}
 }  // namespace
 
 bool get_encode() {
@@ -28,6 +37,7 @@ bool get_encode() {
 
 // 2-D K-major operand [rows][cols] (elements of `esize` bytes), box 128 bytes x box_rows.
 bool make_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows, bool bf16) {
+  if (injected_failure()) return false;
   const int esize = bf16 ? 2 : 1;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * esize)};
@@ -42,6 +52,7 @@ bool make_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int
 
 // 2-D bf16 output [rows][cols] written by TMA stores, box 64 columns x 128 rows, 128-byte swizzle.
 bool make_tmap_out(CUtensorMap* m, void* base, int64_t rows, int64_t cols) {
+  if (injected_failure()) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
   cuuint32_t box[2] = {64, 128};
@@ -54,6 +65,7 @@ bool make_tmap_out(CUtensorMap* m, void* base, int64_t rows, int64_t cols) {
 // Scale atoms of a tiled-scale array as a 2-D map of uint32 [atoms][128]: one
 // box = one 512-byte atom (128 rows x 4 blocks), selected by its row coordinate.
 bool make_tmap_sf(CUtensorMap* m, const void* base, int64_t atoms) {
+  if (injected_failure()) return false;
   cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(atoms)};
   cuuint64_t strides[1] = {512};
   cuuint32_t box[2] = {128, 1};
@@ -263,6 +275,11 @@ int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int
 }
 
 }  // namespace moe
+
+extern "C" int moe_debug_fail_tensor_maps(int count) {
+  moe::g_fail_tmaps.store(count > 0 ? count : 0, std::memory_order_relaxed);
+  return MOE_OK;
+}
 
 extern "C" int moe_gemm_mxfp8(int M, int N, int K, const void* a, const void* a_sf, const void* b, const void* b_sf,
                               float* c, moe_stream_t stream) {
