@@ -141,6 +141,31 @@ def probe_peak(args):
                                   1.0, c.data_ptr(), sp)
     nv["tflops_burst"], nv["tflops_sustained"] = timeit(fn)
     out["ours_nvfp4"] = nv
+    del a4, b4, sf4, c
+    # the grouped NVFP4 expert GEMM over a real schedule (dsv3_e64 routing), GEMM2's
+    # shape: rank rows x d, K = I; FLOPs on the T*(k+S) assignment rows only
+    from moe_layer_dsv3_gb300.layer import MoELayer
+    shp = gen.config("dsv3_e64")
+    inp = gen.make_inputs(shp, seed=0, device=dev, weights=False)
+    L = MoELayer.from_shape(shp)
+    L.route(inp["x"], inp["w_router"], inp["bias"])
+    L.schedule()
+    Ep = shp.E + shp.S
+    Rmax = -(-shp.T * (shp.k + shp.S) // 128) * 128 + 128 * Ep
+    Ng, Kg = shp.d, shp.I
+    ag = torch.randint(0, 256, (Rmax, Kg // 2), dtype=torch.uint8, device=dev)
+    wg = torch.randint(0, 256, (Ep * Ng, Kg // 2), dtype=torch.uint8, device=dev)
+    sfa = torch.full((Rmax * Kg // 16,), 0x38, dtype=torch.uint8, device=dev)
+    sfw = torch.full((Ep * Ng * Kg // 16,), 0x38, dtype=torch.uint8, device=dev)
+    og = torch.empty((Rmax, Ng), dtype=torch.float32, device=dev)
+    fn = lambda: M.moe_expert_gemm_nvfp4(L.cfg, Ng, Kg, ag.data_ptr(), sfa.data_ptr(), wg.data_ptr(),  # noqa: E731
+                                         sfw.data_ptr(), 1.0, og.data_ptr(), L.ws.data_ptr(), sp)
+    flop_g = 2.0 * shp.T * (shp.k + shp.S) * Ng * Kg
+    b, su = timeit(fn)
+    out["ours_nvfp4_grouped"] = {
+        "name": "moe_expert_gemm_nvfp4 (grouped over the schedule, fp32 rank-ordered rows)",
+        "shape": "dsv3_e64 routing: %d assignment rows x N=%d x K=%d, %d experts" % (shp.T * (shp.k + shp.S), Ng, Kg, Ep),
+        "tflops_burst": b * flop_g / flop, "tflops_sustained": su * flop_g / flop}
     out["clocks"] = clocks.stop()
     print(json.dumps(out), flush=True)
 

@@ -344,6 +344,25 @@ MOE_API int moe_quantize_nvfp4(const void* src_bf16, int rows, int K, float g, v
 MOE_API int moe_gemm_nvfp4(int M, int N, int K, const void* a, const void* a_sf, const void* b, const void* b_sf,
                            float alpha, float* c, moe_stream_t stream);
 
+/* NVFP4 expert GEMM grouped by the schedule in `ws` (moe_schedule must have
+ * run on the same stream): for every expert e, routed and shared, and every
+ * padded rank row r of its segment [POFF[e], POFF[e+1]) (moe_ws_view),
+ *   out[r][n] (fp32) = alpha * sum_k dequant(a)[r][k] * dequant(w)[e*N + n][k],
+ * n < N: the expert GEMMs' grouped product in the 4-bit format (NVFP4 read as
+ * above; Cursor blog summary, opening paragraph).
+ *   a: packed E2M1 codes [Rmax][K/2] in rank order, a_sf their tiled E4M3
+ *      scales (moe_quantize_nvfp4, rows = Rmax); Rmax = the padded rank rows
+ *      of the workspace, ceil128(T*(k+S)) + 128*(E+S). Rows a segment pads
+ *      (past its expert's count) are multiplied like any other.
+ *   w: packed codes [(E+S)*N][K/2], expert e's block at rows e*N, w_sf tiled.
+ *   alpha: the product of the two tensor scales.
+ *   out: fp32 [Rmax][N]; rows at or past POFF[E+S] are not written.
+ * N a multiple of 128, K of 256; 16-byte aligned pointers.
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED_ARCH, MOE_ERR_CUDA. */
+MOE_API int moe_expert_gemm_nvfp4(const moe_config_t* cfg, int N, int K, const void* a, const void* a_sf,
+                                  const void* w, const void* w_sf, float alpha, float* out, void* ws,
+                                  moe_stream_t stream);
+
 /* Re-lay canonical scales [rows][K/32] into the tiled layout the tensor
  * cores read: 512-byte atoms of 128 rows x 4 blocks, atom (r/128, kb/4) at
  * ((r/128)*(K/128) + kb/4)*512, byte (r%32)*16 + (r/32%4)*4 + kb%4.

@@ -89,7 +89,7 @@ struct GemmCfg {
   static constexpr bool kBf16 = MODE == kRouterMode;
   // NVFP4: a 128-byte stage row holds 256 E2M1 values; the scales (one E4M3
   // per 16) of a stage are 4 atoms per 128 rows, one atom per K = 64 MMA.
-  static constexpr bool kNv4 = MODE == kPlainNv4;
+  static constexpr bool kNv4 = MODE == kPlainNv4 || MODE == kGroupedNv4;
   // Weight gradients stage their bf16 output tile in shared memory and write
   // it with TMA stores, so the tile's DRAM write overlaps the next mainloop.
   static constexpr bool kTmaOut = MODE == kWgrad;
@@ -150,7 +150,7 @@ __device__ __forceinline__ int gemm_num_tiles(const GemmParams& p) {
     return p.lapbase[p.Lb] * (p.N / BN);
   } else if constexpr (MODE == kSwigluFwd || MODE == kSwigluBwd) {
     return p.lap_tiles[p.lap * (p.Ep + 1) + p.Ep] * (p.N / BN);
-  } else if constexpr (MODE == kPush) {
+  } else if constexpr (MODE == kPush || MODE == kGroupedNv4) {
     return (p.poff[p.Ep] / 128) * (p.N / BN);
   } else if constexpr (MODE == kWgrad) {
     // positions of the two-ended schedule (see gemm_decode): enough rounds for the heavy half
@@ -208,7 +208,8 @@ __device__ __forceinline__ bool gemm_decode(const GemmParams& p, int tile, TileI
     const int nt = p.N / BN;
     const int g = tile / nt, n = tile - (tile / nt) * nt;
     return lap_decode<BN>(p, p.lap, g, n, 0, t);
-  } else if constexpr (MODE == kPush) {
+  } else if constexpr (MODE == kPush || MODE == kGroupedNv4) {
+    // padded rank rows of the schedule: m-tile g belongs to the expert whose segment holds it
     const int nt = p.N / BN;
     const int g = tile / nt, n = tile - (tile / nt) * nt;
     const int64_t prow0 = static_cast<int64_t>(g) * 128;
@@ -223,7 +224,7 @@ __device__ __forceinline__ bool gemm_decode(const GemmParams& p, int tile, TileI
     const int64_t v = p.counts[e] - (prow0 - p.poff[e]);
     t.valid = v < 0 ? 0 : (v > 128 ? 128 : static_cast<int>(v));
     t.n0 = n * BN;
-    t.m0 = 0;
+    t.m0 = MODE == kGroupedNv4 ? static_cast<int>(prow0) : 0;   // rank-ordered output rows
     return true;
   } else if constexpr (MODE == kWgrad) {
     // Two-ended schedule: in each round half of the CTAs take the next tile from
@@ -563,14 +564,14 @@ __device__ __forceinline__ void gemm_epilogue_tile(const GemmParams& p, const Ti
       for (int b = 0; b < BN / 64; ++b) tma_store_2d(routed ? tma_o : tma_o2, t.n0 + 64 * b, y, out_smem + b * 128 * 128);
       bulk_commit();
     }
-  } else {   // plain (fp32 out, M x N) and router logits (fp32 [M][N] for columns < N)
+  } else {   // plain and grouped NVFP4 (fp32 out, M x N) and router logits (fp32 [M][N] for columns < N)
     float* out = static_cast<float*>(p.out);
     const int64_t orow = t.m0 + row;
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
       float v[32];
       tmem_ld32(tacc + c * 32, v);
-      if constexpr (MODE == kPlainNv4) {
+      if constexpr (MODE == kPlainNv4 || MODE == kGroupedNv4) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(v[j], p.alpha);
       }

@@ -201,7 +201,8 @@ int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int
   p.out2 = ep.out2;
   p.ldo = ep.ldo;
   p.alpha = ep.alpha;
-  if (mode == kPlainNv4) p.a_ktiles = p.b_ktiles = K / 64;   // scale atoms (64 elements) per 128-row tile
+  if (mode == kPlainNv4 || mode == kGroupedNv4)
+    p.a_ktiles = p.b_ktiles = K / 64;   // scale atoms (64 elements) per 128-row tile
   p.q_rows = ep.q_rows;
   p.q_rows_sf = ep.q_rows_sf;
   p.q_rows_ktiles = ep.q_rows_ktiles;
@@ -230,7 +231,7 @@ int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int
     upper = lap_mtiles_max(m) * nt;
   } else if (mode == kSwigluFwd || mode == kSwigluBwd) {
     upper = (static_cast<int64_t>(m.E) * (m.C / 128) + (lap == 0 ? m.S * (m.Tpad / 128) : 0)) * nt;
-  } else if (mode == kPush) {
+  } else if (mode == kPush || mode == kGroupedNv4) {
     upper = (m.Rmax / 128) * nt;
   } else if (mode == kWgrad) {
     upper = static_cast<int64_t>(m.Ep) * (M / 128) * nt;
@@ -267,6 +268,9 @@ int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int
       return BN == 256 ? run<256, kPlain>(name, ta, ta2, tb, to, to2, p, grid, s) : run<128, kPlain>(name, ta, ta2, tb, to, to2, p, grid, s);
     case kPlainNv4:
       return BN == 256 ? run<256, kPlainNv4>(name, ta, ta2, tb, to, to2, p, grid, s) : run<128, kPlainNv4>(name, ta, ta2, tb, to, to2, p, grid, s);
+    case kGroupedNv4:
+      return BN == 256 ? run<256, kGroupedNv4>(name, ta, ta2, tb, to, to2, p, grid, s)
+                       : run<128, kGroupedNv4>(name, ta, ta2, tb, to, to2, p, grid, s);
     case kRouterMode:
       if (BN == 32) return run<32, kRouterMode>(name, ta, ta2, tb, to, to2, p, grid, s);
       return BN == 256 ? run<256, kRouterMode>(name, ta, ta2, tb, to, to2, p, grid, s) : run<128, kRouterMode>(name, ta, ta2, tb, to, to2, p, grid, s);

@@ -80,6 +80,40 @@ extern "C" int moe_quantize_nvfp4(const void* src, int rows, int K, float g, voi
   return call.status();
 }
 
+extern "C" int moe_expert_gemm_nvfp4(const moe_config_t* cfg, int N, int K, const void* a, const void* a_sf,
+                                     const void* w, const void* w_sf, float alpha, float* out, void* ws,
+                                     moe_stream_t stream) {
+  if (int r = moe::validate(cfg)) return r;
+  if (N <= 0 || K <= 0 || N % 128 || K % 256 || !a || !a_sf || !w || !w_sf || !out || !ws) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(a_sf) |
+       reinterpret_cast<uintptr_t>(w_sf) | reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(ws)) & 15u)
+    return MOE_ERR_INVALID_ARG;
+  if (!moe::arch_ok()) return MOE_ERR_UNSUPPORTED_ARCH;
+  moe::CallScope call;
+  const moe::Layout L = moe::make_layout(cfg);
+  const moe::Dims& m = L.m;
+  if (m.T == 0) return MOE_OK;
+  moe::GemmOperands op{};
+  op.a = static_cast<const uint8_t*>(a);
+  op.a_rows = m.Rmax;
+  op.a_cols = K / 2;      // packed bytes per row
+  op.a_sf = static_cast<const uint8_t*>(a_sf);
+  op.b = static_cast<const uint8_t*>(w);
+  op.b_rows = static_cast<int64_t>(m.Ep) * N;
+  op.b_cols = K / 2;
+  op.b_sf = static_cast<const uint8_t*>(w_sf);
+  moe::GemmEpilogue ep{};
+  ep.out = out;
+  ep.ldo = N;
+  ep.alpha = alpha;
+  if (int r = moe::gemm_dispatch("expert_gemm_nvfp4", moe::kGroupedNv4, m, 0, N, K, static_cast<int>(m.Rmax), op, ep,
+                                 moe::ws_ptr<int>(L, ws, MOE_WS_COUNTS), moe::ws_ptr<int>(L, ws, MOE_WS_POFF),
+                                 nullptr, nullptr, moe::ws_ptr<int>(L, ws, MOE_WS_STATUS),
+                                 static_cast<cudaStream_t>(stream)))
+    return r;
+  return call.status();
+}
+
 extern "C" int moe_gemm_nvfp4(int M, int N, int K, const void* a, const void* a_sf, const void* b, const void* b_sf,
                               float alpha, float* c, moe_stream_t stream) {
   if (M <= 0 || N <= 0 || K <= 0 || M % 128 || N % 128 || K % 256 || !a || !a_sf || !b || !b_sf || !c)

@@ -119,3 +119,49 @@ def test_quantise_then_gemm_matches_oracle_chain(lib):
     qb, sb, _ = N.quantize(b.float().numpy(), gb)
     ref = N.dequantize(qa, sa, 1.0) @ N.dequantize(qb, sb, 1.0).T * (float(ga) * float(gb))
     assert rel_frob(C.cpu().numpy(), ref) < 1e-5
+
+
+@pytest.mark.parametrize("Nn,K", [(384, 512), (256, 1024)])
+def test_expert_gemm_nvfp4_grouped(lib, Nn, K):
+    """The grouped NVFP4 expert GEMM over a real schedule (routed and shared experts, ragged
+    counts, one expert without tokens) against per-expert fp64 products of the oracle's codes;
+    rows past the last segment stay untouched."""
+    import gen
+    from moe_layer_dsv3_gb300.layer import MoELayer
+    shape = gen.make_shape("nv4g", 300, 256, 8, 2, 1, 1, 128, 1, "normal0.1", 0.02)
+    inp = gen.make_inputs(shape, seed=21, device="cuda", weights=False)
+    bias = inp["bias"].clone()
+    bias[3] = -1.0e4                                                   # expert 3 never selected
+    L = MoELayer.from_shape(shape)
+    L.route(inp["x"], inp["w_router"], bias)
+    L.schedule()
+    torch.cuda.synchronize()
+    Ep = shape.E + shape.S
+    poff = L.ws_tensor("POFF", torch.int32, (Ep + 1,)).cpu().numpy().astype(np.int64)
+    counts = L.ws_tensor("COUNTS", torch.int32, (Ep,)).cpu().numpy()
+    assert counts[3] == 0 and counts[shape.E] == shape.T
+    Rmax = -(-shape.T * (shape.k + shape.S) // 128) * 128 + 128 * Ep
+    R = int(poff[Ep])
+    rng = np.random.default_rng(Nn + K)
+    a = rng.normal(0, 1, (Rmax, K)) * np.exp2(rng.integers(-3, 4, (Rmax, 1)))
+    a[R:] = 0.0
+    w = rng.normal(0, 1, (Ep * Nn, K)) * np.exp2(rng.integers(-3, 4, (Ep * Nn, 1)))
+    qa, sa, ga = N.quantize(a.astype(np.float32))
+    qw, sw, gw = N.quantize(w.astype(np.float32))
+    dev = lambda z: torch.from_numpy(np.ascontiguousarray(z)).cuda()   # noqa: E731
+    A, W = dev(N.pack(qa)), dev(N.pack(qw))
+    Asf, Wsf = dev(_tile16(sa, Rmax, K)), dev(_tile16(sw, Ep * Nn, K))
+    out = torch.full((Rmax, Nn), 7.0, dtype=torch.float32, device="cuda")
+    alpha = np.float32(np.float32(ga) * np.float32(gw))
+    lib.moe_expert_gemm_nvfp4(L.cfg, Nn, K, A.data_ptr(), Asf.data_ptr(), W.data_ptr(), Wsf.data_ptr(), float(alpha),
+                              out.data_ptr(), L.ws.data_ptr())
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().astype(np.float64)
+    da, dw = N.dequantize(qa, sa, 1.0), N.dequantize(qw, sw, 1.0)
+    for e in range(Ep):
+        rows = slice(int(poff[e]), int(poff[e + 1]))
+        if poff[e + 1] == poff[e]:
+            continue
+        ref = da[rows] @ dw[e * Nn:(e + 1) * Nn].T * (float(ga) * float(gw))
+        assert rel_frob(got[rows], ref) < 1e-5, e
+    assert (got[R:] == 7.0).all()
