@@ -286,6 +286,9 @@ enum {
   MOE_WS_MOVED,        /* int32[...]   per lap m-tile: 8-row groups moved into the ring */
   MOE_WS_CONSUMED,     /* int32[...]   per lap m-tile: GEMM tiles that finished reading it */
   MOE_WS_DH,           /* f32[Rmax][I] dh = dO W_d at padded rank rows (input of the SwiGLU backward) */
+  MOE_WS_LAPORDER,     /* int32[...]   position -> lap-major m-tile: the order the all-laps launches walk
+                          (an expert's laps 2P and 2P+1 side by side; its pairs spread over the walk) */
+  MOE_WS_LAPKEY,       /* int32[3][...] scratch of the walk-order sort: lap-pair units, their ranks, prefix sums */
   MOE_WS_COUNT
 };
 MOE_API int moe_ws_view(const moe_config_t* cfg, void* ws, int which, void** ptr, size_t* bytes);

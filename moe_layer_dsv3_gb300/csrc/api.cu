@@ -105,6 +105,7 @@ inline bool all_al16(const P*... p) { return (al16(p) && ...); }
 RingMovers ring_movers(const Layout& L, void* ws, cudaStream_t s) {
   RingMovers mv{};
   mv.lapbase = ws_ptr<int>(L, ws, MOE_WS_LAPBASE);
+  mv.laporder = ws_ptr<int>(L, ws, MOE_WS_LAPORDER);
   mv.moved = ws_ptr<int>(L, ws, MOE_WS_MOVED);
   mv.consumed = ws_ptr<int>(L, ws, MOE_WS_CONSUMED);
   note(cudaMemsetAsync(mv.moved, 0, L.bytes[MOE_WS_MOVED], s));
@@ -210,6 +211,8 @@ Layout make_layout(const moe_config_t* c) {
   b.add(L.off, L.bytes, MOE_WS_MOVED, 4 * static_cast<size_t>(lap_mtiles_max(m)));
   b.add(L.off, L.bytes, MOE_WS_CONSUMED, 4 * static_cast<size_t>(lap_mtiles_max(m)));
   b.add(L.off, L.bytes, MOE_WS_DH, 4 * static_cast<size_t>(m.Rmax) * m.I);
+  b.add(L.off, L.bytes, MOE_WS_LAPORDER, 4 * static_cast<size_t>(lap_mtiles_max(m)));
+  b.add(L.off, L.bytes, MOE_WS_LAPKEY, 12 * static_cast<size_t>(lap_mtiles_max(m)));
   L.total = b.cur;
   return L;
 }

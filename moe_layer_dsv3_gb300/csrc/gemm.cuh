@@ -21,9 +21,13 @@
 //                producer waits for all 16 before its first TMA load of gm;
 //   consumed[gm] tiles of gm whose A loads have landed; the movers of the
 //                same slot's next tenant (lap + 2) wait for all N / BN.
-// Both lists are walked in increasing (lap-major) order by every CTA and
-// every wait points to an earlier lap or to a move of the same lap, so the
-// waits cannot form a cycle once all CTAs are resident (cooperative launch).
+// Both lists are walked by every CTA in increasing position of the schedule's
+// walk order (LAPORDER: laps 2P and 2P+1 of an expert side by side, so its
+// weights stream once for both, and each expert's pairs spread evenly over
+// the launch). Every position's previous ring tenant (lap - 2) sits at an
+// earlier position, so every wait points to an earlier position or to a move
+// of the same one, and the waits cannot form a cycle once all CTAs are
+// resident (cooperative launch).
 #pragma once
 #include <cuda_bf16.h>
 
@@ -79,6 +83,7 @@ struct GemmParams {
   int* status;
   // all-laps ring modes
   const int* lapbase; int Lb; int d;
+  const int* laporder;   // position -> global m-tile (pair-spread order), walked in position order
   int* moved; int* consumed;
   const uint8_t* mv_xq; const uint8_t* mv_xq_sf;
   uint8_t* ring; uint8_t* ring_sf;
@@ -196,9 +201,10 @@ __device__ __forceinline__ bool gemm_decode(const GemmParams& p, int tile, TileI
   using Cf = GemmCfg<BN, MODE>;
   t.gm = -1;
   if constexpr (ring_mode(MODE)) {
-    // global m-tile gm (laps in order), n-tile n
+    // position pos of the walk (laporder maps it to the lap-major global m-tile gm), n-tile n
     const int nt = p.N / BN;
-    const int gm = tile / nt, n = tile - gm * nt;
+    const int pos = tile / nt, n = tile - pos * nt;
+    const int gm = p.laporder[pos];
     const int L = seg_search(p.lapbase, p.Lb, gm);
     const bool ok = lap_decode<BN>(p, L, gm - p.lapbase[L], n,
                                    static_cast<int64_t>(L % kRingBufs) * p.E * p.C, t);
@@ -393,7 +399,8 @@ __device__ void ring_mover(const GemmParams& p, int wid, int lane) {
   const int total = p.lapbase[p.Lb] * kMoveItems;
   const int stride = gridDim.x * MV;
   for (int j = blockIdx.x * MV + wid; j < total; j += stride) {
-    const int gm = j / kMoveItems, part = j - gm * kMoveItems;
+    const int pos = j / kMoveItems, part = j - pos * kMoveItems;
+    const int gm = p.laporder[pos];
     const int L = seg_search(p.lapbase, p.Lb, gm);
     const int g = gm - p.lapbase[L];
     const int* lt = p.lap_tiles + static_cast<int64_t>(L) * (p.Ep + 1);

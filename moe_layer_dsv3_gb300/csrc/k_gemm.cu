@@ -215,6 +215,7 @@ int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int
   p.status = status;
   if (mv != nullptr) {
     p.lapbase = mv->lapbase;
+    p.laporder = mv->laporder;
     p.Lb = m.Lb;
     p.d = m.d;
     p.moved = mv->moved;

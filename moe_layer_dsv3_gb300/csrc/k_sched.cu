@@ -142,6 +142,124 @@ __global__ void sched_offsets_kernel(const int* counts, int E, int Ep, int C, in
   }
 }
 
+// Exclusive prefix sum of one value per thread over the block (1024 threads).
+__device__ __forceinline__ int block_exscan(int v, int* sm, int& total) {
+  sm[threadIdx.x] = v;
+  __syncthreads();
+  for (int off = 1; off < blockDim.x; off <<= 1) {
+    const int t = threadIdx.x >= off ? sm[threadIdx.x - off] : 0;
+    __syncthreads();
+    sm[threadIdx.x] += t;
+    __syncthreads();
+  }
+  const int incl = sm[threadIdx.x];
+  total = sm[blockDim.x - 1];
+  __syncthreads();
+  return incl - v;
+}
+
+constexpr int kKeyUnits = 2048;
+
+// Walk order of the all-laps launches (order[position] = lap-major m-tile gm).
+// A unit is an expert's lap pair P (laps 2P and 2P + 1, whose tiles stay side
+// by side, lap 2P first, so the expert's weights stream once for both). An
+// expert with two or more pairs has its pairs at key (2P + 1) / (2 pairs),
+// spread evenly over the walk; the experts with one pair (at most two laps,
+// and the shared experts) take (2i + 1) / (2 n_one) in expert order. Units go
+// by ascending key (compared exactly as integers), then expert, then pair.
+// One block of 1024 threads; scratch holds 3 * cap ints (units, their ranks,
+// the tile counts in rank order, then their prefix sums).
+__global__ void __launch_bounds__(1024) sched_laporder_kernel(const int* __restrict__ counts, int E, int Ep, int C,
+                                                              int Lb, const int* __restrict__ lapbase,
+                                                              const int* __restrict__ lap_tiles, int64_t cap,
+                                                              int* __restrict__ scratch, int* __restrict__ order) {
+  __shared__ int sm[1024];
+  __shared__ int s_pairs[1024], s_one[1024];
+  __shared__ int s_num[kKeyUnits], s_den[kKeyUnits], s_unit[kKeyUnits];
+  int* unit = scratch;             // e | P << 16
+  int* urank = scratch + cap;
+  int* stile = scratch + 2 * cap;  // tiles by rank, then their exclusive prefix
+  const int e = threadIdx.x;
+  int pairs = 0;
+  if (e < Ep) {
+    const int n = counts[e];
+    const int laps = e < E ? (n + C - 1) / C : (n > 0 ? 1 : 0);
+    pairs = (laps + 1) / 2;
+  }
+  int U = 0, n_one = 0;
+  const int ubase = block_exscan(pairs, sm, U);
+  const int one = block_exscan(pairs == 1 ? 1 : 0, sm, n_one);
+  s_pairs[e] = pairs;
+  s_one[e] = one;
+  for (int P = 0; P < pairs; ++P) unit[ubase + P] = e | (P << 16);
+  __syncthreads();
+  auto tiles_of = [&](int ue, int P) {
+    int t = 0;
+    for (int L = 2 * P; L < 2 * P + 2 && L < Lb; ++L) {
+      const int* lt = lap_tiles + static_cast<int64_t>(L) * (Ep + 1);
+      t += lt[ue + 1] - lt[ue];
+    }
+    return t;
+  };
+  // key of unit u: num / den; units of up to kKeyUnits are compared from shared memory
+  auto key_of = [&](int u, int& num, int& den) {
+    const int ue = unit[u] & 0xFFFF, P = unit[u] >> 16;
+    const bool spread = s_pairs[ue] >= 2;
+    num = spread ? 2 * P + 1 : 2 * s_one[ue] + 1;
+    den = spread ? 2 * s_pairs[ue] : 2 * n_one;
+  };
+  const bool in_smem = U <= kKeyUnits;
+  if (in_smem) {
+    for (int u = threadIdx.x; u < U; u += blockDim.x) {
+      key_of(u, s_num[u], s_den[u]);
+      s_unit[u] = unit[u];
+    }
+    __syncthreads();
+  }
+  for (int u = threadIdx.x; u < U; u += blockDim.x) {
+    const int uu = unit[u];
+    int num, den;
+    key_of(u, num, den);
+    int rank = 0;
+    for (int v = 0; v < U; ++v) {
+      int vn, vd, vu;
+      if (in_smem) {
+        vn = s_num[v]; vd = s_den[v]; vu = s_unit[v];
+      } else {
+        key_of(v, vn, vd);
+        vu = unit[v];
+      }
+      const int64_t lhs = static_cast<int64_t>(vn) * den, rhs = static_cast<int64_t>(num) * vd;   // key(v) < key(u)
+      // ties: lower expert, then lower pair (unit = e | P << 16 with e < 2^16)
+      const bool before = lhs < rhs || (lhs == rhs && ((vu & 0xFFFF) < (uu & 0xFFFF) ||
+                                                        ((vu & 0xFFFF) == (uu & 0xFFFF) && (vu >> 16) < (uu >> 16))));
+      rank += before ? 1 : 0;
+    }
+    urank[u] = rank;
+    stile[rank] = tiles_of(uu & 0xFFFF, uu >> 16);
+  }
+  __syncthreads();
+  int carry = 0;   // exclusive prefix of stile over ranks, 1024 at a time
+  for (int c0 = 0; c0 < U; c0 += blockDim.x) {
+    const int r = c0 + threadIdx.x;
+    const int v = r < U ? stile[r] : 0;
+    int chunk = 0;
+    const int ex = block_exscan(v, sm, chunk);
+    if (r < U) stile[r] = carry + ex;
+    carry += chunk;
+    __syncthreads();
+  }
+  for (int u = threadIdx.x; u < U; u += blockDim.x) {
+    const int ue = unit[u] & 0xFFFF, P = unit[u] >> 16;
+    int pos = stile[urank[u]];
+    for (int L = 2 * P; L < 2 * P + 2 && L < Lb; ++L) {
+      const int* lt = lap_tiles + static_cast<int64_t>(L) * (Ep + 1);
+      const int base = lapbase[L] + lt[ue];
+      for (int mt = 0; mt < lt[ue + 1] - lt[ue]; ++mt) order[pos++] = base + mt;
+    }
+  }
+}
+
 // Experts ordered by descending count, ties to the lower index (order[rank] = e).
 __global__ void sched_order_kernel(const int* __restrict__ counts, int Ep, int* __restrict__ order) {
   for (int e = threadIdx.x; e < Ep; e += blockDim.x) {
@@ -213,6 +331,9 @@ void launch_schedule(const Dims& m, const int32_t* idx, const Layout& L, void* w
   }
   launch_kernel("sched_offsets", sched_offsets_kernel, dim3(1), dim3(256), 0, s, counts, m.E, m.Ep, m.C, m.Lb, offsets,
                 poff, lap_tiles, meta, ws_ptr<int>(L, ws, MOE_WS_LAPBASE));
+  launch_kernel("sched_laporder", sched_laporder_kernel, dim3(1), dim3(1024), 0, s, counts, m.E, m.Ep, m.C, m.Lb,
+                ws_ptr<int>(L, ws, MOE_WS_LAPBASE), lap_tiles, lap_mtiles_max(m), ws_ptr<int>(L, ws, MOE_WS_LAPKEY),
+                ws_ptr<int>(L, ws, MOE_WS_LAPORDER));
   launch_kernel("sched_order", sched_order_kernel, dim3(1), dim3(512), 0, s, counts, m.Ep, ws_ptr<int>(L, ws, MOE_WS_ORDER));
   if (m.units > 0) {
     launch_kernel("sched_rank", sched_rank_kernel, dim3(blocks), dim3(kWarps * 32), shm, s, idx, m.T, m.k, m.kp, m.E,

@@ -160,6 +160,7 @@ enum GemmMode : int {
 // Where the mover warps of the all-laps ring modes take each ring row from.
 struct RingMovers {
   const int* lapbase;            // [Lb+1] first global m-tile of each lap
+  const int* laporder;           // position -> global m-tile: the order CTAs walk tiles and move items
   int* moved;                    // per global m-tile: 8-row groups written (target 16)
   int* consumed;                 // per global m-tile: GEMM tiles whose A loads landed (target N / BN)
   const uint8_t* xq; const uint8_t* xq_sf;   // MX rows along d (x forward, dy backward), tiled scales

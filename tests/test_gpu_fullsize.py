@@ -342,6 +342,16 @@ def test_bitwise_rerun(full):
     assert _checksum(L.dw_d) == h_d
 
 
+def test_walk_order_full_size(full):
+    """LAPORDER at full size (17 laps at dsv3_zipf) equals the host model's walk order."""
+    from tests.test_ring_protocol import walk_order
+    s = full.shape
+    counts = [int(c) for c in full.L.ws_tensor("COUNTS", torch.int32, (full.Ep,)).cpu().numpy()]
+    ref = walk_order(counts, s.E, s.S, s.C, s.T)
+    got = full.L.ws_tensor("LAPORDER", torch.int32, (len(ref),)).cpu().numpy()
+    assert np.array_equal(got, np.asarray(ref))
+
+
 def test_idle_expert_weight_grads_full_size(full):
     """Experts without tokens get all-zero weight gradients whatever the buffers held (their
     tiles are stored by the weight-gradient kernels' zero-fill warp), and rewriting the buffers

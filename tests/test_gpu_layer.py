@@ -198,6 +198,18 @@ def _rings(run, name):
     return codes, sf
 
 
+def test_walk_order_matches_model(run):
+    """The schedule's walk order of the all-laps launches (LAPORDER) equals the order the
+    host protocol model restates from its definition (the model's replay checks it cannot
+    deadlock)."""
+    from tests.test_ring_protocol import walk_order
+    m = run.shape
+    counts = [int(c) for c in run.ws("COUNTS", torch.int32, (run.Ep,)).cpu().numpy()]
+    ref = walk_order(counts, m.E, m.S, m.C, m.T)
+    got = run.ws("LAPORDER", torch.int32, (len(ref),)).cpu().numpy()
+    assert np.array_equal(got, np.asarray(ref))
+
+
 def test_ring_holds_last_laps(run):
     """Lap L of an expert goes to ring buffer L % NBUF: after forward, buffer (last % NBUF) holds
     the expert's final lap (zeros past it up to the tile end) and buffer ((last-1) % NBUF) its

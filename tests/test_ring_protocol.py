@@ -3,12 +3,17 @@
 The cooperative GEMM launch of modes 6/7 orders ring refills with two
 per-m-tile counters: producers wait for moved[gm] == 16 before loading an
 m-tile, and the movers of lap L wait for consumed[gm'] == N/BN of the same
-slot's previous tenant (lap L - 2). This model replays that protocol on
-concrete schedules with every CTA walking its tiles and move items in the
-kernel's order, and checks that it always makes progress (no wait cycle),
-that the previous tenant is the same (expert, m-tile), and that every index
-stays inside the buffers the host sizes, for 1, 2 and 4 mover warps per CTA.
+slot's previous tenant (lap L - 2). CTAs walk tiles and move items in the
+schedule's walk order (LAPORDER: position -> lap-major m-tile gm). This model
+restates that order from its definition, replays the protocol on concrete
+schedules with every CTA walking its tiles and move items in that order, and
+checks that it always makes progress (no wait cycle), that the previous
+tenant is the same (expert, m-tile) at an earlier position, and that every
+index stays inside the buffers the host sizes, for 1, 2 and 4 mover warps
+per CTA. The lap-major order (identity walk) is replayed too.
 """
+from fractions import Fraction
+
 import numpy as np
 import pytest
 
@@ -48,7 +53,33 @@ def seg(v, n, x):
     return lo
 
 
-def replay(counts, E, S, T, C, grid, nt, mv=2):
+def walk_order(counts, E, S, C, T):
+    """LAPORDER: lap-major m-tiles sorted by (key, expert, gm). An expert's unit is
+    its lap pair P = L // 2; an expert with two or more pairs has key (2P+1) / (2 pairs),
+    the experts with one pair take (2i+1) / (2 n_one) in expert order."""
+    Ep = E + S
+    lt, lapbase, Lb = lap_schedule(counts, E, S, C, T)
+    laps = [cdiv(counts[e], C) if e < E else (1 if counts[e] > 0 else 0) for e in range(Ep)]
+    pairs = [(n + 1) // 2 for n in laps]
+    one_idx, n_one = {}, 0
+    for e in range(Ep):
+        if pairs[e] == 1:
+            one_idx[e] = n_one
+            n_one += 1
+    keys = []
+    for L in range(Lb):
+        for e in range(Ep):
+            for mt in range(lt[L, e + 1] - lt[L, e] if e + 1 <= Ep else 0):
+                gm = int(lapbase[L] + lt[L, e] + mt)
+                key = Fraction(2 * (L // 2) + 1, 2 * pairs[e]) if pairs[e] >= 2 else Fraction(2 * one_idx[e] + 1, 2 * n_one)
+                keys.append((key, e, gm))
+    keys.sort()
+    order = [gm for _, _, gm in keys]
+    assert sorted(order) == list(range(int(lapbase[-1])))
+    return order
+
+
+def replay(counts, E, S, T, C, grid, nt, mv=2, order=None):
     Ep = E + S
     lt, lapbase, Lb = lap_schedule(counts, E, S, C, T)
     A = int(sum(counts[:E]))
@@ -62,6 +93,9 @@ def replay(counts, E, S, T, C, grid, nt, mv=2):
         e = seg(lt[L], Ep, g)
         return L, g, e, g - lt[L, e]
 
+    if order is None:
+        order = walk_order(counts, E, S, C, T)
+    position = {gm: i for i, gm in enumerate(order)}
     moved = np.zeros(ntot, int)
     consumed = np.zeros(ntot, int)
     prod = [list(range(c, ntot * nt, grid)) for c in range(grid)]
@@ -72,7 +106,7 @@ def replay(counts, E, S, T, C, grid, nt, mv=2):
         progressed = False
         for c, tiles in enumerate(prod):
             while pi[c] < len(tiles):
-                gm = tiles[pi[c]] // nt
+                gm = order[tiles[pi[c]] // nt]
                 L, g, e, mt = decode(gm)
                 if e < E:
                     row = ((L % RING_BUFS) * E + e) * C + mt * 128
@@ -84,7 +118,7 @@ def replay(counts, E, S, T, C, grid, nt, mv=2):
                 progressed = True
         for w, items in enumerate(movers):
             while mi[w] < len(items):
-                gm = items[mi[w]] // MOVE_ITEMS
+                gm = order[items[mi[w]] // MOVE_ITEMS]
                 L, g, e, mt = decode(gm)
                 if g >= lt[L, E]:               # shared-expert tile: no move
                     mi[w] += 1
@@ -93,6 +127,7 @@ def replay(counts, E, S, T, C, grid, nt, mv=2):
                 if L >= RING_BUFS:
                     gp = lapbase[L - RING_BUFS] + lt[L - RING_BUFS, e] + mt
                     assert decode(gp)[2:] == (e, mt)
+                    assert position[gp] < position[gm]     # the previous tenant is walked first
                     if consumed[gp] < nt:
                         break
                 moved[gm] += 1
@@ -118,6 +153,30 @@ def test_zipf_wrap_schedule_progresses(grid, mv):
     counts = zipf_counts(64, 2048, 8, 1.1, 0) + [2048]
     assert max(counts[:64]) > 3 * 128                    # several laps of C=128
     replay(counts, 64, 1, 2048, 128, grid, 16, mv)
+    replay(counts, 64, 1, 2048, 128, grid, 16, mv, order=list(range(replay(counts, 64, 1, 2048, 128, 1, 16, 1))))
+
+
+def test_walk_order_pairs_and_spread():
+    """The walk keeps an expert's laps 2P and 2P+1 side by side and spreads its pairs:
+    every hot expert's pair P starts later than its pair P-1, and the hottest
+    expert's pairs are not bunched at the end of the walk."""
+    counts = zipf_counts(64, 2048, 8, 1.1, 0) + [2048]
+    E, S, C, T = 64, 1, 128, 2048
+    lt, lapbase, Lb = lap_schedule(counts, E, S, C, T)
+    order = walk_order(counts, E, S, C, T)
+    pos = {gm: i for i, gm in enumerate(order)}
+
+    def tiles(e, L):
+        return [int(lapbase[L] + lt[L, e] + mt) for mt in range(lt[L, e + 1] - lt[L, e])]
+    hot = int(np.argmax(counts[:E]))
+    laps = cdiv(counts[hot], C)
+    first = []
+    for P in range((laps + 1) // 2):
+        span = [pos[g] for L in (2 * P, 2 * P + 1) if L < laps for g in tiles(hot, L)]
+        assert max(span) - min(span) + 1 == len(span)    # the pair is contiguous in the walk
+        first.append(min(span))
+    assert first == sorted(first)
+    assert first[0] < len(order) // 4 and first[-1] > len(order) // 2
 
 
 @pytest.mark.parametrize("mv", [1, 2, 4])
