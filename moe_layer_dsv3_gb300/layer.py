@@ -94,7 +94,7 @@ class MoELayer:
         """Record one whole step (route, schedule, forward, backward) into a CUDA graph.
 
         The library allocates nothing and never synchronises inside these calls,
-        so the step captures as-is: 22 kernel nodes (plus the counter memsets),
+        so the step captures as-is: 23 kernel nodes (plus the counter memsets),
         including the cooperative all-laps GEMM launches and the backward's
         side-stream branch (reverse-dispatch beside the weight gradients). Replaying the graph
         re-runs the step on whatever x, dy, w_router and bias hold at that time
