@@ -345,33 +345,39 @@ constexpr int kFwdU = 8;
 
 __device__ __forceinline__ void move_rows(const GemmParams& p, int lane, int a_lane, int64_t ring_row0) {
   const int d = p.d;
-  const int chunks = d >> 4;
-  const int total = kMoveRows * chunks;
-  const int rounds = (total + 32 * kFwdU - 1) / (32 * kFwdU);
+  const int chunks = d >> 4;   // 16-byte chunks per row (d is a multiple of 128: at least 8)
+  const int rounds = (kMoveRows * chunks + 32 * kFwdU - 1) / (32 * kFwdU);
   const int tok_l = a_lane >= 0 ? a_lane / p.k : -1;
   const uint4 zero = make_uint4(0, 0, 0, 0);
+  // Flat chunk f = (round * kFwdU + u) * 32 + lane is (row r, chunk c); both
+  // cursors advance by 32 chunks a step, so no division per chunk.
+  int lr = lane / chunks, lc = lane - lr * chunks;   // load cursor
+  int sr = lr, sc = lc;                              // store cursor (one round behind)
+  auto step = [&](int& r, int& c) {
+    c += 32;
+    while (c >= chunks) { c -= chunks; ++r; }   // at most 32 / chunks times
+  };
   uint4 nxt[kFwdU];
-  auto load = [&](int rd, uint4* v) {
+  auto load = [&](uint4* v) {
 #pragma unroll
     for (int u = 0; u < kFwdU; ++u) {
-      const int f = (rd * kFwdU + u) * 32 + lane;
-      const int r = f / chunks, c = f - (f / chunks) * chunks;
-      const int t = __shfl_sync(0xffffffffu, tok_l, r < kMoveRows ? r : kMoveRows - 1);
-      v[u] = (f < total && t >= 0) ? __ldg(reinterpret_cast<const uint4*>(p.mv_xq + static_cast<int64_t>(t) * d) + c)
-                                   : zero;
+      const int t = __shfl_sync(0xffffffffu, tok_l, lr < kMoveRows ? lr : kMoveRows - 1);
+      v[u] = (lr < kMoveRows && t >= 0)
+                 ? __ldg(reinterpret_cast<const uint4*>(p.mv_xq + static_cast<int64_t>(t) * d) + lc)
+                 : zero;
+      step(lr, lc);
     }
   };
-  load(0, nxt);
+  load(nxt);
   for (int rd = 0; rd < rounds; ++rd) {
     uint4 cur[kFwdU];
 #pragma unroll
     for (int u = 0; u < kFwdU; ++u) cur[u] = nxt[u];
-    if (rd + 1 < rounds) load(rd + 1, nxt);
+    if (rd + 1 < rounds) load(nxt);
 #pragma unroll
     for (int u = 0; u < kFwdU; ++u) {
-      const int f = (rd * kFwdU + u) * 32 + lane;
-      const int r = f / chunks, c = f - (f / chunks) * chunks;
-      if (f < total) reinterpret_cast<uint4*>(p.ring + (ring_row0 + r) * d)[c] = cur[u];
+      if (sr < kMoveRows) reinterpret_cast<uint4*>(p.ring + (ring_row0 + sr) * d)[sc] = cur[u];
+      step(sr, sc);
     }
   }
   const int ktiles = d >> 7;
