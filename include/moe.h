@@ -289,6 +289,8 @@ enum {
   MOE_WS_LAPORDER,     /* int32[...]   position -> lap-major m-tile: the order the all-laps launches walk
                           (an expert's laps 2P and 2P+1 side by side; its pairs spread over the walk) */
   MOE_WS_LAPKEY,       /* int32[3][...] scratch of the walk-order sort: lap-pair units, their ranks, prefix sums */
+  MOE_WS_XQ_SFC,       /* u8[T][d/32]   scales of XQ, row-major (the ring movers' source) */
+  MOE_WS_DOS_SFC,      /* u8[T][d/32]   scales of DOS, row-major (the dO-ring movers' source) */
   MOE_WS_COUNT
 };
 MOE_API int moe_ws_view(const moe_config_t* cfg, void* ws, int which, void** ptr, size_t* bytes);

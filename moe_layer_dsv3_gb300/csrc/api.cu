@@ -213,6 +213,8 @@ Layout make_layout(const moe_config_t* c) {
   b.add(L.off, L.bytes, MOE_WS_DH, 4 * static_cast<size_t>(m.Rmax) * m.I);
   b.add(L.off, L.bytes, MOE_WS_LAPORDER, 4 * static_cast<size_t>(lap_mtiles_max(m)));
   b.add(L.off, L.bytes, MOE_WS_LAPKEY, 12 * static_cast<size_t>(lap_mtiles_max(m)));
+  b.add(L.off, L.bytes, MOE_WS_XQ_SFC, T * d / 32);
+  b.add(L.off, L.bytes, MOE_WS_DOS_SFC, T * d / 32);
   L.total = b.cur;
   return L;
 }
@@ -374,7 +376,7 @@ int moe_dispatch(const moe_config_t* cfg, const void* x, void* ws, moe_stream_t 
     note(cudaMemsetAsync(xq + m.T * m.d, 0, (m.Tpad - m.T) * m.d, s));
     note(cudaMemsetAsync(xq_sf + (m.T / 128) * 128 * (m.d / 32), 0, (m.Tpad - m.T / 128 * 128) * (m.d / 32), s));
   }
-  launch_quant_rows(x, m.T, m.d, m.d, xq, xq_sf, true, 0, s);
+  launch_quant_rows(x, m.T, m.d, m.d, xq, xq_sf, true, 0, s, ws_ptr<uint8_t>(L, ws, MOE_WS_XQ_SFC));
   launch_dispatch_all(m, L, ws, s);
   return call.status();
 }
@@ -398,7 +400,7 @@ int moe_forward(const moe_config_t* cfg, const void* x, const void* wq, const fl
     note(cudaMemsetAsync(xq + m.T * m.d, 0, (m.Tpad - m.T) * m.d, s));
     note(cudaMemsetAsync(xq_sf + (m.T / 128) * 128 * (m.d / 32), 0, (m.Tpad - m.T / 128 * 128) * (m.d / 32), s));
   }
-  launch_quant_rows(x, m.T, m.d, m.d, xq, xq_sf, true, 0, s);
+  launch_quant_rows(x, m.T, m.d, m.d, xq, xq_sf, true, 0, s, ws_ptr<uint8_t>(L, ws, MOE_WS_XQ_SFC));
   int* counts = ws_ptr<int>(L, ws, MOE_WS_COUNTS);
   int* poff = ws_ptr<int>(L, ws, MOE_WS_POFF);
   int* lap_tiles = ws_ptr<int>(L, ws, MOE_WS_LAPTILES);
@@ -430,6 +432,7 @@ int moe_forward(const moe_config_t* cfg, const void* x, const void* wq, const fl
     RingMovers mv = ring_movers(L, ws, s);
     mv.xq = xq;
     mv.xq_sf = xq_sf;
+    mv.xq_sfr = ws_ptr<uint8_t>(L, ws, MOE_WS_XQ_SFC);
     mv.ring = ws_ptr<uint8_t>(L, ws, MOE_WS_RING_X);
     mv.ring_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_RING_X_SF);
     op1.a_rows = static_cast<int64_t>(kRingBufs) * m.E * m.C;
@@ -521,7 +524,7 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
     note(cudaMemsetAsync(dos + m.T * m.d, 0, (m.Tpad - m.T) * m.d, s));
     note(cudaMemsetAsync(dos_sf + (m.T / 128) * 128 * (m.d / 32), 0, (m.Tpad - m.T / 128 * 128) * (m.d / 32), s));
   }
-  launch_quant_rows(dy, m.T, m.d, m.d, dos, dos_sf, true, 0, s);
+  launch_quant_rows(dy, m.T, m.d, m.d, dos, dos_sf, true, 0, s, ws_ptr<uint8_t>(L, ws, MOE_WS_DOS_SFC));
   // Token-axis operands of the weight gradients (and router dW partial sums).
   launch_tok_gather(m, x, false, topk_w, true, L, ws, ws_ptr<uint8_t>(L, ws, MOE_WS_XTOK),
                     ws_ptr<uint8_t>(L, ws, MOE_WS_XTOK_SF), s);
@@ -548,6 +551,7 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
     RingMovers mv = ring_movers(L, ws, s);
     mv.xq = dos;
     mv.xq_sf = dos_sf;
+    mv.xq_sfr = ws_ptr<uint8_t>(L, ws, MOE_WS_DOS_SFC);
     mv.ring = ws_ptr<uint8_t>(L, ws, MOE_WS_RING_DO);
     mv.ring_sf = ws_ptr<uint8_t>(L, ws, MOE_WS_RING_DO_SF);
     opb2.a_rows = static_cast<int64_t>(kRingBufs) * m.E * m.C;

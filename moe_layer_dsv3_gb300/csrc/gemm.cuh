@@ -86,6 +86,7 @@ struct GemmParams {
   const int* laporder;   // position -> global m-tile (pair-spread order), walked in position order
   int* moved; int* consumed;
   const uint8_t* mv_xq; const uint8_t* mv_xq_sf;
+  const uint8_t* mv_xq_sfr;   // the same scales row-major [T][d/32]
   uint8_t* ring; uint8_t* ring_sf;
 };
 
@@ -337,10 +338,11 @@ __device__ __forceinline__ void publish_move(int* ctr, int lane) {
   if (lane == 0) red_release_add(ctr, 1);
 }
 
-// Ring row <- the MX row of its token (x in the forward, dy in the backward),
-// codes and tiled scales. The item's 16-byte chunks are walked flat (consecutive lanes, consecutive
-// chunks) in rounds of kFwdU chunks a lane; the next round's loads are issued
-// before this round's stores, so two rounds are in flight.
+// Ring row <- the MX row codes of its token (x in the forward, dy in the
+// backward). The item's 16-byte chunks are walked flat (consecutive lanes,
+// consecutive chunks) in rounds of kFwdU chunks a lane; the next round's loads
+// are issued before this round's stores, so two rounds are in flight. The
+// scales go per m-tile (move_tile_scales).
 constexpr int kFwdU = 8;
 
 __device__ __forceinline__ void move_rows(const GemmParams& p, int lane, int a_lane, int64_t ring_row0) {
@@ -380,21 +382,23 @@ __device__ __forceinline__ void move_rows(const GemmParams& p, int lane, int a_l
       step(sr, sc);
     }
   }
-  const int ktiles = d >> 7;
-  int tok[kMoveRows];
+}
+
+// Scales of one ring m-tile (128 rows) in the tiled atom layout, copied from
+// the row-major scales of the rows' tokens (tile_scales_from_rows): the
+// tile's item `part` takes k-tile groups part, part + kMoveItems, ...
+__device__ __forceinline__ void move_tile_scales(const GemmParams& p, const uint8_t* sfr, int lane, int e,
+                                                 int64_t rank_tile0, int64_t ring_tile_row0, int part) {
+  const int cnt = p.counts[e];
+  int tok[4];
 #pragma unroll
-  for (int r = 0; r < kMoveRows; ++r) tok[r] = __shfl_sync(0xffffffffu, tok_l, r);
-  for (int kt = lane; kt < ktiles; kt += 32) {
-    uint32_t sv[kMoveRows];
-#pragma unroll
-    for (int r = 0; r < kMoveRows; ++r)
-      sv[r] = tok[r] >= 0
-                  ? __ldg(reinterpret_cast<const uint32_t*>(p.mv_xq_sf + sf_tiled_offset(tok[r], kt * 4, ktiles)))
-                  : 0u;
-#pragma unroll
-    for (int r = 0; r < kMoveRows; ++r)
-      *reinterpret_cast<uint32_t*>(p.ring_sf + sf_tiled_offset(ring_row0 + r, kt * 4, ktiles)) = sv[r];
+  for (int j = 0; j < 4; ++j) {
+    const int64_t rank = rank_tile0 + lane + 32 * j;
+    const int a = rank < cnt ? p.row_src[p.poff[e] + rank] : -1;
+    tok[j] = a >= 0 ? a / p.k : -1;
   }
+  tile_scales_from_rows(sfr, tok, p.d, p.ring_sf + (ring_tile_row0 >> 7) * (p.d >> 7) * 512 + lane * 16, part,
+                        kMoveItems);
 }
 
 // Mover warp `wid` of this CTA (MV per CTA): items j = blockIdx.x * MV + wid,
@@ -428,6 +432,8 @@ __device__ void ring_mover(const GemmParams& p, int wid, int lane) {
     const int cnt = p.counts[e];
     const int a = (lane < kMoveRows && rank0 + lane < cnt) ? p.row_src[p.poff[e] + rank0 + lane] : -1;
     move_rows(p, lane, a, ring_row0);
+    // this item's share of the m-tile's scales (all 128 rows, some k-tiles)
+    move_tile_scales(p, p.mv_xq_sfr, lane, e, rank0 - part * kMoveRows, ring_row0 - part * kMoveRows, part);
     publish_move(p.moved + gm, lane);
   }
 }

@@ -222,6 +222,7 @@ int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int
     p.consumed = mv->consumed;
     p.mv_xq = mv->xq;
     p.mv_xq_sf = mv->xq_sf;
+    p.mv_xq_sfr = mv->xq_sfr;
     p.ring = mv->ring;
     p.ring_sf = mv->ring_sf;
   }

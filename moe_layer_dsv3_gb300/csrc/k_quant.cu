@@ -17,9 +17,10 @@ __device__ __forceinline__ int64_t gu_interleave_row(int64_t r, int I) {
 }
 
 // One thread per 32-element block along K.
+// sf_rows (optional): a second, row-major copy of the scale bytes.
 __global__ void quant_rows_kernel(const __nv_bfloat16* __restrict__ src, int64_t rows, int K, int64_t ld,
                                   uint8_t* __restrict__ codes, uint8_t* __restrict__ sf, int tiled,
-                                  int interleave_I) {
+                                  int interleave_I, uint8_t* __restrict__ sf_rows) {
   const int64_t nb = K / 32;
   const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (gid >= rows * nb) return;
@@ -33,6 +34,7 @@ __global__ void quant_rows_kernel(const __nv_bfloat16* __restrict__ src, int64_t
   const int64_t orow = interleave_I > 0 ? gu_interleave_row(r, interleave_I) : r;
   store32(codes + orow * K + kb * 32, w);
   sf[tiled ? sf_off(orow, kb, K / 128) : orow * nb + kb] = static_cast<uint8_t>(b);
+  if (sf_rows != nullptr) sf_rows[orow * nb + kb] = static_cast<uint8_t>(b);
 }
 
 // Token-axis MX of src[rows][K]: block = 32 consecutive rows of one column.
@@ -276,12 +278,12 @@ __global__ void scales_to_tiled_kernel(const uint8_t* __restrict__ canon, int64_
 }
 
 void launch_quant_rows(const void* src, int64_t rows, int K, int64_t ld, uint8_t* codes, uint8_t* sf, bool tiled,
-                       int interleave_I, cudaStream_t s) {
+                       int interleave_I, cudaStream_t s, uint8_t* sf_rows) {
   const int64_t n = rows * (K / 32);
   if (n == 0) return;
   const int threads = 256;
   launch_kernel("quant_rows", quant_rows_kernel, dim3(static_cast<unsigned>(ceil_div(n, threads))), dim3(threads), 0, s,
-      static_cast<const __nv_bfloat16*>(src), rows, K, ld, codes, sf, tiled ? 1 : 0, interleave_I);
+      static_cast<const __nv_bfloat16*>(src), rows, K, ld, codes, sf, tiled ? 1 : 0, interleave_I, sf_rows);
 }
 
 void launch_quant_cols(const void* src, int64_t rows, int K, int64_t ld, int64_t rows_pad, uint8_t* codes,

@@ -102,8 +102,9 @@ struct CallScope {
 // Row-wise MX quantisation of bf16 src[rows][K] (row pitch ld elements).
 // Output row r goes to row out_row(r) = (interleave ? gate/up interleave : r).
 // Scales canonical [rows][K/32] (sf_k_tiles == 0) or tiled with K/128 k-tiles.
+// sf_rows (optional): also write the scales row-major [rows][K/32].
 void launch_quant_rows(const void* src, int64_t rows, int K, int64_t ld, uint8_t* codes, uint8_t* sf, bool tiled,
-                       int interleave_I, cudaStream_t s);
+                       int interleave_I, cudaStream_t s, uint8_t* sf_rows = nullptr);
 // Column-wise (token-axis) MX quantisation: src[rows][K] bf16 -> codes[K][rows_pad], blocks of 32 rows.
 // `batch` equally shaped matrices laid out back to back (grid z).
 void launch_quant_cols(const void* src, int64_t rows, int K, int64_t ld, int64_t rows_pad, uint8_t* codes,
@@ -164,6 +165,7 @@ struct RingMovers {
   int* moved;                    // per global m-tile: 8-row groups written (target 16)
   int* consumed;                 // per global m-tile: GEMM tiles whose A loads landed (target N / BN)
   const uint8_t* xq; const uint8_t* xq_sf;   // MX rows along d (x forward, dy backward), tiled scales
+  const uint8_t* xq_sfr;                     // the same scales row-major [T][d/32]
   uint8_t* ring; uint8_t* ring_sf;           // [kRingBufs][E][C] rows, tiled scales
 };
 

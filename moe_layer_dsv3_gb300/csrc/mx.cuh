@@ -74,6 +74,40 @@ __device__ __forceinline__ int64_t sf_off(int64_t r, int64_t kb, int64_t k_tiles
   return ((r >> 7) * k_tiles + (kb >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (kb & 3);
 }
 
+// Scales of one 128-row tile in the tiled atom layout, from row-major scales
+// sfr [tokens][d/32]. Lane l covers tile rows l, l+32, l+64, l+96 (tokens
+// tok[0..3], -1 for a zero row), whose words of one k-tile form one 16-byte
+// chunk of the atom, so a warp writes each atom as 512 contiguous bytes.
+// atoms = the tile's first atom + 16 * lane. With d a multiple of 512 each
+// row's words of 4 k-tiles are one 16-byte load: the call covers the k-tile
+// groups first, first + step, ... (k-tiles first, first + step, ... otherwise),
+// so that several warps can share a tile, each with one round of loads.
+__device__ __forceinline__ void tile_scales_from_rows(const uint8_t* sfr, const int* tok, int d, uint8_t* atoms,
+                                                      int first, int step) {
+  const int ktiles = d >> 7;
+  const int64_t rowb = d >> 5;
+  if ((d & 511) == 0) {
+    for (int kc = first; kc < ktiles / 4; kc += step) {
+      uint4 v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        v[j] = tok[j] >= 0 ? __ldg(reinterpret_cast<const uint4*>(sfr + tok[j] * rowb) + kc) : make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(atoms + (4 * kc + 0) * 512) = make_uint4(v[0].x, v[1].x, v[2].x, v[3].x);
+      *reinterpret_cast<uint4*>(atoms + (4 * kc + 1) * 512) = make_uint4(v[0].y, v[1].y, v[2].y, v[3].y);
+      *reinterpret_cast<uint4*>(atoms + (4 * kc + 2) * 512) = make_uint4(v[0].z, v[1].z, v[2].z, v[3].z);
+      *reinterpret_cast<uint4*>(atoms + (4 * kc + 3) * 512) = make_uint4(v[0].w, v[1].w, v[2].w, v[3].w);
+    }
+  } else {
+    for (int kt = first; kt < ktiles; kt += step) {
+      uint32_t w[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        w[j] = tok[j] >= 0 ? __ldg(reinterpret_cast<const uint32_t*>(sfr + tok[j] * rowb) + kt) : 0u;
+      *reinterpret_cast<uint4*>(atoms + kt * 512) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
 // Row-wise MX of 32 values: codes to dst (16-byte aligned), scale byte to sf.
 __device__ __forceinline__ void emit_rowq(const float* v, uint8_t* dst, uint8_t* sf_byte) {
   const int b = mx_scale_byte(amax32(v));
