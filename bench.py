@@ -542,7 +542,8 @@ def run_ours(args, rank, world, local_rank):
     # ---- end to end through the C ABI with host buffers (H2D of x, dy; D2H of y, dx).
     # Every step copies its inputs from pinned host memory and its outputs back.
     # The copies run on two copy streams, double-buffered on the device, so
-    # step i+1's upload and step i's download overlap step i's compute.
+    # step i+1's upload and step i's download overlap step i's compute; within
+    # a step the forward waits only for x and y leaves during the backward.
     xh = x.cpu().pin_memory()
     dyh = dy.cpu().pin_memory()
     yh = torch.empty_like(xh).pin_memory()
@@ -554,33 +555,41 @@ def run_ours(args, rank, world, local_rank):
     h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
 
     def e2e_run(n, start_ev):
-        loaded = [torch.cuda.Event() for _ in range(2)]
-        done = [torch.cuda.Event() for _ in range(2)]
-        drained = [torch.cuda.Event() for _ in range(2)]
+        ev = lambda: [torch.cuda.Event() for _ in range(2)]   # noqa: E731
+        loaded_x, loaded_dy, fwd_done, done, drained_y, drained_dx = ev(), ev(), ev(), ev(), ev(), ev()
 
         def upload(b, after):
+            # x first: the forward starts once x is in; dy is only needed by the backward
             h2d_s.wait_event(after)
             with torch.cuda.stream(h2d_s):
                 xd[b].copy_(xh, non_blocking=True)
+                loaded_x[b].record(h2d_s)
                 dyd[b].copy_(dyh, non_blocking=True)
-            loaded[b].record(h2d_s)
+                loaded_dy[b].record(h2d_s)
 
         upload(0, start_ev)
         for i in range(n):
             b = i % 2
             if i + 1 < n:
                 upload(1 - b, done[1 - b] if i >= 1 else start_ev)
-            stream.wait_event(loaded[b])
+            stream.wait_event(loaded_x[b])
             if i >= 2:
-                stream.wait_event(drained[b])
+                stream.wait_event(drained_y[b])
             L.forward(xd[b], wr, bias, sp, y=yd[b])          # outputs go straight to this step's buffers
+            fwd_done[b].record(stream)
+            d2h_s.wait_event(fwd_done[b])                     # y leaves while the backward runs
+            with torch.cuda.stream(d2h_s):
+                yh.copy_(yd[b], non_blocking=True)
+            drained_y[b].record(d2h_s)
+            stream.wait_event(loaded_dy[b])
+            if i >= 2:
+                stream.wait_event(drained_dx[b])
             L.backward(dyd[b], sp, dx=dxd[b])
             done[b].record(stream)
             d2h_s.wait_event(done[b])
             with torch.cuda.stream(d2h_s):
-                yh.copy_(yd[b], non_blocking=True)
                 dxh.copy_(dxd[b], non_blocking=True)
-            drained[b].record(d2h_s)
+            drained_dx[b].record(d2h_s)
         stream.wait_stream(d2h_s)
         stream.wait_stream(h2d_s)
 
