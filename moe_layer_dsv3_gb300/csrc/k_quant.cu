@@ -74,8 +74,9 @@ __device__ __forceinline__ int token_of(int a, int T, int k) {
 // (shared-expert assignments have gate 1). Optionally also accumulates the
 // router weight-gradient partial sums part[pr/32][c] = sum_r dl_a x[t_a][c]
 // over the routed rows of the 32-row block, in rank order.
-// CTA: 128 rows x 128 columns, warp g on rows 32g..32g+31; lane l loads 8
-// bytes (columns 4l..4l+3) of each of its 32 rows and owns those 4 columns.
+// CTA: 128 rows x 128 columns (blockIdx.x: row tile, blockIdx.y: column
+// block), warp g on rows 32g..32g+31; lane l loads 8 bytes (columns
+// 4l..4l+3) of each of its 32 rows and owns those 4 columns.
 // The 4 warps' codes meet in shared memory, so each column's 128 rows are
 // stored as one 128-byte run.
 constexpr int kTokCols = 4;
@@ -91,7 +92,7 @@ __global__ void __launch_bounds__(kTokThreads, 4) tok_gather_kernel(
     const __nv_bfloat16* __restrict__ src, const int* __restrict__ row_src, const int* __restrict__ poff_end, int T,
     int k, int d, int64_t Rmax, const float* __restrict__ topk_w, const float* __restrict__ dl,
     float* __restrict__ part, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 128;
   if (r0 >= *poff_end) return;
   __shared__ int s_tok[128];
   __shared__ float s_w[128];
@@ -111,7 +112,7 @@ __global__ void __launch_bounds__(kTokThreads, 4) tok_gather_kernel(
   }
   __syncthreads();
   const int q = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int cb = blockIdx.x * 128;
+  const int cb = blockIdx.y * 128;
   const int c0 = cb + lane * kTokCols;
   const int* tok = s_tok + 32 * q;
   const float* wr = s_w + 32 * q;
@@ -307,7 +308,10 @@ void launch_swiglu_bwd_quant(const Dims& m, const Layout& L, void* ws, cudaStrea
 void launch_tok_gather(const Dims& m, const void* src_rows, bool scale_by_gate, const float* topk_w,
                        bool router_partials, const Layout& L, void* ws, uint8_t* codes, uint8_t* sf,
                        cudaStream_t s) {
-  dim3 grid(static_cast<unsigned>(m.d / 128), static_cast<unsigned>(m.Rmax / 128));
+  // Rank tiles vary fastest: the CTAs resident at one time share one 128-column
+  // block, whose slice of every token (256 bytes of each source row) stays in
+  // L2 across the token's k + S gathered copies.
+  dim3 grid(static_cast<unsigned>(m.Rmax / 128), static_cast<unsigned>(m.d / 128));
   const int* poff = ws_ptr<int>(L, ws, MOE_WS_POFF);
   const auto* sp = static_cast<const __nv_bfloat16*>(src_rows);
   const int* rs = ws_ptr<int>(L, ws, MOE_WS_ROWSRC);
