@@ -291,6 +291,12 @@ enum {
   MOE_WS_LAPKEY,       /* int32[3][...] scratch of the walk-order sort: lap-pair units, their ranks, prefix sums */
   MOE_WS_XQ_SFC,       /* u8[T][d/32]   scales of XQ, row-major (the ring movers' source) */
   MOE_WS_DOS_SFC,      /* u8[T][d/32]   scales of DOS, row-major (the dO-ring movers' source) */
+  MOE_WS_RINGINFO,     /* int32[...][8] per walk position: the decoded ring m-tile the all-laps launches
+                          and their movers read with one load instead of searching the lap and expert
+                          prefix sums: {gm, e | valid << 16 | ok << 24 | shared << 25, A row, padded rank
+                          row}, {previous tenant's gm or -1, rank of the first row, count, poff[e]} */
+  MOE_WS_PUSHINFO,     /* int32[Rmax/128] per m-tile of the padded rank rows: e | valid rows << 16 */
+  MOE_WS_WGINFO,       /* int32[E+S][4] per rank of ORDER: {e, first K tile, K tiles, 0} of the weight gradients */
   MOE_WS_COUNT
 };
 MOE_API int moe_ws_view(const moe_config_t* cfg, void* ws, int which, void** ptr, size_t* bytes);

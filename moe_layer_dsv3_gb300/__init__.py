@@ -36,7 +36,8 @@ WS_NAMES = ["STATUS", "META", "COUNTS", "OFFSETS", "POFF", "RANK", "POS", "INV",
             "BASE", "LOGITS", "SSEL", "XQ", "XQ_SF", "RING_X", "RING_X_SF", "GU", "HQ", "HQ_SF", "HTOK", "HTOK_SF",
             "O", "DW", "DL", "RING_DO", "RING_DO_SF", "DOS", "DOS_SF", "DOTOK", "DOTOK_SF", "DGU", "DGU_SF",
             "DGUTOK", "DGUTOK_SF", "XTOK", "XTOK_SF", "DXE", "DWR_PART", "ORDER",
-            "LAPBASE", "MOVED", "CONSUMED", "DH", "LAPORDER", "LAPKEY", "XQ_SFC", "DOS_SFC"]
+            "LAPBASE", "MOVED", "CONSUMED", "DH", "LAPORDER", "LAPKEY", "XQ_SFC", "DOS_SFC",
+            "RINGINFO", "PUSHINFO", "WGINFO"]
 WS = {n: i for i, n in enumerate(WS_NAMES)}
 WQ_NAMES = ["W1F", "W1F_SF", "W2F", "W2F_SF", "W2B", "W2B_SF", "W1B", "W1B_SF"]
 WQ = {n: i for i, n in enumerate(WQ_NAMES)}

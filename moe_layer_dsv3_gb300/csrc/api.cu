@@ -105,7 +105,7 @@ inline bool all_al16(const P*... p) { return (al16(p) && ...); }
 RingMovers ring_movers(const Layout& L, void* ws, cudaStream_t s) {
   RingMovers mv{};
   mv.lapbase = ws_ptr<int>(L, ws, MOE_WS_LAPBASE);
-  mv.laporder = ws_ptr<int>(L, ws, MOE_WS_LAPORDER);
+  mv.ring_info = ws_ptr<int4>(L, ws, MOE_WS_RINGINFO);
   mv.moved = ws_ptr<int>(L, ws, MOE_WS_MOVED);
   mv.consumed = ws_ptr<int>(L, ws, MOE_WS_CONSUMED);
   note(cudaMemsetAsync(mv.moved, 0, L.bytes[MOE_WS_MOVED], s));
@@ -215,6 +215,9 @@ Layout make_layout(const moe_config_t* c) {
   b.add(L.off, L.bytes, MOE_WS_LAPKEY, 12 * static_cast<size_t>(lap_mtiles_max(m)));
   b.add(L.off, L.bytes, MOE_WS_XQ_SFC, T * d / 32);
   b.add(L.off, L.bytes, MOE_WS_DOS_SFC, T * d / 32);
+  b.add(L.off, L.bytes, MOE_WS_RINGINFO, 32 * static_cast<size_t>(lap_mtiles_max(m)));
+  b.add(L.off, L.bytes, MOE_WS_PUSHINFO, 4 * static_cast<size_t>(m.Rmax / 128));
+  b.add(L.off, L.bytes, MOE_WS_WGINFO, 16 * Ep);
   L.total = b.cur;
   return L;
 }
@@ -476,7 +479,9 @@ int moe_forward(const moe_config_t* cfg, const void* x, const void* wq, const fl
   GemmEpilogue ep2{};
   ep2.out = ws_ptr<void>(L, ws, MOE_WS_O);
   ep2.ldo = m.d;
-  if (int r = gemm_dispatch("gemm2_fwd", kPush, m, 0, m.d, m.I, 0, op2, ep2, counts, poff, lap_tiles, row_src, status, s)) return r;
+  if (int r = gemm_dispatch("gemm2_fwd", kPush, m, 0, m.d, m.I, 0, op2, ep2, counts, poff, lap_tiles, row_src, status,
+                            s, 0, nullptr, nullptr, ws_ptr<int>(L, ws, MOE_WS_PUSHINFO)))
+    return r;
   launch_combine(m, topk_w, L, ws, y, s);
   return call.status();
 }
@@ -598,7 +603,8 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
   GemmEpilogue epb4{};
   epb4.out = ws_ptr<void>(L, ws, MOE_WS_DXE);
   epb4.ldo = m.d;
-  if (int r = gemm_dispatch("gemm_dgrad_gu", kPush, m, 0, m.d, 2 * m.I, 0, opb4, epb4, counts, poff, lap_tiles, row_src, status, s))
+  if (int r = gemm_dispatch("gemm_dgrad_gu", kPush, m, 0, m.d, 2 * m.I, 0, opb4, epb4, counts, poff, lap_tiles,
+                            row_src, status, s, 0, nullptr, nullptr, ws_ptr<int>(L, ws, MOE_WS_PUSHINFO)))
     return r;
   // Weight gradients: K = the expert's ranks (token axis), all laps at once.
   GemmOperands opw{};
@@ -626,9 +632,10 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
   const bool pair_d = (cfg->flags & MOE_FLAG_WGRAD_PAIR) && m.d % kPairRows == 0;
   const bool pair_gu = (cfg->flags & MOE_FLAG_WGRAD_PAIR) && (2 * m.I) % kPairRows == 0;
   const int* order = ws_ptr<int>(L, ws, MOE_WS_ORDER);
+  const int4* wg_info = ws_ptr<int4>(L, ws, MOE_WS_WGINFO);
   if (int r = pair_d ? gemm_pair_dispatch("gemm_wgrad_d", kWgrad, m, m.I, m.d, 0, opw, epw, poff, order, status, s)
                      : gemm_dispatch("gemm_wgrad_d", kWgrad, m, 0, m.I, 0, m.d, opw, epw, counts, poff, lap_tiles,
-                                     row_src, status, s, 256, order))
+                                     row_src, status, s, 256, order, nullptr, wg_info))
     return r;
   note(cudaStreamWaitEvent(ls->aux[0], ls->fork, 0));
   launch_reverse_dispatch(m, topk_idx, w_router, L, ws, dx, ls->aux[0]);
@@ -646,7 +653,7 @@ int moe_backward(const moe_config_t* cfg, const void* x, const void* w_router, c
   const int r = pair_gu ? gemm_pair_dispatch("gemm_wgrad_gu", kWgrad, m, m.d, 2 * m.I, 0, opw, epw, poff, order,
                                              status, s)
                         : gemm_dispatch("gemm_wgrad_gu", kWgrad, m, 0, m.d, 0, 2 * m.I, opw, epw, counts, poff,
-                                        lap_tiles, row_src, status, s, 256, order);
+                                        lap_tiles, row_src, status, s, 256, order, nullptr, wg_info);
   note(cudaStreamWaitEvent(s, ls->join[0], 0));
   if (r) return r;
   return call.status();

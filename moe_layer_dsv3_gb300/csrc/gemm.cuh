@@ -19,8 +19,9 @@
 // covers every lap. Ordering goes through per-m-tile device counters:
 //   moved[gm]    8-row groups of m-tile gm written into its ring slot; the
 //                producer waits for all 16 before its first TMA load of gm;
-//   consumed[gm] tiles of gm whose A loads have landed; the movers of the
-//                same slot's next tenant (lap + 2) wait for all N / BN.
+//   consumed[gm] tiles of gm whose accumulators are complete (so all their A
+//                loads have landed), bumped by the epilogue; the movers of
+//                the same slot's next tenant (lap + 2) wait for all N / BN.
 // Both lists are walked by every CTA in increasing position of the schedule's
 // walk order (LAPORDER: laps 2P and 2P+1 of an expert side by side, so its
 // weights stream once for both, and each expert's pairs spread evenly over
@@ -28,6 +29,12 @@
 // earlier position, so every wait points to an earlier position or to a move
 // of the same one, and the waits cannot form a cycle once all CTAs are
 // resident (cooperative launch).
+//
+// A tile learns its expert, rows and ring slot from one entry of a table the
+// schedule writes (the ring positions' entries, the push m-tiles' experts, the
+// weight gradients' per-expert K ranges). Searching the lap and expert prefix
+// sums instead costs a chain of dependent global loads per tile, which the
+// producer and MMA threads would pay between tiles while the tensor pipe idles.
 #pragma once
 #include <cuda_bf16.h>
 
@@ -83,7 +90,10 @@ struct GemmParams {
   int* status;
   // all-laps ring modes
   const int* lapbase; int Lb; int d;
-  const int* laporder;   // position -> global m-tile (pair-spread order), walked in position order
+  const int4* ring_info; // per walk position (pair-spread order): the decoded ring m-tile (two int4,
+                         // written by the schedule); tiles and move items go in position order
+  const int* push_info;  // push modes, per m-tile of the padded rank rows: e | valid << 16 (or null: search)
+  const int4* wg_info;   // weight gradients, per rank of `order`: {e, first K tile, K tiles, 0} (or null)
   int* moved; int* consumed;
   const uint8_t* mv_xq; const uint8_t* mv_xq_sf;
   const uint8_t* mv_xq_sfr;   // the same scales row-major [T][d/32]
@@ -202,15 +212,24 @@ __device__ __forceinline__ bool gemm_decode(const GemmParams& p, int tile, TileI
   using Cf = GemmCfg<BN, MODE>;
   t.gm = -1;
   if constexpr (ring_mode(MODE)) {
-    // position pos of the walk (laporder maps it to the lap-major global m-tile gm), n-tile n
+    // position pos of the walk, n-tile n; the schedule decoded the position's
+    // m-tile (lap-major global m-tile gm, expert, rows) into one table entry
     const int nt = p.N / BN;
     const int pos = tile / nt, n = tile - pos * nt;
-    const int gm = p.laporder[pos];
-    const int L = seg_search(p.lapbase, p.Lb, gm);
-    const bool ok = lap_decode<BN>(p, L, gm - p.lapbase[L], n,
-                                   static_cast<int64_t>(L % kRingBufs) * p.E * p.C, t);
-    if (!t.use_a2) t.gm = gm;
-    return ok;
+    const int4 a = p.ring_info[2 * pos];
+    const int e = a.y & 0xFFFF;
+    t.e = e;
+    t.use_a2 = ((a.y >> 25) & 1) != 0;
+    t.a_row = a.z;
+    t.b_row = static_cast<int64_t>(e) * p.N + static_cast<int64_t>(n) * BN;
+    t.k0 = 0;
+    t.nk = p.K / kTileK;
+    t.prow0 = a.w;
+    t.valid = (a.y >> 16) & 0xFF;
+    t.n0 = n * BN;
+    t.m0 = 0;
+    t.gm = t.use_a2 ? -1 : a.x;
+    return ((a.y >> 24) & 1) != 0;
   } else if constexpr (MODE == kSwigluFwd || MODE == kSwigluBwd) {
     const int nt = p.N / BN;
     const int g = tile / nt, n = tile - (tile / nt) * nt;
@@ -220,7 +239,16 @@ __device__ __forceinline__ bool gemm_decode(const GemmParams& p, int tile, TileI
     const int nt = p.N / BN;
     const int g = tile / nt, n = tile - (tile / nt) * nt;
     const int64_t prow0 = static_cast<int64_t>(g) * 128;
-    const int e = seg_search(p.poff, p.Ep, prow0);
+    int e, valid;
+    if (p.push_info != nullptr) {   // decoded by the schedule
+      const int v = p.push_info[g];
+      e = v & 0xFFFF;
+      valid = v >> 16;
+    } else {
+      e = seg_search(p.poff, p.Ep, prow0);
+      const int64_t v = p.counts[e] - (prow0 - p.poff[e]);
+      valid = v < 0 ? 0 : (v > 128 ? 128 : static_cast<int>(v));
+    }
     t.e = e;
     t.use_a2 = false;
     t.a_row = prow0;
@@ -228,8 +256,7 @@ __device__ __forceinline__ bool gemm_decode(const GemmParams& p, int tile, TileI
     t.k0 = 0;
     t.nk = p.K / Cf::kKElems;
     t.prow0 = prow0;
-    const int64_t v = p.counts[e] - (prow0 - p.poff[e]);
-    t.valid = v < 0 ? 0 : (v > 128 ? 128 : static_cast<int>(v));
+    t.valid = valid;
     t.n0 = n * BN;
     t.m0 = MODE == kGroupedNv4 ? static_cast<int>(prow0) : 0;   // rank-ordered output rows
     return true;
@@ -255,15 +282,22 @@ __device__ __forceinline__ bool gemm_decode(const GemmParams& p, int tile, TileI
         q = N - 1 - k;
       }
     }
-    const int e = p.order[q / per];
     const int rem = q - (q / per) * per;
     const int mi = rem / nt, n = rem - (rem / nt) * nt;
-    t.e = e;
+    if (p.wg_info != nullptr) {   // decoded by the schedule
+      const int4 w = p.wg_info[q / per];
+      t.e = w.x;
+      t.k0 = w.y;
+      t.nk = w.z;
+    } else {
+      const int e = p.order[q / per];
+      t.e = e;
+      t.k0 = p.poff[e] / 128;
+      t.nk = (p.poff[e + 1] - p.poff[e]) / 128;
+    }
     t.use_a2 = false;
     t.a_row = static_cast<int64_t>(mi) * 128;
     t.b_row = static_cast<int64_t>(n) * BN;
-    t.k0 = p.poff[e] / 128;
-    t.nk = (p.poff[e + 1] - p.poff[e]) / 128;
     t.prow0 = 0;
     t.valid = 128;
     t.n0 = n * BN;
@@ -387,14 +421,13 @@ __device__ __forceinline__ void move_rows(const GemmParams& p, int lane, int a_l
 // Scales of one ring m-tile (128 rows) in the tiled atom layout, copied from
 // the row-major scales of the rows' tokens (tile_scales_from_rows): the
 // tile's item `part` takes k-tile groups part, part + kMoveItems, ...
-__device__ __forceinline__ void move_tile_scales(const GemmParams& p, const uint8_t* sfr, int lane, int e,
-                                                 int64_t rank_tile0, int64_t ring_tile_row0, int part) {
-  const int cnt = p.counts[e];
+__device__ __forceinline__ void move_tile_scales(const GemmParams& p, const uint8_t* sfr, int lane, int cnt,
+                                                 int poff_e, int64_t rank_tile0, int64_t ring_tile_row0, int part) {
   int tok[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int64_t rank = rank_tile0 + lane + 32 * j;
-    const int a = rank < cnt ? p.row_src[p.poff[e] + rank] : -1;
+    const int a = rank < cnt ? p.row_src[poff_e + rank] : -1;
     tok[j] = a >= 0 ? a / p.k : -1;
   }
   tile_scales_from_rows(sfr, tok, p.d, p.ring_sf + (ring_tile_row0 >> 7) * (p.d >> 7) * 512 + lane * 16, part,
@@ -410,30 +443,26 @@ __device__ void ring_mover(const GemmParams& p, int wid, int lane) {
   const int stride = gridDim.x * MV;
   for (int j = blockIdx.x * MV + wid; j < total; j += stride) {
     const int pos = j / kMoveItems, part = j - pos * kMoveItems;
-    const int gm = p.laporder[pos];
-    const int L = seg_search(p.lapbase, p.Lb, gm);
-    const int g = gm - p.lapbase[L];
-    const int* lt = p.lap_tiles + static_cast<int64_t>(L) * (p.Ep + 1);
-    if (g >= lt[p.E]) continue;                 // shared-expert tile: A2 is read in place
-    const int e = seg_search(lt, p.E, g);
-    const int mt = g - lt[e];
-    if (L >= kRingBufs) {
-      // The slot's previous tenant is the same expert's m-tile mt of lap L - kRingBufs.
-      const int Lp = L - kRingBufs;
-      const int gp = p.lapbase[Lp] + p.lap_tiles[static_cast<int64_t>(Lp) * (p.Ep + 1) + e] + mt;
+    const int4 a = p.ring_info[2 * pos];        // the position's m-tile, decoded by the schedule
+    if ((a.y >> 25) & 1) continue;              // shared-expert tile: A2 is read in place
+    const int4 b = p.ring_info[2 * pos + 1];
+    const int gm = a.x;
+    const int gp = b.x;
+    if (gp >= 0) {
+      // The slot's previous tenant: the same expert's m-tile of lap L - kRingBufs.
       int ok = 1;
       if (lane == 0) ok = wait_counter(p.consumed + gp, nt, p.status, 40) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       (void)ld_acquire_gpu(p.consumed + gp);   // every lane orders its writes after the reads
     }
-    const int64_t rank0 = static_cast<int64_t>(L) * p.C + mt * 128 + part * kMoveRows;
-    const int64_t ring_row0 = (static_cast<int64_t>(L % kRingBufs) * p.E + e) * p.C + mt * 128 + part * kMoveRows;
-    const int cnt = p.counts[e];
-    const int a = (lane < kMoveRows && rank0 + lane < cnt) ? p.row_src[p.poff[e] + rank0 + lane] : -1;
-    move_rows(p, lane, a, ring_row0);
+    const int64_t rank0 = static_cast<int64_t>(b.y) + part * kMoveRows;
+    const int64_t ring_row0 = static_cast<int64_t>(a.z) + part * kMoveRows;
+    const int cnt = b.z, poff_e = b.w;
+    const int src = (lane < kMoveRows && rank0 + lane < cnt) ? p.row_src[poff_e + rank0 + lane] : -1;
+    move_rows(p, lane, src, ring_row0);
     // this item's share of the m-tile's scales (all 128 rows, some k-tiles)
-    move_tile_scales(p, p.mv_xq_sfr, lane, e, rank0 - part * kMoveRows, ring_row0 - part * kMoveRows, part);
+    move_tile_scales(p, p.mv_xq_sfr, lane, cnt, poff_e, rank0 - part * kMoveRows, ring_row0 - part * kMoveRows, part);
     publish_move(p.moved + gm, lane);
   }
 }
@@ -455,6 +484,16 @@ __device__ __forceinline__ void warp_store_rows128(uint8_t* buf, int lane, const
     if (d != nullptr) d[ch] = val;
   }
   __syncwarp();
+}
+
+// All-laps ring tiles (t.gm >= 0): the accumulator is complete, so every A
+// load of the tile landed long ago; one thread reports the tile's ring rows
+// consumed, and the movers of the slot's next tenant may overwrite them.
+__device__ __forceinline__ void ring_consumed(const GemmParams& p, const TileInfo& t, int q, int lane) {
+  if (t.gm >= 0 && q == 0 && lane == 0) {
+    fence_proxy_async_global();
+    red_release_add(p.consumed + t.gm, 1);
+  }
 }
 
 template <int BN, int MODE>
@@ -493,6 +532,7 @@ __device__ __forceinline__ void gemm_epilogue_tile(const GemmParams& p, const Ti
     }
     tc_fence_before();
     mbar_arrive(acce);
+    ring_consumed(p, t, q, lane);
 #pragma unroll
     for (int c = 0; c < BN / 64; ++c) {
       const int64_t icol = i_base + c * 32;
@@ -523,6 +563,7 @@ __device__ __forceinline__ void gemm_epilogue_tile(const GemmParams& p, const Ti
       if (c + 2 == BN / 32) {   // whole accumulator row read: hand TMEM back
         tc_fence_before();
         mbar_arrive(acce);
+        ring_consumed(p, t, q, lane);
       }
       uint4 v0[8], v1[8];
 #pragma unroll
@@ -763,12 +804,9 @@ __global__ void __launch_bounds__(gemm_threads(MODE, MV), 1)
           tc_commit(&empty[stage]);
           if (++stage == Cf::kStages) { stage = 0; phase ^= 1u; }
         }
-        if constexpr (ring_mode(MODE)) {
-          if (ok && t.gm >= 0) {   // every A load of this tile has landed: its ring rows may be refilled
-            fence_proxy_async_global();
-            red_release_add(p.consumed + t.gm, 1);
-          }
-        }
+        // (ring modes: the epilogue reports the tile's ring rows consumed once
+        // the accumulator is complete, so this thread never waits on a proxy
+        // fence behind its queued MMAs)
         tc_commit(&accf[acc]);
         if (++acc == Cf::kNumAcc) { acc = 0; acc_phase ^= 1u; }
       }

@@ -148,7 +148,7 @@ int num_sms() {
 int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int K, int M, const GemmOperands& op,
                   const GemmEpilogue& ep, const int* counts, const int* poff, const int* lap_tiles,
                   const int* row_src, int* status, cudaStream_t s, int bn_hint, const int* order,
-                  const RingMovers* mv) {
+                  const RingMovers* mv, const void* tile_info) {
   if (!get_encode()) return MOE_ERR_CUDA;
   const bool bf16 = mode == kRouterMode;
   int BN;
@@ -213,9 +213,12 @@ int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int
   p.gate = ep.gate;
   p.I = m.I;
   p.status = status;
+  // decode tables written by the schedule (one load per tile instead of searches)
+  if (mode == kPush) p.push_info = static_cast<const int*>(tile_info);
+  if (mode == kWgrad) p.wg_info = static_cast<const int4*>(tile_info);
   if (mv != nullptr) {
     p.lapbase = mv->lapbase;
-    p.laporder = mv->laporder;
+    p.ring_info = mv->ring_info;
     p.Lb = m.Lb;
     p.d = m.d;
     p.moved = mv->moved;

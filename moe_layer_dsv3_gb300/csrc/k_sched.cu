@@ -169,10 +169,20 @@ constexpr int kKeyUnits = 2048;
 // by ascending key (compared exactly as integers), then expert, then pair.
 // One block of 1024 threads; scratch holds 3 * cap ints (units, their ranks,
 // the tile counts in rank order, then their prefix sums).
-__global__ void __launch_bounds__(1024) sched_laporder_kernel(const int* __restrict__ counts, int E, int Ep, int C,
+//
+// The same kernel writes the decode tables of the grouped GEMMs, so that a
+// tile's expert, rows and ring slot cost one load instead of a chain of
+// dependent searches through the lap and expert prefix sums:
+//   info[2 pos]     = {gm, e | valid << 16 | ok << 24 | shared << 25, A row, padded rank row}
+//   info[2 pos + 1] = {gm of the slot's previous tenant (lap L - kRingBufs) or -1,
+//                      rank of the tile's first row, count of e, poff[e]}
+//   push_info[g]    = e | valid << 16 for m-tile g of the padded rank rows.
+__global__ void __launch_bounds__(1024) sched_laporder_kernel(const int* __restrict__ counts,
+                                                              const int* __restrict__ poff, int E, int Ep, int C,
                                                               int Lb, const int* __restrict__ lapbase,
                                                               const int* __restrict__ lap_tiles, int64_t cap,
-                                                              int* __restrict__ scratch, int* __restrict__ order) {
+                                                              int* __restrict__ scratch, int* __restrict__ order,
+                                                              int4* __restrict__ info, int* __restrict__ push_info) {
   __shared__ int sm[1024];
   __shared__ int s_pairs[1024], s_one[1024];
   __shared__ int s_num[kKeyUnits], s_den[kKeyUnits], s_unit[kKeyUnits];
@@ -251,17 +261,47 @@ __global__ void __launch_bounds__(1024) sched_laporder_kernel(const int* __restr
   }
   for (int u = threadIdx.x; u < U; u += blockDim.x) {
     const int ue = unit[u] & 0xFFFF, P = unit[u] >> 16;
+    const bool shared = ue >= E;
+    const int cnt = counts[ue], pe = poff[ue], pe1 = poff[ue + 1];
     int pos = stile[urank[u]];
     for (int L = 2 * P; L < 2 * P + 2 && L < Lb; ++L) {
       const int* lt = lap_tiles + static_cast<int64_t>(L) * (Ep + 1);
       const int base = lapbase[L] + lt[ue];
-      for (int mt = 0; mt < lt[ue + 1] - lt[ue]; ++mt) order[pos++] = base + mt;
+      for (int mt = 0; mt < lt[ue + 1] - lt[ue]; ++mt) {
+        // A shared expert is read in place (token rows mt*128..); a routed
+        // expert's lap L sits in ring buffer L % kRingBufs at row e*C + mt*128.
+        const int rank0 = shared ? mt * 128 : L * C + mt * 128;
+        const int a_row = shared ? mt * 128 : ((L % kRingBufs) * E + ue) * C + mt * 128;
+        const int prow0 = pe + rank0;
+        const int v = cnt - rank0;
+        const int valid = v < 0 ? 0 : (v > 128 ? 128 : v);
+        const int ok = (prow0 + 128 <= pe1 && valid > 0) ? 1 : 0;
+        int gp = -1;
+        if (!shared && L >= kRingBufs) {
+          const int Lp = L - kRingBufs;
+          gp = lapbase[Lp] + lap_tiles[static_cast<int64_t>(Lp) * (Ep + 1) + ue] + mt;
+        }
+        order[pos] = base + mt;
+        info[2 * pos] = make_int4(base + mt, ue | (valid << 16) | (ok << 24) | ((shared ? 1 : 0) << 25), a_row, prow0);
+        info[2 * pos + 1] = make_int4(gp, rank0, cnt, pe);
+        ++pos;
+      }
+    }
+  }
+  for (int e = threadIdx.x; e < Ep; e += blockDim.x) {
+    const int pe = poff[e], pe1 = poff[e + 1], cnt = counts[e];
+    for (int g = pe / 128; g < pe1 / 128; ++g) {
+      const int v = cnt - (g * 128 - pe);
+      push_info[g] = e | ((v < 0 ? 0 : (v > 128 ? 128 : v)) << 16);
     }
   }
 }
 
-// Experts ordered by descending count, ties to the lower index (order[rank] = e).
-__global__ void sched_order_kernel(const int* __restrict__ counts, int Ep, int* __restrict__ order) {
+// Experts ordered by descending count, ties to the lower index (order[rank] = e),
+// and the weight gradients' decode table: wg_info[rank] = {e, first K tile,
+// K tiles, 0} (K = the expert's padded token rows).
+__global__ void sched_order_kernel(const int* __restrict__ counts, const int* __restrict__ poff, int Ep,
+                                   int* __restrict__ order, int4* __restrict__ wg_info) {
   for (int e = threadIdx.x; e < Ep; e += blockDim.x) {
     const int n = counts[e];
     int r = 0;
@@ -270,6 +310,7 @@ __global__ void sched_order_kernel(const int* __restrict__ counts, int Ep, int* 
       r += (m > n || (m == n && f < e)) ? 1 : 0;
     }
     order[r] = e;
+    wg_info[r] = make_int4(e, poff[e] / 128, (poff[e + 1] - poff[e]) / 128, 0);
   }
 }
 
@@ -331,10 +372,12 @@ void launch_schedule(const Dims& m, const int32_t* idx, const Layout& L, void* w
   }
   launch_kernel("sched_offsets", sched_offsets_kernel, dim3(1), dim3(256), 0, s, counts, m.E, m.Ep, m.C, m.Lb, offsets,
                 poff, lap_tiles, meta, ws_ptr<int>(L, ws, MOE_WS_LAPBASE));
-  launch_kernel("sched_laporder", sched_laporder_kernel, dim3(1), dim3(1024), 0, s, counts, m.E, m.Ep, m.C, m.Lb,
-                ws_ptr<int>(L, ws, MOE_WS_LAPBASE), lap_tiles, lap_mtiles_max(m), ws_ptr<int>(L, ws, MOE_WS_LAPKEY),
-                ws_ptr<int>(L, ws, MOE_WS_LAPORDER));
-  launch_kernel("sched_order", sched_order_kernel, dim3(1), dim3(512), 0, s, counts, m.Ep, ws_ptr<int>(L, ws, MOE_WS_ORDER));
+  launch_kernel("sched_laporder", sched_laporder_kernel, dim3(1), dim3(1024), 0, s, counts, poff, m.E, m.Ep, m.C,
+                m.Lb, ws_ptr<int>(L, ws, MOE_WS_LAPBASE), lap_tiles, lap_mtiles_max(m),
+                ws_ptr<int>(L, ws, MOE_WS_LAPKEY), ws_ptr<int>(L, ws, MOE_WS_LAPORDER),
+                ws_ptr<int4>(L, ws, MOE_WS_RINGINFO), ws_ptr<int>(L, ws, MOE_WS_PUSHINFO));
+  launch_kernel("sched_order", sched_order_kernel, dim3(1), dim3(512), 0, s, counts, poff, m.Ep,
+                ws_ptr<int>(L, ws, MOE_WS_ORDER), ws_ptr<int4>(L, ws, MOE_WS_WGINFO));
   if (m.units > 0) {
     launch_kernel("sched_rank", sched_rank_kernel, dim3(blocks), dim3(kWarps * 32), shm, s, idx, m.T, m.k, m.kp, m.E,
                   m.Ep, m.Ap, m.units, base, offsets, poff, ws_ptr<int>(L, ws, MOE_WS_RANK),

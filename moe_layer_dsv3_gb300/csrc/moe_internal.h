@@ -161,9 +161,10 @@ enum GemmMode : int {
 // Where the mover warps of the all-laps ring modes take each ring row from.
 struct RingMovers {
   const int* lapbase;            // [Lb+1] first global m-tile of each lap
-  const int* laporder;           // position -> global m-tile: the order CTAs walk tiles and move items
+  const int4* ring_info;         // per walk position: the decoded m-tile (two int4, see MOE_WS_RINGINFO);
+                                 // CTAs walk tiles and move items in position order
   int* moved;                    // per global m-tile: 8-row groups written (target 16)
-  int* consumed;                 // per global m-tile: GEMM tiles whose A loads landed (target N / BN)
+  int* consumed;                 // per global m-tile: GEMM tiles whose accumulators completed (target N / BN)
   const uint8_t* xq; const uint8_t* xq_sf;   // MX rows along d (x forward, dy backward), tiled scales
   const uint8_t* xq_sfr;                     // the same scales row-major [T][d/32]
   uint8_t* ring; uint8_t* ring_sf;           // [kRingBufs][E][C] rows, tiled scales
@@ -189,7 +190,7 @@ struct GemmEpilogue {
 int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int K, int M, const GemmOperands& op,
                   const GemmEpilogue& ep, const int* counts, const int* poff, const int* lap_tiles,
                   const int* row_src, int* status, cudaStream_t s, int bn_hint = 0, const int* order = nullptr,
-                  const RingMovers* mv = nullptr);
+                  const RingMovers* mv = nullptr, const void* tile_info = nullptr);
 
 // The weight-gradient (kWgrad) or plain (kPlain, fp32 out) GEMM on CTA pairs:
 // 256 x 128 output tiles, tcgen05 MMAs issued for both SMs of a cluster of two

@@ -352,9 +352,20 @@ def test_walk_order_full_size(full):
     assert np.array_equal(got, np.asarray(ref))
 
 
+def test_decode_tables_full_size(full):
+    """The GEMMs' decode tables at full size equal the host restatement."""
+    from tests.test_ring_protocol import decode_tables
+    s = full.shape
+    counts = [int(c) for c in full.L.ws_tensor("COUNTS", torch.int32, (full.Ep,)).cpu().numpy()]
+    ring, push, wg = decode_tables(counts, s.E, s.S, s.C, s.T)
+    assert np.array_equal(full.L.ws_tensor("RINGINFO", torch.int32, ring.shape).cpu().numpy(), ring)
+    assert np.array_equal(full.L.ws_tensor("PUSHINFO", torch.int32, push.shape).cpu().numpy(), push)
+    assert np.array_equal(full.L.ws_tensor("WGINFO", torch.int32, wg.shape).cpu().numpy(), wg)
+
+
 def test_idle_expert_weight_grads_full_size(full):
     """Experts without tokens get all-zero weight gradients whatever the buffers held (their
-    tiles are stored by the weight-gradient kernels' zero-fill warp), and rewriting the buffers
+    tiles are the weight-gradient kernels' zero tiles), and rewriting the buffers
     from a NaN pattern leaves the other experts' gradient bytes unchanged."""
     L, i = full.L, full.inp
     s = full.shape

@@ -210,6 +210,19 @@ def test_walk_order_matches_model(run):
     assert np.array_equal(got, np.asarray(ref))
 
 
+def test_decode_tables_match_model(run):
+    """The decode tables the schedule writes for the grouped GEMMs (ring positions, push
+    m-tiles, weight-gradient experts) equal the host restatement that searches the lap and
+    expert prefix sums."""
+    from tests.test_ring_protocol import decode_tables
+    m = run.shape
+    counts = [int(c) for c in run.ws("COUNTS", torch.int32, (run.Ep,)).cpu().numpy()]
+    ring, push, wg = decode_tables(counts, m.E, m.S, m.C, m.T)
+    assert np.array_equal(run.ws("RINGINFO", torch.int32, ring.shape).cpu().numpy(), ring)
+    assert np.array_equal(run.ws("PUSHINFO", torch.int32, push.shape).cpu().numpy(), push)
+    assert np.array_equal(run.ws("WGINFO", torch.int32, wg.shape).cpu().numpy(), wg)
+
+
 def test_ring_holds_last_laps(run):
     """Lap L of an expert goes to ring buffer L % NBUF: after forward, buffer (last % NBUF) holds
     the expert's final lap (zeros past it up to the tile end) and buffer ((last-1) % NBUF) its

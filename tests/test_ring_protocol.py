@@ -79,6 +79,42 @@ def walk_order(counts, E, S, C, T):
     return order
 
 
+def decode_tables(counts, E, S, C, T):
+    """The GEMMs' decode tables restated by searching the lap and expert prefix sums
+    (the device builds them while it expands the walk order):
+      ring[pos] = {gm, e | valid << 16 | ok << 24 | shared << 25, A row, padded rank row,
+                   previous tenant's gm or -1, rank of the first row, count, poff[e]};
+      push[g]   = e | valid << 16 for m-tile g of the padded rank rows;
+      wg[r]     = {e, poff[e] / 128, tiles of e, 0} for the r-th expert by descending count."""
+    Ep = E + S
+    lt, lapbase, Lb = lap_schedule(counts, E, S, C, T)
+    poff = np.concatenate([[0], np.cumsum([cdiv(c, 128) * 128 for c in counts])]).astype(np.int64)
+    order = walk_order(counts, E, S, C, T)
+    ring = np.zeros((len(order), 8), np.int64)
+    for pos, gm in enumerate(order):
+        L = seg(lapbase, Lb, gm)
+        g = gm - lapbase[L]
+        e = seg(lt[L], Ep, g)
+        mt = g - lt[L, e]
+        shared = e >= E
+        rank0 = mt * 128 if shared else L * C + mt * 128
+        a_row = mt * 128 if shared else ((L % RING_BUFS) * E + e) * C + mt * 128
+        prow0 = poff[e] + rank0
+        valid = min(max(counts[e] - rank0, 0), 128)
+        ok = int(prow0 + 128 <= poff[e + 1] and valid > 0)
+        gp = -1
+        if not shared and L >= RING_BUFS:
+            gp = lapbase[L - RING_BUFS] + lt[L - RING_BUFS, e] + mt
+        ring[pos] = [gm, e | valid << 16 | ok << 24 | int(shared) << 25, a_row, prow0, gp, rank0, counts[e], poff[e]]
+    push = np.zeros(int(poff[-1]) // 128, np.int64)
+    for g in range(len(push)):
+        e = seg(poff, Ep, g * 128)
+        push[g] = e | min(max(counts[e] - (g * 128 - poff[e]), 0), 128) << 16
+    by_count = sorted(range(Ep), key=lambda e: (-counts[e], e))
+    wg = np.array([[e, poff[e] // 128, (poff[e + 1] - poff[e]) // 128, 0] for e in by_count], np.int64).reshape(-1, 4)
+    return ring, push, wg
+
+
 def replay(counts, E, S, T, C, grid, nt, mv=2, order=None):
     Ep = E + S
     lt, lapbase, Lb = lap_schedule(counts, E, S, C, T)
@@ -177,6 +213,33 @@ def test_walk_order_pairs_and_spread():
         first.append(min(span))
     assert first == sorted(first)
     assert first[0] < len(order) // 4 and first[-1] > len(order) // 2
+
+
+@pytest.mark.parametrize("counts,E,S,T,C", [
+    (zipf_counts(64, 2048, 8, 1.1, 0) + [2048], 64, 1, 2048, 128),
+    ([300, 0, 5, 128, 129, 640, 1000, 20], 8, 0, 1000, 128),
+    ([515] * 8 + [515], 8, 1, 515, 128),
+])
+def test_decode_tables_consistent(counts, E, S, T, C):
+    """Every ring position decodes to an in-bounds ring slot whose previous tenant is the
+    same (expert, m-tile) at an earlier position, the push table covers each expert's
+    padded rows with its valid counts, and the weight-gradient table lists every expert."""
+    Ep = E + S
+    ring, push, wg = decode_tables(counts, E, S, C, T)
+    order = walk_order(counts, E, S, C, T)
+    pos = {gm: i for i, gm in enumerate(order)}
+    assert list(ring[:, 0]) == order
+    for r in ring:
+        e, valid, ok, shared = r[1] & 0xFFFF, (r[1] >> 16) & 0xFF, (r[1] >> 24) & 1, (r[1] >> 25) & 1
+        assert ok == 1 and 0 < valid <= 128 and shared == (e >= E)
+        if not shared:
+            assert r[2] + 128 <= RING_BUFS * E * C and r[5] % C + 128 <= C
+        if r[4] >= 0:
+            prev = ring[pos[int(r[4])]]
+            assert pos[int(r[4])] < pos[int(r[0])] and prev[1] & 0xFFFF == e and prev[2] == r[2]
+            assert prev[5] + RING_BUFS * C == r[5]
+    assert sum(((v >> 16) & 0xFF) for v in push) == sum(counts)
+    assert sorted(wg[:, 0]) == list(range(Ep)) and sum(wg[:, 2]) == len(push)
 
 
 @pytest.mark.parametrize("mv", [1, 2, 4])
