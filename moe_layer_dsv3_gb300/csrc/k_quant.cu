@@ -87,8 +87,11 @@ __device__ __forceinline__ float bf16_lane(const uint2& u, int j) {
   return (j & 1) ? __uint_as_float(w & 0xFFFF0000u) : __uint_as_float(w << 16);
 }
 
+// The gate-scaled form runs 3 CTAs per SM: the registers it needs for the
+// gates of both passes then fit without spilling (0.55 -> 0.52 ms at the
+// benchmark shape, against 4 CTAs per SM with a 96-byte spill).
 template <bool kGate, bool kPart>
-__global__ void __launch_bounds__(kTokThreads, 4) tok_gather_kernel(
+__global__ void __launch_bounds__(kTokThreads, kGate ? 3 : 4) tok_gather_kernel(
     const __nv_bfloat16* __restrict__ src, const int* __restrict__ row_src, const int* __restrict__ poff_end, int T,
     int k, int d, int64_t Rmax, const float* __restrict__ topk_w, const float* __restrict__ dl,
     float* __restrict__ part, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
