@@ -259,7 +259,8 @@ enum {
   MOE_WS_XQ_SF,        /* tiled scales of XQ */
   MOE_WS_RING_X,       /* u8[2][E][C][d]    two ring token buffers (dispatch); lap L uses buffer L % 2 */
   MOE_WS_RING_X_SF,
-  MOE_WS_GU,           /* bf16[Rmax][2I]    saved g|u */
+  MOE_WS_GU,           /* bf16[Rmax][2I]    saved g, u: chunk j (columns 64j..64j+63) of a row holds
+                          g[32j..32j+31] then u[32j..32j+31] */
   MOE_WS_HQ,           /* u8[Rmax][I]       MX(h) along I */
   MOE_WS_HQ_SF,
   MOE_WS_HTOK,         /* u8[I][Rmax]       MX(h) along tokens */

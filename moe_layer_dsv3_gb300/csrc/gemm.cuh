@@ -526,9 +526,21 @@ __device__ __forceinline__ void gemm_epilogue_tile(const GemmParams& p, const Ti
         // silu(g) u with the fast reciprocal-based divide (about 2 ulp)
         h[c * 32 + j] = __fdividef(g[j], 1.0f + __expf(-g[j])) * u[j];
       }
-      const int64_t icol = i_base + c * 32;
-      store_bf16x32(p.gu + prow * (2 * I) + icol, g);
-      store_bf16x32(p.gu + prow * (2 * I) + I + icol, u);
+      // saved g,u: 32-column chunk k of a row holds g then u (128 contiguous bytes),
+      // stored 4 rows x 128 bytes per instruction through this warp's scratch tile
+      const int64_t chunk = (i_base >> 5) + c;
+      uint4 v[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[i] = make_uint4(pack_bf16x2(g[8 * i], g[8 * i + 1]), pack_bf16x2(g[8 * i + 2], g[8 * i + 3]),
+                          pack_bf16x2(g[8 * i + 4], g[8 * i + 5]), pack_bf16x2(g[8 * i + 6], g[8 * i + 7]));
+        v[4 + i] = make_uint4(pack_bf16x2(u[8 * i], u[8 * i + 1]), pack_bf16x2(u[8 * i + 2], u[8 * i + 3]),
+                              pack_bf16x2(u[8 * i + 4], u[8 * i + 5]), pack_bf16x2(u[8 * i + 6], u[8 * i + 7]));
+      }
+      __nv_bfloat16* gu_rows0 = p.gu + (t.prow0 + q * 32) * (2 * I) + chunk * 64;
+      warp_store_rows128(reinterpret_cast<uint8_t*>(scr), lane, v, [&](int r) {
+        return reinterpret_cast<uint4*>(gu_rows0 + static_cast<int64_t>(r) * (2 * I));
+      });
     }
     tc_fence_before();
     mbar_arrive(acce);

@@ -200,8 +200,9 @@ __global__ void __launch_bounds__(128) swiglu_bwd_quant_kernel(
   uint4 graw[4], uraw[4];
   {
     const float4* pd = reinterpret_cast<const float4*>(dh + prow * I + c0);
-    const uint4* pg = reinterpret_cast<const uint4*>(gu + prow * (2 * I) + c0);
-    const uint4* pu = reinterpret_cast<const uint4*>(gu + prow * (2 * I) + I + c0);
+    // saved g,u: 32-column chunk c0 / 32 of the row holds g then u
+    const uint4* pg = reinterpret_cast<const uint4*>(gu + prow * (2 * I) + 2 * c0);
+    const uint4* pu = pg + 4;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const float4 v = pd[i];

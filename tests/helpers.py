@@ -50,3 +50,10 @@ def np_f64(t: torch.Tensor) -> np.ndarray:
 
 def bf16_tensor(a: np.ndarray, device="cuda") -> torch.Tensor:
     return torch.from_numpy(np.asarray(a, dtype=np.float32)).to(torch.bfloat16).to(device)
+
+
+def gu_split(gu: np.ndarray, I: int) -> np.ndarray:
+    """Saved g,u rows as [g | u]: the workspace keeps them interleaved per 32-column chunk
+    (chunk j of a row holds g[32j..32j+31] then u[32j..32j+31])."""
+    c = np.asarray(gu).reshape(gu.shape[0], I // 32, 2, 32)
+    return np.concatenate([c[:, :, 0, :].reshape(gu.shape[0], I), c[:, :, 1, :].reshape(gu.shape[0], I)], axis=1)

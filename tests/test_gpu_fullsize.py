@@ -19,7 +19,7 @@ from oracle import layer as OL
 from oracle import mxfp8
 from oracle import route as OR
 from oracle import schedule as OS
-from tests.helpers import np_f64, np_u8, rel_frob, untile_scales
+from tests.helpers import gu_split, np_f64, np_u8, rel_frob, untile_scales
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-3
@@ -217,7 +217,7 @@ def test_expert_stages(full):
         assert np.array_equal(full.rows_sf("XQ_SF", full.Tpad, d, tok), xq.scales)
         # GEMM1 + SwiGLU on identical MX x rows
         r1 = OL.expert_gemm1(xq.val, W)
-        gu = _f64(full.ws("GU", torch.bfloat16, (full.Rmax, 2 * I))[torch.as_tensor(prow, device="cuda")])
+        gu = gu_split(_f64(full.ws("GU", torch.bfloat16, (full.Rmax, 2 * I))[torch.as_tensor(prow, device="cuda")]), I)
         assert rel_frob(gu, r1["gu_saved"]) < TOL, e
         hq = mxfp8.dequantize(full.rows_u8("HQ", full.Rmax, I, prow), full.rows_sf("HQ_SF", full.Rmax, I, prow), 1)
         assert rel_frob(hq, mxfp8.roundtrip(r1["h"], 1)) < TOL, e

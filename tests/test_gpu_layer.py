@@ -17,7 +17,7 @@ from oracle import mxfp8
 from oracle import route as OR
 from oracle import schedule as OS
 from oracle.sigmoid import sigmoid_spec
-from tests.helpers import np_f64, np_u8, rel_frob, untile_scales
+from tests.helpers import gu_split, np_f64, np_u8, rel_frob, untile_scales
 
 pytestmark = pytest.mark.gpu
 # Tolerances (relative Frobenius error against the oracle rounded to bf16):
@@ -265,7 +265,7 @@ def _expert_weights(run, e):
 
 def test_gemm1_swiglu_stage(run):
     m = run.shape
-    gu = np_f64(run.ws("GU", torch.bfloat16, (run.Rmax, 2 * m.I)))
+    gu = gu_split(np_f64(run.ws("GU", torch.bfloat16, (run.Rmax, 2 * m.I))), m.I)
     hq = run.u8("HQ", run.Rmax, m.I)
     hsf = run.sf("HQ_SF", run.Rmax, m.I)
     for e in range(run.Ep):
@@ -351,7 +351,7 @@ def test_dO_ring_holds_last_laps(run):
 
 def test_dgrad_down_swiglu_stage(run):
     m = run.shape
-    gu = np_f64(run.ws("GU", torch.bfloat16, (run.Rmax, 2 * m.I)))
+    gu = gu_split(np_f64(run.ws("GU", torch.bfloat16, (run.Rmax, 2 * m.I))), m.I)
     dq = run.u8("DGU", run.Rmax, 2 * m.I)
     dsf = run.sf("DGU_SF", run.Rmax, 2 * m.I)
     for e in range(run.Ep):
