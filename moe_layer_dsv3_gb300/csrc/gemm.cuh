@@ -496,7 +496,9 @@ __device__ __forceinline__ void ring_consumed(const GemmParams& p, const TileInf
   }
 }
 
-template <int BN, int MODE>
+// HOLD: accumulator chunks of 32 columns the dh epilogue keeps in registers
+// at once (5 at 256 threads per CTA; fewer when more warps share the file).
+template <int BN, int MODE, int HOLD = 5>
 __device__ __forceinline__ void gemm_epilogue_tile(const GemmParams& p, const TileInfo& t, uint32_t tacc, int q,
                                                    int lane, float* scr, uint8_t* out_smem, const CUtensorMap* tma_o,
                                                    const CUtensorMap* tma_o2, uint64_t* acce) {
@@ -559,37 +561,45 @@ __device__ __forceinline__ void gemm_epilogue_tile(const GemmParams& p, const Ti
     uint8_t* buf = reinterpret_cast<uint8_t*>(scr);
     float* rows0 = static_cast<float*>(p.out) + (t.prow0 + q * 32) * static_cast<int64_t>(p.ldo) + t.n0;
     const float gw = (valid && t.e < p.E) ? p.gate[p.row_src[t.prow0 + row]] : 1.0f;
-#pragma unroll
-    for (int c = 0; c < BN / 32; c += 2) {
-      uint32_t r0[32], r1[32];
-      tmem_ld32_async(tacc + c * 32, r0);
-      tmem_ld32_async(tacc + (c + 1) * 32, r1);
-      tmem_wait_ld();
+    // Up to HOLD of the row's 32-column chunks are held in registers: the first
+    // ones are stored while the last ones are read, so the accumulator goes
+    // back to the MMA thread after only NC - H chunk stores.
+    constexpr int NC = BN / 32;
+    constexpr int H = NC < HOLD ? NC : HOLD;
+    uint32_t r[H][32];
+    auto scale = [&](uint32_t* v) {
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        reg_fence(r0[j]);
-        reg_fence(r1[j]);
-        r0[j] = __float_as_uint(__fmul_rn(__uint_as_float(r0[j]), gw));
-        r1[j] = __float_as_uint(__fmul_rn(__uint_as_float(r1[j]), gw));
+        reg_fence(v[j]);
+        v[j] = __float_as_uint(__fmul_rn(__uint_as_float(v[j]), gw));
       }
-      if (c + 2 == BN / 32) {   // whole accumulator row read: hand TMEM back
-        tc_fence_before();
-        mbar_arrive(acce);
-        ring_consumed(p, t, q, lane);
-      }
-      uint4 v0[8], v1[8];
+    };
+    auto store = [&](const uint32_t* v, int c) {
+      uint4 w[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        v0[i] = make_uint4(r0[4 * i], r0[4 * i + 1], r0[4 * i + 2], r0[4 * i + 3]);
-        v1[i] = make_uint4(r1[4 * i], r1[4 * i + 1], r1[4 * i + 2], r1[4 * i + 3]);
-      }
-      warp_store_rows128(buf, lane, v0, [&](int r) {
-        return reinterpret_cast<uint4*>(rows0 + static_cast<int64_t>(r) * p.ldo + c * 32);
+      for (int k = 0; k < 8; ++k) w[k] = make_uint4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+      warp_store_rows128(buf, lane, w, [&](int rr) {
+        return reinterpret_cast<uint4*>(rows0 + static_cast<int64_t>(rr) * p.ldo + c * 32);
       });
-      warp_store_rows128(buf, lane, v1, [&](int r) {
-        return reinterpret_cast<uint4*>(rows0 + static_cast<int64_t>(r) * p.ldo + (c + 1) * 32);
-      });
+    };
+    // chunk c lives in slot c % H
+#pragma unroll
+    for (int c = 0; c < H; ++c) tmem_ld32_async(tacc + c * 32, r[c]);
+    tmem_wait_ld();
+#pragma unroll
+    for (int c = 0; c < H; ++c) scale(r[c]);
+#pragma unroll
+    for (int c = H; c < NC; ++c) {       // chunk c - H leaves its slot to chunk c
+      store(r[c % H], c - H);
+      tmem_ld32_async(tacc + c * 32, r[c % H]);
+      tmem_wait_ld();
+      scale(r[c % H]);
     }
+    tc_fence_before();                   // whole accumulator row read: hand TMEM back
+    mbar_arrive(acce);
+    ring_consumed(p, t, q, lane);
+#pragma unroll
+    for (int c = NC - H; c < NC; ++c) store(r[c % H], c);
   } else if constexpr (MODE == kPush) {
     const int64_t prow = t.prow0 + row;
     const int a = valid ? p.row_src[prow] : -1;
@@ -833,7 +843,8 @@ __global__ void __launch_bounds__(gemm_threads(MODE, MV), 1)
       if (!gemm_decode<BN, MODE>(p, tile, t)) continue;
       if (!mbar_wait(&accf[acc], acc_phase, p.status, 30)) break;
       tc_fence_after();
-      gemm_epilogue_tile<BN, BM>(p, t, tmem + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(q * 32) << 16),
+      gemm_epilogue_tile<BN, BM, (gemm_threads(MODE, MV) > 256 ? 2 : 5)>(
+          p, t, tmem + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(q * 32) << 16),
                                    q, lane, scr, out_smem, &tma_o, &tma_o2, &acce[acc]);
       if constexpr (BM != kPush && BM != kWgrad && BM != kSwigluFwd && BM != kSwigluBwd) {   // others release TMEM inside
         tc_fence_before();
