@@ -14,8 +14,8 @@
 // Work list: "tiles" of 128 rows x BN columns, decoded from the device-side
 // schedule, so the host never learns per-expert counts.
 //
-// The all-laps ring modes add two mover warps (256 threads) that fill the
-// ring token buffers while the other warps compute, so one persistent launch
+// The all-laps ring modes add mover warps (two by default: 256 threads) that
+// fill the ring token buffers while the other warps compute, so one persistent launch
 // covers every lap. Ordering goes through per-m-tile device counters:
 //   moved[gm]    8-row groups of m-tile gm written into its ring slot; the
 //                producer waits for all 16 before its first TMA load of gm;
