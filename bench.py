@@ -603,6 +603,16 @@ def run_ours(args, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize()
     ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, "cuda")
+    # the machine's host link alone: one copy of x each way between pinned host memory and the device
+    link = {}
+    for name, dst, src, st in (("h2d_gbs", xd[0], xh, h2d_s), ("d2h_gbs", yh, yd[0], d2h_s)):
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(st)
+        with torch.cuda.stream(st):
+            dst.copy_(src, non_blocking=True)
+        c1.record(st)
+        c1.synchronize()
+        link[name] = xh.numel() * xh.element_size() / (c0.elapsed_time(c1) * 1e-3) / 1e9
     code, site = L.status()
     if code:
         raise RuntimeError("device status %d at site %d" % (code, site))
@@ -696,7 +706,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": job_tokens_per_s(shape.T, world, ms_e2e), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e, "host_link_gbs": {k: round(v, 1) for k, v in link.items()}},
         "gpu_launches": launches,
         "clocks": clk,
     }
