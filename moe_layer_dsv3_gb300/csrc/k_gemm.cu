@@ -214,7 +214,7 @@ int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int
   p.I = m.I;
   p.status = status;
   // decode tables written by the schedule (one load per tile instead of searches)
-  if (mode == kPush) p.push_info = static_cast<const int*>(tile_info);
+  if (mode == kPush || mode == kGroupedNv4) p.push_info = static_cast<const int*>(tile_info);
   if (mode == kWgrad) p.wg_info = static_cast<const int4*>(tile_info);
   if (mv != nullptr) {
     p.lapbase = mv->lapbase;

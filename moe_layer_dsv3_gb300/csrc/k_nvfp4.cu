@@ -109,7 +109,8 @@ extern "C" int moe_expert_gemm_nvfp4(const moe_config_t* cfg, int N, int K, cons
   if (int r = moe::gemm_dispatch("expert_gemm_nvfp4", moe::kGroupedNv4, m, 0, N, K, static_cast<int>(m.Rmax), op, ep,
                                  moe::ws_ptr<int>(L, ws, MOE_WS_COUNTS), moe::ws_ptr<int>(L, ws, MOE_WS_POFF),
                                  nullptr, nullptr, moe::ws_ptr<int>(L, ws, MOE_WS_STATUS),
-                                 static_cast<cudaStream_t>(stream)))
+                                 static_cast<cudaStream_t>(stream), 0, nullptr, nullptr,
+                                 moe::ws_ptr<int>(L, ws, MOE_WS_PUSHINFO)))
     return r;
   return call.status();
 }
