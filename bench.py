@@ -166,6 +166,15 @@ def probe_peak(args):
         "name": "moe_expert_gemm_nvfp4 (grouped over the schedule, fp32 rank-ordered rows)",
         "shape": "dsv3_e64 routing: %d assignment rows x N=%d x K=%d, %d experts" % (shp.T * (shp.k + shp.S), Ng, Kg, Ep),
         "tflops_burst": b * flop_g / flop, "tflops_sustained": su * flop_g / flop}
+    # the same product with GEMM2's epilogue: bf16 rows pushed to their assignments
+    ob = torch.empty((shp.T * (shp.k + shp.S), Ng), dtype=torch.bfloat16, device=dev)
+    fn = lambda: M.moe_expert_gemm_nvfp4_push(L.cfg, Ng, Kg, ag.data_ptr(), sfa.data_ptr(), wg.data_ptr(),  # noqa: E731
+                                              sfw.data_ptr(), 1.0, ob.data_ptr(), L.ws.data_ptr(), sp)
+    b, su = timeit(fn)
+    out["ours_nvfp4_push"] = {
+        "name": "moe_expert_gemm_nvfp4_push (grouped over the schedule, bf16 rows pushed to their assignments)",
+        "shape": out["ours_nvfp4_grouped"]["shape"],
+        "tflops_burst": b * flop_g / flop, "tflops_sustained": su * flop_g / flop}
     out["clocks"] = clocks.stop()
     print(json.dumps(out), flush=True)
 

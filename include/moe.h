@@ -375,6 +375,18 @@ MOE_API int moe_expert_gemm_nvfp4(const moe_config_t* cfg, int N, int K, const v
                                   const void* w, const void* w_sf, float alpha, float* out, void* ws,
                                   moe_stream_t stream);
 
+/* The same NVFP4 expert GEMM with GEMM2's epilogue: each row r of an expert's
+ * segment that holds an assignment a = ROWSRC[r] (moe_ws_view) is written as
+ *   out[a][n] (bf16, round to nearest even) = alpha * sum_k dequant(a)[r][k] * dequant(w)[e*N + n][k],
+ * the fp32 product of moe_expert_gemm_nvfp4 rounded to bf16, at the
+ * assignment's row (a < T*(k+S), the routed then the shared assignments, as
+ * the layer's expert outputs O). Padding rows are not written.
+ *   out: bf16 [T*(k+S)][N], 16-byte aligned. Other arguments, requirements and
+ *   errors as moe_expert_gemm_nvfp4. */
+MOE_API int moe_expert_gemm_nvfp4_push(const moe_config_t* cfg, int N, int K, const void* a, const void* a_sf,
+                                       const void* w, const void* w_sf, float alpha, void* out, void* ws,
+                                       moe_stream_t stream);
+
 /* Re-lay canonical scales [rows][K/32] into the tiled layout the tensor
  * cores read: 512-byte atoms of 128 rows x 4 blocks, atom (r/128, kb/4) at
  * ((r/128)*(K/128) + kb/4)*512, byte (r%32)*16 + (r/32%4)*4 + kb%4.

@@ -79,6 +79,7 @@ _SIGS = {
     "moe_quantize_nvfp4": [_P, _I, _I, ctypes.c_float, _P, _P, _I, _P],
     "moe_gemm_nvfp4": [_I, _I, _I, _P, _P, _P, _P, ctypes.c_float, _P, _P],
     "moe_expert_gemm_nvfp4": [_CFG, _I, _I, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P],
+    "moe_expert_gemm_nvfp4_push": [_CFG, _I, _I, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P],
     "moe_scales_to_tiled": [_P, _I, _I, _P, _P],
     "moe_profile_enable": [_I],
     "moe_profile_read": [ctypes.c_void_p, _I, ctypes.POINTER(_I)],
@@ -208,6 +209,12 @@ def moe_expert_gemm_nvfp4(cfg, N, K, a, a_sf, w, w_sf, alpha, out, ws, stream=0)
     _check("moe_expert_gemm_nvfp4",
            _lib.moe_expert_gemm_nvfp4(ctypes.byref(cfg), N, K, _p(a), _p(a_sf), _p(w), _p(w_sf), float(alpha),
                                       _p(out), _p(ws), _p(stream)))
+
+
+def moe_expert_gemm_nvfp4_push(cfg, N, K, a, a_sf, w, w_sf, alpha, out, ws, stream=0):
+    _check("moe_expert_gemm_nvfp4_push",
+           _lib.moe_expert_gemm_nvfp4_push(ctypes.byref(cfg), N, K, _p(a), _p(a_sf), _p(w), _p(w_sf), float(alpha),
+                                           _p(out), _p(ws), _p(stream)))
 
 
 def moe_gemm_nvfp4(M, N, K, a, a_sf, b, b_sf, alpha, c, stream=0):

@@ -57,7 +57,7 @@ bool make_tmap_sf(CUtensorMap* m, const void* base, int64_t atoms);
 
 // The epilogue / tile shape a mode shares with its per-lap form.
 __host__ __device__ constexpr int base_mode(int mode) {
-  return mode == kSwigluFwdRing ? kSwigluFwd : (mode == kSwigluBwdRing ? kSwigluBwd : mode);
+  return mode == kSwigluFwdRing ? kSwigluFwd : (mode == kSwigluBwdRing ? kSwigluBwd : (mode == kPushNv4 ? kPush : mode));
 }
 __host__ __device__ constexpr bool ring_mode(int mode) { return mode == kSwigluFwdRing || mode == kSwigluBwdRing; }
 // 192 threads (producer, MMA, 4 epilogue warps), plus MV mover warps in the all-laps ring modes.
@@ -105,11 +105,15 @@ struct GemmCfg {
   static constexpr bool kBf16 = MODE == kRouterMode;
   // NVFP4: a 128-byte stage row holds 256 E2M1 values; the scales (one E4M3
   // per 16) of a stage are 4 atoms per 128 rows, one atom per K = 64 MMA.
-  static constexpr bool kNv4 = MODE == kPlainNv4 || MODE == kGroupedNv4;
+  static constexpr bool kNv4 = MODE == kPlainNv4 || MODE == kGroupedNv4 || MODE == kPushNv4;
   // Weight gradients stage their bf16 output tile in shared memory and write
   // it with TMA stores, so the tile's DRAM write overlaps the next mainloop.
   static constexpr bool kTmaOut = MODE == kWgrad;
-  static constexpr int kStages = kTmaOut ? (BN >= 256 ? 3 : 5) : (BN >= 256 ? 4 : (BN >= 128 ? 6 : 8));
+  // (the NVFP4 push mode's stages carry 4 scale atoms per operand tile and
+  // its epilogue a scratch tile per warp: 3 stages fit at BN = 256, 5 at 128)
+  static constexpr int kStages = kTmaOut ? (BN >= 256 ? 3 : 5)
+                                         : (MODE == kPushNv4 ? (BN >= 256 ? 3 : 5)
+                                                             : (BN >= 256 ? 4 : (BN >= 128 ? 6 : 8)));
   static constexpr int kOutBytes = kTmaOut ? 128 * BN * 2 : 0;
   static constexpr int kABytes = 128 * 128;
   static constexpr int kBBytes = BN * 128;
@@ -166,7 +170,7 @@ __device__ __forceinline__ int gemm_num_tiles(const GemmParams& p) {
     return p.lapbase[p.Lb] * (p.N / BN);
   } else if constexpr (MODE == kSwigluFwd || MODE == kSwigluBwd) {
     return p.lap_tiles[p.lap * (p.Ep + 1) + p.Ep] * (p.N / BN);
-  } else if constexpr (MODE == kPush || MODE == kGroupedNv4) {
+  } else if constexpr (MODE == kPush || MODE == kGroupedNv4 || MODE == kPushNv4) {
     return (p.poff[p.Ep] / 128) * (p.N / BN);
   } else if constexpr (MODE == kWgrad) {
     // positions of the two-ended schedule (see gemm_decode): enough rounds for the heavy half
@@ -234,7 +238,7 @@ __device__ __forceinline__ bool gemm_decode(const GemmParams& p, int tile, TileI
     const int nt = p.N / BN;
     const int g = tile / nt, n = tile - (tile / nt) * nt;
     return lap_decode<BN>(p, p.lap, g, n, 0, t);
-  } else if constexpr (MODE == kPush || MODE == kGroupedNv4) {
+  } else if constexpr (MODE == kPush || MODE == kGroupedNv4 || MODE == kPushNv4) {
     // padded rank rows of the schedule: m-tile g belongs to the expert whose segment holds it
     const int nt = p.N / BN;
     const int g = tile / nt, n = tile - (tile / nt) * nt;
@@ -331,9 +335,25 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v
 // Read this thread's whole accumulator row (BN fp32 columns) into packed bf16
 // pairs, then hand the TMEM buffer back to the MMA warp at once, so the next
 // tile's MMAs start while the row is still being written out.
-template <int BN>
-__device__ __forceinline__ void drain_acc_bf16(uint32_t tacc, bool have_acc, uint32_t* packed, uint64_t* acce) {
-  if (have_acc) {
+// kAlpha: the row is scaled by alpha first (NVFP4: the operands' tensor scales).
+template <int BN, bool kAlpha = false>
+__device__ __forceinline__ void drain_acc_bf16(uint32_t tacc, bool have_acc, uint32_t* packed, uint64_t* acce,
+                                               float alpha = 1.0f) {
+  if (have_acc && kAlpha) {
+    // one load per wait: the scaling leaves no registers for a second one
+#pragma unroll
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t r0[32];
+      tmem_ld32_async(tacc + c * 32, r0);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) reg_fence(r0[j]);
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        packed[c * 16 + j] = pack_bf16x2(__fmul_rn(__uint_as_float(r0[2 * j]), alpha),
+                                         __fmul_rn(__uint_as_float(r0[2 * j + 1]), alpha));
+    }
+  } else if (have_acc) {
     // two loads in flight per wait
 #pragma unroll
     for (int c = 0; c < BN / 32; c += 2) {
@@ -498,7 +518,8 @@ __device__ __forceinline__ void ring_consumed(const GemmParams& p, const TileInf
 
 // HOLD: accumulator chunks of 32 columns the dh epilogue keeps in registers
 // at once (5 at 256 threads per CTA; fewer when more warps share the file).
-template <int BN, int MODE, int HOLD = 5>
+// kAlpha: push rows scaled by p.alpha (the NVFP4 push mode).
+template <int BN, int MODE, int HOLD = 5, bool kAlpha = false>
 __device__ __forceinline__ void gemm_epilogue_tile(const GemmParams& p, const TileInfo& t, uint32_t tacc, int q,
                                                    int lane, float* scr, uint8_t* out_smem, const CUtensorMap* tma_o,
                                                    const CUtensorMap* tma_o2, uint64_t* acce) {
@@ -604,7 +625,7 @@ __device__ __forceinline__ void gemm_epilogue_tile(const GemmParams& p, const Ti
     const int64_t prow = t.prow0 + row;
     const int a = valid ? p.row_src[prow] : -1;
     uint32_t packed[BN / 2];
-    drain_acc_bf16<BN>(tacc, true, packed, acce);
+    drain_acc_bf16<BN, kAlpha>(tacc, true, packed, acce, p.alpha);
     // Each lane holds one row; rows go to scattered assignments. Per 64-column
     // chunk the warp swaps the tile through shared memory so that each store
     // instruction writes 4 rows x 128 contiguous bytes instead of 32 x 16.
@@ -843,7 +864,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE, MV), 1)
       if (!gemm_decode<BN, MODE>(p, tile, t)) continue;
       if (!mbar_wait(&accf[acc], acc_phase, p.status, 30)) break;
       tc_fence_after();
-      gemm_epilogue_tile<BN, BM, (gemm_threads(MODE, MV) > 256 ? 2 : 5)>(
+      gemm_epilogue_tile<BN, BM, (gemm_threads(MODE, MV) > 256 ? 2 : 5), MODE == kPushNv4>(
           p, t, tmem + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(q * 32) << 16),
                                    q, lane, scr, out_smem, &tma_o, &tma_o2, &acce[acc]);
       if constexpr (BM != kPush && BM != kWgrad && BM != kSwigluFwd && BM != kSwigluBwd) {   // others release TMEM inside

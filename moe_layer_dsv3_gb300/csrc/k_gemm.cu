@@ -201,7 +201,7 @@ int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int
   p.out2 = ep.out2;
   p.ldo = ep.ldo;
   p.alpha = ep.alpha;
-  if (mode == kPlainNv4 || mode == kGroupedNv4)
+  if (mode == kPlainNv4 || mode == kGroupedNv4 || mode == kPushNv4)
     p.a_ktiles = p.b_ktiles = K / 64;   // scale atoms (64 elements) per 128-row tile
   p.q_rows = ep.q_rows;
   p.q_rows_sf = ep.q_rows_sf;
@@ -214,7 +214,7 @@ int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int
   p.I = m.I;
   p.status = status;
   // decode tables written by the schedule (one load per tile instead of searches)
-  if (mode == kPush || mode == kGroupedNv4) p.push_info = static_cast<const int*>(tile_info);
+  if (mode == kPush || mode == kGroupedNv4 || mode == kPushNv4) p.push_info = static_cast<const int*>(tile_info);
   if (mode == kWgrad) p.wg_info = static_cast<const int4*>(tile_info);
   if (mv != nullptr) {
     p.lapbase = mv->lapbase;
@@ -236,7 +236,7 @@ int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int
     upper = lap_mtiles_max(m) * nt;
   } else if (mode == kSwigluFwd || mode == kSwigluBwd) {
     upper = (static_cast<int64_t>(m.E) * (m.C / 128) + (lap == 0 ? m.S * (m.Tpad / 128) : 0)) * nt;
-  } else if (mode == kPush || mode == kGroupedNv4) {
+  } else if (mode == kPush || mode == kGroupedNv4 || mode == kPushNv4) {
     upper = (m.Rmax / 128) * nt;
   } else if (mode == kWgrad) {
     upper = static_cast<int64_t>(m.Ep) * (M / 128) * nt;
@@ -276,6 +276,9 @@ int gemm_dispatch(const char* name, int mode, const Dims& m, int lap, int N, int
     case kGroupedNv4:
       return BN == 256 ? run<256, kGroupedNv4>(name, ta, ta2, tb, to, to2, p, grid, s)
                        : run<128, kGroupedNv4>(name, ta, ta2, tb, to, to2, p, grid, s);
+    case kPushNv4:
+      return BN == 256 ? run<256, kPushNv4>(name, ta, ta2, tb, to, to2, p, grid, s)
+                       : run<128, kPushNv4>(name, ta, ta2, tb, to, to2, p, grid, s);
     case kRouterMode:
       if (BN == 32) return run<32, kRouterMode>(name, ta, ta2, tb, to, to2, p, grid, s);
       return BN == 256 ? run<256, kRouterMode>(name, ta, ta2, tb, to, to2, p, grid, s) : run<128, kRouterMode>(name, ta, ta2, tb, to, to2, p, grid, s);

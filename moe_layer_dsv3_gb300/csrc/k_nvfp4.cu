@@ -80,9 +80,12 @@ extern "C" int moe_quantize_nvfp4(const void* src, int rows, int K, float g, voi
   return call.status();
 }
 
-extern "C" int moe_expert_gemm_nvfp4(const moe_config_t* cfg, int N, int K, const void* a, const void* a_sf,
-                                     const void* w, const void* w_sf, float alpha, float* out, void* ws,
-                                     moe_stream_t stream) {
+namespace {
+
+// The NVFP4 expert GEMM over the schedule in ws: fp32 rank-ordered rows
+// (kGroupedNv4) or bf16 rows pushed to their assignment (kPushNv4).
+int expert_gemm_nvfp4(const moe_config_t* cfg, int mode, int N, int K, const void* a, const void* a_sf,
+                      const void* w, const void* w_sf, float alpha, void* out, void* ws, moe_stream_t stream) {
   if (int r = moe::validate(cfg)) return r;
   if (N <= 0 || K <= 0 || N % 128 || K % 256 || !a || !a_sf || !w || !w_sf || !out || !ws) return MOE_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(a_sf) |
@@ -106,13 +109,27 @@ extern "C" int moe_expert_gemm_nvfp4(const moe_config_t* cfg, int N, int K, cons
   ep.out = out;
   ep.ldo = N;
   ep.alpha = alpha;
-  if (int r = moe::gemm_dispatch("expert_gemm_nvfp4", moe::kGroupedNv4, m, 0, N, K, static_cast<int>(m.Rmax), op, ep,
-                                 moe::ws_ptr<int>(L, ws, MOE_WS_COUNTS), moe::ws_ptr<int>(L, ws, MOE_WS_POFF),
-                                 nullptr, nullptr, moe::ws_ptr<int>(L, ws, MOE_WS_STATUS),
-                                 static_cast<cudaStream_t>(stream), 0, nullptr, nullptr,
-                                 moe::ws_ptr<int>(L, ws, MOE_WS_PUSHINFO)))
+  if (int r = moe::gemm_dispatch(mode == moe::kPushNv4 ? "expert_gemm_nvfp4_push" : "expert_gemm_nvfp4", mode, m, 0,
+                                 N, K, static_cast<int>(m.Rmax), op, ep, moe::ws_ptr<int>(L, ws, MOE_WS_COUNTS),
+                                 moe::ws_ptr<int>(L, ws, MOE_WS_POFF), nullptr, moe::ws_ptr<int>(L, ws, MOE_WS_ROWSRC),
+                                 moe::ws_ptr<int>(L, ws, MOE_WS_STATUS), static_cast<cudaStream_t>(stream), 0, nullptr,
+                                 nullptr, moe::ws_ptr<int>(L, ws, MOE_WS_PUSHINFO)))
     return r;
   return call.status();
+}
+
+}  // namespace
+
+extern "C" int moe_expert_gemm_nvfp4(const moe_config_t* cfg, int N, int K, const void* a, const void* a_sf,
+                                     const void* w, const void* w_sf, float alpha, float* out, void* ws,
+                                     moe_stream_t stream) {
+  return expert_gemm_nvfp4(cfg, moe::kGroupedNv4, N, K, a, a_sf, w, w_sf, alpha, out, ws, stream);
+}
+
+extern "C" int moe_expert_gemm_nvfp4_push(const moe_config_t* cfg, int N, int K, const void* a, const void* a_sf,
+                                          const void* w, const void* w_sf, float alpha, void* out, void* ws,
+                                          moe_stream_t stream) {
+  return expert_gemm_nvfp4(cfg, moe::kPushNv4, N, K, a, a_sf, w, w_sf, alpha, out, ws, stream);
 }
 
 extern "C" int moe_gemm_nvfp4(int M, int N, int K, const void* a, const void* a_sf, const void* b, const void* b_sf,

@@ -156,6 +156,7 @@ enum GemmMode : int {
   kSwigluBwdRing = 7,  // kSwigluBwd over all ring laps in one launch, mover warps fill the dO ring
   kPlainNv4 = 8,       // single dense NVFP4 problem (E2M1, E4M3 scale per 16), fp32 output times alpha
   kGroupedNv4 = 9,     // NVFP4 expert GEMM over the schedule's padded rank rows, fp32 rank-ordered rows times alpha
+  kPushNv4 = 10,       // the same NVFP4 expert GEMM with the kPush epilogue: bf16 rows times alpha to their assignment
 };
 
 // Where the mover warps of the all-laps ring modes take each ring row from.

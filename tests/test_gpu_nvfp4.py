@@ -165,3 +165,14 @@ def test_expert_gemm_nvfp4_grouped(lib, Nn, K):
         ref = da[rows] @ dw[e * Nn:(e + 1) * Nn].T * (float(ga) * float(gw))
         assert rel_frob(got[rows], ref) < 1e-5, e
     assert (got[R:] == 7.0).all()
+    # the push form (GEMM2's epilogue): each assignment's row is the fp32 product rounded to bf16
+    Ap = shape.T * (shape.k + shape.S)
+    O = torch.full((Ap, Nn), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lib.moe_expert_gemm_nvfp4_push(L.cfg, Nn, K, A.data_ptr(), Asf.data_ptr(), W.data_ptr(), Wsf.data_ptr(),
+                                   float(alpha), O.data_ptr(), L.ws.data_ptr())
+    torch.cuda.synchronize()
+    row_src = L.ws_tensor("ROWSRC", torch.int32, (Rmax,)).cpu().numpy()
+    live = np.flatnonzero(row_src >= 0)
+    assert len(live) == Ap and sorted(row_src[live]) == list(range(Ap))
+    want = out[torch.as_tensor(live, device="cuda")].to(torch.bfloat16)
+    assert torch.equal(O[torch.as_tensor(row_src[live], device="cuda").long()].view(torch.int16), want.view(torch.int16))
