@@ -550,39 +550,44 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- end to end through the C ABI with host buffers (H2D of x, dy; D2H of y, dx).
     # Every step copies its inputs from pinned host memory and its outputs back.
-    # The copies run on two copy streams, double-buffered on the device, so
-    # step i+1's upload and step i's download overlap step i's compute; within
-    # a step the forward waits only for x and y leaves during the backward.
+    # The copies run on two copy streams into NB device buffers per tensor, so a
+    # step's inputs are uploaded NB - 1 steps ahead and its outputs have NB steps
+    # to leave, which absorbs copy jitter on shared hosts; within a step the
+    # forward waits only for x and y leaves during the backward.
+    NB = 3
     xh = x.cpu().pin_memory()
     dyh = dy.cpu().pin_memory()
     yh = torch.empty_like(xh).pin_memory()
     dxh = torch.empty_like(xh).pin_memory()
-    xd = [torch.empty_like(x) for _ in range(2)]
-    dyd = [torch.empty_like(dy) for _ in range(2)]
-    yd = [torch.empty_like(x) for _ in range(2)]
-    dxd = [torch.empty_like(x) for _ in range(2)]
+    xd = [torch.empty_like(x) for _ in range(NB)]
+    dyd = [torch.empty_like(dy) for _ in range(NB)]
+    yd = [torch.empty_like(x) for _ in range(NB)]
+    dxd = [torch.empty_like(x) for _ in range(NB)]
     h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
 
     def e2e_run(n, start_ev):
-        ev = lambda: [torch.cuda.Event() for _ in range(2)]   # noqa: E731
+        ev = lambda: [torch.cuda.Event() for _ in range(NB)]   # noqa: E731
         loaded_x, loaded_dy, fwd_done, done, drained_y, drained_dx = ev(), ev(), ev(), ev(), ev(), ev()
 
-        def upload(b, after):
-            # x first: the forward starts once x is in; dy is only needed by the backward
-            h2d_s.wait_event(after)
+        def upload(i):
+            # step i's inputs into buffer i % NB once step i - NB has finished with it;
+            # x first: the forward starts once x is in, dy is only needed by the backward
+            b = i % NB
+            h2d_s.wait_event(done[b] if i >= NB else start_ev)
             with torch.cuda.stream(h2d_s):
                 xd[b].copy_(xh, non_blocking=True)
                 loaded_x[b].record(h2d_s)
                 dyd[b].copy_(dyh, non_blocking=True)
                 loaded_dy[b].record(h2d_s)
 
-        upload(0, start_ev)
+        for i in range(min(NB - 1, n)):
+            upload(i)
         for i in range(n):
-            b = i % 2
-            if i + 1 < n:
-                upload(1 - b, done[1 - b] if i >= 1 else start_ev)
+            b = i % NB
+            if i + NB - 1 < n:
+                upload(i + NB - 1)
             stream.wait_event(loaded_x[b])
-            if i >= 2:
+            if i >= NB:
                 stream.wait_event(drained_y[b])
             L.forward(xd[b], wr, bias, sp, y=yd[b])          # outputs go straight to this step's buffers
             fwd_done[b].record(stream)
@@ -591,7 +596,7 @@ def run_ours(args, rank, world, local_rank):
                 yh.copy_(yd[b], non_blocking=True)
             drained_y[b].record(d2h_s)
             stream.wait_event(loaded_dy[b])
-            if i >= 2:
+            if i >= NB:
                 stream.wait_event(drained_dx[b])
             L.backward(dyd[b], sp, dx=dxd[b])
             done[b].record(stream)
