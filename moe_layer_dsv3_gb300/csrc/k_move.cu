@@ -118,6 +118,29 @@ __global__ void __launch_bounds__(256, 3) permute_lap_kernel(
 // many rows; each row is then copied with kDispChunks 16-byte chunks a lane
 // in flight. Measured (one GB300, dsv3_zipf): 2 slots per item beat 1, 4 and
 // 8, and a TMA bulk-copy form through shared memory.
+// L2 cache policies of the dispatch copies: the gathered MX(x) rows (about
+// the size of L2 at the benchmark shape, each read k times) are kept, and the
+// ring rows this stand-alone form writes, read by nothing soon after, go first.
+__device__ __forceinline__ uint64_t pol_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t pol_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint4 ld_hint(const uint4* a, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(a), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ void st_hint(uint4* a, uint4 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;"
+               :: "l"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol) : "memory");
+}
 constexpr int kDispSlots = 2;
 constexpr int kDispScaleJobs = 16;   // warps sharing one ring m-tile's scales
 constexpr int kDispChunks = 7;
@@ -141,6 +164,7 @@ __global__ void __launch_bounds__(256, 4) dispatch_all_kernel(
   const int laps = static_cast<int>((n - static_cast<int64_t>(b) * C + 2LL * C - 1) / (2LL * C));   // laps b, b+2, ...
   const int p0 = poff[e];
   const int chunks = d >> 4;
+  const uint64_t pfirst = pol_evict_first(), plast = pol_evict_last();
   for (int jb = 0; jb < laps; jb += kLapsPerBatch) {
     // lane: lap jb + lane / kDispSlots, slot s0 + lane % kDispSlots -> token, -1 (zero row) or -2 (no row)
     int tok = -2;
@@ -167,12 +191,12 @@ __global__ void __launch_bounds__(256, 4) dispatch_all_kernel(
 #pragma unroll
           for (int u = 0; u < kDispChunks; ++u) {
             const int c = c0 + u * 32 + lane;
-            v[u] = (t >= 0 && c < chunks) ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+            v[u] = (t >= 0 && c < chunks) ? ld_hint(src + c, plast) : make_uint4(0, 0, 0, 0);
           }
 #pragma unroll
           for (int u = 0; u < kDispChunks; ++u) {
             const int c = c0 + u * 32 + lane;
-            if (c < chunks) dst[c] = v[u];
+            if (c < chunks) st_hint(dst + c, v[u], pfirst);
           }
         }
 
