@@ -175,90 +175,126 @@ __global__ void __launch_bounds__(kTokThreads, kGate ? 3 : 4) tok_gather_kernel(
   *reinterpret_cast<uint32_t*>(sf + sf_off(cb + threadIdx.x, r0 >> 5, Rmax >> 7)) = ssf[threadIdx.x];
 }
 
+// Plain (coherent) global loads in volatile asm. Issued before a warp barrier,
+// they all stay ahead of it; the compiler may sink ordinary and read-only
+// (.nc) loads toward their first use, past such a barrier too, and a warp
+// then waits on one load after another instead of on all of them at once.
+__device__ __forceinline__ float4 ldg_f4(const float* p) {
+  float4 v;
+  asm volatile("ld.global.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint2 ldg_u2(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+
 // SwiGLU backward of padded rank rows and the two MX forms of dGU = [dg | du]:
 // along 2I per row (q_rows, tiled scales) and along ranks per column (q_tok,
 // [2I][Rmax], tiled scales). Row pr is an assignment iff row_src[pr] >= 0;
-// other rows of an expert's padded segment give zeros. CTA: 128 rows x 32
-// columns of I, warp q on rows 32q..32q+31 (lane = row). The token-axis
-// codes of the 4 warps meet in shared memory, so each column's 128 rows are
-// stored as one 128-byte run.
+// other rows of an expert's padded segment give zeros.
 //   sg = sigmoid(g), dg = dh u sg (1 + g (1 - sg)), du = dh g sg   (fp32)
-__global__ void __launch_bounds__(128) swiglu_bwd_quant_kernel(
+// CTA: 128 rows x 32 columns of I; warp q takes rows 32q..32q+31. Lane
+// (gq = lane / 8, cq = lane % 8) holds rows 8gq..8gq+7 of the warp's block
+// and columns 4cq..4cq+3, so each load instruction reads 4 rows' contiguous
+// 128-byte (dh) or 64-byte (g, u) runs, and a row's 32-column MX block is
+// spread over the 8 lanes of one group (amax by 3 shuffles) while a column's
+// 32-row token block is spread over the 4 groups (amax by 2 shuffles). The
+// token-axis codes of the 4 warps meet in shared memory, so each column's
+// 128 rows are stored as one 128-byte run. 6 CTAs per SM (80 registers, a
+// 32-byte spill): 0.76 against 0.77 ms at 5 CTAs without it.
+__global__ void __launch_bounds__(128, 6) swiglu_bwd_quant_kernel(
     const float* __restrict__ dh, const __nv_bfloat16* __restrict__ gu, const int* __restrict__ row_src,
     const int* __restrict__ poff_end, int I, int64_t Rmax, uint8_t* __restrict__ q_rows,
     uint8_t* __restrict__ q_rows_sf, uint8_t* __restrict__ q_tok, uint8_t* __restrict__ q_tok_sf) {
-  __shared__ float scr[4][32 * 33];
   __shared__ __align__(16) uint8_t tst[2][32 * 128];   // [dg|du][column][128 rows], 16-byte chunks swizzled
   __shared__ uint32_t tsf[2][32];                        // [dg|du][column]: 4 scale bytes (row blocks)
-  const int q = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 3, cq = lane & 7;
   const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128;
   if (r0 >= *poff_end) return;
   const int c0 = blockIdx.x * 32;
-  const int64_t prow = r0 + q * 32 + lane;
-  const bool valid = row_src[prow] >= 0;
-  float h[32];
-  uint4 graw[4], uraw[4];
-  {
-    const float4* pd = reinterpret_cast<const float4*>(dh + prow * I + c0);
+  const int64_t wrow = r0 + q * 32;                       // first row of this warp's block
+  const uint32_t valid = __ballot_sync(0xFFFFFFFFu, row_src[wrow + lane] >= 0);
+  // All 24 loads are issued before any arithmetic (ldg_f4, ldg_u2 and the
+  // warp barrier after them): left to itself the compiler sinks them toward
+  // their uses, and the kernel took 1.22 instead of 0.78 ms at full size.
+  float4 hv[8];
+  uint2 gv[8], uv[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int64_t prow = wrow + 8 * gq + i;
+    hv[i] = ldg_f4(dh + prow * I + c0 + 4 * cq);
     // saved g,u: 32-column chunk c0 / 32 of the row holds g then u
-    const uint4* pg = reinterpret_cast<const uint4*>(gu + prow * (2 * I) + 2 * c0);
-    const uint4* pu = pg + 4;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float4 v = pd[i];
-      h[4 * i] = v.x; h[4 * i + 1] = v.y; h[4 * i + 2] = v.z; h[4 * i + 3] = v.w;
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) { graw[i] = pg[i]; uraw[i] = pu[i]; }
+    const __nv_bfloat16* pg = gu + prow * (2 * I) + 2 * c0 + 4 * cq;
+    gv[i] = ldg_u2(pg);
+    uv[i] = ldg_u2(pg + 32);
   }
-  float g[32], u[32], dg[32];
+  __syncwarp();
+  float dg[8][4], du[8][4];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const uint32_t wg[4] = {graw[k].x, graw[k].y, graw[k].z, graw[k].w};
-    const uint32_t wu[4] = {uraw[k].x, uraw[k].y, uraw[k].z, uraw[k].w};
+  for (int i = 0; i < 8; ++i) {
+    const float h[4] = {hv[i].x, hv[i].y, hv[i].z, hv[i].w};
+    const float g[4] = {__uint_as_float(gv[i].x << 16), __uint_as_float(gv[i].x & 0xFFFF0000u),
+                        __uint_as_float(gv[i].y << 16), __uint_as_float(gv[i].y & 0xFFFF0000u)};
+    const float u[4] = {__uint_as_float(uv[i].x << 16), __uint_as_float(uv[i].x & 0xFFFF0000u),
+                        __uint_as_float(uv[i].y << 16), __uint_as_float(uv[i].y & 0xFFFF0000u)};
+    const bool ok = (valid >> (8 * gq + i)) & 1u;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      g[8 * k + 2 * i] = __uint_as_float(wg[i] << 16);
-      g[8 * k + 2 * i + 1] = __uint_as_float(wg[i] & 0xFFFF0000u);
-      u[8 * k + 2 * i] = __uint_as_float(wu[i] << 16);
-      u[8 * k + 2 * i + 1] = __uint_as_float(wu[i] & 0xFFFF0000u);
-    }
-  }
-  // du overwrites g (g * sg is kept in u's slot once u is used), dg its own array
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    if (valid) {
-      const float sg = 1.0f / (1.0f + __expf(-g[j]));
-      dg[j] = h[j] * u[j] * sg * (1.0f + g[j] * (1.0f - sg));
-      g[j] = h[j] * (g[j] * sg);
-    } else {
-      dg[j] = 0.0f;
-      g[j] = 0.0f;
+    for (int j = 0; j < 4; ++j) {
+      if (ok) {
+        const float sg = __fdividef(1.0f, 1.0f + __expf(-g[j]));
+        dg[i][j] = h[j] * u[j] * sg * (1.0f + g[j] * (1.0f - sg));
+        du[i][j] = h[j] * (g[j] * sg);
+      } else {
+        dg[i][j] = 0.0f;
+        du[i][j] = 0.0f;
+      }
     }
   }
+  // Row form: 32-column block of one row = the 8 lanes of a group, 4 code bytes each.
   const int ktl = 2 * I / 128;
-  uint8_t* qr = q_rows + prow * (2 * I);
-  emit_rowq(dg, qr + c0, q_rows_sf + sf_off(prow, c0 >> 5, ktl));
-  emit_rowq(g, qr + I + c0, q_rows_sf + sf_off(prow, (I + c0) >> 5, ktl));
-  // Token-axis codes: transpose this warp's 32 x 32 block (lane = column), quantise the column's 32 rows.
-  float* sw = scr[q];
 #pragma unroll
   for (int x = 0; x < 2; ++x) {
-    const float* v = x == 0 ? dg : g;
+    float (*v)[4] = x == 0 ? dg : du;
+    const int col = x * I + c0;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) sw[lane * 33 + j] = v[j];
-    __syncwarp();
-    float cv[32];
+    for (int i = 0; i < 8; ++i) {
+      float m = fmaxf(fmaxf(fabsf(v[i][0]), fabsf(v[i][1])), fmaxf(fabsf(v[i][2]), fabsf(v[i][3])));
+      m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+      m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+      m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+      const int b = mx_scale_byte(m);
+      const float inv = mx_inv_scale(b);
+      const int64_t prow = wrow + 8 * gq + i;
+      *reinterpret_cast<uint32_t*>(q_rows + prow * (2 * I) + col + 4 * cq) =
+          e4m3x2(v[i][0] * inv, v[i][1] * inv) | (e4m3x2(v[i][2] * inv, v[i][3] * inv) << 16);
+      if (cq == 0) q_rows_sf[sf_off(prow, col >> 5, ktl)] = static_cast<uint8_t>(b);
+    }
+  }
+  // Token form: column 4cq + j, 32 rows = 4 groups x 8 rows; this lane's 8 rows give 8 contiguous code bytes.
 #pragma unroll
-    for (int r = 0; r < 32; ++r) cv[r] = sw[r * 33 + lane];
-    __syncwarp();
-    const int b = mx_scale_byte(amax32(cv));
-    uint32_t w[8];
-    mx_pack32(cv, mx_inv_scale(b), w);
-    uint8_t* col_run = tst[x] + lane * 128;
-    *reinterpret_cast<uint4*>(col_run + (((2 * q) ^ (lane & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-    *reinterpret_cast<uint4*>(col_run + (((2 * q + 1) ^ (lane & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
-    reinterpret_cast<uint8_t*>(tsf[x])[lane * 4 + q] = static_cast<uint8_t>(b);
+  for (int x = 0; x < 2; ++x) {
+    float (*v)[4] = x == 0 ? dg : du;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float m = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i][j]));
+      m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
+      m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
+      const int b = mx_scale_byte(m);
+      const float inv = mx_inv_scale(b);
+      const uint32_t w0 = e4m3x2(v[0][j] * inv, v[1][j] * inv) | (e4m3x2(v[2][j] * inv, v[3][j] * inv) << 16);
+      const uint32_t w1 = e4m3x2(v[4][j] * inv, v[5][j] * inv) | (e4m3x2(v[6][j] * inv, v[7][j] * inv) << 16);
+      const int col = 4 * cq + j;
+      // rows 32q + 8gq .. +7 of the column: chunk 2q + gq/2, half gq % 2; chunks swizzled by col / 4
+      const int ch = (2 * q + (gq >> 1)) ^ cq;
+      *reinterpret_cast<uint2*>(tst[x] + col * 128 + ch * 16 + (gq & 1) * 8) = make_uint2(w0, w1);
+      if (gq == 0) reinterpret_cast<uint8_t*>(tsf[x])[col * 4 + q] = static_cast<uint8_t>(b);
+    }
   }
   __syncthreads();
   // 2 x 32 columns x 128 rows of codes: 8 threads per 128-byte column run.
@@ -266,7 +302,7 @@ __global__ void __launch_bounds__(128) swiglu_bwd_quant_kernel(
   for (int i = 0; i < 4; ++i) {
     const int idx = threadIdx.x + 128 * i;
     const int x = idx >> 8, col = (idx >> 3) & 31, ch = idx & 7;
-    const uint4 v = *reinterpret_cast<const uint4*>(tst[x] + col * 128 + ((ch ^ (col & 7)) << 4));
+    const uint4 v = *reinterpret_cast<const uint4*>(tst[x] + col * 128 + ((ch ^ ((col >> 2) & 7)) << 4));
     *reinterpret_cast<uint4*>(q_tok + static_cast<int64_t>(x * I + c0 + col) * Rmax + r0 + ch * 16) = v;
   }
   if (threadIdx.x < 64) {

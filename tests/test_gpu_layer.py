@@ -354,6 +354,9 @@ def test_dgrad_down_swiglu_stage(run):
     gu = gu_split(np_f64(run.ws("GU", torch.bfloat16, (run.Rmax, 2 * m.I))), m.I)
     dq = run.u8("DGU", run.Rmax, 2 * m.I)
     dsf = run.sf("DGU_SF", run.Rmax, 2 * m.I)
+    tq = run.u8("DGUTOK", 2 * m.I, run.Rmax)
+    tsf = run.sf("DGUTOK_SF", 2 * m.I, run.Rmax)
+    po = run.poff()
     for e in range(run.Ep):
         a, rows = run.expert_rows(e)
         if len(a) == 0:
@@ -364,6 +367,14 @@ def test_dgrad_down_swiglu_stage(run):
         r = OL.expert_backward(dOv, gu[rows], W, row_gate=gate)
         got = mxfp8.dequantize(dq[rows], dsf[rows], 1)
         assert rel_frob(got, mxfp8.roundtrip(r["dgu"], 1)) < TOL, e
+        # token-axis form: 32-rank blocks of each column from the segment start, zero rows past the count
+        n, n32 = len(a), -(-len(a) // 32) * 32
+        seg = slice(po[e], po[e] + n32)
+        ref_tok = np.zeros((n32, 2 * m.I))
+        ref_tok[:n] = r["dgu"]
+        got_tok = mxfp8.dequantize(tq[:, seg], tsf[:, po[e] // 32:(po[e] + n32) // 32], 1)
+        assert rel_frob(got_tok, mxfp8.roundtrip(ref_tok.T, 1)) < TOL, e
+        assert not tq[:, po[e] + n:po[e + 1]].any(), e
 
 
 def test_dgrad_gate_up_stage(run):
