@@ -255,11 +255,15 @@ __global__ void __launch_bounds__(128, 6) swiglu_bwd_quant_kernel(
     }
   }
   // Row form: 32-column block of one row = the 8 lanes of a group, 4 code bytes each.
+  // The lane's 8 rows lie in one 32-row block of the tiled scales: row i's byte is 16 i past row 0's.
   const int ktl = 2 * I / 128;
+  const int64_t prow0 = wrow + 8 * gq;
 #pragma unroll
   for (int x = 0; x < 2; ++x) {
     float (*v)[4] = x == 0 ? dg : du;
     const int col = x * I + c0;
+    uint8_t* qr = q_rows + prow0 * (2 * I) + col + 4 * cq;
+    uint8_t* qs = q_rows_sf + sf_off(prow0, col >> 5, ktl);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       float m = fmaxf(fmaxf(fabsf(v[i][0]), fabsf(v[i][1])), fmaxf(fabsf(v[i][2]), fabsf(v[i][3])));
@@ -268,10 +272,9 @@ __global__ void __launch_bounds__(128, 6) swiglu_bwd_quant_kernel(
       m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
       const int b = mx_scale_byte(m);
       const float inv = mx_inv_scale(b);
-      const int64_t prow = wrow + 8 * gq + i;
-      *reinterpret_cast<uint32_t*>(q_rows + prow * (2 * I) + col + 4 * cq) =
+      *reinterpret_cast<uint32_t*>(qr + static_cast<int64_t>(i) * (2 * I)) =
           e4m3x2(v[i][0] * inv, v[i][1] * inv) | (e4m3x2(v[i][2] * inv, v[i][3] * inv) << 16);
-      if (cq == 0) q_rows_sf[sf_off(prow, col >> 5, ktl)] = static_cast<uint8_t>(b);
+      if (cq == 0) qs[16 * i] = static_cast<uint8_t>(b);
     }
   }
   // Token form: column 4cq + j, 32 rows = 4 groups x 8 rows; this lane's 8 rows give 8 contiguous code bytes.
@@ -280,9 +283,8 @@ __global__ void __launch_bounds__(128, 6) swiglu_bwd_quant_kernel(
     float (*v)[4] = x == 0 ? dg : du;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      float m = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i][j]));
+      float m = fmaxf(fmaxf(fmaxf(fabsf(v[0][j]), fabsf(v[1][j])), fmaxf(fabsf(v[2][j]), fabsf(v[3][j]))),
+                      fmaxf(fmaxf(fabsf(v[4][j]), fabsf(v[5][j])), fmaxf(fabsf(v[6][j]), fabsf(v[7][j]))));
       m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
       m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
       const int b = mx_scale_byte(m);
