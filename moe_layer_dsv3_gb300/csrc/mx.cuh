@@ -37,11 +37,15 @@ __device__ __forceinline__ void mx_pack32(const float* v, float inv, uint32_t* w
   }
 }
 
+// Absolute maximum of 32 values as four interleaved chains of 8 (10
+// dependent maxima deep rather than 32, with 4 live temporaries).
 __device__ __forceinline__ float amax32(const float* v) {
-  float m = 0.0f;
+  float m[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-  for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(v[i]));
-  return m;
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) m[j] = fmaxf(m[j], fabsf(v[4 * i + j]));
+  return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
 }
 
 __device__ __forceinline__ void store32(uint8_t* dst, const uint32_t* w) {
