@@ -419,7 +419,7 @@ __device__ __forceinline__ void move_rows(const GemmParams& p, int lane, int a_l
     for (int u = 0; u < kFwdU; ++u) {
       const int t = __shfl_sync(0xffffffffu, tok_l, lr < kMoveRows ? lr : kMoveRows - 1);
       v[u] = (lr < kMoveRows && t >= 0)
-                 ? __ldg(reinterpret_cast<const uint4*>(p.mv_xq + static_cast<int64_t>(t) * d) + lc)
+                 ? ld_global_u4(reinterpret_cast<const uint4*>(p.mv_xq + static_cast<int64_t>(t) * d) + lc)
                  : zero;
       step(lr, lc);
     }
@@ -430,6 +430,7 @@ __device__ __forceinline__ void move_rows(const GemmParams& p, int lane, int a_l
 #pragma unroll
     for (int u = 0; u < kFwdU; ++u) cur[u] = nxt[u];
     if (rd + 1 < rounds) load(nxt);
+    __syncwarp();   // keeps the next round's loads ahead of this round's stores
 #pragma unroll
     for (int u = 0; u < kFwdU; ++u) {
       if (sr < kMoveRows) reinterpret_cast<uint4*>(p.ring + (ring_row0 + sr) * d)[sc] = cur[u];

@@ -85,6 +85,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
 }
 
 // ----------------------------------------------------------------- cross-CTA flags
+// Plain (coherent) 16-byte global load in volatile asm. The compiler keeps
+// such loads ahead of a later warp barrier; read-only (.nc) and ordinary loads
+// it may sink past one, toward their first use.
+__device__ __forceinline__ uint4 ld_global_u4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
