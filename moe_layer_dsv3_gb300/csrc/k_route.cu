@@ -107,17 +107,27 @@ __global__ void router_topk_kernel(const float* __restrict__ logits, const float
       kept |= 1u << be;
     }
   }
+  // This lane's candidates (experts of kept groups), one bit per slot i:
+  // the group of each slot is found once, not in every selection round.
   const int per = G > 1 ? E / G : E;
+  uint32_t cand = 0;
+#pragma unroll
+  for (int i = 0; i < kMaxPerLane; ++i) {
+    const int e = lane + 32 * i;
+    if (i < per_lane && e < E && ((kept >> (e / per)) & 1u)) cand |= 1u << i;
+  }
   uint32_t taken = 0;
-  int sel_e[8];
+  int sel_e[8];          // k <= 8 (checked by the API); unrolled, so both stay in registers
   float sel_s[8];
-  for (int j = 0; j < k; ++j) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j >= k) break;   // k is the same in every lane
     float bv = -INFINITY;
     int be = 0x7fffffff;
 #pragma unroll
     for (int i = 0; i < kMaxPerLane; ++i) {
       const int e = lane + 32 * i;
-      if (i < per_lane && e < E && !((taken >> i) & 1u) && ((kept >> (e / per)) & 1u)) {
+      if (((cand & ~taken) >> i) & 1u) {
         if (better(v[i], e, bv, be)) { bv = v[i]; be = e; }
       }
     }
@@ -130,14 +140,21 @@ __global__ void router_topk_kernel(const float* __restrict__ logits, const float
     sel_s[j] = __shfl_sync(0xffffffffu, sw, be & 31);
     sel_e[j] = be;
   }
-  if (lane == 0) {
-    float tot = sel_s[0];
-    for (int j = 1; j < k; ++j) tot = __fadd_rn(tot, sel_s[j]);
-    for (int j = 0; j < k; ++j) {
-      idx_out[static_cast<int64_t>(t) * k + j] = sel_e[j];
-      w_out[static_cast<int64_t>(t) * k + j] = __fdiv_rn(sel_s[j], tot);
-      if (s_out != nullptr) s_out[static_cast<int64_t>(t) * k + j] = sel_s[j];
-    }
+  // Every lane sums the selected scores in slot order; lane j writes slot j.
+  float tot = sel_s[0];
+#pragma unroll
+  for (int j = 1; j < 8; ++j)
+    if (j < k) tot = __fadd_rn(tot, sel_s[j]);
+  float my_s = 0.0f;
+  int my_e = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    if (j == lane && j < k) { my_s = sel_s[j]; my_e = sel_e[j]; }
+  if (lane < k) {
+    const int64_t o = static_cast<int64_t>(t) * k + lane;
+    idx_out[o] = my_e;
+    w_out[o] = __fdiv_rn(my_s, tot);
+    if (s_out != nullptr) s_out[o] = my_s;
   }
 }
 
