@@ -196,7 +196,8 @@ __device__ __forceinline__ uint2 ldg_u2(const void* p) {
 // along 2I per row (q_rows, tiled scales) and along ranks per column (q_tok,
 // [2I][Rmax], tiled scales). Row pr is an assignment iff row_src[pr] >= 0;
 // other rows of an expert's padded segment give zeros.
-//   sg = sigmoid(g), dg = dh u sg (1 + g (1 - sg)), du = dh g sg   (fp32)
+//   sg = sigmoid(g), dg = dh u sg (1 + g (1 - sg)), du = dh g sg   (fp32;
+//   sg from __expf and a fast divide, a few ulp, as in the forward)
 // CTA: 128 rows x 32 columns of I; warp q takes rows 32q..32q+31. Lane
 // (gq = lane / 8, cq = lane % 8) holds rows 8gq..8gq+7 of the warp's block
 // and columns 4cq..4cq+3, so each load instruction reads 4 rows' contiguous
