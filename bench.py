@@ -218,24 +218,45 @@ def hbm_bytes(shape):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples during the timed region."""
+    """nvidia-smi clock / throttle samples, every 50 ms with their timestamps.
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Start it before the warm-up (nvidia-smi takes a moment to start), bracket
+    the timed region with window(), and stop() keeps the samples taken inside
+    that window. A window shorter than the sampling period may hold none: the
+    samples nearest to it are kept then, and "in_window" says so.
+    """
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.proc = None
         self.path = None
+        self.t0 = self.t1 = None
         try:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+                 "-lms", "50"], stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+
+    def window(self, start: bool):
+        if start:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    @staticmethod
+    def _when(stamp):
+        import datetime
+        try:
+            return datetime.datetime.strptime(stamp.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
 
     def stop(self):
         if self.proc is None:
@@ -249,18 +270,27 @@ class ClockSampler:
         rows = []
         with open(self.path) as f:
             for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
+                parts = [q.strip() for q in line.split(",")]
+                if len(parts) >= 10:
+                    rows.append((self._when(parts[0]), parts[1:]))
         os.unlink(self.path)
         if not rows:
             return None
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        in_window = True
+        if self.t0 is not None and self.t1 is not None:
+            sel = [r for w, r in rows if w is not None and self.t0 <= w <= self.t1]
+            if not sel:   # window shorter than the sampling period: the nearest samples
+                in_window = False
+                timed = [(abs(w - 0.5 * (self.t0 + self.t1)), r) for w, r in rows if w is not None]
+                sel = [r for _, r in sorted(timed, key=lambda x: x[0])[:2]] or [r for _, r in rows]
+        else:
+            sel = [r for _, r in rows]
+        sm = [float(r[1]) for r in sel if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in sel if r[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        reasons = sorted({names[i] for r in sel for i in range(4) if r[5 + i].lower().startswith("active")})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(sel), "in_window": in_window}
 
 
 # ---------------------------------------------------------------- CPU oracle sample
@@ -486,6 +516,7 @@ def run_ours(args, rank, world, local_rank):
         L.forward(x, wr, bias, sp)
         L.backward(dy, sp)
 
+    clocks = ClockSampler(local_rank)   # started before the warm-up: nvidia-smi takes a moment to start
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -497,18 +528,19 @@ def run_ours(args, rank, world, local_rank):
         rank_barrier(world)
 
     # ---- timed region: K steps, inputs resident in HBM
-    clocks = ClockSampler(local_rank)
     M.moe_profile_enable(True)
     M.moe_profile_read()
     n0 = M.moe_launch_count()
     barrier()
     torch.cuda.synchronize()
+    clocks.window(True)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
         step()
     e1.record(stream)
     torch.cuda.synchronize()
+    clocks.window(False)
     barrier()
     launches = M.moe_launch_count() - n0
     kern = M.moe_profile_read()
