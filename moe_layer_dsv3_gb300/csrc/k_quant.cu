@@ -192,6 +192,28 @@ __device__ __forceinline__ uint2 ldg_u2(const void* p) {
   return v;
 }
 
+// Packed two-wide fp32 arithmetic (one instruction for two lanes of values;
+// each result rounded to nearest like the scalar operation).
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+// Two E4M3 codes of (a.x, a.y) * inv.
+__device__ __forceinline__ uint32_t e4m3x2_scaled(float2 a, float inv) {
+  const float2 v = fmul2(a, make_float2(inv, inv));
+  return e4m3x2(v.x, v.y);
+}
+
 // SwiGLU backward of padded rank rows and the two MX forms of dGU = [dg | du]:
 // along 2I per row (q_rows, tiled scales) and along ranks per column (q_tok,
 // [2I][Rmax], tiled scales). Row pr is an assignment iff row_src[pr] >= 0;
@@ -244,14 +266,20 @@ __global__ void __launch_bounds__(128, 6) swiglu_bwd_quant_kernel(
                         __uint_as_float(uv[i].y << 16), __uint_as_float(uv[i].y & 0xFFFF0000u)};
     const bool ok = (valid >> (8 * gq + i)) & 1u;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < 4; j += 2) {   // columns j, j + 1 as one packed pair
       if (ok) {
-        const float sg = __fdividef(1.0f, 1.0f + __expf(-g[j]));
-        dg[i][j] = h[j] * u[j] * sg * (1.0f + g[j] * (1.0f - sg));
-        du[i][j] = h[j] * (g[j] * sg);
+        const float2 sg = make_float2(__fdividef(1.0f, 1.0f + __expf(-g[j])),
+                                      __fdividef(1.0f, 1.0f + __expf(-g[j + 1])));
+        const float2 hh = make_float2(h[j], h[j + 1]), gg = make_float2(g[j], g[j + 1]);
+        const float2 uu = make_float2(u[j], u[j + 1]), one = make_float2(1.0f, 1.0f);
+        const float2 om = ffma2(sg, make_float2(-1.0f, -1.0f), one);            // 1 - sg
+        const float2 d = fmul2(fmul2(fmul2(hh, uu), sg), ffma2(gg, om, one));   // h u sg (1 + g (1 - sg))
+        const float2 e = fmul2(hh, fmul2(gg, sg));                              // h (g sg)
+        dg[i][j] = d.x; dg[i][j + 1] = d.y;
+        du[i][j] = e.x; du[i][j + 1] = e.y;
       } else {
-        dg[i][j] = 0.0f;
-        du[i][j] = 0.0f;
+        dg[i][j] = dg[i][j + 1] = 0.0f;
+        du[i][j] = du[i][j + 1] = 0.0f;
       }
     }
   }
@@ -274,7 +302,7 @@ __global__ void __launch_bounds__(128, 6) swiglu_bwd_quant_kernel(
       const int b = mx_scale_byte(m);
       const float inv = mx_inv_scale(b);
       *reinterpret_cast<uint32_t*>(qr + static_cast<int64_t>(i) * (2 * I)) =
-          e4m3x2(v[i][0] * inv, v[i][1] * inv) | (e4m3x2(v[i][2] * inv, v[i][3] * inv) << 16);
+          e4m3x2_scaled(make_float2(v[i][0], v[i][1]), inv) | (e4m3x2_scaled(make_float2(v[i][2], v[i][3]), inv) << 16);
       if (cq == 0) qs[16 * i] = static_cast<uint8_t>(b);
     }
   }
@@ -290,8 +318,10 @@ __global__ void __launch_bounds__(128, 6) swiglu_bwd_quant_kernel(
       m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
       const int b = mx_scale_byte(m);
       const float inv = mx_inv_scale(b);
-      const uint32_t w0 = e4m3x2(v[0][j] * inv, v[1][j] * inv) | (e4m3x2(v[2][j] * inv, v[3][j] * inv) << 16);
-      const uint32_t w1 = e4m3x2(v[4][j] * inv, v[5][j] * inv) | (e4m3x2(v[6][j] * inv, v[7][j] * inv) << 16);
+      const uint32_t w0 = e4m3x2_scaled(make_float2(v[0][j], v[1][j]), inv) |
+                          (e4m3x2_scaled(make_float2(v[2][j], v[3][j]), inv) << 16);
+      const uint32_t w1 = e4m3x2_scaled(make_float2(v[4][j], v[5][j]), inv) |
+                          (e4m3x2_scaled(make_float2(v[6][j], v[7][j]), inv) << 16);
       const int col = 4 * cq + j;
       // rows 32q + 8gq .. +7 of the column: chunk 2q + gq/2, half gq % 2; chunks swizzled by col / 4
       const int ch = (2 * q + (gq >> 1)) ^ cq;
