@@ -16,6 +16,7 @@ bounded sample of the same workload on all host cores.
 from __future__ import annotations
 
 import argparse
+import atexit
 import dataclasses
 import json
 import os
@@ -241,8 +242,17 @@ class ClockSampler:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
                  "-lms", "50"], stdout=self.fh, stderr=subprocess.DEVNULL)
+            atexit.register(self._end)   # no sampler outlives the bench, even one that raised before stop()
         except (OSError, FileNotFoundError):
             self.proc = None
+
+    def _end(self):
+        if self.proc is not None and self.proc.poll() is None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
 
     def window(self, start: bool):
         if start:
@@ -261,11 +271,7 @@ class ClockSampler:
     def stop(self):
         if self.proc is None:
             return None
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
+        self._end()
         self.fh.close()
         rows = []
         with open(self.path) as f:

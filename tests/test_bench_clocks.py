@@ -12,6 +12,9 @@ import bench  # noqa: E402
 
 
 class _DoneProc:
+    def poll(self):
+        return 0
+
     def terminate(self):
         pass
 
