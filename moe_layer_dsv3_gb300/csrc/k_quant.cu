@@ -2,6 +2,7 @@
 // token-axis gathers through the schedule, and scale re-tiling.
 #include "moe_internal.h"
 #include "mx.cuh"
+#include "ptx.cuh"
 #include "prof.h"
 
 namespace moe {
@@ -175,23 +176,6 @@ __global__ void __launch_bounds__(kTokThreads, kGate ? 3 : 4) tok_gather_kernel(
   *reinterpret_cast<uint32_t*>(sf + sf_off(cb + threadIdx.x, r0 >> 5, Rmax >> 7)) = ssf[threadIdx.x];
 }
 
-// Plain (coherent) global loads in volatile asm. Issued before a warp barrier,
-// they all stay ahead of it; the compiler may sink ordinary and read-only
-// (.nc) loads toward their first use, past such a barrier too, and a warp
-// then waits on one load after another instead of on all of them at once.
-__device__ __forceinline__ float4 ldg_f4(const float* p) {
-  float4 v;
-  asm volatile("ld.global.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
-  return v;
-}
-
-__device__ __forceinline__ uint2 ldg_u2(const void* p) {
-  uint2 v;
-  asm volatile("ld.global.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-  return v;
-}
-
 // Packed two-wide fp32 arithmetic (one instruction for two lanes of values;
 // each result rounded to nearest like the scalar operation).
 __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
@@ -241,7 +225,7 @@ __global__ void __launch_bounds__(128, 6) swiglu_bwd_quant_kernel(
   const int c0 = blockIdx.x * 32;
   const int64_t wrow = r0 + q * 32;                       // first row of this warp's block
   const uint32_t valid = __ballot_sync(0xFFFFFFFFu, row_src[wrow + lane] >= 0);
-  // All 24 loads are issued before any arithmetic (ldg_f4, ldg_u2 and the
+  // All 24 loads are issued before any arithmetic (coherent ld_global_* loads and the
   // warp barrier after them): left to itself the compiler sinks them toward
   // their uses, and the kernel took 1.22 instead of 0.78 ms at full size.
   float4 hv[8];
@@ -249,11 +233,11 @@ __global__ void __launch_bounds__(128, 6) swiglu_bwd_quant_kernel(
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int64_t prow = wrow + 8 * gq + i;
-    hv[i] = ldg_f4(dh + prow * I + c0 + 4 * cq);
+    hv[i] = ld_global_f4(dh + prow * I + c0 + 4 * cq);
     // saved g,u: 32-column chunk c0 / 32 of the row holds g then u
     const __nv_bfloat16* pg = gu + prow * (2 * I) + 2 * c0 + 4 * cq;
-    gv[i] = ldg_u2(pg);
-    uv[i] = ldg_u2(pg + 32);
+    gv[i] = ld_global_u2(pg);
+    uv[i] = ld_global_u2(pg + 32);
   }
   __syncwarp();
   float dg[8][4], du[8][4];

@@ -85,12 +85,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
 }
 
 // ----------------------------------------------------------------- cross-CTA flags
-// Plain (coherent) 16-byte global load in volatile asm. The compiler keeps
-// such loads ahead of a later warp barrier; read-only (.nc) and ordinary loads
-// it may sink past one, toward their first use.
+// Plain (coherent) global loads in volatile asm. The compiler keeps such
+// loads ahead of a later warp barrier; read-only (.nc) and ordinary loads it
+// may sink past one, toward their first use, and a warp then waits on one
+// load after another instead of on all of them at once.
 __device__ __forceinline__ uint4 ld_global_u4(const void* p) {
   uint4 v;
   asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float4 ld_global_f4(const void* p) {
+  float4 v;
+  asm volatile("ld.global.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint2 ld_global_u2(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
   return v;
 }
 
